@@ -1,0 +1,543 @@
+/*
+ * zero_oracle.c -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, obviously correct, single-threaded CPU oracle of the ZeRO-DP
+ * optimizer step: rank-ordered fp32 reduce of the simulated ranks' gradients,
+ * mixed-precision Adam on fp32 master weights / momentum / variance, cast to
+ * 16 bits and replicate (all-gather).  It is loaded only by the tests, by the
+ * smoke check and by the benchmark's CPU-baseline leg.
+ *
+ * Compile with -O2 -ffp-contract=off and no fast-math: every fp32 operation
+ * below is one IEEE-754 round-to-nearest-even operation in the order written.
+ *
+ * Sources (page title, section):
+ *   [DP-notes]  "Data parallelism and ZeRO optimization -- Hinglish notes" (6.1.8)
+ *   [LLM-par]   "大模型并行技术" (LLM parallelism techniques)
+ *   [itwiki]    "ZeRO (딥 러닝)"
+ *   [MP-notes]  "Model parallelism (tensor, pipeline) -- Hinglish notes" (6.1.7)
+ * Where the pages are silent (the Adam equations, the clipping rule, loss
+ * scaling, the quantizer's rounding) the reading used is stated at the
+ * function and listed with the other readings in the design notes.
+ */
+#include "zero_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+static uint32_t bits_of(float x) { uint32_t u; memcpy(&u, &x, 4); return u; }
+static float float_of(uint32_t u) { float x; memcpy(&x, &u, 4); return x; }
+
+/* ------------------------------------------------------------------------ */
+/* Partition.  [DP-notes] "ZeRO-1: Optimizer State Partitioning": the        */
+/* parameters are split into N groups theta = [theta_1 .. theta_N] and rank  */
+/* r owns theta_r.  [itwiki] "FSDP와의 관계": parameters of a unit are       */
+/* flattened, then sharded.  Reading: equal contiguous shards of padded size  */
+/* S = roundup(ceil(psi / n_d), shard_pad); the last shards may be short or  */
+/* empty.                                                                     */
+/* ------------------------------------------------------------------------ */
+long long zo_shard_size(long long psi, int n_d, int shard_pad)
+{
+    long long per_rank = (psi + n_d - 1) / n_d;          /* ceil(psi / n_d) */
+    long long groups = (per_rank + shard_pad - 1) / shard_pad;
+    return groups * shard_pad;
+}
+
+long long zo_valid_len(long long psi, long long shard, int r)
+{
+    long long left = psi - (long long)r * shard;
+    if (left < 0) return 0;
+    if (left > shard) return shard;
+    return left;
+}
+
+void zo_owner(long long j, long long shard, int* r, long long* i)
+{
+    *r = (int)(j / shard);
+    *i = j % shard;
+}
+
+/* ------------------------------------------------------------------------ */
+/* 16-bit encodings, from the IEEE-754 definitions: keep the top bits, then   */
+/* round the dropped part to nearest, ties to the even result.               */
+/* ------------------------------------------------------------------------ */
+
+/* Shift a non-negative value right by s bits, rounding to nearest even. */
+static uint64_t shift_rne(uint64_t v, int s)
+{
+    if (s <= 0) return v;
+    if (s >= 63) return 0;
+    uint64_t kept = v >> s;
+    uint64_t dropped = v - (kept << s);
+    uint64_t half = (uint64_t)1 << (s - 1);
+    if (dropped > half || (dropped == half && (kept & 1))) kept += 1;
+    return kept;
+}
+
+uint16_t zo_f32_to_bf16(float x)
+{
+    uint32_t u = bits_of(x);
+    if ((u & 0x7FFFFFFFu) > 0x7F800000u) {
+        /* NaN: keep the sign, force a quiet NaN */
+        return (uint16_t)(((u >> 16) & 0x8000u) | 0x7FC0u);
+    }
+    /* bf16 is the top half of the fp32 pattern; a carry out of the mantissa
+     * moves into the exponent, which is what rounding up to the next binade
+     * (or to infinity) means. */
+    return (uint16_t)shift_rne(u, 16);
+}
+
+float zo_bf16_to_f32(uint16_t h)
+{
+    return float_of((uint32_t)h << 16);
+}
+
+uint16_t zo_f32_to_fp16(float x)
+{
+    uint32_t u = bits_of(x);
+    uint16_t sign = (uint16_t)((u >> 16) & 0x8000u);
+    uint32_t a = u & 0x7FFFFFFFu;
+    if (a > 0x7F800000u) return (uint16_t)(sign | 0x7E00u);  /* NaN */
+    if (a == 0x7F800000u) return (uint16_t)(sign | 0x7C00u); /* inf */
+    int e = (int)(a >> 23);              /* biased fp32 exponent */
+    uint32_t mant = a & 0x7FFFFFu;
+    if (e == 0) return sign;             /* fp32 subnormals are far below fp16's range */
+    uint64_t sig = (uint64_t)(mant | 0x800000u);   /* value = sig * 2^(e - 150) */
+    int e16 = e - 127 + 15;              /* biased fp16 exponent if normal */
+    if (e16 >= 1) {
+        /* normal: 10 mantissa bits kept, 13 dropped */
+        uint64_t r = shift_rne(sig, 13);                /* in [2^10, 2^11] */
+        uint64_t out = ((uint64_t)e16 << 10) + (r - 1024); /* carry into the exponent is fine */
+        if (out >= 0x7C00u) return (uint16_t)(sign | 0x7C00u);
+        return (uint16_t)(sign | out);
+    }
+    /* subnormal fp16: units of 2^-24; value / 2^-24 = sig * 2^(e - 126) */
+    int s = 126 - e;                     /* >= 14 here */
+    uint64_t q = shift_rne(sig, s);      /* may reach 1024 = smallest normal */
+    return (uint16_t)(sign | q);
+}
+
+float zo_fp16_to_f32(uint16_t h)
+{
+    uint32_t sign = ((uint32_t)h & 0x8000u) << 16;
+    uint32_t e = ((uint32_t)h >> 10) & 0x1Fu;
+    uint32_t mant = (uint32_t)h & 0x3FFu;
+    if (e == 0) {
+        float mag = ldexpf((float)mant, -24);            /* exact */
+        return sign ? -mag : mag;
+    }
+    if (e == 31) return float_of(sign | 0x7F800000u | (mant << 13));
+    return float_of(sign | ((e - 15 + 127) << 23) | (mant << 13));
+}
+
+float zo_lp_to_f32(uint16_t h, int dtype)
+{
+    return dtype == ZO_FP16 ? zo_fp16_to_f32(h) : zo_bf16_to_f32(h);
+}
+
+uint16_t zo_f32_to_lp(float x, int dtype)
+{
+    return dtype == ZO_FP16 ? zo_f32_to_fp16(x) : zo_f32_to_bf16(x);
+}
+
+void zo_f32_to_lp_array(long long n, const float* x, uint16_t* out, int dtype)
+{
+    for (long long i = 0; i < n; ++i) out[i] = zo_f32_to_lp(x[i], dtype);
+}
+
+void zo_lp_to_f32_array(long long n, const uint16_t* h, float* out, int dtype)
+{
+    for (long long i = 0; i < n; ++i) out[i] = zo_lp_to_f32(h[i], dtype);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Memory accounting.  [itwiki] "학습 메모리는 어디에 쓰이나" (model-state    */
+/* table: 2 + 2 + K bytes per parameter, K = 12) and "ZeRO-DP의 세 단계"      */
+/* (stage table): stage 0 keeps everything, stage 1 divides the optimizer    */
+/* term by N_d, stage 2 also the gradients, stage 3 also the parameters.     */
+/* out = {params, grads, optimizer, total} in bytes.                          */
+/* ------------------------------------------------------------------------ */
+void zo_model_state_bytes(double psi, double n_d, int stage, double k, double out[4])
+{
+    double params = 2.0 * psi, grads = 2.0 * psi, optim = k * psi;
+    switch (stage) {
+    case 0:
+        break;
+    case 1:
+        optim = k * psi / n_d;
+        break;
+    case 2:
+        grads = 2.0 * psi / n_d;
+        optim = k * psi / n_d;
+        break;
+    default: /* 3 */
+        params = 2.0 * psi / n_d;
+        grads = 2.0 * psi / n_d;
+        optim = k * psi / n_d;
+        break;
+    }
+    out[0] = params;
+    out[1] = grads;
+    out[2] = optim;
+    out[3] = params + grads + optim;
+}
+
+/* [itwiki] "왜 통신량이 늘지 않는가": stages 0-2 move one reduce-scatter and
+ * one all-gather (psi each); stage 3 gathers twice (forward and backward) and
+ * reduce-scatters once.  Result in units of psi. */
+double zo_comm_volume(int stage)
+{
+    double reduce_scatter = 1.0, all_gather = 1.0;
+    if (stage >= 3) return reduce_scatter + 2.0 * all_gather;
+    return reduce_scatter + all_gather;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Collectives.  [DP-notes] "How Standard Data Parallelism Works": the        */
+/* all-reduce averages, grad = (1/N) sum_r grad_r.  [itwiki] "FSDP와의 관계"   */
+/* reduces in fp32 (reduce_dtype=float32).  Reading: widen each rank's value */
+/* to fp32, add ranks in order 0..N-1 starting from +0.0f, divide once by    */
+/* the divisor (N_d times the loss scale).                                    */
+/* ------------------------------------------------------------------------ */
+static float reduce_one(int n_d, const uint16_t* const* grads, int dtype, long long j, float divisor)
+{
+    float sum = 0.0f;
+    for (int q = 0; q < n_d; ++q) sum = sum + zo_lp_to_f32(grads[q][j], dtype);
+    return sum / divisor;
+}
+
+void zo_all_reduce_mean(int n_d, long long psi, const uint16_t* const* grads, int dtype,
+                        float divisor, float* out)
+{
+    for (long long j = 0; j < psi; ++j) out[j] = reduce_one(n_d, grads, dtype, j, divisor);
+}
+
+/* [DP-notes] "ZeRO-2: Gradient Partitioning": rank r receives only the
+ * averaged gradient of its own partition.  shards is n_d * S long; shard r
+ * starts at r * S; its entries past the valid length are +0. */
+void zo_reduce_scatter(int n_d, long long psi, long long shard, const uint16_t* const* grads,
+                       int dtype, float divisor, float* shards)
+{
+    for (int r = 0; r < n_d; ++r) {
+        long long len = zo_valid_len(psi, shard, r);
+        for (long long i = 0; i < shard; ++i) {
+            long long j = (long long)r * shard + i;
+            shards[j] = (i < len) ? reduce_one(n_d, grads, dtype, j, divisor) : 0.0f;
+        }
+    }
+}
+
+/* [DP-notes] "ZeRO-1": the updated partitions are all-gathered so every rank
+ * holds the full model.  Shard r lands at global offset r * S; only [0, psi)
+ * of the gathered buffer is written. */
+void zo_all_gather_u16(int n_d, long long psi, long long shard, const uint16_t* const* shards,
+                       uint16_t* gathered)
+{
+    for (int r = 0; r < n_d; ++r) {
+        long long len = zo_valid_len(psi, shard, r);
+        for (long long i = 0; i < len; ++i) gathered[(long long)r * shard + i] = shards[r][i];
+    }
+}
+
+void zo_all_gather_f32(int n_d, long long psi, long long shard, const float* const* shards,
+                       float* gathered)
+{
+    for (int r = 0; r < n_d; ++r) {
+        long long len = zo_valid_len(psi, shard, r);
+        for (long long i = 0; i < len; ++i) gathered[(long long)r * shard + i] = shards[r][i];
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Adam.  The pages size Adam's state ([DP-notes] "Memory Consumption        */
+/* Analysis": fp32 momentum, variance and master copy) but print no update    */
+/* rule.  Reading: textbook Adam (Kingma & Ba, Algorithm 1) with bias         */
+/* correction and eps outside the square root; weight decay decoupled as in  */
+/* AdamW ([itwiki] "FSDP와의 관계" uses AdamW).  Per committed step t the     */
+/* fp64 products beta^t are extended by one multiplication, never pow().      */
+/* ------------------------------------------------------------------------ */
+void zo_adam_consts_for(const zo_hparams* hp, double beta1_pow_t, double beta2_pow_t,
+                        zo_adam_consts* c)
+{
+    float bc1 = (float)(1.0 - beta1_pow_t);
+    float bc2 = (float)(1.0 - beta2_pow_t);
+    c->step_size = hp->lr / bc1;
+    c->sbc2 = sqrtf(bc2);
+    c->omb1 = 1.0f - hp->beta1;
+    c->omb2 = 1.0f - hp->beta2;
+    float lr_wd = hp->lr * hp->weight_decay;
+    c->decay = 1.0f - lr_wd;
+}
+
+void zo_adam_update(const zo_hparams* hp, const zo_adam_consts* c, long long n, const float* g,
+                    float* p, float* m, float* v)
+{
+    for (long long i = 0; i < n; ++i) {
+        float gi = g[i];
+        float pi = p[i];
+        if (hp->weight_decay != 0.0f) pi = pi * c->decay;
+        float mi = hp->beta1 * m[i] + c->omb1 * gi;          /* no contraction: two roundings, then the add */
+        float g2 = gi * gi;
+        float vi = hp->beta2 * v[i] + c->omb2 * g2;
+        float denom = sqrtf(vi) / c->sbc2 + hp->eps;
+        float ratio = mi / denom;
+        pi = pi - c->step_size * ratio;
+        p[i] = pi;
+        m[i] = mi;
+        v[i] = vi;
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Clipping.  [itwiki] "DeepSpeed에서 쓰기" sets gradient_clipping = 1.0      */
+/* without the rule.  Reading: global L2 norm of the unscaled averaged        */
+/* gradient over all psi entries, squares and sum in fp64 in index order;     */
+/* coef = max_norm / (norm + 1e-6), applied only when below one.              */
+/* ------------------------------------------------------------------------ */
+double zo_sqnorm(long long n, const float* g)
+{
+    double acc = 0.0;
+    for (long long i = 0; i < n; ++i) acc += (double)g[i] * (double)g[i];
+    return acc;
+}
+
+float zo_clip_coef(float max_norm, double sqnorm, int* applied)
+{
+    double norm = sqrt(sqnorm);
+    float coef = (float)((double)max_norm / (norm + 1e-6));
+    *applied = coef < 1.0f;
+    return coef;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Step bookkeeping.  Loss scaling is not on the pages; the reading: only in */
+/* loss-scaling mode, a step whose averaged gradient holds a non-finite value */
+/* is skipped (state untouched, t not advanced), the scale halves (floored    */
+/* at min_scale) and the good-step counter resets; after scale_window good    */
+/* steps in a row the scale doubles.                                          */
+/* ------------------------------------------------------------------------ */
+void zo_scalars_init(zo_scalars* sc, float loss_scale)
+{
+    sc->t = 0;
+    sc->beta1_pow = 1.0;
+    sc->beta2_pow = 1.0;
+    sc->loss_scale = loss_scale;
+    sc->good_steps = 0;
+    sc->overflow = 0;
+    sc->sqnorm = 0.0;
+    sc->clip_coef = 1.0f;
+}
+
+static void commit_skip(const zo_hparams* hp, zo_scalars* sc)
+{
+    float half = sc->loss_scale * 0.5f;
+    sc->loss_scale = half > hp->min_scale ? half : hp->min_scale;
+    sc->good_steps = 0;
+    sc->overflow = 1;
+}
+
+static void commit_step(const zo_hparams* hp, zo_scalars* sc)
+{
+    sc->t += 1;
+    sc->beta1_pow = sc->beta1_pow * (double)hp->beta1;
+    sc->beta2_pow = sc->beta2_pow * (double)hp->beta2;
+    sc->overflow = 0;
+    if (hp->loss_scaling) {
+        sc->good_steps += 1;
+        if (sc->good_steps >= hp->scale_window) {
+            sc->loss_scale = sc->loss_scale * 2.0f;
+            sc->good_steps = 0;
+        }
+    }
+}
+
+static float step_divisor(int n_d, const zo_hparams* hp, const zo_scalars* sc)
+{
+    float scale = hp->loss_scaling ? sc->loss_scale : 1.0f;
+    return (float)n_d * scale;
+}
+
+/* Plain data parallelism ([DP-notes] "How Standard Data Parallelism Works",
+ * [LLM-par] "数据并行"): all-reduce the mean, update the full model, cast and
+ * replicate.  Returns 1 if the step was skipped, 0 otherwise. */
+int zo_plain_dp_step(int n_d, long long psi, const uint16_t* const* grads, int grad_dtype,
+                     const zo_hparams* hp, zo_scalars* sc, float* master, float* m, float* v,
+                     uint16_t* params_lp, int param_dtype)
+{
+    float divisor = step_divisor(n_d, hp, sc);
+    float* g = (float*)malloc(sizeof(float) * (size_t)(psi > 0 ? psi : 1));
+    zo_all_reduce_mean(n_d, psi, grads, grad_dtype, divisor, g);
+
+    int overflow = 0;
+    if (hp->loss_scaling)
+        for (long long j = 0; j < psi; ++j)
+            if (!isfinite(g[j])) overflow = 1;
+
+    sc->sqnorm = 0.0;
+    sc->clip_coef = 1.0f;
+    int applied = 0;
+    float coef = 1.0f;
+    if (hp->max_norm > 0.0f) {
+        sc->sqnorm = zo_sqnorm(psi, g);
+        coef = zo_clip_coef(hp->max_norm, sc->sqnorm, &applied);
+    }
+    if (overflow) {
+        commit_skip(hp, sc);
+        free(g);
+        return 1;
+    }
+    if (applied) {
+        for (long long j = 0; j < psi; ++j) g[j] = g[j] * coef;
+        sc->clip_coef = coef;
+    }
+    zo_adam_consts c;
+    zo_adam_consts_for(hp, sc->beta1_pow * (double)hp->beta1, sc->beta2_pow * (double)hp->beta2, &c);
+    zo_adam_update(hp, &c, psi, g, master, m, v);
+    for (long long j = 0; j < psi; ++j) params_lp[j] = zo_f32_to_lp(master[j], param_dtype);
+    commit_step(hp, sc);
+    free(g);
+    return 0;
+}
+
+/* The ZeRO path, written literally ([DP-notes] "ZeRO-1", "ZeRO-2", "ZeRO-3";
+ * [LLM-par] "优化状态与梯度分割" steps (2)-(3); [itwiki] "왜 통신량이 늘지
+ * 않는가"): each rank receives its shard of the averaged gradient (stage 1:
+ * all-reduce then keep the own slice; stages 2-3: reduce-scatter), the two
+ * global scalars (overflow flag, squared norm) are combined across shards in
+ * rank order, each rank updates its own fp32 shard, casts it, and the 16-bit
+ * shards are all-gathered (stages 1-2) or left sharded (stage 3, gathered
+ * per layer before use).  State arrays are n_d * S long; their padding is
+ * never touched.  lp_shards (stage 3) is n_d * S long; gathered is psi long. */
+int zo_zero_step(int n_d, long long psi, int shard_pad, int stage, const uint16_t* const* grads,
+                 int grad_dtype, const zo_hparams* hp, zo_scalars* sc, float* master, float* m,
+                 float* v, uint16_t* lp_shards, uint16_t* gathered, int param_dtype)
+{
+    long long S = zo_shard_size(psi, n_d, shard_pad);
+    long long padded = S * n_d;
+    float divisor = step_divisor(n_d, hp, sc);
+    float* shards = (float*)malloc(sizeof(float) * (size_t)(padded > 0 ? padded : 1));
+
+    if (stage == 1) {
+        /* all-reduce the full averaged gradient, then each rank keeps its slice */
+        float* full = (float*)malloc(sizeof(float) * (size_t)(psi > 0 ? psi : 1));
+        zo_all_reduce_mean(n_d, psi, grads, grad_dtype, divisor, full);
+        for (int r = 0; r < n_d; ++r) {
+            long long len = zo_valid_len(psi, S, r);
+            for (long long i = 0; i < S; ++i)
+                shards[(long long)r * S + i] = i < len ? full[(long long)r * S + i] : 0.0f;
+        }
+        free(full);
+    } else {
+        zo_reduce_scatter(n_d, psi, S, grads, grad_dtype, divisor, shards);
+    }
+
+    /* scalar all-reduce across shards: one running value, rank order */
+    int overflow = 0;
+    double sq = 0.0;
+    for (int r = 0; r < n_d; ++r) {
+        long long len = zo_valid_len(psi, S, r);
+        const float* gr = shards + (long long)r * S;
+        for (long long i = 0; i < len; ++i) {
+            if (hp->loss_scaling && !isfinite(gr[i])) overflow = 1;
+            sq += (double)gr[i] * (double)gr[i];
+        }
+    }
+    sc->sqnorm = 0.0;
+    sc->clip_coef = 1.0f;
+    int applied = 0;
+    float coef = 1.0f;
+    if (hp->max_norm > 0.0f) {
+        sc->sqnorm = sq;
+        coef = zo_clip_coef(hp->max_norm, sq, &applied);
+    }
+    if (overflow) {
+        commit_skip(hp, sc);
+        free(shards);
+        return 1;
+    }
+    if (applied) sc->clip_coef = coef;
+
+    zo_adam_consts c;
+    zo_adam_consts_for(hp, sc->beta1_pow * (double)hp->beta1, sc->beta2_pow * (double)hp->beta2, &c);
+    uint16_t* own_lp = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(padded > 0 ? padded : 1));
+    const uint16_t** lp_ptrs = (const uint16_t**)malloc(sizeof(uint16_t*) * (size_t)n_d);
+    for (int r = 0; r < n_d; ++r) {
+        long long off = (long long)r * S;
+        long long len = zo_valid_len(psi, S, r);
+        float* gr = shards + off;
+        if (applied)
+            for (long long i = 0; i < len; ++i) gr[i] = gr[i] * coef;
+        zo_adam_update(hp, &c, len, gr, master + off, m + off, v + off);
+        for (long long i = 0; i < len; ++i) own_lp[off + i] = zo_f32_to_lp(master[off + i], param_dtype);
+        lp_ptrs[r] = own_lp + off;
+    }
+    if (stage >= 3) {
+        for (int r = 0; r < n_d; ++r) {
+            long long off = (long long)r * S;
+            long long len = zo_valid_len(psi, S, r);
+            for (long long i = 0; i < len; ++i) lp_shards[off + i] = own_lp[off + i];
+        }
+    } else {
+        zo_all_gather_u16(n_d, psi, S, lp_ptrs, gathered);
+    }
+    commit_step(hp, sc);
+    free((void*)lp_ptrs);
+    free(own_lp);
+    free(shards);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Block-int8 quantized gather.  [itwiki] "후속 기법", ZeRO++ row: weights    */
+/* are block-quantized before the all-gather (qwZ); bit width, block size and */
+/* rounding are not given.  Reading: symmetric int8 in [-127, 127], one fp32  */
+/* scale per block = absmax / 127, code = round-half-even(x / scale),         */
+/* dequantized value = bf16(code * scale); an all-zero block has scale 0 and  */
+/* codes 0.                                                                   */
+/* ------------------------------------------------------------------------ */
+void zo_quantize_block(long long n, const uint16_t* x_bf16, int8_t* codes, float* scale,
+                       uint16_t* deq_bf16)
+{
+    float amax = 0.0f;
+    for (long long i = 0; i < n; ++i) {
+        float a = fabsf(zo_bf16_to_f32(x_bf16[i]));
+        if (a > amax) amax = a;
+    }
+    float s = amax / 127.0f;
+    *scale = s;
+    for (long long i = 0; i < n; ++i) {
+        float q = 0.0f;
+        if (s != 0.0f) {
+            q = rintf(zo_bf16_to_f32(x_bf16[i]) / s);   /* default rounding mode: ties to even */
+            if (q > 127.0f) q = 127.0f;
+            if (q < -127.0f) q = -127.0f;
+        }
+        codes[i] = (int8_t)q;
+        /* the receiver sees only the integer code, which has no negative zero */
+        deq_bf16[i] = zo_f32_to_bf16((float)codes[i] * s);
+    }
+}
+
+/* Blocks start at each shard's first element; the last block of a shard may
+ * be short.  scales has n_d * ceil(S / block) entries (shard-major); blocks
+ * past a shard's valid length get scale 0.  codes is flat (n_d * S, written
+ * for j < psi); gathered receives the dequantized bf16 values for j < psi. */
+void zo_quant_gather(int n_d, long long psi, long long shard, int block, const uint16_t* shards,
+                     int8_t* codes, float* scales, uint16_t* gathered)
+{
+    long long blocks_per_shard = (shard + block - 1) / block;
+    for (int r = 0; r < n_d; ++r) {
+        long long len = zo_valid_len(psi, shard, r);
+        for (long long b = 0; b < blocks_per_shard; ++b) {
+            long long lo = b * block;
+            long long hi = lo + block < len ? lo + block : len;
+            float* sc = scales + (long long)r * blocks_per_shard + b;
+            if (hi <= lo) {
+                *sc = 0.0f;
+                continue;
+            }
+            long long off = (long long)r * shard + lo;
+            zo_quantize_block(hi - lo, shards + off, codes + off, sc, gathered + off);
+        }
+    }
+}
