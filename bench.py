@@ -1,0 +1,492 @@
+"""Benchmark of the GB300 ZeRO-DP optimizer step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+                    [--config 1..5] [--nd N] [--qgather] [--no-cpu-baseline]
+
+A step is one pass of the whole hot path (reduce-scatter of the simulated
+ranks' gradients, global checks, Adam on every shard, 16-bit cast and gather)
+over one batch of synthetic gradients already resident in HBM.  The default
+workload is the GPT-2-small one: Psi = 124,439,808 flat parameters, N_d = 8
+simulated ranks, bf16 gradients ~N(0, 1e-2) with a 1% x100 tail, AdamW
+(lr 3e-4, betas 0.9/0.95, wd 0.1), global-norm clipping at 1.0.
+
+One JSON line is printed (rank 0).  value = parameters updated per second over
+the whole job; roofline = the dominant kernel's algorithmic bytes per launch
+over its CUDA-event duration, against the measured HBM copy bandwidth;
+cpu_baseline = the CPU oracle timed on a bounded sample on this host;
+e2e = the same metric with the gradients copied from pinned host memory and
+the gathered parameters copied back inside the timed region.
+
+--gpus N under torchrun runs N independent replicas (one per GPU): the
+ranks of the method are buffers inside one GPU, so nothing is exchanged
+between GPUs; the timed region is bracketed by barriers and the max over
+ranks is taken.  --impl reference times the CPU oracle instead.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "ZeRO step params/s and achieved HBM GB/s (% of GB300 roofline), 1 GPU"
+UNIT = "params/s"
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ----------------------------------------------------------------- workloads
+def workload(cfg, nd=None, qgather=False):
+    """Sizes, hyper-parameters and the algorithmic bytes of one step."""
+    if cfg == 1:
+        w = dict(name="zero2_psi1000003_nd4_adam", psi=1_000_003, n_d=4, stage=2, pad=8, gdt="bf16",
+                 sigma=1e-3, tail=False, lr=1e-3, b2=0.999, wd=0.0, clip=0.0, ls=False, layers=1)
+    elif cfg == 2:
+        w = dict(name="zero2_gpt2small_psi124439808_nd8_adamw_clip1", psi=124_439_808, n_d=8, stage=2, pad=8,
+                 gdt="bf16", sigma=1e-2, tail=True, lr=3e-4, b2=0.95, wd=0.1, clip=1.0, ls=False, layers=1)
+    elif cfg == 3:
+        w = dict(name="zero2_gpt2xl_psi1500000000_nd8_fp16_lossscale", psi=1_500_000_000, n_d=8, stage=2, pad=8,
+                 gdt="fp16", sigma=1e-4, tail=False, lr=1e-4, b2=0.999, wd=0.0, clip=0.0, ls=True, layers=1)
+    elif cfg == 4:
+        w = dict(name="zero3_llama3_8b_8layers_psil218112000_nd16", psi=218_112_000, n_d=16, stage=3, pad=8,
+                 gdt="bf16", sigma=1e-3, tail=False, lr=1e-3, b2=0.999, wd=0.0, clip=0.0, ls=False, layers=8)
+    elif cfg == 5:
+        n = nd or 8
+        w = dict(name="zero2_psi2p28_nd%d%s" % (n, "_qgather" if qgather else ""), psi=1 << 28, n_d=n, stage=2,
+                 pad=8, gdt="bf16", sigma=1e-3, tail=False, lr=1e-3, b2=0.999, wd=0.0, clip=0.0, ls=False,
+                 layers=1, qgather=qgather)
+    else:
+        raise SystemExit("unknown config %r" % cfg)
+    n_d = w["n_d"]
+    # algorithmic bytes per parameter of one step (minimum HBM traffic)
+    if w["clip"] > 0:
+        w["bytes_per_param"] = 2 * n_d + 34 if n_d > 4 else 4 * n_d + 26
+    elif w["stage"] == 3:
+        w["bytes_per_param"] = 2 * n_d + 30
+    elif w.get("qgather"):
+        w["bytes_per_param"] = 2 * n_d + 27 + 4.0 / 2048
+    else:
+        w["bytes_per_param"] = 2 * n_d + 26
+    w["psi_total"] = w["psi"] * w["layers"]
+    return w
+
+
+# ------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for k, n in enumerate(names):
+                if f[5 + k].lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- GPU arm
+def measured_hbm_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ncu DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum), per
+# kernel and workload, with a hash of the kernel sources they were taken on;
+# reported as null once the sources change.
+TRAFFIC = {}
+
+
+def kernel_source_hash():
+    h = hashlib.sha1()
+    for f in ("zk_stream.cu", "zk_common.cuh", "zk_aux.cu", "zk_capi.cu"):
+        with open(os.path.join(ROOT, "zero_optimizer_step_02_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+class Job:
+    """Device buffers of one replica's workload."""
+
+    def __init__(self, w, device, pool=2):
+        import torch
+        import zero_optimizer_step_02_gb300 as z
+        from zero_optimizer_step_02_gb300 import synth
+        self.z, self.torch, self.w = z, torch, w
+        gdt = z.ZERO_FP16 if w["gdt"] == "fp16" else z.ZERO_BF16
+        self.hp = z.hparams(lr=w["lr"], beta1=0.9, beta2=w["b2"], eps=1e-8, weight_decay=w["wd"],
+                            max_norm=w["clip"], loss_scaling=w["ls"])
+        self.plan = z.Plan(w["psi"], w["n_d"], stage=w["stage"], grad_dtype=gdt, shard_pad=w["pad"])
+        tdt = torch.float16 if gdt == z.ZERO_FP16 else torch.bfloat16
+        row = z.row_len(w["psi"])
+        scale = 1024.0 if w["ls"] else 1.0
+        # gradient sets: one per layer for ZeRO-3, else a small pool used in turn
+        nsets = w["layers"] if w["layers"] > 1 else pool
+        self.grads = []
+        for k in range(nsets):
+            g = torch.empty(w["n_d"], row, dtype=tdt, device=device)
+            for r in range(w["n_d"]):
+                synth.gaussian_(g[r, :w["psi"]], w["sigma"], 20261202 + k, r, heavy_tail=w["tail"], scale=scale)
+            self.grads.append(g)
+        L = w["layers"]
+        n = self.plan.padded
+        self.master = [synth.master_init(n, w["psi"], 7 + l, device=device) for l in range(L)]
+        self.m = [torch.zeros(n, device=device) for _ in range(L)]
+        self.v = [torch.zeros(n, device=device) for _ in range(L)]
+        self.pingpong = w["ls"]
+        if self.pingpong:
+            self.master2 = [torch.zeros(n, device=device) for _ in range(L)]
+            self.m2 = [torch.zeros(n, device=device) for _ in range(L)]
+            self.v2 = [torch.zeros(n, device=device) for _ in range(L)]
+        lp_n = n if w["stage"] == 3 else w["psi"]
+        self.lp = [torch.zeros(lp_n, dtype=torch.bfloat16, device=device) for _ in range(L)]
+        if w["stage"] == 3:
+            self.gathered = torch.zeros(w["psi"], dtype=torch.bfloat16, device=device)
+        if w.get("qgather"):
+            nbs = -(-self.plan.shard // 2048)
+            self.codes = torch.zeros(n, dtype=torch.int8, device=device)
+            self.scales = torch.zeros(w["n_d"] * nbs, device=device)
+        self.ws = torch.zeros(max(self.plan.workspace_bytes(self.hp), 256), dtype=torch.uint8, device=device)
+        self.scalars = torch.zeros(256, dtype=torch.uint8, device=device)
+        z.zero_scalars_init(self.scalars, scale)
+        self.k = 0
+
+    def ranks(self, l):
+        g = self.grads[l % len(self.grads)]
+        return [g[r] for r in range(self.w["n_d"])]
+
+    def step(self):
+        """One pass of the hot path through the public C ABI."""
+        z, w = self.z, self.w
+        h = self.plan.handle
+        for l in range(w["layers"]):
+            gsel = l if w["layers"] > 1 else self.k
+            if w["stage"] == 3:
+                S = self.plan.shard
+                # per-layer gather of the bf16 shards before use (itwiki: ZeRO-3)
+                z.zero_all_gather(h, [self.lp[l][r * S:(r + 1) * S] for r in range(w["n_d"])], self.gathered,
+                                  self.scalars)
+            if w.get("qgather"):
+                z.zero_step_fused_qgather(h, self.hp, self.ranks(gsel), self.master[l], self.m[l], self.v[l],
+                                          self.master[l], self.m[l], self.v[l], 2048, self.codes, self.scales,
+                                          self.lp[l], self.scalars, self.ws)
+            elif self.pingpong:
+                z.zero_step_fused(h, self.hp, self.ranks(gsel), self.master[l], self.m[l], self.v[l],
+                                  self.master2[l], self.m2[l], self.v2[l], self.lp[l], self.scalars, self.ws)
+                self.master[l], self.master2[l] = self.master2[l], self.master[l]
+                self.m[l], self.m2[l] = self.m2[l], self.m[l]
+                self.v[l], self.v2[l] = self.v2[l], self.v[l]
+            else:
+                z.zero_step_fused(h, self.hp, self.ranks(gsel), self.master[l], self.m[l], self.v[l],
+                                  self.master[l], self.m[l], self.v[l], self.lp[l], self.scalars, self.ws)
+        self.k += 1
+
+    def parts_step(self, ev):
+        """The clipped step through its parts, with an event between kernels:
+        reduce-scatter (+ squared-norm partials) | finalize | Adam (+ epilogue)."""
+        z = self.z
+        h = self.plan.handle
+        g = self.ghat
+        ev[0].record()
+        z.zero_reduce_scatter(h, self.ranks(self.k), self.hp, self.scalars, g, self.ws)
+        ev[1].record()
+        z.zero_grad_sqnorm(h, None, self.hp, self.scalars, self.ws)
+        ev[2].record()
+        z.zero_adam_shard_step(h, self.hp, g, self.master[0], self.m[0], self.v[0], self.lp[0], self.scalars)
+        ev[3].record()
+        self.k += 1
+
+
+def l2_flush(torch, device, buf=[]):
+    if not buf:
+        buf.append(torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device))
+    buf[0].fill_(1.0)
+
+
+def gpu_arm(args, rank, world, device):
+    import torch
+    import zero_optimizer_step_02_gb300 as z
+    w = workload(args.config, args.nd, args.qgather)
+    torch.cuda.set_device(device)
+    job = Job(w, device)
+    torch.cuda.synchronize()
+    small = w["psi_total"] * w["bytes_per_param"] < 4 * L2_BYTES   # flush L2 between timed steps
+    for _ in range(args.warmup):
+        job.step()
+    torch.cuda.synchronize()
+    dist_barrier(world)
+
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    n0 = z.zero_launch_count()
+    if small:
+        total_ms = 0.0
+        for _ in range(args.steps):
+            l2_flush(torch, device)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            job.step()
+            b.record()
+            torch.cuda.synchronize()
+            total_ms += a.elapsed_time(b)
+        launches = z.zero_launch_count() - n0
+    else:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record()
+        for _ in range(args.steps):
+            job.step()
+        b.record()
+        torch.cuda.synchronize()
+        total_ms = a.elapsed_time(b)
+        launches = z.zero_launch_count() - n0
+    clk = clocks.stop()
+    total_ms = dist_max(total_ms, world)
+    ms_per_step = total_ms / args.steps
+    value = world * w["psi_total"] * args.steps / (total_ms / 1e3)
+    step_gbs = w["psi_total"] * w["bytes_per_param"] / (ms_per_step / 1e3) / 1e9
+
+    # dominant kernel: per-kernel CUDA events on the launching stream
+    peak, peak_kind = measured_hbm_peak()
+    if w["clip"] > 0 and w["n_d"] > 4:
+        job.ghat = torch.zeros(job.plan.padded, device=device)
+        n_rep = max(3, args.steps)
+        dur = [0.0, 0.0, 0.0]
+        for _ in range(n_rep):
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            job.parts_step(ev)
+            torch.cuda.synchronize()
+            for i in range(3):
+                dur[i] += ev[i].elapsed_time(ev[i + 1]) / n_rep
+        names = ["reduce_scatter", "finalize", "adam_shard"]
+        per_param = [2 * w["n_d"] + 4, 0.0, 30.0]
+        k = max(range(3), key=lambda i: dur[i])
+        kernel, kms, kbytes = names[k], dur[k], per_param[k] * w["psi"]
+        breakdown = {names[i]: round(dur[i], 4) for i in range(3)}
+    else:
+        kernel = "fused_step" if not w.get("qgather") else "fused_step_qgather"
+        kms = ms_per_step / w["layers"] if w["stage"] != 3 else None
+        if w["stage"] == 3:
+            # time the per-layer fused step alone
+            evs = []
+            for _ in range(max(3, args.steps)):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                z.zero_step_fused(job.plan.handle, job.hp, job.ranks(0), job.master[0], job.m[0], job.v[0],
+                                  job.master[0], job.m[0], job.v[0], job.lp[0], job.scalars, job.ws)
+                b.record()
+                torch.cuda.synchronize()
+                evs.append(a.elapsed_time(b))
+            kms = statistics.mean(evs)
+            kbytes = (2 * w["n_d"] + 26) * w["psi"]
+        else:
+            kbytes = w["bytes_per_param"] * w["psi"]
+        breakdown = None
+    achieved = kbytes / (kms / 1e3) / 1e9
+    tr = TRAFFIC.get((kernel, w["name"]))
+    traffic = tr["bytes"] if tr and tr["src"] == kernel_source_hash() else None
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": kernel,
+                "kernel_ms": round(kms, 4), "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)"}
+
+    e2e = e2e_measure(job, w, args, device, world)
+    out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f32 (state), %s (grads), bf16 (params)" % w["gdt"],
+           "data": "synthetic", "impl": "gb300",
+           "config": {"workload": w["name"], "psi": w["psi"], "layers": w["layers"], "n_d": w["n_d"],
+                      "stage": w["stage"], "grad_dtype": w["gdt"], "clip": w["clip"], "loss_scaling": w["ls"],
+                      "bytes_per_param": w["bytes_per_param"], "parallelism": "replicas x%d" % world,
+                      "l2": "flushed between steps" if small else "inputs larger than L2"},
+           "step_gbs": round(step_gbs, 1), "step_frac_of_peak": round(step_gbs / peak, 4),
+           "roofline": roofline, "gpu_launches": int(launches), "e2e": e2e, "clocks": clk}
+    if breakdown:
+        out["kernel_ms"] = breakdown
+    return out
+
+
+def e2e_measure(job, w, args, device, world):
+    """Gradients from pinned host memory in, gathered parameters out, per step."""
+    import torch
+    if w["layers"] > 1 or w["psi"] * w["n_d"] * 2 > 40e9:
+        return None
+    z = job.z
+    host_g = torch.empty(job.grads[0].shape, dtype=job.grads[0].dtype, pin_memory=True)
+    host_g.copy_(job.grads[0])
+    host_out = torch.empty(job.lp[0].numel(), dtype=torch.bfloat16, pin_memory=True)
+    steps = max(1, min(args.steps, 5))
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        job.grads[0].copy_(host_g, non_blocking=True)
+        job.k = 0
+        job.step()
+        host_out.copy_(job.lp[0], non_blocking=True)
+    b.record()
+    torch.cuda.synchronize()
+    ms = dist_max(a.elapsed_time(b), world)
+    return {"value": world * w["psi"] * steps / (ms / 1e3), "unit": UNIT,
+            "h2d_bytes_per_step": host_g.numel() * host_g.element_size(),
+            "d2h_bytes_per_step": host_out.numel() * host_out.element_size(), "steps": steps}
+
+
+# ------------------------------------------------------------- CPU oracle arm
+def oracle_sample(w, budget_s, max_steps=None):
+    """Time the CPU oracle (as it stands, one thread) on a bounded sample of the
+    workload: the same n_d, dtype and hyper-parameters on fewer parameters."""
+    import numpy as np
+    import oracle
+    psi = min(w["psi"], 4_000_000)
+    n_d = w["n_d"]
+    rng = np.random.default_rng(1)
+    dt = oracle.FP16 if w["gdt"] == "fp16" else oracle.BF16
+    scale = 1024.0 if w["ls"] else 1.0
+    rows = [oracle.f32_to_lp((rng.standard_normal(psi) * w["sigma"] * scale).astype(np.float32), dt)
+            for _ in range(n_d)]
+    S = oracle.shard_size(psi, n_d, w["pad"])
+    st = oracle.State(np.zeros(n_d * S, np.float32), np.zeros(n_d * S, np.float32),
+                      np.zeros(n_d * S, np.float32), oracle.new_scalars(scale))
+    hp = oracle.hparams(lr=w["lr"], beta2=w["b2"], weight_decay=w["wd"], max_norm=w["clip"],
+                        loss_scaling=w["ls"])
+    lp = np.zeros(n_d * S, np.uint16)
+    gath = np.zeros(psi, np.uint16)
+    steps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.zero_step(rows, dt, hp, st, w["pad"], min(w["stage"], 3), lp_shards=lp, gathered=gath)
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or (max_steps and steps >= max_steps):
+            break
+    return psi, n_d, steps, el
+
+
+def reference_arm(args, rank, world):
+    w = workload(args.config, args.nd, args.qgather)
+    if rank != 0:
+        return None
+    for _ in range(args.warmup):
+        oracle_sample(w, 0.0, max_steps=1)
+    psi, n_d, steps, el = oracle_sample(w, 0.0, max_steps=args.steps)
+    value = psi * steps / el
+    sample = "%d of %d params, n_d=%d, %d steps, single-threaded C oracle" % (psi, w["psi"], n_d, steps)
+    return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * el / steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32 (state), %s (grads)" % w["gdt"], "data": "synthetic",
+            "impl": "reference", "config": {"workload": w["name"], "psi": w["psi"], "n_d": n_d},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# -------------------------------------------------------------- distributed
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("gloo", rank=rank, world_size=world)
+    return rank, world, local
+
+
+def dist_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def dist_max(x, world):
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--nd", type=int, default=None)
+    ap.add_argument("--qgather", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        out = reference_arm(args, rank, world)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+    import torch
+    device = torch.device("cuda", local)
+    out = gpu_arm(args, rank, world, device)
+    if rank == 0:
+        if not args.no_cpu_baseline and world == 1:
+            w = workload(args.config, args.nd, args.qgather)
+            psi, n_d, steps, el = oracle_sample(w, args.cpu_budget)
+            out["cpu_baseline"] = {"value": psi * steps / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                   "sample": "%d of %d params, n_d=%d, %d steps in %.1f s, single-threaded C "
+                                             "oracle" % (psi, w["psi"], n_d, steps, el)}
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

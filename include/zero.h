@@ -1,0 +1,277 @@
+/*
+ * zero.h -- C ABI of libzero.so, the GB300 (sm_103a) ZeRO-DP optimizer step.
+ *
+ * One GPU simulates n_d data-parallel ranks: each rank is a gradient buffer
+ * in HBM.  A step reduce-scatters the ranks' 16-bit gradients (rank-ordered
+ * fp32 sum divided by n_d times the loss scale), applies mixed-precision Adam
+ * to each shard's fp32 master weights, momentum and variance, and all-gathers
+ * the updated weights as 16-bit values.
+ *
+ * Sources (page title, section):
+ *   DP-notes  "Data parallelism and ZeRO optimization -- Hinglish notes" (6.1.8)
+ *   LLM-par   "大模型并行技术" (LLM parallelism techniques)
+ *   itwiki    "ZeRO (딥 러닝)"
+ *
+ * Conventions for every call below.
+ *   - Pointers named *_dev / device buffers are device pointers of the current
+ *     device; the caller allocates and owns all of them.  No call allocates
+ *     device memory and no call synchronises the stream.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Every kernel is launched on it; results are ready when it is.
+ *   - Device pointers must be 16-byte aligned (ZERO_ERR_MISALIGNED otherwise);
+ *     the workspace and the scalars block 256-byte aligned.
+ *   - Argument errors are returned synchronously and launch nothing.  A failed
+ *     launch returns ZERO_ERR_CUDA.  Errors found on the device (a bounded wait
+ *     that ran out) are OR-ed into zero_dev_scalars.status as ZERO_DEV_*.
+ *   - Index domain: Psi parameters, split into n_d contiguous shards of S
+ *     elements, S = roundup(ceil(Psi / n_d), shard_pad); shard r covers global
+ *     [r*S, min((r+1)*S, Psi)).  Arrays "of n_d*S" are indexed by the global
+ *     index j for j < Psi; their entries in [Psi, n_d*S) are padding that no
+ *     call changes (zero them once; they stay zero).  Rank gradient buffers
+ *     hold at least Psi elements; nothing past Psi is read.  A gathered buffer
+ *     is written only in [0, Psi).
+ *   - A plan is host memory only, immutable after creation, safe to share
+ *     between threads.  Calls that share a workspace or a scalars block must
+ *     be ordered on one stream.
+ */
+#ifndef ZERO_H
+#define ZERO_H
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define ZERO_API __attribute__((visibility("default")))
+#else
+#define ZERO_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ZERO_ABI_VERSION 1
+#define ZERO_MAX_RANKS 256      /* largest n_d */
+#define ZERO_MAX_SHARD_PAD 4096 /* largest shard_pad */
+
+typedef enum {
+    ZERO_OK = 0,
+    ZERO_ERR_INVALID_ARG = 1, /* a size, a dtype, a stage or a NULL pointer is wrong  */
+    ZERO_ERR_MISALIGNED = 2,  /* a device pointer breaks the alignment rule above     */
+    ZERO_ERR_UNSUPPORTED = 3, /* a valid request this build does not implement        */
+    ZERO_ERR_CUDA = 4,        /* the CUDA runtime reported an error at launch         */
+    ZERO_ERR_TIMEOUT = 5,     /* a bounded device wait ran out (see ZERO_DEV_TIMEOUT) */
+    ZERO_ERR_BOUNDS = 6       /* a request exceeds a fixed capacity of the library   */
+} zero_status;
+
+typedef enum { ZERO_BF16 = 0, ZERO_FP16 = 1 } zero_dtype;
+
+/* bits of zero_dev_scalars.status */
+#define ZERO_DEV_TIMEOUT 1 /* a bounded wait inside a kernel ran out; that kernel stopped early */
+
+typedef struct zero_plan zero_plan;
+
+/* Optional plan settings (zero_plan_create_ex).  Zero-initialised = defaults. */
+typedef struct {
+    int param_dtype_set;           /* 0: parameters are bf16; 1: use param_dtype              */
+    zero_dtype param_dtype;        /* dtype of the gathered / sharded 16-bit parameters       */
+    long long reduce_bucket_elems; /* itwiki DeepSpeed config "reduce_bucket_size": the fused
+                                      step runs in buckets of at most this many parameters;
+                                      <= 0 means one bucket.  Rounded up to 2048.            */
+} zero_plan_opts;
+
+/* Adam hyper-parameters, copied by value at each call.  Adam itself is not
+ * printed on the pages (DP-notes "Memory Consumption Analysis" sizes its fp32
+ * momentum, variance and master copy); the update is textbook Adam with bias
+ * correction and eps outside the square root, with decoupled weight decay
+ * (AdamW) when weight_decay > 0:
+ *     p <- p * (1 - lr*wd)              (only when wd != 0)
+ *     m <- b1*m + (1-b1)*g
+ *     v <- b2*v + (1-b2)*(g*g)
+ *     p <- p - (lr/(1-b1^t)) * (m / (sqrt(v)/sqrt(1-b2^t) + eps))
+ * each operation one IEEE fp32 rounding, in this order.                       */
+typedef struct {
+    float lr, beta1, beta2, eps, weight_decay;
+    float max_norm;   /* > 0: clip the averaged gradient to this global L2 norm
+                         (itwiki DeepSpeed config "gradient_clipping"); coef =
+                         max_norm/(norm+1e-6), applied when < 1                   */
+    int loss_scaling; /* 1: fp16 dynamic loss scaling: the divisor includes the
+                         loss scale; a step with a non-finite averaged gradient is
+                         skipped, the scale halves (floor min_scale); after
+                         scale_window good steps in a row it doubles              */
+    int scale_window; /* e.g. 1000 */
+    float min_scale;  /* e.g. 1 */
+} zero_hparams;
+
+/* Step scalars, resident in device memory (64 bytes, 256-byte aligned),
+ * written by zero_scalars_init and advanced by every step call.             */
+typedef struct {
+    long long t;          /* committed steps (skipped steps do not count)          */
+    double beta1_pow;     /* beta1^t as a running fp64 product                     */
+    double beta2_pow;     /* beta2^t                                               */
+    double sqnorm;        /* squared L2 norm of the averaged gradient (clipping)   */
+    float loss_scale;     /* current loss scale                                    */
+    float clip_coef;      /* coefficient applied in the latest step, 1 if none     */
+    int good_steps;       /* consecutive committed steps since the scale changed   */
+    int overflow;         /* 1 if the latest step was skipped                      */
+    int status;           /* sticky ZERO_DEV_* bits                                */
+    int nonfinite;        /* internal: the step in flight saw a non-finite value   */
+    int reserved[2];
+} zero_dev_scalars;
+
+/* ---------------------------------------------------------------- misc --- */
+ZERO_API const char* zero_status_str(zero_status s);
+ZERO_API int zero_abi_version(void);
+ZERO_API size_t zero_dev_scalars_size(void);
+
+/* ---------------------------------------------------------------- plan --- */
+/* Partition of Psi parameters over n_d ranks (DP-notes "ZeRO-1: Optimizer
+ * State Partitioning": theta = [theta_1 .. theta_N], rank r owns theta_r;
+ * itwiki "FSDP와의 관계": flatten, then shard).  stage 1, 2 or 3 (itwiki
+ * "ZeRO-DP의 세 단계"): stages 1-2 write the updated parameters into a
+ * gathered buffer of Psi, stage 3 into a sharded buffer of n_d*S; the math
+ * is the same.  1 <= n_d <= ZERO_MAX_RANKS, Psi >= 1,
+ * 1 <= shard_pad <= ZERO_MAX_SHARD_PAD.  *out receives a new plan.          */
+ZERO_API zero_status zero_plan_create(zero_plan** out, long long psi, int n_d, int stage,
+                                      zero_dtype grad_dtype, int shard_pad);
+ZERO_API zero_status zero_plan_create_ex(zero_plan** out, long long psi, int n_d, int stage,
+                                         zero_dtype grad_dtype, int shard_pad,
+                                         const zero_plan_opts* opts);
+ZERO_API void zero_plan_destroy(zero_plan* plan);
+
+/* shard_size = S, padded_psi = n_d*S; valid_len (host array of n_d, or NULL)
+ * receives each shard's valid length min(max(Psi - r*S, 0), S).             */
+ZERO_API zero_status zero_plan_query(const zero_plan* plan, long long* shard_size,
+                                     long long* padded_psi, long long* valid_len);
+
+/* Model-state bytes per rank at `stage` (0..3) with K optimizer bytes per
+ * parameter (itwiki memory table: 2 + 2 + K, K = 12; stage table: stage 1
+ * divides K*Psi by n_d, stage 2 also the gradients, stage 3 also the
+ * parameters).  bytes_out[4] = {params, grads, optimizer, total}.            */
+ZERO_API zero_status zero_plan_memory(const zero_plan* plan, int stage, double k,
+                                      double bytes_out[4]);
+
+/* Elements each rank sends per step at `stage` (itwiki "왜 통신량이 늘지
+ * 않는가": reduce-scatter Psi + all-gather Psi; stage 3 gathers twice).     */
+ZERO_API zero_status zero_plan_comm_volume(const zero_plan* plan, int stage, double* elems_out);
+
+/* Bytes of workspace the calls below need with these hyper-parameters (an
+ * upper bound valid on every device).  Only the step and reduce calls use it.*/
+ZERO_API size_t zero_workspace_bytes(const zero_plan* plan, const zero_hparams* hp);
+
+/* Write initial step scalars: t = 0, beta powers 1, loss_scale, counters 0.  */
+ZERO_API zero_status zero_scalars_init(zero_dev_scalars* scalars_dev, float loss_scale,
+                                       void* stream);
+
+/* ------------------------------------------------------ step, in parts --- */
+/* Reduce-scatter (DP-notes "ZeRO-2: Gradient Partitioning": rank r receives
+ * the averaged gradient of its partition; itwiki FSDP reduces in fp32):
+ *   grad_shards[j] = (sum over ranks q = 0..n_d-1, in order, from +0.0f, of
+ *                     float(rank_grads[q][j])) / D,   j < Psi
+ * with D = (float)n_d * (hp->loss_scaling ? loss_scale : 1).
+ * rank_grads: host array of n_d device pointers (plan grad dtype, >= Psi
+ * elements each).  grad_shards: n_d*S floats; its padding is set to +0.
+ * Also leaves per-block partial sums of grad_shards[j]^2 in `ws` for
+ * zero_grad_sqnorm, and, in loss-scaling mode, records a non-finite value in
+ * scalars->nonfinite for the following Adam call.                           */
+ZERO_API zero_status zero_reduce_scatter(const zero_plan* plan, const void* const* rank_grads,
+                                         const zero_hparams* hp, zero_dev_scalars* scalars_dev,
+                                         float* grad_shards, void* ws, void* stream);
+
+/* Global squared L2 norm of the averaged gradient, sum over j < Psi of
+ * grad_shards[j]^2, into scalars->sqnorm; with hp->max_norm > 0 also
+ * scalars->clip_coef = coef when coef < 1, else 1.  grad_shards == NULL:
+ * finish the partial sums the preceding zero_reduce_scatter left in ws
+ * (no second read of the gradient).  Deterministic for a given device.      */
+ZERO_API zero_status zero_grad_sqnorm(const zero_plan* plan, const float* grad_shards,
+                                      const zero_hparams* hp, zero_dev_scalars* scalars_dev,
+                                      void* ws, void* stream);
+
+/* Adam on every shard (DP-notes "ZeRO-1": rank r updates only theta_r with
+ * its local optimizer states), in place on master/m/v (n_d*S floats each),
+ * from grad_shards (n_d*S).  With hp->max_norm > 0 the gradient is first
+ * multiplied by scalars->clip_coef.  In loss-scaling mode a step flagged
+ * non-finite by the preceding reduce is skipped.  lp_out (NULL: none): the
+ * 16-bit cast of the updated master, at index j < Psi -- the gathered buffer
+ * for stages 1-2, the sharded buffer (n_d*S) for stage 3.  Commits the step
+ * scalars (t, beta powers, loss scale).                                      */
+ZERO_API zero_status zero_adam_shard_step(const zero_plan* plan, const zero_hparams* hp,
+                                          const float* grad_shards, float* master, float* m,
+                                          float* v, void* lp_out, zero_dev_scalars* scalars_dev,
+                                          void* stream);
+
+/* All-gather (DP-notes "ZeRO-1": updated partitions are gathered so every
+ * rank holds the full model; itwiki: ZeRO-3 gathers each layer before use):
+ * gathered[r*S + i] = shards_lp[r][i] for i < valid_len(r).  shards_lp: host
+ * array of n_d device pointers to S 16-bit values (plan parameter dtype),
+ * each needing only 2-byte alignment (shards cut from one flat n_d*S buffer
+ * at any S are accepted; the fast path wants 16-byte aligned shards).
+ * scalars_dev (may be NULL) receives ZERO_DEV_TIMEOUT if a wait runs out.   */
+ZERO_API zero_status zero_all_gather(const zero_plan* plan, const void* const* shards_lp,
+                                     void* gathered, zero_dev_scalars* scalars_dev, void* stream);
+
+/* --------------------------------------------------------- fused step --- */
+/* The whole step in as few passes as the global checks allow: reduce-scatter,
+ * Adam and the 16-bit cast written straight to lp_out (gathered buffer for
+ * stages 1-2, sharded buffer for stage 3), the reduced gradient kept in
+ * registers.  State is read from *_in and written to *_out (each n_d*S); an
+ * *_out may equal its *_in.  Passes:
+ *   no clipping, no loss scaling : 1 pass
+ *   loss scaling, out != in      : 1 pass, speculative; on overflow the out
+ *                                  state is restored from in and lp_out is
+ *                                  re-cast from master_in
+ *   loss scaling, out == in      : a read-only check pass, then the update
+ *   clipping                     : a reduce pass (writes the fp32 reduced
+ *                                  gradient to ws when n_d > 4, else only the
+ *                                  norm), then the update
+ * In every case, after the call lp_out[j] (j < Psi) is the 16-bit cast of
+ * master_out[j] if the call wrote it, and scalars are advanced.  Runs in
+ * buckets of the plan's reduce_bucket_elems when no global check is needed.  */
+ZERO_API zero_status zero_step_fused(const zero_plan* plan, const zero_hparams* hp,
+                                     const void* const* rank_grads, const float* master_in,
+                                     const float* m_in, const float* v_in, float* master_out,
+                                     float* m_out, float* v_out, void* lp_out,
+                                     zero_dev_scalars* scalars_dev, void* ws, void* stream);
+
+/* ----------------------------------------------------- quantized gather --- */
+/* ZeRO++ qwZ (itwiki "후속 기법", ZeRO++ row: weights are block-quantized for
+ * the all-gather).  Per block of `block` consecutive elements of a shard
+ * (blocks start at each shard's first element; a shard's last block may be
+ * short): amax = max |x|, s = amax/127, code = clamp(rint(x/s), -127, 127)
+ * (0 when s = 0), dequantized = bf16(code * s).  shards_bf16: n_d*S bf16
+ * (flat).  codes_out: n_d*S int8, written for j < Psi.  scales_out:
+ * n_d*ceil(S/block) floats, shard-major, 0 for blocks past a shard's valid
+ * length.  gathered_bf16: Psi bf16 dequantized values (the owner's shard
+ * too).  32 <= block <= 65536, block a multiple of 32.                       */
+ZERO_API zero_status zero_quant_gather(const zero_plan* plan, const void* shards_bf16, int block,
+                                       signed char* codes_out, float* scales_out,
+                                       void* gathered_bf16, void* stream);
+
+/* The fused step of zero_step_fused (no clipping, no loss scaling) whose
+ * epilogue is the quantized gather above instead of the plain 16-bit write:
+ * codes, scales and dequantized bf16 gathered values come from the updated
+ * master of each block (block must be 2048; parameter dtype bf16).           */
+ZERO_API zero_status zero_step_fused_qgather(const zero_plan* plan, const zero_hparams* hp,
+                                             const void* const* rank_grads,
+                                             const float* master_in, const float* m_in,
+                                             const float* v_in, float* master_out, float* m_out,
+                                             float* v_out, int block, signed char* codes_out,
+                                             float* scales_out, void* gathered_bf16,
+                                             zero_dev_scalars* scalars_dev, void* ws,
+                                             void* stream);
+
+/* ----------------------------------------------------------- diagnostics --- */
+/* Launch one kernel that waits on a barrier nothing completes, with a wait
+ * limit of timeout_ns (at most 10 s).  When the limit runs out the kernel sets
+ * ZERO_DEV_TIMEOUT in scalars->status and returns, leaving the context usable.
+ * Exists so that the bounded-wait path can be tested.                       */
+ZERO_API zero_status zero_debug_wait_timeout(zero_dev_scalars* scalars_dev, long long timeout_ns,
+                                             void* stream);
+
+/* Number of kernels this library has launched in this process so far (all
+ * threads, all devices).  Lets a caller count the launches of a region.     */
+ZERO_API unsigned long long zero_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ZERO_H */

@@ -11,6 +11,10 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a) and the built libzero.so")
+    # the suite imports the library: make sure it and the oracle are built
+    # (incremental: a no-op when they are current)
+    import __graft_entry__
+    __graft_entry__.build()
 
 
 def pytest_collection_modifyitems(config, items):

@@ -1,0 +1,104 @@
+"""Helpers of the GPU parity tests: seeded inputs made once on the CPU, the
+same bytes given to the CUDA path (through the C ABI) and to the oracle."""
+import numpy as np
+import torch
+
+import oracle
+import zero_optimizer_step_02_gb300 as z
+from zero_optimizer_step_02_gb300 import synth
+
+TORCH_DT = {z.ZERO_BF16: torch.bfloat16, z.ZERO_FP16: torch.float16}
+ORACLE_DT = {z.ZERO_BF16: oracle.BF16, z.ZERO_FP16: oracle.FP16}
+
+
+def u16(t):
+    """A 16-bit torch tensor (any device) as numpy uint16 bit patterns."""
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def u32(a):
+    return np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
+
+
+def oracle_hp(hp):
+    return oracle.hparams(lr=hp.lr, beta1=hp.beta1, beta2=hp.beta2, eps=hp.eps, weight_decay=hp.weight_decay,
+                          max_norm=hp.max_norm, loss_scaling=bool(hp.loss_scaling), scale_window=hp.scale_window,
+                          min_scale=hp.min_scale)
+
+
+class Job:
+    """One simulated job on both sides: GPU buffers and the oracle's state."""
+
+    def __init__(self, psi, n_d, stage=2, pad=8, gdt=z.ZERO_BF16, pdt=None, hp=None, seed=1, pingpong=False,
+                 loss_scale=1.0, bucket=0, row_extra=0):
+        self.hp = hp if hp is not None else z.hparams()
+        self.plan = z.Plan(psi, n_d, stage=stage, grad_dtype=gdt, shard_pad=pad, param_dtype=pdt,
+                           reduce_bucket_elems=bucket)
+        self.psi, self.n_d, self.stage, self.pad, self.gdt = psi, n_d, stage, pad, gdt
+        self.pdt = self.plan.param_dtype
+        self.seed = seed
+        self.buf = z.StepBuffers(self.plan, self.hp, device="cuda", pingpong=pingpong, row_extra=row_extra)
+        master = synth.master_init(self.plan.padded, psi, seed)
+        self.buf.master.copy_(master.cuda())
+        self.buf.init_scalars(loss_scale)
+        sc = oracle.new_scalars(loss_scale)
+        self.ost = oracle.State(master.numpy().copy(), np.zeros(self.plan.padded, np.float32),
+                                np.zeros(self.plan.padded, np.float32), sc)
+        self.o_lp_shards = np.zeros(self.plan.padded, np.uint16)
+        self.o_gathered = np.zeros(psi, np.uint16)
+
+    def new_grads(self, step, sigma=1e-3, heavy_tail=False, scale=1.0, inf_at=None):
+        g = synth.rank_grads(self.n_d, self.psi, sigma, self.seed, step, dtype=TORCH_DT[self.gdt],
+                             heavy_tail=heavy_tail, scale=scale, row_pad=self.buf.grads.shape[1] - self.psi)
+        if inf_at is not None:
+            r, j = inf_at
+            g[r, j] = float("inf")
+        self.buf.grads.copy_(g.cuda())
+        self.rows = [u16(g[r, :self.psi]) for r in range(self.n_d)]
+        return g
+
+    def gpu_step(self):
+        self.buf.step(self.hp)
+
+    def oracle_step(self):
+        return oracle.zero_step(self.rows, ORACLE_DT[self.gdt], oracle_hp(self.hp), self.ost, self.pad,
+                                self.stage, param_dtype=ORACLE_DT[self.pdt], lp_shards=self.o_lp_shards,
+                                gathered=self.o_gathered)
+
+    def gpu_state(self):
+        torch.cuda.synchronize()
+        b = self.buf
+        lp = u16(b.lp)[: (self.plan.padded if self.stage == 3 else self.psi)]
+        return b.master.cpu().numpy(), b.m.cpu().numpy(), b.v.cpu().numpy(), lp
+
+    def oracle_lp(self):
+        return self.o_lp_shards if self.stage == 3 else self.o_gathered
+
+    def assert_bit_exact(self):
+        gm, gmm, gv, glp = self.gpu_state()
+        for name, a, b in (("master", gm, self.ost.master), ("m", gmm, self.ost.m), ("v", gv, self.ost.v)):
+            bad = np.flatnonzero(u32(a) != u32(b))
+            assert bad.size == 0, "%s differs at %d places, first %s: gpu %r oracle %r" % (
+                name, bad.size, bad[:5], a[bad[:5]], b[bad[:5]])
+        olp = self.oracle_lp()
+        bad = np.flatnonzero(glp != olp[: glp.size])
+        assert bad.size == 0, "16-bit params differ at %d places, first %s" % (bad.size, bad[:5])
+
+    def assert_within_tolerance(self, rel=1e-6, lp_ulp=1):
+        """The stated tolerance: per array max|gpu - cpu| / max|cpu| <= rel,
+        16-bit parameters within lp_ulp units in the last place."""
+        gm, gmm, gv, glp = self.gpu_state()
+        for name, a, b in (("master", gm, self.ost.master), ("m", gmm, self.ost.m), ("v", gv, self.ost.v)):
+            denom = max(float(np.max(np.abs(b))), 1e-30)
+            err = float(np.max(np.abs(a.astype(np.float64) - b.astype(np.float64)))) / denom
+            assert err <= rel, "%s relative error %.3g > %.1g" % (name, err, rel)
+        olp = self.oracle_lp()[: glp.size]
+        # 16-bit patterns of same-sign values are ordered like the values
+        d = np.abs(glp.astype(np.int64) - olp.astype(np.int64))
+        same_sign = (glp >> 15) == (olp >> 15)
+        assert np.all(d[same_sign] <= lp_ulp) and np.all(
+            (glp[~same_sign] & 0x7FFF) + (olp[~same_sign] & 0x7FFF) <= lp_ulp)
+
+    def scalars(self):
+        torch.cuda.synchronize()
+        return self.buf.scalars_host()

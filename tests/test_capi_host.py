@@ -1,0 +1,149 @@
+"""C-ABI tests that need no GPU: the library builds and loads, exports every
+function include/zero.h declares, and its host logic (plans, accounting,
+argument checks) behaves.  No call here reaches a kernel launch: every call
+that takes device pointers is made to fail its argument checks first."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def z():
+    import __graft_entry__
+    __graft_entry__.build()
+    import zero_optimizer_step_02_gb300 as z
+    return z
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "zero.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"ZERO_API\s+[\w\s\*]+?\b(zero_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(z):
+    names = _declared()
+    assert len(names) >= 18
+    lib = z._capi.library()
+    for n in names:
+        assert hasattr(lib, n), n
+    # and the binding offers each under the same name
+    for n in names:
+        assert hasattr(z._capi, n), n
+
+
+def test_abi_and_struct_layout(z):
+    assert z.zero_abi_version() == 1
+    assert z.zero_dev_scalars_size() == ctypes.sizeof(z.ZeroDevScalars) == 64
+    assert z.zero_status_str(0) == "ok"
+    assert "misaligned" in z.zero_status_str(2)
+
+
+@pytest.mark.parametrize("psi,n_d,pad", [(1, 1, 1), (1_000_003, 4, 8), (1_000_003, 4, 1), (7, 8, 8),
+                                         (124_439_808, 8, 8), (268_435_456, 64, 8), (218_112_000, 16, 8),
+                                         (5, 3, 4096)])
+def test_plan_layout_matches_the_oracle(z, psi, n_d, pad):
+    p = z.Plan(psi, n_d, stage=2, shard_pad=pad)
+    S = oracle.shard_size(psi, n_d, pad)
+    assert p.shard == S and p.padded == n_d * S
+    assert p.valid_len == [oracle.valid_len(psi, S, r) for r in range(n_d)]
+
+
+@pytest.mark.parametrize("stage", [0, 1, 2, 3])
+@pytest.mark.parametrize("psi,n_d", [(7.5e9, 64), (1.3e9, 8), (1.5e9, 1), (124_439_808, 8)])
+def test_plan_accounting_matches_the_oracle(z, stage, psi, n_d):
+    p = z.Plan(int(psi), n_d, stage=2)
+    got = p.memory(stage)
+    want = oracle.model_state_bytes(int(psi), n_d, stage)
+    assert got == pytest.approx(want, rel=1e-15)
+    assert p.comm_volume(stage) == oracle.comm_volume(stage) * int(psi)
+
+
+def test_stage_table_from_the_library(z):
+    # "ZeRO (딥 러닝)", ZeRO-DP의 세 단계: 120 / 31.4 / 16.6 / 1.9 GB at 7.5B, 64 GPUs
+    p = z.Plan(7_500_000_000, 64, stage=2)
+    assert [round(p.memory(s)[3] / 1e9, 1) for s in range(4)] == [120.0, 31.4, 16.6, 1.9]
+
+
+def test_workspace_size(z):
+    hp = z.hparams()
+    p = z.Plan(1000, 8, stage=2)
+    base = p.workspace_bytes(hp)
+    assert base >= 8 * 4096 and base % 256 == 0
+    assert p.workspace_bytes(z.hparams(max_norm=1.0)) == base + 4 * p.padded   # n_d > 4: reduced grad in ws
+    p4 = z.Plan(1000, 4, stage=2)
+    assert p4.workspace_bytes(z.hparams(max_norm=1.0)) == base                  # n_d <= 4: re-read instead
+
+
+@pytest.mark.parametrize("args", [(0, 4, 2, 0, 8), (10, 0, 2, 0, 8), (10, 257, 2, 0, 8), (10, 4, 0, 0, 8),
+                                  (10, 4, 4, 0, 8), (10, 4, 2, 2, 8), (10, 4, 2, 0, 0), (10, 4, 2, 0, 4097)])
+def test_plan_rejects_bad_arguments(z, args):
+    with pytest.raises(z.ZeroError) as e:
+        z.zero_plan_create(*args)
+    assert e.value.status == 1
+
+
+def test_bucket_rounding_and_param_dtype(z):
+    p = z.Plan(10_000_000, 8, stage=2, param_dtype=z.ZERO_FP16, reduce_bucket_elems=1000)
+    assert p.param_dtype == z.ZERO_FP16
+    with pytest.raises(z.ZeroError):
+        z.zero_plan_create_ex(100, 2, 2, 0, 8, param_dtype=7)
+
+
+def _raw(z, name, *args):
+    return z._capi.raw_status(name, *args)
+
+
+def test_calls_check_arguments_before_touching_the_device(z):
+    hp = z.hparams()
+    p = z.Plan(1000, 2, stage=2)
+    h = p.handle
+    A = 0x10000          # 16- and 256-byte aligned fake addresses: never dereferenced,
+    B = 0x20000          # every call below fails its checks first
+    ranks_ok = (ctypes.c_void_p * 2)(A, B)
+    ranks_bad = (ctypes.c_void_p * 2)(A, B + 2)
+    ranks_null = (ctypes.c_void_p * 2)(A, None)
+    hpp = ctypes.byref(hp)
+    # NULL plan / hparams
+    assert _raw(z, "zero_step_fused", None, hpp, ranks_ok, A, A, A, A, A, A, A, A, A, None) == 1
+    assert _raw(z, "zero_step_fused", h, None, ranks_ok, A, A, A, A, A, A, A, A, A, None) == 1
+    # misaligned rank pointer, NULL rank pointer
+    assert _raw(z, "zero_step_fused", h, hpp, ranks_bad, A, A, A, A, A, A, A, A, A, None) == 2
+    assert _raw(z, "zero_step_fused", h, hpp, ranks_null, A, A, A, A, A, A, A, A, A, None) == 1
+    # misaligned state, partly aliased state
+    assert _raw(z, "zero_step_fused", h, hpp, ranks_ok, A + 4, A, A, A, A, A, A, A, A, None) == 2
+    assert _raw(z, "zero_step_fused", h, hpp, ranks_ok, A, A, A, A, B, B, A, A, A, None) == 1
+    # scalars not 256-aligned
+    assert _raw(z, "zero_step_fused", h, hpp, ranks_ok, A, A, A, A, A, A, A, A + 16, A, None) == 2
+    # bad hyper-parameters
+    bad = z.hparams(beta1=1.0)
+    assert _raw(z, "zero_step_fused", h, ctypes.byref(bad), ranks_ok, A, A, A, A, A, A, A, A, A, None) == 1
+    nan = z.hparams(lr=float("nan"))
+    assert _raw(z, "zero_adam_shard_step", h, ctypes.byref(nan), A, A, A, A, A, A, None) == 1
+    ls = z.hparams(loss_scaling=True, scale_window=0)
+    assert _raw(z, "zero_reduce_scatter", h, ranks_ok, ctypes.byref(ls), A, A, A, None) == 1
+    # workspace required with clipping
+    clip = z.hparams(max_norm=1.0)
+    assert _raw(z, "zero_step_fused", h, ctypes.byref(clip), ranks_ok, A, A, A, A, A, A, A, A, None, None) == 1
+    # quantized gather: block limits, fused variant only with block 2048 and no clipping
+    assert _raw(z, "zero_quant_gather", h, A, 31, A, A, A, None) == 1
+    assert _raw(z, "zero_quant_gather", h, A, 70000, A, A, A, None) == 1
+    assert _raw(z, "zero_step_fused_qgather", h, hpp, ranks_ok, A, A, A, A, A, A, 1024, A, A, A, A, A, None) == 3
+    assert _raw(z, "zero_step_fused_qgather", h, ctypes.byref(clip), ranks_ok, A, A, A, A, A, A, 2048, A, A, A,
+                A, A, None) == 3
+    # the timeout probe rejects limits outside (0, 10 s]
+    assert _raw(z, "zero_debug_wait_timeout", A, 0, None) == 1
+    assert _raw(z, "zero_debug_wait_timeout", A, 20_000_000_000, None) == 1
+    # fp16 parameters cannot take the bf16 quantizer
+    p16 = z.Plan(1000, 2, stage=2, param_dtype=z.ZERO_FP16)
+    assert _raw(z, "zero_quant_gather", p16.handle, A, 2048, A, A, A, None) == 3
+
+
+def test_library_is_built_in_tree(z):
+    assert os.path.dirname(z._capi.LIB_PATH) == os.path.join(ROOT, "zero_optimizer_step_02_gb300")

@@ -1,0 +1,483 @@
+// zk_aux.cu -- the smaller kernels of the ZeRO-DP step.
+//
+//   k_all_gather     shard r's valid elements -> gathered[r*S ...] through a
+//                    ring of shared-memory stages filled and drained by 1-D
+//                    bulk copies (DP-notes "ZeRO-1": gather the updated
+//                    partitions; itwiki: ZeRO-3 gathers each layer before use)
+//   k_quant_gather   block-int8 quantize + dequantize (itwiki "후속 기법",
+//                    ZeRO++ qwZ), one warp per block
+//   k_sqnorm_f32     per-CTA partial sums of g^2 of an fp32 array
+//   k_finalize       fixed-order fp64 sum of the partials, clip coefficient
+//   k_epilogue       commits the step scalars (t, beta powers, loss scale)
+//   k_repair         restores a speculative step that turned out to overflow
+//   k_scalars_init, k_debug_wait
+#include "zk_common.cuh"
+#include "zk_launch.h"
+
+namespace zk {
+
+namespace {
+
+unsigned long long g_launches = 0;
+
+int sm_count()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+}  // namespace
+
+void count_launch() { __atomic_add_fetch(&g_launches, 1ull, __ATOMIC_RELAXED); }
+unsigned long long launch_count() { return __atomic_load_n(&g_launches, __ATOMIC_RELAXED); }
+
+// ------------------------------------------------------------------ scalars
+__global__ void k_scalars_init(zero_dev_scalars* sc, float loss_scale)
+{
+    zero_dev_scalars s = {};
+    s.t = 0;
+    s.beta1_pow = 1.0;
+    s.beta2_pow = 1.0;
+    s.sqnorm = 0.0;
+    s.loss_scale = loss_scale;
+    s.clip_coef = 1.0f;
+    *sc = s;
+}
+
+cudaError_t launch_scalars_init(zero_dev_scalars* sc, float loss_scale, cudaStream_t st)
+{
+    count_launch();
+    k_scalars_init<<<1, 1, 0, st>>>(sc, loss_scale);
+    return cudaGetLastError();
+}
+
+// Commit (or skip) the step: the loss-scaling reading -- a step whose reduced
+// gradient held a non-finite value leaves the state alone, halves the scale
+// (floor min_scale) and resets the good-step count; otherwise t advances, the
+// beta powers take one more factor, and after scale_window good steps the
+// scale doubles.
+__global__ void k_epilogue(zero_hparams hp, zero_dev_scalars* sc)
+{
+    const bool skip = hp.loss_scaling && sc->nonfinite != 0;
+    if (skip) {
+        const float half = __fmul_rn(sc->loss_scale, 0.5f);
+        sc->loss_scale = half > hp.min_scale ? half : hp.min_scale;
+        sc->good_steps = 0;
+        sc->overflow = 1;
+        sc->clip_coef = 1.0f;
+    } else {
+        sc->t += 1;
+        sc->beta1_pow = __dmul_rn(sc->beta1_pow, static_cast<double>(hp.beta1));
+        sc->beta2_pow = __dmul_rn(sc->beta2_pow, static_cast<double>(hp.beta2));
+        sc->overflow = 0;
+        if (hp.loss_scaling) {
+            sc->good_steps += 1;
+            if (sc->good_steps >= hp.scale_window) {
+                sc->loss_scale = __fmul_rn(sc->loss_scale, 2.0f);
+                sc->good_steps = 0;
+            }
+        }
+    }
+    if (!(hp.max_norm > 0.0f)) {
+        sc->sqnorm = 0.0;
+        sc->clip_coef = 1.0f;
+    }
+    sc->nonfinite = 0;
+}
+
+cudaError_t launch_epilogue(const zero_hparams& hp, zero_dev_scalars* sc, cudaStream_t st)
+{
+    count_launch();
+    k_epilogue<<<1, 1, 0, st>>>(hp, sc);
+    return cudaGetLastError();
+}
+
+// --------------------------------------------------------------- squared norm
+// Fixed-order fp64 sum of the per-CTA partials by one warp (lane l takes
+// partials l, l+32, ... in order; then a butterfly that gives every lane the
+// same bits), then norm and coefficient: coef = max_norm / (norm + 1e-6),
+// applied when below one.
+__global__ void k_finalize(const double* partials, int n, zero_hparams hp, zero_dev_scalars* sc)
+{
+    double x = 0.0;
+    for (int i = threadIdx.x; i < n; i += 32) x = __dadd_rn(x, partials[i]);
+    x = warp_sum_f64(x);
+    if (threadIdx.x == 0) {
+        sc->sqnorm = x;
+        float coef = 1.0f;
+        if (hp.max_norm > 0.0f) {
+            const double norm = __dsqrt_rn(x);
+            const float c = __double2float_rn(__ddiv_rn(static_cast<double>(hp.max_norm), __dadd_rn(norm, 1e-6)));
+            if (c < 1.0f) coef = c;
+        }
+        sc->clip_coef = coef;
+    }
+}
+
+cudaError_t launch_finalize_sqnorm(const double* partials, int n, const zero_hparams& hp,
+                                   zero_dev_scalars* sc, cudaStream_t st)
+{
+    count_launch();
+    k_finalize<<<1, 32, 0, st>>>(partials, n, hp, sc);
+    return cudaGetLastError();
+}
+
+__global__ void __launch_bounds__(256) k_sqnorm_f32(const float* __restrict__ g, long long n, double* partials)
+{
+    float hi = 0.0f, lo = 0.0f;
+    const long long n4 = n / 4;
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) {
+        const float4 f = reinterpret_cast<const float4*>(g)[i];
+        sq_accumulate(f.x, hi, lo);
+        sq_accumulate(f.y, hi, lo);
+        sq_accumulate(f.z, hi, lo);
+        sq_accumulate(f.w, hi, lo);
+    }
+    if (blockIdx.x == 0 && threadIdx.x < n - n4 * 4) sq_accumulate(g[n4 * 4 + threadIdx.x], hi, lo);
+    __shared__ double red[8];
+    double part = warp_sum_f64(__dadd_rn(static_cast<double>(hi), static_cast<double>(lo)));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = part;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double tot = 0.0;
+        for (int w = 0; w < 8; ++w) tot = __dadd_rn(tot, red[w]);
+        partials[blockIdx.x] = tot;
+    }
+}
+
+cudaError_t launch_sqnorm_f32(const float* g, long long n, double* partials, int* n_partials, cudaStream_t st)
+{
+    const int sms = sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    long long blocks = (n / 4 + 255) / 256;
+    if (blocks > 4LL * sms) blocks = 4LL * sms;
+    if (blocks > kMaxPartials) blocks = kMaxPartials;
+    if (blocks < 1) blocks = 1;
+    *n_partials = static_cast<int>(blocks);
+    count_launch();
+    k_sqnorm_f32<<<static_cast<unsigned>(blocks), 256, 0, st>>>(g, n, partials);
+    return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------- repair
+// Speculative loss-scaled step that met a non-finite gradient: the out state
+// gets the in state back and the 16-bit parameters are re-cast from it.
+template <int PT>
+__global__ void k_repair(const float* __restrict__ mi, const float* __restrict__ m_in,
+                         const float* __restrict__ v_in, float* mo, float* m_out, float* v_out,
+                         uint16_t* lp, long long psi, const zero_dev_scalars* sc)
+{
+    if (sc->nonfinite == 0) return;
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    for (long long j = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; j < psi; j += stride) {
+        const float p = mi[j];
+        if (mo != mi) {
+            mo[j] = p;
+            m_out[j] = m_in[j];
+            v_out[j] = v_in[j];
+        }
+        if (lp != nullptr) lp[j] = Lp<PT>::narrow(p);
+    }
+}
+
+cudaError_t launch_repair(const zero_hparams& hp, const float* master_in, const float* m_in,
+                          const float* v_in, float* master_out, float* m_out, float* v_out,
+                          void* lp_out, int param_dtype, long long psi, zero_dev_scalars* sc,
+                          cudaStream_t st)
+{
+    (void)hp;
+    const int sms = sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    long long blocks = (psi + 255) / 256;
+    if (blocks > 8LL * sms) blocks = 8LL * sms;
+    if (blocks < 1) blocks = 1;
+    uint16_t* lp = static_cast<uint16_t*>(lp_out);
+    count_launch();
+    if (param_dtype == ZERO_BF16)
+        k_repair<ZERO_BF16><<<static_cast<unsigned>(blocks), 256, 0, st>>>(master_in, m_in, v_in, master_out, m_out, v_out, lp, psi, sc);
+    else
+        k_repair<ZERO_FP16><<<static_cast<unsigned>(blocks), 256, 0, st>>>(master_in, m_in, v_in, master_out, m_out, v_out, lp, psi, sc);
+    return cudaGetLastError();
+}
+
+// --------------------------------------------------------------- all-gather
+constexpr int kAgTile = 8192;    // 16-bit elements per bulk copy (16 KB)
+constexpr int kAgStages = 8;
+constexpr int kAgThreads = 256;
+
+struct AgArgs {
+    const void* shard[ZERO_MAX_RANKS];
+    void* gathered;
+    long long shard_len;          // S
+    long long psi;
+    long long tiles_per_shard;    // ceil(S / kAgTile)
+    int n_d;
+    int tma_ok;                   // S % 8 == 0 (every tile 16-byte aligned at both ends)
+    unsigned long long timeout_ns;
+    zero_dev_scalars* sc;
+};
+
+__device__ __forceinline__ void ag_span(const AgArgs& a, long long tile, int& r, long long& i0, int& len)
+{
+    r = static_cast<int>(tile / a.tiles_per_shard);
+    i0 = (tile - static_cast<long long>(r) * a.tiles_per_shard) * kAgTile;
+    long long valid = a.psi - static_cast<long long>(r) * a.shard_len;
+    valid = valid < 0 ? 0 : (valid > a.shard_len ? a.shard_len : valid);
+    const long long l = valid - i0;
+    len = l <= 0 ? 0 : (l > kAgTile ? kAgTile : static_cast<int>(l));
+}
+
+__global__ void __launch_bounds__(kAgThreads) k_all_gather(const __grid_constant__ AgArgs a)
+{
+    extern __shared__ __align__(1024) unsigned char smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    int* issued = reinterpret_cast<int*>(smem + 8 * kAgStages);
+    unsigned char* ring = smem + 1024;
+    const long long ntiles = a.tiles_per_shard * a.n_d;
+    uint16_t* out = static_cast<uint16_t*>(a.gathered);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kAgStages; ++s) {
+            mbar_init(&full[s], 1);
+            issued[s] = -1;
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (threadIdx.x < 32) {
+        if (threadIdx.x == 0 && a.tma_ok) {
+            // one thread drives the ring: bulk load tile -> stage, bulk store stage -> gathered
+            const uint64_t pol = l2_policy_evict_first();
+            auto next_full = [&](long long t) {
+                for (; t < ntiles; t += gridDim.x) {
+                    int r;
+                    long long i0;
+                    int len;
+                    ag_span(a, t, r, i0, len);
+                    if (len == kAgTile) return t;
+                }
+                return ntiles;
+            };
+            auto issue_load = [&](long long t, int s, uint32_t ph) {
+                int r;
+                long long i0;
+                int len;
+                ag_span(a, t, r, i0, len);
+                mbar_arrive_expect_tx(&full[s], kAgTile * 2);
+                bulk_load(ring + s * (kAgTile * 2), static_cast<const uint16_t*>(a.shard[r]) + i0, kAgTile * 2,
+                          &full[s], pol);
+                issued[s] = static_cast<int>(ph);
+            };
+            long long load_t = next_full(blockIdx.x);
+            long long k_load = 0;
+            for (int s = 0; s < kAgStages && load_t < ntiles; ++s) {
+                issue_load(load_t, s, 0u);
+                ++k_load;
+                load_t = next_full(load_t + gridDim.x);
+            }
+            long long k = 0;
+            bool ok = true;
+            for (long long t = next_full(blockIdx.x); t < ntiles; t = next_full(t + gridDim.x), ++k) {
+                const int s = static_cast<int>(k % kAgStages);
+                const uint32_t ph = static_cast<uint32_t>((k / kAgStages) & 1);
+                if (!mbar_wait_bounded(&full[s], ph, nullptr, a.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                int r;
+                long long i0;
+                int len;
+                ag_span(a, t, r, i0, len);
+                bulk_store(out + static_cast<long long>(r) * a.shard_len + i0, ring + s * (kAgTile * 2), kAgTile * 2);
+                bulk_commit();
+                if (k >= 1 && load_t < ntiles) {
+                    // the store of tile k-1 has finished reading its stage: refill it
+                    bulk_wait_read<1>();
+                    const long long kk = k - 1 + kAgStages;
+                    issue_load(load_t, static_cast<int>((k - 1) % kAgStages), static_cast<uint32_t>((kk / kAgStages) & 1));
+                    ++k_load;
+                    load_t = next_full(load_t + gridDim.x);
+                }
+            }
+            bulk_wait_all<0>();
+            if (!ok) {
+                for (int s = 0; s < kAgStages; ++s)
+                    if (issued[s] >= 0) mbar_wait_bounded(&full[s], static_cast<uint32_t>(issued[s]), nullptr, a.timeout_ns);
+                if (a.sc != nullptr) atomicOr(&a.sc->status, ZERO_DEV_TIMEOUT);
+            }
+        }
+        __syncwarp();
+    } else {
+        // warps 1..7: tiles the ring does not take (short, or unaligned shards)
+        const int t0 = threadIdx.x - 32;
+        const int nt = kAgThreads - 32;
+        for (long long t = blockIdx.x; t < ntiles; t += gridDim.x) {
+            int r;
+            long long i0;
+            int len;
+            ag_span(a, t, r, i0, len);
+            if (len <= 0 || (len == kAgTile && a.tma_ok)) continue;
+            const uint16_t* src = static_cast<const uint16_t*>(a.shard[r]) + i0;
+            uint16_t* dst = out + static_cast<long long>(r) * a.shard_len + i0;
+            for (int i = t0; i < len; i += nt) dst[i] = src[i];
+        }
+    }
+    __syncthreads();
+}
+
+cudaError_t launch_all_gather(const void* const* shards, int n_d, long long shard, long long psi,
+                              void* gathered, zero_dev_scalars* sc, cudaStream_t st)
+{
+    const int sms = sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    AgArgs a = {};
+    for (int r = 0; r < n_d; ++r) a.shard[r] = shards[r];
+    a.gathered = gathered;
+    a.shard_len = shard;
+    a.psi = psi;
+    a.tiles_per_shard = (shard + kAgTile - 1) / kAgTile;
+    a.n_d = n_d;
+    bool aligned = shard % 8 == 0 && (reinterpret_cast<uintptr_t>(gathered) & 15) == 0;
+    for (int r = 0; r < n_d; ++r) aligned = aligned && (reinterpret_cast<uintptr_t>(shards[r]) & 15) == 0;
+    a.tma_ok = aligned ? 1 : 0;
+    a.timeout_ns = kDefaultTimeoutNs;
+    a.sc = sc;
+    const long long ntiles = a.tiles_per_shard * n_d;
+    if (ntiles <= 0) return cudaSuccess;
+    const size_t smem = 1024 + static_cast<size_t>(kAgStages) * kAgTile * 2;
+    static int attr_done[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !__atomic_load_n(&attr_done[dev], __ATOMIC_ACQUIRE)) {
+        cudaError_t e = cudaFuncSetAttribute(k_all_gather, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        __atomic_store_n(&attr_done[dev], 1, __ATOMIC_RELEASE);
+    }
+    long long grid = ntiles < sms ? ntiles : sms;
+    count_launch();
+    k_all_gather<<<static_cast<unsigned>(grid), kAgThreads, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------- quantized gather
+// One warp per block of `block` elements of a shard.  Pass 1: amax (16-byte
+// loads when aligned).  Pass 2: re-read (the block is hot in L1/L2), quantize,
+// write codes and dequantized bf16.
+__global__ void __launch_bounds__(256) k_quant_gather(const uint16_t* __restrict__ x, int n_d, long long shard,
+                                                      long long psi, int block, long long nbs,
+                                                      signed char* __restrict__ codes, float* __restrict__ scales,
+                                                      uint16_t* __restrict__ gathered)
+{
+    const int lane = threadIdx.x & 31;
+    const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+    const long long nblocks = nbs * n_d;
+    const bool vec = (shard % 8) == 0;
+    for (long long bi = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); bi < nblocks;
+         bi += warps) {
+        const int r = static_cast<int>(bi / nbs);
+        const long long b = bi - static_cast<long long>(r) * nbs;
+        long long valid = psi - static_cast<long long>(r) * shard;
+        valid = valid < 0 ? 0 : (valid > shard ? shard : valid);
+        const long long lo = b * block;
+        const long long hi = lo + block < valid ? lo + block : valid;
+        if (hi <= lo) {
+            if (lane == 0) scales[bi] = 0.0f;
+            continue;
+        }
+        const long long j0 = static_cast<long long>(r) * shard + lo;
+        const int n = static_cast<int>(hi - lo);
+        const int nv = vec ? n / 8 : 0;  // 16-byte vectors
+        float amax = 0.0f;
+        for (int v = lane; v < nv; v += 32) {
+            const uint4 w = reinterpret_cast<const uint4*>(x + j0)[v];
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                amax = fmaxf(amax, fmaxf(fabsf(Lp<ZERO_BF16>::lo(ws[k])), fabsf(Lp<ZERO_BF16>::hi(ws[k]))));
+        }
+        for (int i = nv * 8 + lane; i < n; i += 32) amax = fmaxf(amax, fabsf(Lp<ZERO_BF16>::widen(x[j0 + i])));
+        amax = warp_max_f32(amax);
+        const float s = __fdiv_rn(amax, 127.0f);
+        if (lane == 0) scales[bi] = s;
+        auto quant = [&](float xv, signed char& q, uint16_t& d) {
+            float rr = 0.0f;
+            if (s != 0.0f) {
+                rr = rintf(__fdiv_rn(xv, s));
+                rr = fminf(fmaxf(rr, -127.0f), 127.0f);
+            }
+            q = static_cast<signed char>(static_cast<int>(rr));
+            d = Lp<ZERO_BF16>::narrow(__fmul_rn(static_cast<float>(q), s));
+        };
+        for (int v = lane; v < nv; v += 32) {
+            const uint4 w = reinterpret_cast<const uint4*>(x + j0)[v];
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+            signed char q[8];
+            uint16_t d[8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                quant(Lp<ZERO_BF16>::lo(ws[k]), q[2 * k], d[2 * k]);
+                quant(Lp<ZERO_BF16>::hi(ws[k]), q[2 * k + 1], d[2 * k + 1]);
+            }
+            uint2 cq;
+            cq.x = (uint32_t)(uint8_t)q[0] | ((uint32_t)(uint8_t)q[1] << 8) | ((uint32_t)(uint8_t)q[2] << 16) | ((uint32_t)(uint8_t)q[3] << 24);
+            cq.y = (uint32_t)(uint8_t)q[4] | ((uint32_t)(uint8_t)q[5] << 8) | ((uint32_t)(uint8_t)q[6] << 16) | ((uint32_t)(uint8_t)q[7] << 24);
+            reinterpret_cast<uint2*>(codes + j0)[v] = cq;
+            uint4 dv;
+            dv.x = d[0] | ((uint32_t)d[1] << 16);
+            dv.y = d[2] | ((uint32_t)d[3] << 16);
+            dv.z = d[4] | ((uint32_t)d[5] << 16);
+            dv.w = d[6] | ((uint32_t)d[7] << 16);
+            reinterpret_cast<uint4*>(gathered + j0)[v] = dv;
+        }
+        for (int i = nv * 8 + lane; i < n; i += 32) {
+            signed char q;
+            uint16_t d;
+            quant(Lp<ZERO_BF16>::widen(x[j0 + i]), q, d);
+            codes[j0 + i] = q;
+            gathered[j0 + i] = d;
+        }
+    }
+}
+
+cudaError_t launch_quant_gather(const void* shards, int n_d, long long shard, long long psi, int block,
+                                signed char* codes, float* scales, void* gathered, cudaStream_t st)
+{
+    const int sms = sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    const long long nbs = (shard + block - 1) / block;
+    const long long nblocks = nbs * n_d;
+    if (nblocks <= 0) return cudaSuccess;
+    long long grid = (nblocks + 7) / 8;
+    if (grid > 16LL * sms) grid = 16LL * sms;
+    count_launch();
+    k_quant_gather<<<static_cast<unsigned>(grid), 256, 0, st>>>(static_cast<const uint16_t*>(shards), n_d, shard,
+                                                                psi, block, nbs, codes, scales,
+                                                                static_cast<uint16_t*>(gathered));
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- diagnostics
+// Waits on a barrier that nothing completes until the limit runs out, then
+// reports ZERO_DEV_TIMEOUT and returns.
+__global__ void k_debug_wait(zero_dev_scalars* sc, unsigned long long timeout_ns)
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+        if (!mbar_wait_bounded(&bar, 0u, nullptr, timeout_ns)) atomicOr(&sc->status, ZERO_DEV_TIMEOUT);
+    }
+}
+
+cudaError_t launch_debug_wait(zero_dev_scalars* sc, unsigned long long timeout_ns, cudaStream_t st)
+{
+    count_launch();
+    k_debug_wait<<<1, 32, 0, st>>>(sc, timeout_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace zk

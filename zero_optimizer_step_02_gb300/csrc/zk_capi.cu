@@ -1,0 +1,506 @@
+// zk_capi.cu -- the C ABI of libzero.so: plans, argument checks, and the pass
+// schedules of the ZeRO-DP step.  Declarations and the contract of every
+// entry point are in include/zero.h.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <new>
+
+#include "zk_common.cuh"
+#include "zk_launch.h"
+
+struct zero_plan {
+    long long psi;
+    int n_d;
+    int stage;
+    int grad_dtype;
+    int param_dtype;
+    int shard_pad;
+    long long shard;   // S
+    long long padded;  // n_d * S
+    long long bucket;  // elements per fused-step bucket (multiple of the tile)
+};
+
+namespace {
+
+using zk::StreamArgs;
+
+constexpr size_t kPartialBytes = sizeof(double) * zk::kMaxPartials;  // 32 KB, 256-aligned
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+zero_status from_cuda(cudaError_t e) { return e == cudaSuccess ? ZERO_OK : ZERO_ERR_CUDA; }
+
+#define ZK_TRY(expr)                              \
+    do {                                          \
+        const cudaError_t e_ = (expr);            \
+        if (e_ != cudaSuccess) return ZERO_ERR_CUDA; \
+    } while (0)
+
+zero_status check_hparams(const zero_hparams* hp)
+{
+    if (hp == nullptr) return ZERO_ERR_INVALID_ARG;
+    const float v[] = {hp->lr, hp->beta1, hp->beta2, hp->eps, hp->weight_decay, hp->max_norm};
+    for (float x : v)
+        if (std::isnan(x)) return ZERO_ERR_INVALID_ARG;
+    if (hp->beta1 < 0.0f || hp->beta1 >= 1.0f || hp->beta2 < 0.0f || hp->beta2 >= 1.0f) return ZERO_ERR_INVALID_ARG;
+    if (hp->lr < 0.0f || hp->eps < 0.0f || hp->weight_decay < 0.0f) return ZERO_ERR_INVALID_ARG;
+    if (hp->loss_scaling != 0 && hp->loss_scaling != 1) return ZERO_ERR_INVALID_ARG;
+    if (hp->loss_scaling && (hp->scale_window < 1 || !(hp->min_scale > 0.0f))) return ZERO_ERR_INVALID_ARG;
+    return ZERO_OK;
+}
+
+zero_status check_ranks(const zero_plan* p, const void* const* ranks)
+{
+    if (ranks == nullptr) return ZERO_ERR_INVALID_ARG;
+    for (int r = 0; r < p->n_d; ++r) {
+        if (ranks[r] == nullptr) return ZERO_ERR_INVALID_ARG;
+        if (!aligned(ranks[r], 16)) return ZERO_ERR_MISALIGNED;
+    }
+    return ZERO_OK;
+}
+
+zero_status check_dev(const void* ptr, uintptr_t align = 16)
+{
+    if (ptr == nullptr) return ZERO_ERR_INVALID_ARG;
+    return aligned(ptr, align) ? ZERO_OK : ZERO_ERR_MISALIGNED;
+}
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+long long tiles_of(long long n) { return (n + zk::kTile - 1) / zk::kTile; }
+
+// flat tile map over [lo, hi)
+void set_flat(StreamArgs& a, long long lo, long long hi)
+{
+    a.base = lo;
+    a.seg_stride = 0;
+    a.seg_len = hi - lo;
+    a.limit = hi;
+    a.n_seg = 1;
+    a.tiles_per_seg = tiles_of(hi - lo);
+    a.tma_ok = (lo % 8) == 0 ? 1 : 0;
+}
+
+StreamArgs base_args(const zero_plan* p, const zero_hparams* hp, zero_dev_scalars* sc)
+{
+    StreamArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.sc = sc;
+    a.timeout_ns = zk::kDefaultTimeoutNs;
+    if (hp != nullptr) a.hp = *hp;
+    (void)p;
+    return a;
+}
+
+void set_ranks(StreamArgs& a, const zero_plan* p, const void* const* ranks)
+{
+    a.n_ranks = p->n_d;
+    for (int r = 0; r < p->n_d; ++r) a.rank[r] = ranks[r];
+}
+
+double* partials_of(void* ws) { return static_cast<double*>(ws); }
+float* ghat_of(void* ws) { return reinterpret_cast<float*>(static_cast<char*>(ws) + kPartialBytes); }
+
+// the reduced gradient goes through HBM only when that moves fewer bytes than
+// reading the rank gradients twice: 4 + 4 bytes against 2 * n_d
+bool clip_materialises(const zero_plan* p) { return p->n_d > 4; }
+
+// grid the streaming launch uses for a flat range of n elements (the partial
+// sums of a reduce are one per CTA; zero_grad_sqnorm recomputes this count)
+int reduce_grid(long long n)
+{
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    long long g = tiles_of(n);
+    if (g > sms) g = sms;
+    if (g > zk::kMaxPartials) g = zk::kMaxPartials;
+    return static_cast<int>(g);
+}
+
+// One reduce pass over [0, psi): optional fp32 output, squared-norm partials,
+// non-finite detection in loss-scaling mode.
+zero_status run_reduce(const zero_plan* p, const zero_hparams* hp, const void* const* ranks, float* out,
+                       bool sqnorm, void* ws, zero_dev_scalars* sc, cudaStream_t st)
+{
+    StreamArgs a = base_args(p, hp, sc);
+    set_ranks(a, p, ranks);
+    set_flat(a, 0, p->psi);
+    a.n_side = 0;
+    a.out_f32[0] = out;
+    a.partials = sqnorm ? partials_of(ws) : nullptr;
+    a.flags = (sqnorm ? zk::F_SQNORM : 0) | (hp->loss_scaling ? (zk::F_DETECT | zk::F_LSCALE) : 0);
+    if (out != nullptr && !aligned(out, 16)) a.tma_ok = 0;
+    return from_cuda(zk::launch_stream(zk::OP_REDUCE, p->grad_dtype, p->param_dtype, a, st));
+}
+
+zero_status run_fused(const zero_plan* p, const zero_hparams* hp, const void* const* ranks, const float* mi,
+                      const float* m_in, const float* vi, float* mo, float* m_out, float* vo, void* lp,
+                      int flags, zero_dev_scalars* sc, cudaStream_t st)
+{
+    // buckets only when no global check ties the pieces together
+    const long long step = (flags & (zk::F_CLIP | zk::F_GUARD | zk::F_DETECT)) ? p->psi : p->bucket;
+    for (long long lo = 0; lo < p->psi; lo += step) {
+        const long long hi = lo + step < p->psi ? lo + step : p->psi;
+        StreamArgs a = base_args(p, hp, sc);
+        set_ranks(a, p, ranks);
+        set_flat(a, lo, hi);
+        a.n_side = 3;
+        a.side[0] = mi;
+        a.side[1] = m_in;
+        a.side[2] = vi;
+        a.out_f32[0] = mo;
+        a.out_f32[1] = m_out;
+        a.out_f32[2] = vo;
+        a.out_lp = lp;
+        a.flags = flags;
+        const zero_status s = from_cuda(zk::launch_stream(zk::OP_FUSED, p->grad_dtype, p->param_dtype, a, st));
+        if (s != ZERO_OK) return s;
+    }
+    return ZERO_OK;
+}
+
+zero_status run_adam(const zero_plan* p, const zero_hparams* hp, const float* g, const float* mi,
+                     const float* m_in, const float* vi, float* mo, float* m_out, float* vo, void* lp, int flags,
+                     zero_dev_scalars* sc, cudaStream_t st)
+{
+    StreamArgs a = base_args(p, hp, sc);
+    set_flat(a, 0, p->psi);
+    a.n_ranks = 0;
+    a.n_side = 4;
+    a.side[0] = g;
+    a.side[1] = mi;
+    a.side[2] = m_in;
+    a.side[3] = vi;
+    a.out_f32[0] = mo;
+    a.out_f32[1] = m_out;
+    a.out_f32[2] = vo;
+    a.out_lp = lp;
+    a.flags = flags;
+    return from_cuda(zk::launch_stream(zk::OP_ADAM, p->grad_dtype, p->param_dtype, a, st));
+}
+
+zero_status check_state(const float* mi, const float* m_in, const float* vi, float* mo, float* m_out, float* vo)
+{
+    const void* ptrs[] = {mi, m_in, vi, mo, m_out, vo};
+    for (const void* q : ptrs) {
+        const zero_status s = check_dev(q);
+        if (s != ZERO_OK) return s;
+    }
+    // out may alias in, array by array, but all three or none
+    const int alias = (mo == mi) + (m_out == m_in) + (vo == vi);
+    if (alias != 0 && alias != 3) return ZERO_ERR_INVALID_ARG;
+    return ZERO_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ZERO_API const char* zero_status_str(zero_status s)
+{
+    switch (s) {
+    case ZERO_OK: return "ok";
+    case ZERO_ERR_INVALID_ARG: return "invalid argument";
+    case ZERO_ERR_MISALIGNED: return "misaligned device pointer";
+    case ZERO_ERR_UNSUPPORTED: return "unsupported request";
+    case ZERO_ERR_CUDA: return "CUDA error";
+    case ZERO_ERR_TIMEOUT: return "device wait timed out";
+    case ZERO_ERR_BOUNDS: return "request exceeds a fixed capacity";
+    }
+    return "unknown status";
+}
+
+ZERO_API int zero_abi_version(void) { return ZERO_ABI_VERSION; }
+
+ZERO_API size_t zero_dev_scalars_size(void) { return sizeof(zero_dev_scalars); }
+
+ZERO_API zero_status zero_plan_create_ex(zero_plan** out, long long psi, int n_d, int stage, zero_dtype grad_dtype,
+                                         int shard_pad, const zero_plan_opts* opts)
+{
+    if (out == nullptr) return ZERO_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (psi < 1 || n_d < 1 || n_d > ZERO_MAX_RANKS || stage < 1 || stage > 3) return ZERO_ERR_INVALID_ARG;
+    if (shard_pad < 1 || shard_pad > ZERO_MAX_SHARD_PAD) return ZERO_ERR_INVALID_ARG;
+    if (grad_dtype != ZERO_BF16 && grad_dtype != ZERO_FP16) return ZERO_ERR_INVALID_ARG;
+    int pdt = ZERO_BF16;
+    long long bucket = 0;
+    if (opts != nullptr) {
+        if (opts->param_dtype_set) {
+            if (opts->param_dtype != ZERO_BF16 && opts->param_dtype != ZERO_FP16) return ZERO_ERR_INVALID_ARG;
+            pdt = opts->param_dtype;
+        }
+        bucket = opts->reduce_bucket_elems;
+    }
+    if (psi > (1LL << 40)) return ZERO_ERR_INVALID_ARG;
+    zero_plan* p = new (std::nothrow) zero_plan;
+    if (p == nullptr) return ZERO_ERR_BOUNDS;
+    p->psi = psi;
+    p->n_d = n_d;
+    p->stage = stage;
+    p->grad_dtype = grad_dtype;
+    p->param_dtype = pdt;
+    p->shard_pad = shard_pad;
+    const long long per_rank = (psi + n_d - 1) / n_d;
+    p->shard = (per_rank + shard_pad - 1) / shard_pad * shard_pad;
+    p->padded = p->shard * n_d;
+    if (bucket <= 0 || bucket >= psi) {
+        p->bucket = psi;
+    } else {
+        p->bucket = (bucket + zk::kTile - 1) / zk::kTile * zk::kTile;
+    }
+    *out = p;
+    return ZERO_OK;
+}
+
+ZERO_API zero_status zero_plan_create(zero_plan** out, long long psi, int n_d, int stage, zero_dtype grad_dtype,
+                                      int shard_pad)
+{
+    return zero_plan_create_ex(out, psi, n_d, stage, grad_dtype, shard_pad, nullptr);
+}
+
+ZERO_API void zero_plan_destroy(zero_plan* plan) { delete plan; }
+
+ZERO_API zero_status zero_plan_query(const zero_plan* p, long long* shard_size, long long* padded_psi,
+                                     long long* valid_len)
+{
+    if (p == nullptr) return ZERO_ERR_INVALID_ARG;
+    if (shard_size) *shard_size = p->shard;
+    if (padded_psi) *padded_psi = p->padded;
+    if (valid_len) {
+        for (int r = 0; r < p->n_d; ++r) {
+            long long v = p->psi - static_cast<long long>(r) * p->shard;
+            valid_len[r] = v < 0 ? 0 : (v > p->shard ? p->shard : v);
+        }
+    }
+    return ZERO_OK;
+}
+
+ZERO_API zero_status zero_plan_memory(const zero_plan* p, int stage, double k, double bytes_out[4])
+{
+    if (p == nullptr || bytes_out == nullptr || stage < 0 || stage > 3 || !(k >= 0.0)) return ZERO_ERR_INVALID_ARG;
+    const double psi = static_cast<double>(p->psi), n = static_cast<double>(p->n_d);
+    // which of the three model states are divided among the ranks at this stage
+    const bool part_opt = stage >= 1, part_grad = stage >= 2, part_param = stage >= 3;
+    bytes_out[0] = part_param ? 2.0 * psi / n : 2.0 * psi;
+    bytes_out[1] = part_grad ? 2.0 * psi / n : 2.0 * psi;
+    bytes_out[2] = part_opt ? k * psi / n : k * psi;
+    bytes_out[3] = bytes_out[0] + bytes_out[1] + bytes_out[2];
+    return ZERO_OK;
+}
+
+ZERO_API zero_status zero_plan_comm_volume(const zero_plan* p, int stage, double* elems_out)
+{
+    if (p == nullptr || elems_out == nullptr || stage < 0 || stage > 3) return ZERO_ERR_INVALID_ARG;
+    const int gathers = stage == 3 ? 2 : 1;  // forward and backward gathers in stage 3
+    *elems_out = static_cast<double>(p->psi) * (1 + gathers);
+    return ZERO_OK;
+}
+
+ZERO_API size_t zero_workspace_bytes(const zero_plan* p, const zero_hparams* hp)
+{
+    if (p == nullptr) return 0;
+    size_t bytes = kPartialBytes;
+    if (hp != nullptr && hp->max_norm > 0.0f && clip_materialises(p)) bytes += sizeof(float) * static_cast<size_t>(p->padded);
+    return bytes;
+}
+
+ZERO_API zero_status zero_scalars_init(zero_dev_scalars* sc, float loss_scale, void* stream)
+{
+    const zero_status s = check_dev(sc, 256);
+    if (s != ZERO_OK) return s;
+    if (!(loss_scale > 0.0f) || std::isinf(loss_scale)) return ZERO_ERR_INVALID_ARG;
+    return from_cuda(zk::launch_scalars_init(sc, loss_scale, as_stream(stream)));
+}
+
+ZERO_API zero_status zero_reduce_scatter(const zero_plan* p, const void* const* ranks, const zero_hparams* hp,
+                                         zero_dev_scalars* sc, float* grad_shards, void* ws, void* stream)
+{
+    if (p == nullptr) return ZERO_ERR_INVALID_ARG;
+    zero_status s;
+    if ((s = check_hparams(hp)) != ZERO_OK) return s;
+    if ((s = check_ranks(p, ranks)) != ZERO_OK) return s;
+    if ((s = check_dev(sc, 256)) != ZERO_OK) return s;
+    if ((s = check_dev(grad_shards)) != ZERO_OK) return s;
+    if ((s = check_dev(ws, 256)) != ZERO_OK) return s;
+    const cudaStream_t st = as_stream(stream);
+    if ((s = run_reduce(p, hp, ranks, grad_shards, true, ws, sc, st)) != ZERO_OK) return s;
+    if (p->padded > p->psi)
+        ZK_TRY(cudaMemsetAsync(grad_shards + p->psi, 0, sizeof(float) * static_cast<size_t>(p->padded - p->psi), st));
+    return ZERO_OK;
+}
+
+ZERO_API zero_status zero_grad_sqnorm(const zero_plan* p, const float* grad_shards, const zero_hparams* hp,
+                                      zero_dev_scalars* sc, void* ws, void* stream)
+{
+    if (p == nullptr) return ZERO_ERR_INVALID_ARG;
+    zero_status s;
+    if ((s = check_hparams(hp)) != ZERO_OK) return s;
+    if ((s = check_dev(sc, 256)) != ZERO_OK) return s;
+    if ((s = check_dev(ws, 256)) != ZERO_OK) return s;
+    const cudaStream_t st = as_stream(stream);
+    int n = 0;
+    if (grad_shards != nullptr) {
+        if (!aligned(grad_shards, 16)) return ZERO_ERR_MISALIGNED;
+        ZK_TRY(zk::launch_sqnorm_f32(grad_shards, p->psi, partials_of(ws), &n, st));
+    } else {
+        n = reduce_grid(p->psi);
+        if (n <= 0) return ZERO_ERR_CUDA;
+    }
+    return from_cuda(zk::launch_finalize_sqnorm(partials_of(ws), n, *hp, sc, st));
+}
+
+ZERO_API zero_status zero_adam_shard_step(const zero_plan* p, const zero_hparams* hp, const float* grad_shards,
+                                          float* master, float* m, float* v, void* lp_out, zero_dev_scalars* sc,
+                                          void* stream)
+{
+    if (p == nullptr) return ZERO_ERR_INVALID_ARG;
+    zero_status s;
+    if ((s = check_hparams(hp)) != ZERO_OK) return s;
+    if ((s = check_dev(sc, 256)) != ZERO_OK) return s;
+    if ((s = check_dev(grad_shards)) != ZERO_OK) return s;
+    if ((s = check_state(master, m, v, master, m, v)) != ZERO_OK) return s;
+    if (lp_out != nullptr && !aligned(lp_out, 16)) return ZERO_ERR_MISALIGNED;
+    const cudaStream_t st = as_stream(stream);
+    const int flags = (hp->max_norm > 0.0f ? zk::F_CLIP : 0) | (hp->loss_scaling ? zk::F_GUARD : 0);
+    if ((s = run_adam(p, hp, grad_shards, master, m, v, master, m, v, lp_out, flags, sc, st)) != ZERO_OK) return s;
+    return from_cuda(zk::launch_epilogue(*hp, sc, st));
+}
+
+ZERO_API zero_status zero_all_gather(const zero_plan* p, const void* const* shards, void* gathered,
+                                     zero_dev_scalars* sc, void* stream)
+{
+    if (p == nullptr || shards == nullptr) return ZERO_ERR_INVALID_ARG;
+    // shard pointers need only element (2-byte) alignment: shards cut from one
+    // flat buffer at an odd S are legal; the bulk-copy ring is used when all
+    // of them are 16-byte aligned and S is a multiple of 8
+    for (int r = 0; r < p->n_d; ++r) {
+        if (shards[r] == nullptr) return ZERO_ERR_INVALID_ARG;
+        if (!aligned(shards[r], 2)) return ZERO_ERR_MISALIGNED;
+    }
+    zero_status s;
+    if ((s = check_dev(gathered)) != ZERO_OK) return s;
+    if (sc != nullptr && !aligned(sc, 256)) return ZERO_ERR_MISALIGNED;
+    return from_cuda(zk::launch_all_gather(shards, p->n_d, p->shard, p->psi, gathered, sc, as_stream(stream)));
+}
+
+ZERO_API zero_status zero_step_fused(const zero_plan* p, const zero_hparams* hp, const void* const* ranks,
+                                     const float* mi, const float* m_in, const float* vi, float* mo, float* m_out,
+                                     float* vo, void* lp, zero_dev_scalars* sc, void* ws, void* stream)
+{
+    if (p == nullptr) return ZERO_ERR_INVALID_ARG;
+    zero_status s;
+    if ((s = check_hparams(hp)) != ZERO_OK) return s;
+    if ((s = check_ranks(p, ranks)) != ZERO_OK) return s;
+    if ((s = check_dev(sc, 256)) != ZERO_OK) return s;
+    if ((s = check_state(mi, m_in, vi, mo, m_out, vo)) != ZERO_OK) return s;
+    if (lp != nullptr && !aligned(lp, 16)) return ZERO_ERR_MISALIGNED;
+    const bool clip = hp->max_norm > 0.0f;
+    const bool ls = hp->loss_scaling != 0;
+    const bool inplace = mo == mi;
+    if ((clip || ls) && (s = check_dev(ws, 256)) != ZERO_OK) return s;
+    const cudaStream_t st = as_stream(stream);
+    const int lsf = ls ? zk::F_LSCALE : 0;
+
+    if (!clip) {
+        if (!ls) {
+            if ((s = run_fused(p, hp, ranks, mi, m_in, vi, mo, m_out, vo, lp, 0, sc, st)) != ZERO_OK) return s;
+        } else if (!inplace) {
+            // speculative: update while detecting; undo from the in state if flagged
+            if ((s = run_fused(p, hp, ranks, mi, m_in, vi, mo, m_out, vo, lp, zk::F_DETECT | lsf, sc, st)) != ZERO_OK) return s;
+            ZK_TRY(zk::launch_repair(*hp, mi, m_in, vi, mo, m_out, vo, lp, p->param_dtype, p->psi, sc, st));
+        } else {
+            // in place: a read-only check pass first, then the guarded update
+            if ((s = run_reduce(p, hp, ranks, nullptr, false, ws, sc, st)) != ZERO_OK) return s;
+            if ((s = run_fused(p, hp, ranks, mi, m_in, vi, mo, m_out, vo, lp, zk::F_GUARD | lsf, sc, st)) != ZERO_OK) return s;
+        }
+    } else {
+        const int guard = ls ? zk::F_GUARD : 0;
+        if (clip_materialises(p)) {
+            float* g = ghat_of(ws);
+            if ((s = run_reduce(p, hp, ranks, g, true, ws, sc, st)) != ZERO_OK) return s;
+            ZK_TRY(zk::launch_finalize_sqnorm(partials_of(ws), reduce_grid(p->psi), *hp, sc, st));
+            if ((s = run_adam(p, hp, g, mi, m_in, vi, mo, m_out, vo, lp, zk::F_CLIP | guard, sc, st)) != ZERO_OK) return s;
+        } else {
+            if ((s = run_reduce(p, hp, ranks, nullptr, true, ws, sc, st)) != ZERO_OK) return s;
+            ZK_TRY(zk::launch_finalize_sqnorm(partials_of(ws), reduce_grid(p->psi), *hp, sc, st));
+            if ((s = run_fused(p, hp, ranks, mi, m_in, vi, mo, m_out, vo, lp, zk::F_CLIP | guard | lsf, sc, st)) != ZERO_OK) return s;
+        }
+        if (ls && !inplace)
+            ZK_TRY(zk::launch_repair(*hp, mi, m_in, vi, mo, m_out, vo, lp, p->param_dtype, p->psi, sc, st));
+    }
+    return from_cuda(zk::launch_epilogue(*hp, sc, st));
+}
+
+ZERO_API zero_status zero_quant_gather(const zero_plan* p, const void* shards, int block, signed char* codes,
+                                       float* scales, void* gathered, void* stream)
+{
+    if (p == nullptr) return ZERO_ERR_INVALID_ARG;
+    if (block < 32 || block > 65536 || block % 32 != 0) return ZERO_ERR_INVALID_ARG;
+    if (p->param_dtype != ZERO_BF16) return ZERO_ERR_UNSUPPORTED;
+    zero_status s;
+    if ((s = check_dev(shards)) != ZERO_OK) return s;
+    if ((s = check_dev(codes)) != ZERO_OK) return s;
+    if ((s = check_dev(scales)) != ZERO_OK) return s;
+    if ((s = check_dev(gathered)) != ZERO_OK) return s;
+    return from_cuda(zk::launch_quant_gather(shards, p->n_d, p->shard, p->psi, block, codes, scales, gathered,
+                                             as_stream(stream)));
+}
+
+ZERO_API zero_status zero_step_fused_qgather(const zero_plan* p, const zero_hparams* hp, const void* const* ranks,
+                                             const float* mi, const float* m_in, const float* vi, float* mo,
+                                             float* m_out, float* vo, int block, signed char* codes, float* scales,
+                                             void* gathered, zero_dev_scalars* sc, void* ws, void* stream)
+{
+    (void)ws;
+    if (p == nullptr) return ZERO_ERR_INVALID_ARG;
+    zero_status s;
+    if ((s = check_hparams(hp)) != ZERO_OK) return s;
+    if (block != zk::kTile) return ZERO_ERR_UNSUPPORTED;
+    if (hp->max_norm > 0.0f || hp->loss_scaling) return ZERO_ERR_UNSUPPORTED;
+    if (p->param_dtype != ZERO_BF16) return ZERO_ERR_UNSUPPORTED;
+    if ((s = check_ranks(p, ranks)) != ZERO_OK) return s;
+    if ((s = check_dev(sc, 256)) != ZERO_OK) return s;
+    if ((s = check_state(mi, m_in, vi, mo, m_out, vo)) != ZERO_OK) return s;
+    if ((s = check_dev(codes)) != ZERO_OK) return s;
+    if ((s = check_dev(scales)) != ZERO_OK) return s;
+    if ((s = check_dev(gathered)) != ZERO_OK) return s;
+    const cudaStream_t st = as_stream(stream);
+    StreamArgs a = base_args(p, hp, sc);
+    set_ranks(a, p, ranks);
+    // one tile per quantization block, blocks starting at each shard's first element
+    a.base = 0;
+    a.seg_stride = p->shard;
+    a.seg_len = p->shard;
+    a.limit = p->psi;
+    a.n_seg = p->n_d;
+    a.tiles_per_seg = tiles_of(p->shard);
+    a.q_blocks_per_shard = a.tiles_per_seg;
+    a.tma_ok = (p->shard % 8) == 0 ? 1 : 0;
+    a.n_side = 3;
+    a.side[0] = mi;
+    a.side[1] = m_in;
+    a.side[2] = vi;
+    a.out_f32[0] = mo;
+    a.out_f32[1] = m_out;
+    a.out_f32[2] = vo;
+    a.q_codes = codes;
+    a.q_scales = scales;
+    a.q_gathered = gathered;
+    a.flags = zk::F_QUANT;
+    ZK_TRY(zk::launch_stream(zk::OP_FUSED, p->grad_dtype, p->param_dtype, a, st));
+    return from_cuda(zk::launch_epilogue(*hp, sc, st));
+}
+
+ZERO_API zero_status zero_debug_wait_timeout(zero_dev_scalars* sc, long long timeout_ns, void* stream)
+{
+    const zero_status s = check_dev(sc, 256);
+    if (s != ZERO_OK) return s;
+    if (timeout_ns < 1 || timeout_ns > 10000000000LL) return ZERO_ERR_INVALID_ARG;
+    return from_cuda(zk::launch_debug_wait(sc, static_cast<unsigned long long>(timeout_ns), as_stream(stream)));
+}
+
+ZERO_API unsigned long long zero_launch_count(void) { return zk::launch_count(); }
+
+}  // extern "C"

@@ -1,0 +1,281 @@
+// zk_common.cuh -- device helpers shared by the libzero kernels (sm_103a).
+//
+// PTX wrappers for mbarriers and 1-D bulk (TMA) copies, bounded waits,
+// 16-bit float conversions and the per-step Adam constants.  All floating
+// point that decides a result is written with explicit round-to-nearest
+// intrinsics so that no multiply-add is contracted and every operation is one
+// IEEE rounding, in the order the update rule states.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "zero.h"
+
+namespace zk {
+
+// ------------------------------------------------------------------ geometry
+constexpr int kTile = 2048;                 // elements per tile of the streaming engine
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kThreads = kConsumers + 32;   // + one producer warp
+constexpr int kChunk = 4;                   // consecutive elements per consumer chunk
+constexpr int kChunksPerThread = kTile / (kChunk * kConsumers);
+static_assert(kChunksPerThread * kChunk * kConsumers == kTile, "tile / consumer mismatch");
+constexpr int kGroupRanks = 8;              // rank slices per pipeline stage
+constexpr int kMaxSide = 4;                 // fp32 side streams (g, master, m, v)
+constexpr int kMaxStages = 8;
+constexpr int kStageOffset = 1024;          // dynamic smem bytes before the stage ring
+constexpr int kMaxPartials = 4096;          // per-CTA partial sums kept in the workspace
+constexpr unsigned long long kDefaultTimeoutNs = 4000000000ull;  // 4 s per wait
+
+// flags of a streaming launch
+enum : int {
+    F_GUARD = 1 << 0,   // skip the whole kernel if scalars->nonfinite is set
+    F_DETECT = 1 << 1,  // OR "non-finite reduced gradient" into scalars->nonfinite
+    F_SQNORM = 1 << 2,  // per-CTA partial sums of the squared reduced gradient
+    F_CLIP = 1 << 3,    // multiply the gradient by scalars->clip_coef
+    F_QUANT = 1 << 4,   // fused block-int8 quantized gather epilogue
+    F_LSCALE = 1 << 5,  // divisor includes scalars->loss_scale
+};
+
+// ------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+// make barrier initialisation visible to the async (bulk copy) proxy
+__device__ __forceinline__ void fence_barrier_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the phase of `bar` with the given parity.  Bounded twice: by a
+// wall-clock limit and by an iteration count.  Returns false when the limit
+// ran out or another thread of the CTA raised *abort.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  const volatile int* abort,
+                                                  unsigned long long timeout_ns)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1; it < (1u << 28); ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0) {
+            if (abort != nullptr && *abort) return false;
+            if (globaltimer_ns() - t0 > timeout_ns) return false;
+        }
+    }
+    return false;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// 1-D bulk copy global -> this CTA's shared memory, completing on `bar`.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src, uint32_t bytes,
+                                          uint64_t* bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(smem_dst)),
+        "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+// 1-D bulk copy shared -> global, tracked by bulk async-groups.
+__device__ __forceinline__ void bulk_store(void* gmem_dst, const void* smem_src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gmem_dst),
+                 "r"(smem_u32(smem_src)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// wait until at most N bulk groups still read shared memory
+template <int N>
+__device__ __forceinline__ void bulk_wait_read()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void bulk_wait_all()
+{
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// -------------------------------------------------------- 16-bit encodings
+template <int DT>
+struct Lp;
+
+template <>
+struct Lp<ZERO_BF16> {
+    // a 32-bit word holds two consecutive elements, the first in the low half
+    __device__ static __forceinline__ float lo(uint32_t w) { return __uint_as_float(w << 16); }
+    __device__ static __forceinline__ float hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+    __device__ static __forceinline__ float widen(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
+    __device__ static __forceinline__ uint16_t narrow(float x)
+    {
+        return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+    }
+};
+
+template <>
+struct Lp<ZERO_FP16> {
+    __device__ static __forceinline__ float lo(uint32_t w)
+    {
+        return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xFFFFu)));
+    }
+    __device__ static __forceinline__ float hi(uint32_t w)
+    {
+        return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+    }
+    __device__ static __forceinline__ float widen(uint16_t h) { return __half2float(__ushort_as_half(h)); }
+    __device__ static __forceinline__ uint16_t narrow(float x) { return __half_as_ushort(__float2half_rn(x)); }
+};
+
+__device__ __forceinline__ bool is_finite_f32(float x)
+{
+    return (__float_as_uint(x) & 0x7F800000u) != 0x7F800000u;
+}
+
+// ------------------------------------------------------------ step constants
+// Everything a kernel needs from the hyper-parameters and the step scalars,
+// computed once per CTA by one thread.
+struct StepConsts {
+    float b1, b2, omb1, omb2, step, sbc2, eps, decay, coef;
+    float divisor, inv_divisor;
+    int wd, clip, div_pow2, skip;
+};
+
+// The divisor of the mean: n_d times the loss scale (when loss scaling).
+// When it is a power of two, x * (1/D) is the same correctly rounded value as
+// x / D (both round the same real number), so the multiply is used.
+__device__ __forceinline__ void set_divisor(StepConsts& c, int n_d, float loss_scale)
+{
+    c.divisor = __fmul_rn(static_cast<float>(n_d), loss_scale);
+    const uint32_t b = __float_as_uint(c.divisor);
+    const uint32_t e = (b >> 23) & 0xFFu;
+    c.div_pow2 = (b & 0x007FFFFFu) == 0 && e != 0 && e != 0xFFu && (b >> 31) == 0;
+    c.inv_divisor = c.div_pow2 ? __frcp_rn(c.divisor) : 0.0f;
+}
+
+// Bias-corrected Adam constants for the step about to be committed: the fp64
+// running products beta^t are extended by one multiplication (never pow).
+__device__ __forceinline__ void set_adam(StepConsts& c, const zero_hparams& hp, double b1pow,
+                                         double b2pow)
+{
+    const double b1t = __dmul_rn(b1pow, static_cast<double>(hp.beta1));
+    const double b2t = __dmul_rn(b2pow, static_cast<double>(hp.beta2));
+    const float bc1 = __double2float_rn(__dsub_rn(1.0, b1t));
+    const float bc2 = __double2float_rn(__dsub_rn(1.0, b2t));
+    c.b1 = hp.beta1;
+    c.b2 = hp.beta2;
+    c.omb1 = __fsub_rn(1.0f, hp.beta1);
+    c.omb2 = __fsub_rn(1.0f, hp.beta2);
+    c.step = __fdiv_rn(hp.lr, bc1);
+    c.sbc2 = __fsqrt_rn(bc2);
+    c.eps = hp.eps;
+    c.decay = __fsub_rn(1.0f, __fmul_rn(hp.lr, hp.weight_decay));
+    c.wd = hp.weight_decay != 0.0f;
+}
+
+__device__ __forceinline__ float mean_of(const StepConsts& c, float sum)
+{
+    return c.div_pow2 ? __fmul_rn(sum, c.inv_divisor) : __fdiv_rn(sum, c.divisor);
+}
+
+// One Adam/AdamW element update in the fixed operation order.
+__device__ __forceinline__ void adam_elem(const StepConsts& c, float g, float& p, float& m, float& v)
+{
+    if (c.wd) p = __fmul_rn(p, c.decay);
+    m = __fadd_rn(__fmul_rn(c.b1, m), __fmul_rn(c.omb1, g));
+    v = __fadd_rn(__fmul_rn(c.b2, v), __fmul_rn(c.omb2, __fmul_rn(g, g)));
+    const float denom = __fadd_rn(__fdiv_rn(__fsqrt_rn(v), c.sbc2), c.eps);
+    p = __fsub_rn(p, __fmul_rn(c.step, __fdiv_rn(m, denom)));
+}
+
+// Squared-norm accumulation with an error-free product and a compensated sum
+// in fp32 (the per-thread partial is then carried in fp64): the result agrees
+// with an fp64 sum of the exact squares to ~1e-14 relative, so the clipping
+// coefficient comes out the same as a sequential fp64 sum's.
+__device__ __forceinline__ void sq_accumulate(float g, float& hi, float& lo)
+{
+    const float p = __fmul_rn(g, g);
+    const float pe = __fmaf_rn(g, g, -p);
+    const float s = __fadd_rn(hi, p);
+    const float bp = __fsub_rn(s, hi);
+    const float e = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(p, bp));
+    hi = s;
+    lo = __fadd_rn(lo, __fadd_rn(e, pe));
+}
+
+__device__ __forceinline__ double warp_sum_f64(double x)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = __dadd_rn(x, __shfl_xor_sync(0xFFFFFFFFu, x, o));
+    return x;
+}
+
+__device__ __forceinline__ float warp_max_f32(float x)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xFFFFFFFFu, x, o));
+    return x;
+}
+
+}  // namespace zk

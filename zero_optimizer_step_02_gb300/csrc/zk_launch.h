@@ -1,0 +1,65 @@
+// zk_launch.h -- host-side launch interface of the libzero kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "zero.h"
+
+namespace zk {
+
+enum { OP_FUSED = 0, OP_REDUCE = 1, OP_ADAM = 2 };
+
+// Arguments of one launch of the streaming engine (kernel parameter space).
+//
+// Tiles: element ranges of 2048 laid over "segments".  A flat launch has one
+// segment [base, limit); a per-shard launch (fused quantized gather) has n_seg
+// segments starting at base + s * seg_stride, each seg_len long and clipped
+// at limit (= Psi), so that no tile crosses a shard boundary.
+struct StreamArgs {
+    const void* rank[ZERO_MAX_RANKS];  // 16-bit gradient buffers, rank order
+    const float* side[4];              // fp32 inputs: OP_FUSED {master, m, v}; OP_ADAM {g, master, m, v}
+    float* out_f32[3];                 // OP_FUSED/OP_ADAM {master, m, v}; OP_REDUCE {g or null}
+    void* out_lp;                      // 16-bit parameters out (null: none)
+    signed char* q_codes;              // fused quantized gather (F_QUANT)
+    float* q_scales;
+    void* q_gathered;
+    zero_dev_scalars* sc;
+    double* partials;                  // OP_REDUCE + F_SQNORM: one fp64 per CTA
+    long long base, seg_stride, seg_len, limit, tiles_per_seg, q_blocks_per_shard;
+    int n_seg;
+    int n_ranks;                       // rank streams (0 for OP_ADAM)
+    int n_side;                        // fp32 side streams
+    int tma_ok;                        // every full tile is 16-byte aligned in every stream
+    int flags;                         // F_* of zk_common.cuh
+    int stages;                        // set by the launcher
+    unsigned stage_bytes;              // set by the launcher
+    int grid;                          // set by the launcher
+    unsigned long long timeout_ns;
+    zero_hparams hp;
+};
+
+cudaError_t launch_stream(int op, int grad_dtype, int param_dtype, StreamArgs& a, cudaStream_t st);
+
+// every kernel launch of the library adds one (zero_launch_count)
+void count_launch();
+unsigned long long launch_count();
+
+// auxiliary kernels (zk_aux.cu)
+cudaError_t launch_scalars_init(zero_dev_scalars* sc, float loss_scale, cudaStream_t st);
+cudaError_t launch_finalize_sqnorm(const double* partials, int n, const zero_hparams& hp,
+                                   zero_dev_scalars* sc, cudaStream_t st);
+cudaError_t launch_sqnorm_f32(const float* g, long long n, double* partials, int* n_partials,
+                              cudaStream_t st);
+cudaError_t launch_epilogue(const zero_hparams& hp, zero_dev_scalars* sc, cudaStream_t st);
+cudaError_t launch_repair(const zero_hparams& hp, const float* master_in, const float* m_in,
+                          const float* v_in, float* master_out, float* m_out, float* v_out,
+                          void* lp_out, int param_dtype, long long psi, zero_dev_scalars* sc,
+                          cudaStream_t st);
+cudaError_t launch_all_gather(const void* const* shards, int n_d, long long shard, long long psi,
+                              void* gathered, zero_dev_scalars* sc, cudaStream_t st);
+cudaError_t launch_quant_gather(const void* shards, int n_d, long long shard, long long psi,
+                                int block, signed char* codes, float* scales, void* gathered,
+                                cudaStream_t st);
+cudaError_t launch_debug_wait(zero_dev_scalars* sc, unsigned long long timeout_ns, cudaStream_t st);
+
+}  // namespace zk

@@ -1,0 +1,467 @@
+// zk_stream.cu -- the streaming engine of the ZeRO-DP step and its three ops.
+//
+// One persistent CTA per SM.  Warp 8 is the producer: one thread issues 1-D
+// bulk (TMA) copies of 2048-element tiles into a ring of shared-memory stages,
+// each stage holding up to 8 ranks' gradient slices plus, with the last rank
+// group of a tile, the fp32 side streams (reduced gradient / master / m / v).
+// Warps 0-7 are consumers: they add the rank slices in rank order into fp32
+// registers, release the stage, then apply the op and store the results with
+// 16-byte coalesced stores.  Tiles shorter than 2048 (the ragged tail, a
+// shard's last tile) or not 16-byte aligned take a plain-load path.
+//
+//   OP_FUSED  : reduce-scatter + Adam + 16-bit cast (or fused int8 gather)
+//   OP_REDUCE : reduce-scatter alone (optional fp32 output, squared-norm
+//               partials, non-finite detection)
+//   OP_ADAM   : Adam from an fp32 reduced gradient + 16-bit cast
+//
+// Sources: DP-notes "ZeRO-2: Gradient Partitioning" (reduce-scatter, then
+// each rank updates its own partition), itwiki "FSDP와의 관계" (fp32
+// reduce), itwiki "후속 기법" ZeRO++ row (block-quantized weight gather).
+#include "zk_common.cuh"
+#include "zk_launch.h"
+
+namespace zk {
+
+struct Shared {
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
+    int issued_parity[kMaxStages];
+    int abort;
+    int pad0;
+    StepConsts c;
+    float red_f[2][kConsumerWarps];
+    double red_d[kConsumerWarps + 1];
+};
+static_assert(sizeof(Shared) <= kStageOffset, "shared header too large");
+
+// tile -> (first element, valid length); see StreamArgs
+__device__ __forceinline__ void tile_span(const StreamArgs& a, long long tile, long long& j0, int& len)
+{
+    const long long seg = tile / a.tiles_per_seg;
+    const long long t = tile - seg * a.tiles_per_seg;
+    const long long lo = a.base + seg * a.seg_stride;
+    long long hi = lo + a.seg_len;
+    if (hi > a.limit) hi = a.limit;
+    j0 = lo + t * kTile;
+    const long long l = hi - j0;
+    len = l <= 0 ? 0 : (l > kTile ? kTile : static_cast<int>(l));
+}
+
+template <int GT>
+__device__ __forceinline__ void add_slice(float (&acc)[4], uint2 w)
+{
+    acc[0] = __fadd_rn(acc[0], Lp<GT>::lo(w.x));
+    acc[1] = __fadd_rn(acc[1], Lp<GT>::hi(w.x));
+    acc[2] = __fadd_rn(acc[2], Lp<GT>::lo(w.y));
+    acc[3] = __fadd_rn(acc[3], Lp<GT>::hi(w.y));
+}
+
+template <int GT, int PT, int OP>
+__global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ StreamArgs a)
+{
+    extern __shared__ __align__(1024) unsigned char smem[];
+    Shared* sh = reinterpret_cast<Shared*>(smem);
+    unsigned char* ring = smem + kStageOffset;
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const bool quant = (OP == OP_FUSED) && (a.flags & F_QUANT);
+
+    if (tid == 0) {
+        for (int s = 0; s < a.stages; ++s) {
+            mbar_init(&sh->full[s], 1);
+            mbar_init(&sh->empty[s], kConsumerWarps);
+            sh->issued_parity[s] = -1;
+        }
+        sh->abort = 0;
+        StepConsts c = {};
+        const zero_dev_scalars* sc = a.sc;
+        c.skip = (a.flags & F_GUARD) ? (sc->nonfinite != 0) : 0;
+        set_divisor(c, a.n_ranks > 0 ? a.n_ranks : 1, (a.flags & F_LSCALE) ? sc->loss_scale : 1.0f);
+        set_adam(c, a.hp, sc->beta1_pow, sc->beta2_pow);
+        c.clip = (a.flags & F_CLIP) != 0;
+        c.coef = c.clip ? sc->clip_coef : 1.0f;
+        sh->c = c;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (sh->c.skip) return;  // uniform: a flagged loss-scaling step writes nothing
+
+    const long long ntiles = a.tiles_per_seg * a.n_seg;
+    const int n_groups = a.n_ranks > 0 ? (a.n_ranks + kGroupRanks - 1) / kGroupRanks : 1;
+    const int rank_slots = a.n_ranks < kGroupRanks ? a.n_ranks : kGroupRanks;
+    const uint32_t side_off = static_cast<uint32_t>(rank_slots) * kTile * sizeof(uint16_t);
+
+    bool nonfinite = false;
+    float sq_hi = 0.0f, sq_lo = 0.0f;
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------- producer
+        if (lane == 0) {
+            const uint64_t pol = l2_policy_evict_first();
+            int s = 0;
+            uint32_t ph = 0;
+            for (long long tile = blockIdx.x; tile < ntiles && !*reinterpret_cast<volatile int*>(&sh->abort);
+                 tile += gridDim.x) {
+                long long j0;
+                int len;
+                tile_span(a, tile, j0, len);
+                if (len != kTile || !a.tma_ok) continue;
+                for (int g = 0; g < n_groups; ++g) {
+                    if (!mbar_wait_bounded(&sh->empty[s], ph ^ 1u, &sh->abort, a.timeout_ns)) {
+                        atomicExch(&sh->abort, 1);
+                        break;
+                    }
+                    const int r0 = g * kGroupRanks;
+                    const int nr = a.n_ranks - r0 < kGroupRanks ? a.n_ranks - r0 : kGroupRanks;
+                    const bool last = g == n_groups - 1;
+                    const uint32_t rank_bytes = kTile * sizeof(uint16_t);
+                    const uint32_t bytes = (nr > 0 ? nr : 0) * rank_bytes + (last ? a.n_side * kTile * 4u : 0u);
+                    unsigned char* st = ring + static_cast<size_t>(s) * a.stage_bytes;
+                    mbar_arrive_expect_tx(&sh->full[s], bytes);
+                    for (int k = 0; k < nr; ++k)
+                        bulk_load(st + k * rank_bytes,
+                                  static_cast<const uint16_t*>(a.rank[r0 + k]) + j0, rank_bytes,
+                                  &sh->full[s], pol);
+                    if (last)
+                        for (int k = 0; k < a.n_side; ++k)
+                            bulk_load(st + side_off + k * kTile * 4u, a.side[k] + j0, kTile * 4u,
+                                      &sh->full[s], pol);
+                    sh->issued_parity[s] = static_cast<int>(ph);
+                    if (++s == a.stages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------- consumers
+        int s = 0;
+        uint32_t ph = 0;
+        bool alive = true;
+        int qiter = 0;  // quantizer barriers passed: picks the reduction buffer
+        const StepConsts& c = sh->c;
+        for (long long tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+            long long j0;
+            int len;
+            tile_span(a, tile, j0, len);
+            if (len <= 0) {
+                if (quant && tid == 0) {
+                    const long long seg = tile / a.tiles_per_seg;
+                    a.q_scales[seg * a.q_blocks_per_shard + (tile - seg * a.tiles_per_seg)] = 0.0f;
+                }
+                continue;
+            }
+            const bool fast = len == kTile && a.tma_ok;
+            float acc[kChunksPerThread][4];
+            float sv[kChunksPerThread][kMaxSide][4];
+#pragma unroll
+            for (int ch = 0; ch < kChunksPerThread; ++ch)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    acc[ch][e] = 0.0f;
+#pragma unroll
+                    for (int k = 0; k < kMaxSide; ++k) sv[ch][k][e] = 0.0f;
+                }
+
+            if (fast) {
+                for (int g = 0; g < n_groups; ++g) {
+                    if (alive && !mbar_wait_bounded(&sh->full[s], ph, &sh->abort, a.timeout_ns)) {
+                        alive = false;
+                        atomicExch(&sh->abort, 1);
+                    }
+                    if (alive) {
+                        const unsigned char* st = ring + static_cast<size_t>(s) * a.stage_bytes;
+                        const int r0 = g * kGroupRanks;
+                        const int nr = a.n_ranks - r0 < kGroupRanks ? a.n_ranks - r0 : kGroupRanks;
+#pragma unroll
+                        for (int ch = 0; ch < kChunksPerThread; ++ch) {
+                            const int q = ch * kConsumers + tid;  // chunk index within the tile
+#pragma unroll 8
+                            for (int k = 0; k < nr; ++k) {
+                                const uint2 w = reinterpret_cast<const uint2*>(st + k * kTile * 2)[q];
+                                add_slice<GT>(acc[ch], w);
+                            }
+                        }
+                        if (g == n_groups - 1) {
+#pragma unroll
+                            for (int ch = 0; ch < kChunksPerThread; ++ch) {
+                                const int q = ch * kConsumers + tid;
+#pragma unroll
+                                for (int k = 0; k < kMaxSide; ++k) {
+                                    if (k < a.n_side) {
+                                        const float4 f = reinterpret_cast<const float4*>(
+                                            st + side_off + k * kTile * 4)[q];
+                                        sv[ch][k][0] = f.x;
+                                        sv[ch][k][1] = f.y;
+                                        sv[ch][k][2] = f.z;
+                                        sv[ch][k][3] = f.w;
+                                    }
+                                }
+                            }
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0 && alive) mbar_arrive(&sh->empty[s]);
+                    if (++s == a.stages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            } else if (alive) {
+                // plain-load path: per element, bounds-checked against len
+#pragma unroll
+                for (int ch = 0; ch < kChunksPerThread; ++ch) {
+                    const int q = ch * kConsumers + tid;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int idx = q * 4 + e;
+                        if (idx < len) {
+                            const long long j = j0 + idx;
+                            for (int r = 0; r < a.n_ranks; ++r)
+                                acc[ch][e] = __fadd_rn(acc[ch][e], Lp<GT>::widen(static_cast<const uint16_t*>(a.rank[r])[j]));
+#pragma unroll
+                            for (int k = 0; k < kMaxSide; ++k)
+                                if (k < a.n_side) sv[ch][k][e] = a.side[k][j];
+                        }
+                    }
+                }
+            }
+
+            // ------------------------------------------------ apply the op
+            float xq[kChunksPerThread][4];  // 16-bit results kept for the quantizer
+#pragma unroll
+            for (int ch = 0; ch < kChunksPerThread; ++ch) {
+                const int q = ch * kConsumers + tid;
+                const long long jc = j0 + q * 4;
+                int cnt = len - q * 4;
+                cnt = cnt < 0 ? 0 : (cnt > 4 ? 4 : cnt);
+                if (OP == OP_REDUCE) {
+                    float gv[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        gv[e] = mean_of(c, acc[ch][e]);
+                        if (e < cnt) {
+                            if (!is_finite_f32(gv[e])) nonfinite = true;
+                            if (a.flags & F_SQNORM) sq_accumulate(gv[e], sq_hi, sq_lo);
+                        }
+                    }
+                    if (alive && a.out_f32[0] != nullptr) {
+                        if (fast) {
+                            *reinterpret_cast<float4*>(a.out_f32[0] + jc) = make_float4(gv[0], gv[1], gv[2], gv[3]);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                if (e < cnt) a.out_f32[0][jc + e] = gv[e];
+                        }
+                    }
+                } else {
+                    // OP_FUSED: side = {master, m, v}; OP_ADAM: side = {g, master, m, v}
+                    constexpr int P = (OP == OP_ADAM) ? 1 : 0;
+                    float pv[4], mv[4], vv[4];
+                    uint16_t lp[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        float g = (OP == OP_ADAM) ? sv[ch][0][e] : mean_of(c, acc[ch][e]);
+                        if (e < cnt && !is_finite_f32(g)) nonfinite = true;
+                        if (c.clip) g = __fmul_rn(g, c.coef);
+                        pv[e] = sv[ch][P + 0][e];
+                        mv[e] = sv[ch][P + 1][e];
+                        vv[e] = sv[ch][P + 2][e];
+                        adam_elem(c, g, pv[e], mv[e], vv[e]);
+                        lp[e] = Lp<PT>::narrow(pv[e]);
+                        xq[ch][e] = Lp<PT>::widen(lp[e]);
+                    }
+                    if (alive) {
+                        if (fast) {
+                            *reinterpret_cast<float4*>(a.out_f32[0] + jc) = make_float4(pv[0], pv[1], pv[2], pv[3]);
+                            *reinterpret_cast<float4*>(a.out_f32[1] + jc) = make_float4(mv[0], mv[1], mv[2], mv[3]);
+                            *reinterpret_cast<float4*>(a.out_f32[2] + jc) = make_float4(vv[0], vv[1], vv[2], vv[3]);
+                            if (!quant && a.out_lp != nullptr) {
+                                uint2 w;
+                                w.x = static_cast<uint32_t>(lp[0]) | (static_cast<uint32_t>(lp[1]) << 16);
+                                w.y = static_cast<uint32_t>(lp[2]) | (static_cast<uint32_t>(lp[3]) << 16);
+                                *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out_lp) + jc) = w;
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                if (e < cnt) {
+                                    a.out_f32[0][jc + e] = pv[e];
+                                    a.out_f32[1][jc + e] = mv[e];
+                                    a.out_f32[2][jc + e] = vv[e];
+                                    if (!quant && a.out_lp != nullptr) static_cast<uint16_t*>(a.out_lp)[jc + e] = lp[e];
+                                }
+                            }
+                        }
+                    }
+                }
+            }
+
+            if (quant) {
+                // block = this tile: amax over the consumers, then codes + dequantized bf16
+                float amax = 0.0f;
+#pragma unroll
+                for (int ch = 0; ch < kChunksPerThread; ++ch)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if ((ch * kConsumers + tid) * 4 + e < len) amax = fmaxf(amax, fabsf(xq[ch][e]));
+                amax = warp_max_f32(amax);
+                // two buffers used alternately: between two uses of one buffer every
+                // consumer has passed the barrier of the other, so reads are done
+                const int par = qiter & 1;
+                ++qiter;
+                if (lane == 0) sh->red_f[par][warp] = amax;
+                named_bar_sync(1, kConsumers);
+                amax = 0.0f;
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) amax = fmaxf(amax, sh->red_f[par][w]);
+                const float scale = __fdiv_rn(amax, 127.0f);
+                if (tid == 0 && alive) {
+                    const long long seg = tile / a.tiles_per_seg;
+                    a.q_scales[seg * a.q_blocks_per_shard + (tile - seg * a.tiles_per_seg)] = scale;
+                }
+#pragma unroll
+                for (int ch = 0; ch < kChunksPerThread; ++ch) {
+                    const int q = ch * kConsumers + tid;
+                    const long long jc = j0 + q * 4;
+                    int cnt = len - q * 4;
+                    cnt = cnt < 0 ? 0 : (cnt > 4 ? 4 : cnt);
+                    int8_t code[4];
+                    uint16_t dq[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        float r = 0.0f;
+                        if (scale != 0.0f) {
+                            r = rintf(__fdiv_rn(xq[ch][e], scale));
+                            r = fminf(fmaxf(r, -127.0f), 127.0f);
+                        }
+                        code[e] = static_cast<int8_t>(static_cast<int>(r));
+                        dq[e] = Lp<ZERO_BF16>::narrow(__fmul_rn(static_cast<float>(code[e]), scale));
+                    }
+                    if (!alive) continue;
+                    if (fast) {
+                        const uint32_t cw = (static_cast<uint32_t>(static_cast<uint8_t>(code[0]))) |
+                                            (static_cast<uint32_t>(static_cast<uint8_t>(code[1])) << 8) |
+                                            (static_cast<uint32_t>(static_cast<uint8_t>(code[2])) << 16) |
+                                            (static_cast<uint32_t>(static_cast<uint8_t>(code[3])) << 24);
+                        *reinterpret_cast<uint32_t*>(a.q_codes + jc) = cw;
+                        uint2 w;
+                        w.x = static_cast<uint32_t>(dq[0]) | (static_cast<uint32_t>(dq[1]) << 16);
+                        w.y = static_cast<uint32_t>(dq[2]) | (static_cast<uint32_t>(dq[3]) << 16);
+                        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.q_gathered) + jc) = w;
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            if (e < cnt) {
+                                a.q_codes[jc + e] = code[e];
+                                static_cast<uint16_t*>(a.q_gathered)[jc + e] = dq[e];
+                            }
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    // ------------------------------------------------------------ CTA end
+    const int any_nonfinite = __syncthreads_or(nonfinite ? 1 : 0);
+    if (tid == 0 && any_nonfinite && (a.flags & F_DETECT)) atomicOr(&a.sc->nonfinite, 1);
+    if (OP == OP_REDUCE && (a.flags & F_SQNORM)) {
+        double part = warp < kConsumerWarps ? __dadd_rn(static_cast<double>(sq_hi), static_cast<double>(sq_lo)) : 0.0;
+        part = warp_sum_f64(part);
+        if (lane == 0 && warp < kConsumerWarps) sh->red_d[warp] = part;
+        __syncthreads();
+        if (tid == 0) {
+            double tot = 0.0;
+            for (int w = 0; w < kConsumerWarps; ++w) tot = __dadd_rn(tot, sh->red_d[w]);
+            a.partials[blockIdx.x] = tot;
+        }
+    }
+    if (tid == 0 && sh->abort) {
+        // a wait ran out: let every copy already issued land before the CTA
+        // gives its shared memory back, then report
+        for (int s = 0; s < a.stages; ++s)
+            if (sh->issued_parity[s] >= 0)
+                mbar_wait_bounded(&sh->full[s], static_cast<uint32_t>(sh->issued_parity[s]), nullptr, a.timeout_ns);
+        atomicOr(&a.sc->status, ZERO_DEV_TIMEOUT);
+    }
+}
+
+// ---------------------------------------------------------------- launching
+namespace {
+
+struct DevInfo {
+    int sms = 0;
+    int smem_optin = 0;
+};
+
+DevInfo device_info(int dev)
+{
+    static DevInfo cache[64];
+    static int ready[64];
+    if (dev < 0 || dev >= 64) return DevInfo{};
+    if (!__atomic_load_n(&ready[dev], __ATOMIC_ACQUIRE)) {
+        DevInfo d;
+        cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        cache[dev] = d;
+        __atomic_store_n(&ready[dev], 1, __ATOMIC_RELEASE);
+    }
+    return cache[dev];
+}
+
+template <int GT, int PT, int OP>
+cudaError_t launch_one(StreamArgs& a, cudaStream_t st)
+{
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    const DevInfo di = device_info(dev);
+    if (di.sms <= 0) return cudaErrorInvalidDevice;
+    // stage size: rank slots + fp32 side streams of one tile
+    const int slots = a.n_ranks < kGroupRanks ? a.n_ranks : kGroupRanks;
+    a.stage_bytes = static_cast<unsigned>(slots * kTile * 2 + a.n_side * kTile * 4);
+    int stages = (di.smem_optin - kStageOffset) / static_cast<int>(a.stage_bytes);
+    if (stages > kMaxStages) stages = kMaxStages;
+    if (stages < 2) return cudaErrorInvalidConfiguration;
+    a.stages = stages;
+    const size_t smem = kStageOffset + static_cast<size_t>(stages) * a.stage_bytes;
+    static int attr_done[64];
+    if (dev < 64 && !__atomic_load_n(&attr_done[dev], __ATOMIC_ACQUIRE)) {
+        err = cudaFuncSetAttribute(k_stream<GT, PT, OP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   di.smem_optin);
+        if (err != cudaSuccess) return err;
+        __atomic_store_n(&attr_done[dev], 1, __ATOMIC_RELEASE);
+    }
+    const long long ntiles = a.tiles_per_seg * a.n_seg;
+    long long grid = ntiles < di.sms ? ntiles : di.sms;
+    if (grid > kMaxPartials) grid = kMaxPartials;
+    if (grid <= 0) return cudaSuccess;
+    a.grid = static_cast<int>(grid);
+    count_launch();
+    k_stream<GT, PT, OP><<<static_cast<unsigned>(grid), kThreads, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_stream(int op, int grad_dtype, int param_dtype, StreamArgs& a, cudaStream_t st)
+{
+    const bool gb = grad_dtype == ZERO_BF16, pb = param_dtype == ZERO_BF16;
+    switch (op) {
+    case OP_FUSED:
+        if (gb) return pb ? launch_one<ZERO_BF16, ZERO_BF16, OP_FUSED>(a, st) : launch_one<ZERO_BF16, ZERO_FP16, OP_FUSED>(a, st);
+        return pb ? launch_one<ZERO_FP16, ZERO_BF16, OP_FUSED>(a, st) : launch_one<ZERO_FP16, ZERO_FP16, OP_FUSED>(a, st);
+    case OP_REDUCE:
+        return gb ? launch_one<ZERO_BF16, ZERO_BF16, OP_REDUCE>(a, st) : launch_one<ZERO_FP16, ZERO_BF16, OP_REDUCE>(a, st);
+    case OP_ADAM:
+        return pb ? launch_one<ZERO_BF16, ZERO_BF16, OP_ADAM>(a, st) : launch_one<ZERO_BF16, ZERO_FP16, OP_ADAM>(a, st);
+    default:
+        return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace zk
