@@ -1,0 +1,210 @@
+"""Parity at the workloads' full sizes, in the launch configuration the bench
+times (the same plans and entry points), on sampled outputs the oracle
+computes element by element.  Global quantities come from the oracle over
+the whole input (the clipping norm) or from properties fixed by the inputs
+(exactly one injected non-finite value).
+
+Workloads (seeded synthetic inputs; see the design notes for the recipe):
+  GPT-2-small ZeRO-2, Psi = 124,439,808, N_d = 8, AdamW, clip 1.0, heavy tail
+  GPT-2-1.5B ZeRO-2, Psi = 1.5e9, N_d = 8, fp16 grads, loss scale 1024, skip
+  Llama-3-8B-shaped ZeRO-3 layer, Psi_l = 218,112,000, N_d = 16
+  Psi = 2^28 sweep ends, N_d = 2 (with the fused int8 gather) and N_d = 64
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import zero_optimizer_step_02_gb300 as z
+from gpu_helpers import oracle_hp, u16, u32
+from zero_optimizer_step_02_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+NSAMPLE = 20_000
+
+
+def _free_gb():
+    free, _ = torch.cuda.mem_get_info()
+    return free / 1e9
+
+
+def _sample(psi, seed):
+    rng = np.random.default_rng(seed)
+    idx = rng.choice(psi, size=NSAMPLE, replace=False)
+    edge = np.array([0, 1, 2047, 2048, psi // 2, psi - 2049, psi - 2048, psi - 1])
+    return np.unique(np.concatenate([idx, edge[(edge >= 0) & (edge < psi)]]))
+
+
+class FullJob:
+    def __init__(self, psi, n_d, stage, gdt, hp, seed, pingpong=False, loss_scale=1.0):
+        self.plan = z.Plan(psi, n_d, stage=stage, grad_dtype=gdt, shard_pad=8)
+        self.hp, self.psi, self.n_d, self.seed = hp, psi, n_d, seed
+        self.gdt = gdt
+        self.buf = z.StepBuffers(self.plan, hp, device="cuda", pingpong=pingpong)
+        self.buf.master.copy_(synth.master_init(self.plan.padded, psi, seed, device="cuda"))
+        self.buf.init_scalars(loss_scale)
+        self.osc = oracle.new_scalars(loss_scale)
+
+    def fill_grads(self, step, sigma, heavy_tail=False, scale=1.0):
+        for r in range(self.n_d):
+            synth.gaussian_(self.buf.grads[r, :self.psi], sigma, self.seed, step, r, heavy_tail=heavy_tail,
+                            scale=scale)
+
+    def take(self, idx):
+        ii = torch.from_numpy(idx).cuda()
+        rows = [u16(self.buf.grads[r][ii]) for r in range(self.n_d)]
+        st = [t[ii].cpu().numpy().copy() for t in (self.buf.master, self.buf.m, self.buf.v)]
+        return rows, st
+
+    def oracle_sampled(self, rows, st, divisor, coef=None):
+        """The oracle's update of the sampled elements: rank-ordered mean,
+        optional clip coefficient, Adam with the step's bias corrections."""
+        odt = oracle.FP16 if self.gdt == z.ZERO_FP16 else oracle.BF16
+        g = oracle.all_reduce_mean(rows, odt, divisor)
+        if coef is not None:
+            g = (g * np.float32(coef)).astype(np.float32)
+        hp = oracle_hp(self.hp)
+        b1 = self.osc.beta1_pow * float(np.float32(hp.beta1))
+        b2 = self.osc.beta2_pow * float(np.float32(hp.beta2))
+        c = oracle.adam_consts(hp, b1, b2)
+        p, m, v = (a.copy() for a in st)
+        oracle.adam_update(hp, c, g, p, m, v)
+        self.osc.beta1_pow, self.osc.beta2_pow, self.osc.t = b1, b2, self.osc.t + 1
+        return p, m, v
+
+    def check(self, idx, want, lp_dtype=oracle.BF16, exact=True):
+        ii = torch.from_numpy(idx).cuda()
+        got = [t[ii].cpu().numpy() for t in (self.buf.master, self.buf.m, self.buf.v)]
+        lp = u16(self.buf.lp[ii])
+        for name, a, b in zip(("master", "m", "v"), got, want):
+            if exact:
+                bad = np.flatnonzero(u32(a) != u32(b))
+                assert bad.size == 0, "%s: %d of %d sampled elements differ" % (name, bad.size, idx.size)
+            else:
+                err = np.max(np.abs(a.astype(np.float64) - b)) / max(np.max(np.abs(b)), 1e-30)
+                assert err <= 1e-6, "%s relative error %.3g" % (name, err)
+        wlp = oracle.f32_to_lp(want[0], lp_dtype)
+        if exact:
+            assert np.array_equal(lp, wlp)
+        else:
+            assert np.max(np.abs(lp.astype(np.int64) - wlp.astype(np.int64))) <= 1
+
+
+def test_gpt2_small_clip_full_size():
+    psi, n_d = 124_439_808, 8
+    hp = z.hparams(lr=3e-4, beta1=0.9, beta2=0.95, weight_decay=0.1, max_norm=1.0)
+    job = FullJob(psi, n_d, 2, z.ZERO_BF16, hp, seed=202)
+    idx = _sample(psi, 1)
+    for step in (1, 2):
+        job.fill_grads(step, 1e-2, heavy_tail=True)
+        rows, st = job.take(idx)
+        # the clip coefficient needs the norm over all of psi: the oracle's
+        # reduce and sequential fp64 sum over the full gradient
+        full = [u16(job.buf.grads[r, :psi]) for r in range(n_d)]
+        g_full = oracle.all_reduce_mean(full, oracle.BF16, float(n_d))
+        sq = oracle.sqnorm(g_full)
+        del full, g_full
+        coef, applied = oracle.clip_coef(1.0, sq)
+        assert applied
+        job.buf.step(hp)
+        sc = job.buf.scalars_host()
+        # the oracle's sequential fp64 sum carries up to (n - 1) * 2^-53 relative error
+        assert sc.sqnorm == pytest.approx(sq, rel=2 * psi * 2.0 ** -53)
+        exact = np.float32(sc.clip_coef) == np.float32(coef)
+        assert abs(int(np.float32(sc.clip_coef).view(np.int32)) - int(np.float32(coef).view(np.int32))) <= 1
+        want = job.oracle_sampled(rows, st, float(n_d), coef)
+        job.check(idx, want, exact=exact)
+
+
+def test_gpt2_xl_fp16_loss_scale_full_size():
+    psi, n_d = 1_500_000_000, 8
+    if _free_gb() < 70:
+        pytest.skip("needs ~64 GB of free device memory")
+    hp = z.hparams(lr=1e-4, loss_scaling=True)
+    job = FullJob(psi, n_d, 2, z.ZERO_FP16, hp, seed=303, pingpong=True, loss_scale=1024.0)
+    idx = _sample(psi, 2)
+    job.fill_grads(1, 1e-4, scale=1024.0)
+    rows, st = job.take(idx)
+    job.buf.step(hp)
+    sc = job.buf.scalars_host()
+    assert sc.overflow == 0 and sc.t == 1
+    want = job.oracle_sampled(rows, st, float(n_d) * 1024.0)
+    job.check(idx, want)
+    # step 2: one rank carries +inf at one index -> skipped, scale halves
+    job.fill_grads(2, 1e-4, scale=1024.0)
+    r, j = synth.pick_index(303, 2, n_d, psi)
+    job.buf.grads[r, j] = float("inf")
+    job.buf.step(hp)
+    sc = job.buf.scalars_host()
+    assert sc.overflow == 1 and sc.t == 1 and sc.loss_scale == 512.0 and sc.good_steps == 0
+    job.check(idx, want)   # the state (now in the other buffer set) is unchanged
+
+
+def test_llama_layer_zero3_full_size():
+    psi, n_d = 218_112_000, 16   # one Llama-3-8B-shaped decoder layer
+    hp = z.hparams(lr=1e-3)
+    job = FullJob(psi, n_d, 3, z.ZERO_BF16, hp, seed=404)
+    idx = _sample(psi, 3)
+    S = job.plan.shard
+    gathered = torch.zeros(psi, dtype=torch.bfloat16, device="cuda")
+    for step in (1, 2):
+        # gather the layer's bf16 shards (as written by the previous step)
+        z.zero_all_gather(job.plan.handle, [job.buf.lp[r * S:(r + 1) * S] for r in range(n_d)], gathered,
+                          job.buf.scalars)
+        ii = torch.from_numpy(idx).cuda()
+        assert torch.equal(gathered[ii], job.buf.lp[ii])
+        job.fill_grads(step, 1e-3)
+        rows, st = job.take(idx)
+        job.buf.step(hp)
+        want = job.oracle_sampled(rows, st, float(n_d))
+        job.check(idx, want)
+    assert job.buf.scalars_host().status == 0
+
+
+@pytest.mark.parametrize("n_d", [2, 64])
+def test_psi_2_28_full_size(n_d):
+    psi = 1 << 28
+    if _free_gb() < 2 * n_d * psi / 1e9 + 20:
+        pytest.skip("not enough free device memory")
+    hp = z.hparams(lr=1e-3)
+    job = FullJob(psi, n_d, 2, z.ZERO_BF16, hp, seed=505 + n_d)
+    idx = _sample(psi, 4)
+    job.fill_grads(1, 1e-3)
+    rows, st = job.take(idx)
+    job.buf.step(hp)
+    want = job.oracle_sampled(rows, st, float(n_d))
+    job.check(idx, want)
+
+
+def test_psi_2_28_fused_quantized_gather_full_size():
+    psi, n_d = 1 << 28, 2
+    hp = z.hparams(lr=1e-3)
+    job = FullJob(psi, n_d, 2, z.ZERO_BF16, hp, seed=606)
+    S = job.plan.shard
+    nbs = -(-S // 2048)
+    codes = torch.zeros(job.plan.padded, dtype=torch.int8, device="cuda")
+    scales = torch.zeros(n_d * nbs, device="cuda")
+    gathered = torch.zeros(psi, dtype=torch.bfloat16, device="cuda")
+    # sample whole quantization blocks (the scale needs the whole block)
+    rng = np.random.default_rng(5)
+    blocks = np.unique(np.concatenate([rng.choice(n_d * nbs, 40, replace=False), [0, n_d * nbs - 1]]))
+    idx = np.concatenate([np.arange(b // nbs * S + (b % nbs) * 2048, b // nbs * S + (b % nbs) * 2048 + 2048)
+                          for b in blocks])
+    job.fill_grads(1, 1e-3)
+    rows, st = job.take(idx)
+    b = job.buf
+    z.zero_step_fused_qgather(job.plan.handle, hp, b.rank_list(), b.master, b.m, b.v, b.master, b.m, b.v, 2048,
+                              codes, scales, gathered, b.scalars, b.ws)
+    want = job.oracle_sampled(rows, st, float(n_d))
+    ii = torch.from_numpy(idx).cuda()
+    assert np.array_equal(u32(b.master[ii].cpu().numpy()), u32(want[0]))
+    lp = oracle.f32_to_bf16(want[0])
+    got_codes = codes[ii].cpu().numpy()
+    got_g = u16(gathered[ii])
+    got_s = scales[torch.from_numpy(blocks).cuda()].cpu().numpy()
+    for k in range(blocks.size):
+        sl = slice(k * 2048, (k + 1) * 2048)
+        c, s, d = oracle.quantize_block(lp[sl])
+        assert got_s[k] == np.float32(s)
+        assert np.array_equal(got_codes[sl], c) and np.array_equal(got_g[sl], d)

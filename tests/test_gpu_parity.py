@@ -8,6 +8,8 @@ the stated tolerance, relative 1e-6 and 1 ulp).  With clipping the global norm
 is summed in another order on the GPU, so the coefficient may differ by an
 ulp: those cases are held to the tolerance.  Layout, padding, skip decisions,
 int8 codes and scales are compared exactly."""
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -99,7 +101,8 @@ def test_fused_step_with_clipping(n_d, pingpong):
         job.gpu_step()
         job.oracle_step()
         sc = job.scalars()
-        assert sc.sqnorm == pytest.approx(job.ost.scalars.sqnorm, rel=1e-12)
+        # both sums within the sequential fp64 sum's error bound of each other
+        assert sc.sqnorm == pytest.approx(job.ost.scalars.sqnorm, rel=2 * psi * 2.0 ** -53)
         o_coef = np.float32(job.ost.scalars.clip_coef)
         assert o_coef < 1.0   # the clip is active in this workload
         assert abs(int(np.float32(sc.clip_coef).view(np.int32)) - int(o_coef.view(np.int32))) <= 1
@@ -182,8 +185,14 @@ def test_grad_sqnorm_and_coefficient(from_partials):
     z.zero_reduce_scatter(job.plan.handle, job.buf.rank_list(), hp, job.buf.scalars, g, job.buf.ws)
     z.zero_grad_sqnorm(job.plan.handle, None if from_partials else g, hp, job.buf.scalars, job.buf.ws)
     sc = job.scalars()
-    want = oracle.sqnorm(oracle.reduce_scatter(job.rows, oracle.BF16, float(n_d), job.plan.shard))
-    assert sc.sqnorm == pytest.approx(want, rel=1e-12)
+    g_or = oracle.reduce_scatter(job.rows, oracle.BF16, float(n_d), job.plan.shard)
+    want = oracle.sqnorm(g_or)
+    # the exactly rounded sum of the exact squares (fp32 squares are exact in
+    # fp64): the GPU's compensated sum must be within 1e-13 of it, the
+    # oracle's sequential fp64 sum within its own bound (n - 1) * 2^-53
+    exact = math.fsum(np.square(g_or.astype(np.float64)))
+    assert abs(sc.sqnorm - exact) <= 1e-13 * exact
+    assert abs(want - exact) <= psi * 2.0 ** -53 * exact
     coef, applied = oracle.clip_coef(1.0, want)
     assert applied
     assert abs(int(np.float32(sc.clip_coef).view(np.int32)) - int(np.float32(coef).view(np.int32))) <= 1
