@@ -267,6 +267,38 @@ ZERO_API zero_status zero_step_fused_qgather(const zero_plan* plan, const zero_h
 ZERO_API zero_status zero_debug_wait_timeout(zero_dev_scalars* scalars_dev, long long timeout_ns,
                                              void* stream);
 
+/* ------------------------------------------------- allocation-free step --- */
+/* The pages have no counterpart to this entry point; it serves callers that
+ * cannot allocate device memory for a workspace: code running where
+ * cudaMalloc is not allowed (for example while a stream is being captured
+ * into a CUDA graph without a memory pool), programs whose device memory is
+ * owned by another allocator that hands out no extra buffers, and
+ * latency-bound services that forbid allocation once they are running.
+ *
+ * It is zero_step_fused with the caller's workspace replaced by one scratch
+ * array that lives in the library (a file-scope __device__ array of
+ * ZERO_NOALLOC_SCRATCH_BYTES = 32 KB of partial sums + 4 MB for the reduced
+ * gradient; every GPU that loads the library holds it until the process
+ * exits).  The call allocates nothing and calls no cudaMalloc/cudaFree.
+ *   - Limit: requests whose zero_workspace_bytes(plan, hp) exceeds the
+ *     scratch -- clipping with n_d > 4 and n_d*S > 2^20 parameters -- are
+ *     rejected with ZERO_ERR_BOUNDS before anything is launched.  Without
+ *     clipping, or with n_d <= 4, any size is accepted.
+ *   - Set-up: the first call on a device (with that device current) looks up
+ *     the scratch's device address once; make that first call before any
+ *     stream capture.
+ *   - Every call shares the one scratch array and it keeps the last call's
+ *     contents; each call writes every scratch entry it reads, so nothing has
+ *     to be cleared.  Calls that overlap on the GPU (other streams, other
+ *     threads, other plans) race on the scratch: order them on one stream.
+ * Arguments, results and errors are otherwise those of zero_step_fused.    */
+#define ZERO_NOALLOC_SCRATCH_BYTES (32768u + 4u * (1u << 20))
+ZERO_API zero_status zero_step_fused_noalloc(const zero_plan* plan, const zero_hparams* hp,
+                                             const void* const* rank_grads, const float* master_in,
+                                             const float* m_in, const float* v_in, float* master_out,
+                                             float* m_out, float* v_out, void* lp_out,
+                                             zero_dev_scalars* scalars_dev, void* stream);
+
 /* Number of kernels this library has launched in this process so far (all
  * threads, all devices).  Lets a caller count the launches of a region.     */
 ZERO_API unsigned long long zero_launch_count(void);

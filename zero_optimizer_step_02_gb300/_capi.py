@@ -78,6 +78,7 @@ _SIGS = {
                                        _vp, _vp, _vp]),
     "zero_debug_wait_timeout": (_i32, [_vp, _ll, _vp]),
     "zero_launch_count": (ctypes.c_ulonglong, []),
+    "zero_step_fused_noalloc": (_i32, [_vp, _hp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -224,6 +225,16 @@ def zero_step_fused_qgather(plan, hp, rank_grads, master_in, m_in, v_in, master_
 
 def zero_debug_wait_timeout(scalars, timeout_ns, stream=None):
     _check(_lib.zero_debug_wait_timeout(_addr(scalars), timeout_ns, _stream(stream)), "zero_debug_wait_timeout")
+
+
+def zero_step_fused_noalloc(plan, hp, rank_grads, master_in, m_in, v_in, master_out, m_out, v_out, lp_out,
+                            scalars, stream=None):
+    """zero_step_fused without a workspace argument: for callers that cannot
+    allocate device memory (see include/zero.h for the limit and set-up)."""
+    _check(_lib.zero_step_fused_noalloc(plan, ctypes.byref(hp), _ptr_array(rank_grads), _addr(master_in),
+                                        _addr(m_in), _addr(v_in), _addr(master_out), _addr(m_out), _addr(v_out),
+                                        _addr(lp_out), _addr(scalars), _stream(stream)),
+           "zero_step_fused_noalloc")
 
 
 def zero_launch_count():
