@@ -357,7 +357,7 @@ def gpu_arm(args, rank, world, device):
 def e2e_measure(job, w, args, device, world):
     """Gradients from pinned host memory in, gathered parameters out, per step."""
     import torch
-    if w["layers"] > 1 or w["psi"] * w["n_d"] * 2 > 40e9:
+    if w["layers"] > 1 or w["psi"] * w["n_d"] * 2 > 8e9:
         return None
     z = job.z
     host_g = torch.empty(job.grads[0].shape, dtype=job.grads[0].dtype, pin_memory=True)
