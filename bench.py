@@ -41,8 +41,10 @@ L2_BYTES = 129 * 1024 * 1024
 
 
 # ----------------------------------------------------------------- workloads
-def workload(cfg, nd=None, qgather=False):
-    """Sizes, hyper-parameters and the algorithmic bytes of one step."""
+def workload(cfg, nd=None, qgather=False, psi=None):
+    """Sizes, hyper-parameters and the algorithmic bytes of one step.  psi
+    overrides the parameter count (a smaller case of the same workload, for
+    profiling)."""
     if cfg == 1:
         w = dict(name="zero2_psi1000003_nd4_adam", psi=1_000_003, n_d=4, stage=2, pad=8, gdt="bf16",
                  sigma=1e-3, tail=False, lr=1e-3, b2=0.999, wd=0.0, clip=0.0, ls=False, layers=1)
@@ -62,6 +64,9 @@ def workload(cfg, nd=None, qgather=False):
                  layers=1, qgather=qgather)
     else:
         raise SystemExit("unknown config %r" % cfg)
+    if psi:
+        w["psi"] = int(psi)
+        w["name"] += "_psi%d" % w["psi"]
     n_d = w["n_d"]
     # algorithmic bytes per parameter of one step (minimum HBM traffic)
     if w["clip"] > 0:
@@ -254,7 +259,7 @@ def l2_flush(torch, device, buf=[]):
 def gpu_arm(args, rank, world, device):
     import torch
     import zero_optimizer_step_02_gb300 as z
-    w = workload(args.config, args.nd, args.qgather)
+    w = workload(args.config, args.nd, args.qgather, args.psi)
     torch.cuda.set_device(device)
     job = Job(w, device)
     torch.cuda.synchronize()
@@ -338,7 +343,7 @@ def gpu_arm(args, rank, world, device):
                 "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": kernel,
                 "kernel_ms": round(kms, 4), "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)"}
 
-    e2e = e2e_measure(job, w, args, device, world)
+    e2e = None if args.no_e2e else e2e_measure(job, w, args, device, world)
     out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f32 (state), %s (grads), bf16 (params)" % w["gdt"],
@@ -411,7 +416,7 @@ def oracle_sample(w, budget_s, max_steps=None):
 
 
 def reference_arm(args, rank, world):
-    w = workload(args.config, args.nd, args.qgather)
+    w = workload(args.config, args.nd, args.qgather, args.psi)
     if rank != 0:
         return None
     for _ in range(args.warmup):
@@ -466,6 +471,8 @@ def main():
     ap.add_argument("--qgather", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--psi", type=int, default=None, help="smaller parameter count (profiling)")
+    ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -480,7 +487,7 @@ def main():
     out = gpu_arm(args, rank, world, device)
     if rank == 0:
         if not args.no_cpu_baseline and world == 1:
-            w = workload(args.config, args.nd, args.qgather)
+            w = workload(args.config, args.nd, args.qgather, args.psi)
             psi, n_d, steps, el = oracle_sample(w, args.cpu_budget)
             out["cpu_baseline"] = {"value": psi * steps / el, "unit": UNIT, "cores": 1, "kind": "oracle",
                                    "sample": "%d of %d params, n_d=%d, %d steps in %.1f s, single-threaded C "

@@ -18,7 +18,7 @@ namespace zk {
 
 // ------------------------------------------------------------------ geometry
 constexpr int kTile = 2048;                 // elements per tile of the streaming engine
-constexpr int kConsumerWarps = 8;
+constexpr int kConsumerWarps = 16;         // one 4-element chunk per consumer thread per tile
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;   // + one producer warp
 constexpr int kChunk = 4;                   // consecutive elements per consumer chunk

@@ -142,7 +142,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
         uint32_t ph = 0;
         bool alive = true;
         int qiter = 0;  // quantizer barriers passed: picks the reduction buffer
-        const StepConsts& c = sh->c;
+        // constants in registers: a reference into shared memory would be
+        // re-read for every element (the stores in the loop may alias it)
+        const StepConsts c = sh->c;
+        const bool detect = (a.flags & (F_DETECT | F_SQNORM)) != 0;
+        const bool want_sq = (a.flags & F_SQNORM) != 0;
         for (long long tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
             long long j0;
             int len;
@@ -244,8 +248,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
                     for (int e = 0; e < 4; ++e) {
                         gv[e] = mean_of(c, acc[ch][e]);
                         if (e < cnt) {
-                            if (!is_finite_f32(gv[e])) nonfinite = true;
-                            if (a.flags & F_SQNORM) sq_accumulate(gv[e], sq_hi, sq_lo);
+                            if (detect && !is_finite_f32(gv[e])) nonfinite = true;
+                            if (want_sq) sq_accumulate(gv[e], sq_hi, sq_lo);
                         }
                     }
                     if (alive && a.out_f32[0] != nullptr) {
@@ -265,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         float g = (OP == OP_ADAM) ? sv[ch][0][e] : mean_of(c, acc[ch][e]);
-                        if (e < cnt && !is_finite_f32(g)) nonfinite = true;
+                        if (detect && e < cnt && !is_finite_f32(g)) nonfinite = true;
                         if (c.clip) g = __fmul_rn(g, c.coef);
                         pv[e] = sv[ch][P + 0][e];
                         mv[e] = sv[ch][P + 1][e];
