@@ -306,10 +306,15 @@ def gpu_arm(args, rank, world, device):
         job.ghat = torch.zeros(job.plan.padded, device=device)
         n_rep = max(3, args.steps)
         dur = [0.0, 0.0, 0.0]
-        for _ in range(n_rep):
-            ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        # enqueue every repetition back to back (one sync at the end) so the
+        # host's launch latency never sits inside an interval; the first
+        # repetition, which starts from an idle GPU, is not counted
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_rep + 1)]
+        torch.cuda.synchronize()
+        for ev in evs:
             job.parts_step(ev)
-            torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        for ev in evs[1:]:
             for i in range(3):
                 dur[i] += ev[i].elapsed_time(ev[i + 1]) / n_rep
         names = ["reduce_scatter", "finalize", "adam_shard"]
@@ -323,15 +328,16 @@ def gpu_arm(args, rank, world, device):
         if w["stage"] == 3:
             # time the per-layer fused step alone
             evs = []
-            for _ in range(max(3, args.steps)):
+            torch.cuda.synchronize()
+            for _ in range(max(3, args.steps) + 1):
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record()
                 z.zero_step_fused(job.plan.handle, job.hp, job.ranks(0), job.master[0], job.m[0], job.v[0],
                                   job.master[0], job.m[0], job.v[0], job.lp[0], job.scalars, job.ws)
                 b.record()
-                torch.cuda.synchronize()
-                evs.append(a.elapsed_time(b))
-            kms = statistics.mean(evs)
+                evs.append((a, b))
+            torch.cuda.synchronize()
+            kms = statistics.mean(a.elapsed_time(b) for a, b in evs[1:])
             kbytes = (2 * w["n_d"] + 26) * w["psi"]
         else:
             kbytes = w["bytes_per_param"] * w["psi"]

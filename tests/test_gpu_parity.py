@@ -322,3 +322,30 @@ def test_padding_is_never_touched():
     gm, gmm, gv, _ = job.gpu_state()
     for a in (gm, gmm, gv):
         assert not u32(a[psi:]).any()
+
+
+def test_quant_codes_at_and_near_ties():
+    # every block holds 127 s (so s = 2^-10 exactly) and values (k + 1/2) s,
+    # which are exact ties of x / s, plus values one bf16 ulp off a tie: the
+    # rounding decision must match the oracle's IEEE quotient in all of them
+    n_d, block = 2, 2048
+    psi = n_d * 4 * block
+    plan = z.Plan(psi, n_d, stage=2, shard_pad=8)
+    k = np.arange(-126, 126)
+    ties = (k + 0.5) * 2.0 ** -10
+    vals = np.concatenate([ties, np.nextafter(ties.astype(np.float32), np.float32(np.inf)),
+                           np.nextafter(ties.astype(np.float32), np.float32(-np.inf))])
+    rng = np.random.default_rng(3)
+    x = rng.choice(vals, size=psi).astype(np.float32)
+    x[::block] = 127 * 2.0 ** -10
+    xb = oracle.f32_to_bf16(x)
+    xd = torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16)
+    S = plan.shard
+    nbs = -(-S // block)
+    codes = torch.zeros(plan.padded, dtype=torch.int8, device="cuda")
+    scales = torch.zeros(n_d * nbs, device="cuda")
+    gathered = torch.zeros(psi, dtype=torch.bfloat16, device="cuda")
+    z.zero_quant_gather(plan.handle, xd, block, codes, scales, gathered)
+    oc, osc, og = oracle.quant_gather(xb, n_d, psi, S, block)
+    assert np.all(osc == np.float32(2.0 ** -10))
+    assert np.array_equal(codes.cpu().numpy(), oc) and np.array_equal(u16(gathered), og)

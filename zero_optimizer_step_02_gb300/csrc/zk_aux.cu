@@ -403,13 +403,9 @@ __global__ void __launch_bounds__(256) k_quant_gather(const uint16_t* __restrict
         amax = warp_max_f32(amax);
         const float s = __fdiv_rn(amax, 127.0f);
         if (lane == 0) scales[bi] = s;
+        const float inv = quant_reciprocal(s);
         auto quant = [&](float xv, signed char& q, uint16_t& d) {
-            float rr = 0.0f;
-            if (s != 0.0f) {
-                rr = rintf(__fdiv_rn(xv, s));
-                rr = fminf(fmaxf(rr, -127.0f), 127.0f);
-            }
-            q = static_cast<signed char>(static_cast<int>(rr));
+            q = quant_code(xv, s, inv);
             d = Lp<ZERO_BF16>::narrow(__fmul_rn(static_cast<float>(q), s));
         };
         for (int v = lane; v < nv; v += 32) {

@@ -264,6 +264,37 @@ __device__ __forceinline__ void sq_accumulate(float g, float& hi, float& lo)
     lo = __fadd_rn(lo, __fadd_rn(e, pe));
 }
 
+// ------------------------------------------------------------- quantizer
+// Block-int8 code of x with scale s: clamp(round-half-even(x / s), -127, 127),
+// 0 when s == 0, where x / s is the IEEE-rounded quotient.  The quotient only
+// feeds a rounding to an integer, so x * (1/s) is used instead, and the exact
+// quotient only when that product lies within 2^-14 of a half-integer: the
+// product and the quotient differ by a few ulp of a value below 128 (an ulp
+// there is at most 2^-17), so away from a tie both round to the same integer.
+// inv = quant_reciprocal(s); 0 when 1/s is not a normal float (then every
+// code takes the exact quotient).
+__device__ __forceinline__ float quant_reciprocal(float s)
+{
+    if (!(s > 0.0f)) return 0.0f;
+    const float r = __frcp_rn(s);
+    return (r < 3.0e38f) ? r : 0.0f;
+}
+
+__device__ __forceinline__ int8_t quant_code(float x, float s, float inv)
+{
+    if (s == 0.0f) return 0;
+    float y;
+    if (inv != 0.0f) {
+        y = __fmul_rn(x, inv);
+        const float d = fabsf(__fsub_rn(__fsub_rn(y, floorf(y)), 0.5f));
+        if (d <= 6.103515625e-05f) y = __fdiv_rn(x, s);   // 2^-14: near a tie, decide exactly
+    } else {
+        y = __fdiv_rn(x, s);
+    }
+    const float q = fminf(fmaxf(rintf(y), -127.0f), 127.0f);
+    return static_cast<int8_t>(static_cast<int>(q));
+}
+
 __device__ __forceinline__ double warp_sum_f64(double x)
 {
 #pragma unroll

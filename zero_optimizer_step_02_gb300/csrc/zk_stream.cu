@@ -34,18 +34,42 @@ struct Shared {
 };
 static_assert(sizeof(Shared) <= kStageOffset, "shared header too large");
 
-// tile -> (first element, valid length); see StreamArgs
-__device__ __forceinline__ void tile_span(const StreamArgs& a, long long tile, long long& j0, int& len)
-{
-    const long long seg = tile / a.tiles_per_seg;
-    const long long t = tile - seg * a.tiles_per_seg;
-    const long long lo = a.base + seg * a.seg_stride;
-    long long hi = lo + a.seg_len;
-    if (hi > a.limit) hi = a.limit;
-    j0 = lo + t * kTile;
-    const long long l = hi - j0;
-    len = l <= 0 ? 0 : (l > kTile ? kTile : static_cast<int>(l));
-}
+// Walks this CTA's tiles (blockIdx.x, + gridDim.x, ...) as (segment, tile in
+// segment) without a 64-bit division per tile: one division at the start,
+// then an add-and-carry per step.
+struct TileCursor {
+    long long seg, t;        // current tile = seg * tiles_per_seg + t
+    long long dseg, dt;      // gridDim.x split the same way
+
+    __device__ __forceinline__ void start(const StreamArgs& a)
+    {
+        const long long first = blockIdx.x, step = gridDim.x;
+        seg = first / a.tiles_per_seg;
+        t = first - seg * a.tiles_per_seg;
+        dseg = step / a.tiles_per_seg;
+        dt = step - dseg * a.tiles_per_seg;
+    }
+    __device__ __forceinline__ bool valid(const StreamArgs& a) const { return seg < a.n_seg; }
+    __device__ __forceinline__ void next(const StreamArgs& a)
+    {
+        seg += dseg;
+        t += dt;
+        if (t >= a.tiles_per_seg) {
+            t -= a.tiles_per_seg;
+            seg += 1;
+        }
+    }
+    // first element and valid length of the current tile
+    __device__ __forceinline__ void span(const StreamArgs& a, long long& j0, int& len) const
+    {
+        const long long lo = a.base + seg * a.seg_stride;
+        long long hi = lo + a.seg_len;
+        if (hi > a.limit) hi = a.limit;
+        j0 = lo + t * kTile;
+        const long long l = hi - j0;
+        len = l <= 0 ? 0 : (l > kTile ? kTile : static_cast<int>(l));
+    }
+};
 
 template <int GT>
 __device__ __forceinline__ void add_slice(float (&acc)[4], uint2 w)
@@ -87,7 +111,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
     __syncthreads();
     if (sh->c.skip) return;  // uniform: a flagged loss-scaling step writes nothing
 
-    const long long ntiles = a.tiles_per_seg * a.n_seg;
     const int n_groups = a.n_ranks > 0 ? (a.n_ranks + kGroupRanks - 1) / kGroupRanks : 1;
     const int rank_slots = a.n_ranks < kGroupRanks ? a.n_ranks : kGroupRanks;
     const uint32_t side_off = static_cast<uint32_t>(rank_slots) * kTile * sizeof(uint16_t);
@@ -101,11 +124,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
             const uint64_t pol = l2_policy_evict_first();
             int s = 0;
             uint32_t ph = 0;
-            for (long long tile = blockIdx.x; tile < ntiles && !*reinterpret_cast<volatile int*>(&sh->abort);
-                 tile += gridDim.x) {
+            TileCursor cur;
+            for (cur.start(a); cur.valid(a) && !*reinterpret_cast<volatile int*>(&sh->abort); cur.next(a)) {
                 long long j0;
                 int len;
-                tile_span(a, tile, j0, len);
+                cur.span(a, j0, len);
                 if (len != kTile || !a.tma_ok) continue;
                 for (int g = 0; g < n_groups; ++g) {
                     if (!mbar_wait_bounded(&sh->empty[s], ph ^ 1u, &sh->abort, a.timeout_ns)) {
@@ -147,15 +170,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
         const StepConsts c = sh->c;
         const bool detect = (a.flags & (F_DETECT | F_SQNORM)) != 0;
         const bool want_sq = (a.flags & F_SQNORM) != 0;
-        for (long long tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        TileCursor cur;
+        for (cur.start(a); cur.valid(a); cur.next(a)) {
             long long j0;
             int len;
-            tile_span(a, tile, j0, len);
+            cur.span(a, j0, len);
             if (len <= 0) {
-                if (quant && tid == 0) {
-                    const long long seg = tile / a.tiles_per_seg;
-                    a.q_scales[seg * a.q_blocks_per_shard + (tile - seg * a.tiles_per_seg)] = 0.0f;
-                }
+                if (quant && tid == 0) a.q_scales[cur.seg * a.q_blocks_per_shard + cur.t] = 0.0f;
                 continue;
             }
             const bool fast = len == kTile && a.tma_ok;
@@ -323,10 +344,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
 #pragma unroll
                 for (int w = 0; w < kConsumerWarps; ++w) amax = fmaxf(amax, sh->red_f[par][w]);
                 const float scale = __fdiv_rn(amax, 127.0f);
-                if (tid == 0 && alive) {
-                    const long long seg = tile / a.tiles_per_seg;
-                    a.q_scales[seg * a.q_blocks_per_shard + (tile - seg * a.tiles_per_seg)] = scale;
-                }
+                if (tid == 0 && alive) a.q_scales[cur.seg * a.q_blocks_per_shard + cur.t] = scale;
+                const float inv_scale = quant_reciprocal(scale);
 #pragma unroll
                 for (int ch = 0; ch < kChunksPerThread; ++ch) {
                     const int q = ch * kConsumers + tid;
@@ -337,12 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
                     uint16_t dq[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        float r = 0.0f;
-                        if (scale != 0.0f) {
-                            r = rintf(__fdiv_rn(xq[ch][e], scale));
-                            r = fminf(fmaxf(r, -127.0f), 127.0f);
-                        }
-                        code[e] = static_cast<int8_t>(static_cast<int>(r));
+                        code[e] = quant_code(xq[ch][e], scale, inv_scale);
                         dq[e] = Lp<ZERO_BF16>::narrow(__fmul_rn(static_cast<float>(code[e]), scale));
                     }
                     if (!alive) continue;
