@@ -115,7 +115,9 @@ typedef struct {
     int overflow;         /* 1 if the latest step was skipped                      */
     int status;           /* sticky ZERO_DEV_* bits                                */
     int nonfinite;        /* internal: the step in flight saw a non-finite value   */
-    int reserved[2];
+    unsigned int ctas_done; /* internal: CTAs of the kernel in flight that finished;
+                               0 between calls                                     */
+    int reserved;
 } zero_dev_scalars;
 
 /* ---------------------------------------------------------------- misc --- */

@@ -43,7 +43,7 @@ class ZeroDevScalars(ctypes.Structure):
     _fields_ = [("t", ctypes.c_longlong), ("beta1_pow", ctypes.c_double), ("beta2_pow", ctypes.c_double),
                 ("sqnorm", ctypes.c_double), ("loss_scale", ctypes.c_float), ("clip_coef", ctypes.c_float),
                 ("good_steps", ctypes.c_int), ("overflow", ctypes.c_int), ("status", ctypes.c_int),
-                ("nonfinite", ctypes.c_int), ("reserved", ctypes.c_int * 2)]
+                ("nonfinite", ctypes.c_int), ("ctas_done", ctypes.c_uint), ("reserved", ctypes.c_int)]
 
 
 if not os.path.exists(LIB_PATH):

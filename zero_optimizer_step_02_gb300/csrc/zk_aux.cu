@@ -53,39 +53,8 @@ cudaError_t launch_scalars_init(zero_dev_scalars* sc, float loss_scale, cudaStre
     return cudaGetLastError();
 }
 
-// Commit (or skip) the step: the loss-scaling reading -- a step whose reduced
-// gradient held a non-finite value leaves the state alone, halves the scale
-// (floor min_scale) and resets the good-step count; otherwise t advances, the
-// beta powers take one more factor, and after scale_window good steps the
-// scale doubles.
-__global__ void k_epilogue(zero_hparams hp, zero_dev_scalars* sc)
-{
-    const bool skip = hp.loss_scaling && sc->nonfinite != 0;
-    if (skip) {
-        const float half = __fmul_rn(sc->loss_scale, 0.5f);
-        sc->loss_scale = half > hp.min_scale ? half : hp.min_scale;
-        sc->good_steps = 0;
-        sc->overflow = 1;
-        sc->clip_coef = 1.0f;
-    } else {
-        sc->t += 1;
-        sc->beta1_pow = __dmul_rn(sc->beta1_pow, static_cast<double>(hp.beta1));
-        sc->beta2_pow = __dmul_rn(sc->beta2_pow, static_cast<double>(hp.beta2));
-        sc->overflow = 0;
-        if (hp.loss_scaling) {
-            sc->good_steps += 1;
-            if (sc->good_steps >= hp.scale_window) {
-                sc->loss_scale = __fmul_rn(sc->loss_scale, 2.0f);
-                sc->good_steps = 0;
-            }
-        }
-    }
-    if (!(hp.max_norm > 0.0f)) {
-        sc->sqnorm = 0.0;
-        sc->clip_coef = 1.0f;
-    }
-    sc->nonfinite = 0;
-}
+// Commits (or skips) the step: commit_scalars in zk_common.cuh.
+__global__ void k_epilogue(zero_hparams hp, zero_dev_scalars* sc) { commit_scalars(hp, sc); }
 
 cudaError_t launch_epilogue(const zero_hparams& hp, zero_dev_scalars* sc, cudaStream_t st)
 {
@@ -106,13 +75,7 @@ __global__ void k_finalize(const double* partials, int n, zero_hparams hp, zero_
     x = warp_sum_f64(x);
     if (threadIdx.x == 0) {
         sc->sqnorm = x;
-        float coef = 1.0f;
-        if (hp.max_norm > 0.0f) {
-            const double norm = __dsqrt_rn(x);
-            const float c = __double2float_rn(__ddiv_rn(static_cast<double>(hp.max_norm), __dadd_rn(norm, 1e-6)));
-            if (c < 1.0f) coef = c;
-        }
-        sc->clip_coef = coef;
+        sc->clip_coef = clip_coefficient(hp.max_norm, x);
     }
 }
 

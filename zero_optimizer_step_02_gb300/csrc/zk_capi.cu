@@ -122,7 +122,7 @@ int reduce_grid(long long n)
 // One reduce pass over [0, psi): optional fp32 output, squared-norm partials,
 // non-finite detection in loss-scaling mode.
 zero_status run_reduce(const zero_plan* p, const zero_hparams* hp, const void* const* ranks, float* out,
-                       bool sqnorm, void* ws, zero_dev_scalars* sc, cudaStream_t st)
+                       bool sqnorm, void* ws, zero_dev_scalars* sc, cudaStream_t st, int* grid_out = nullptr)
 {
     StreamArgs a = base_args(p, hp, sc);
     set_ranks(a, p, ranks);
@@ -132,18 +132,31 @@ zero_status run_reduce(const zero_plan* p, const zero_hparams* hp, const void* c
     a.partials = sqnorm ? partials_of(ws) : nullptr;
     a.flags = (sqnorm ? zk::F_SQNORM : 0) | (hp->loss_scaling ? (zk::F_DETECT | zk::F_LSCALE) : 0);
     if (out != nullptr && !aligned(out, 16)) a.tma_ok = 0;
-    return from_cuda(zk::launch_stream(zk::OP_REDUCE, p->grad_dtype, p->param_dtype, a, st));
+    const zero_status s = from_cuda(zk::launch_stream(zk::OP_REDUCE, p->grad_dtype, p->param_dtype, a, st));
+    if (grid_out != nullptr) *grid_out = a.grid;
+    return s;
 }
 
+// F_FINALIZE inputs: the partial sums a reduce pass left in the workspace
+void set_finalize(StreamArgs& a, void* ws, int n)
+{
+    a.fin_partials = partials_of(ws);
+    a.fin_n = n;
+}
+
+// flags may hold F_EPILOGUE (given to the last bucket only) and F_FINALIZE
+// (fin_ws / fin_n: the partials of the preceding reduce pass)
 zero_status run_fused(const zero_plan* p, const zero_hparams* hp, const void* const* ranks, const float* mi,
                       const float* m_in, const float* vi, float* mo, float* m_out, float* vo, void* lp,
-                      int flags, zero_dev_scalars* sc, cudaStream_t st)
+                      int flags, zero_dev_scalars* sc, cudaStream_t st, void* fin_ws = nullptr, int fin_n = 0)
 {
     // buckets only when no global check ties the pieces together
-    const long long step = (flags & (zk::F_CLIP | zk::F_GUARD | zk::F_DETECT)) ? p->psi : p->bucket;
+    const long long step =
+        (flags & (zk::F_CLIP | zk::F_GUARD | zk::F_DETECT | zk::F_FINALIZE)) ? p->psi : p->bucket;
     for (long long lo = 0; lo < p->psi; lo += step) {
         const long long hi = lo + step < p->psi ? lo + step : p->psi;
         StreamArgs a = base_args(p, hp, sc);
+        if (flags & zk::F_FINALIZE) set_finalize(a, fin_ws, fin_n);
         set_ranks(a, p, ranks);
         set_flat(a, lo, hi);
         a.n_side = 3;
@@ -154,7 +167,7 @@ zero_status run_fused(const zero_plan* p, const zero_hparams* hp, const void* co
         a.out_f32[1] = m_out;
         a.out_f32[2] = vo;
         a.out_lp = lp;
-        a.flags = flags;
+        a.flags = hi == p->psi ? flags : (flags & ~zk::F_EPILOGUE);
         const zero_status s = from_cuda(zk::launch_stream(zk::OP_FUSED, p->grad_dtype, p->param_dtype, a, st));
         if (s != ZERO_OK) return s;
     }
@@ -163,9 +176,10 @@ zero_status run_fused(const zero_plan* p, const zero_hparams* hp, const void* co
 
 zero_status run_adam(const zero_plan* p, const zero_hparams* hp, const float* g, const float* mi,
                      const float* m_in, const float* vi, float* mo, float* m_out, float* vo, void* lp, int flags,
-                     zero_dev_scalars* sc, cudaStream_t st)
+                     zero_dev_scalars* sc, cudaStream_t st, void* fin_ws = nullptr, int fin_n = 0)
 {
     StreamArgs a = base_args(p, hp, sc);
+    if (flags & zk::F_FINALIZE) set_finalize(a, fin_ws, fin_n);
     set_flat(a, 0, p->psi);
     a.n_ranks = 0;
     a.n_side = 4;
@@ -363,9 +377,9 @@ ZERO_API zero_status zero_adam_shard_step(const zero_plan* p, const zero_hparams
     if ((s = check_state(master, m, v, master, m, v)) != ZERO_OK) return s;
     if (lp_out != nullptr && !aligned(lp_out, 16)) return ZERO_ERR_MISALIGNED;
     const cudaStream_t st = as_stream(stream);
-    const int flags = (hp->max_norm > 0.0f ? zk::F_CLIP : 0) | (hp->loss_scaling ? zk::F_GUARD : 0);
-    if ((s = run_adam(p, hp, grad_shards, master, m, v, master, m, v, lp_out, flags, sc, st)) != ZERO_OK) return s;
-    return from_cuda(zk::launch_epilogue(*hp, sc, st));
+    const int flags =
+        (hp->max_norm > 0.0f ? zk::F_CLIP : 0) | (hp->loss_scaling ? zk::F_GUARD : 0) | zk::F_EPILOGUE;
+    return run_adam(p, hp, grad_shards, master, m, v, master, m, v, lp_out, flags, sc, st);
 }
 
 ZERO_API zero_status zero_all_gather(const zero_plan* p, const void* const* shards, void* gathered,
@@ -402,34 +416,41 @@ ZERO_API zero_status zero_step_fused(const zero_plan* p, const zero_hparams* hp,
     if ((clip || ls) && (s = check_dev(ws, 256)) != ZERO_OK) return s;
     const cudaStream_t st = as_stream(stream);
     const int lsf = ls ? zk::F_LSCALE : 0;
+    // the kernel that ends the step commits the scalars itself (F_EPILOGUE),
+    // except when a repair pass still has to read the step's overflow flag
+    const bool speculative = ls && !inplace;
+    const int epi = speculative ? 0 : zk::F_EPILOGUE;
 
     if (!clip) {
         if (!ls) {
-            if ((s = run_fused(p, hp, ranks, mi, m_in, vi, mo, m_out, vo, lp, 0, sc, st)) != ZERO_OK) return s;
-        } else if (!inplace) {
-            // speculative: update while detecting; undo from the in state if flagged
+            if ((s = run_fused(p, hp, ranks, mi, m_in, vi, mo, m_out, vo, lp, epi, sc, st)) != ZERO_OK) return s;
+        } else if (speculative) {
+            // update while detecting; undo from the in state if flagged
             if ((s = run_fused(p, hp, ranks, mi, m_in, vi, mo, m_out, vo, lp, zk::F_DETECT | lsf, sc, st)) != ZERO_OK) return s;
-            ZK_TRY(zk::launch_repair(*hp, mi, m_in, vi, mo, m_out, vo, lp, p->param_dtype, p->psi, sc, st));
         } else {
             // in place: a read-only check pass first, then the guarded update
             if ((s = run_reduce(p, hp, ranks, nullptr, false, ws, sc, st)) != ZERO_OK) return s;
-            if ((s = run_fused(p, hp, ranks, mi, m_in, vi, mo, m_out, vo, lp, zk::F_GUARD | lsf, sc, st)) != ZERO_OK) return s;
+            if ((s = run_fused(p, hp, ranks, mi, m_in, vi, mo, m_out, vo, lp, zk::F_GUARD | lsf | epi, sc, st)) != ZERO_OK) return s;
         }
     } else {
+        // the update kernel finishes the reduce pass's norm in its prologue
         const int guard = ls ? zk::F_GUARD : 0;
+        int n = 0;
         if (clip_materialises(p)) {
             float* g = ghat_of(ws);
-            if ((s = run_reduce(p, hp, ranks, g, true, ws, sc, st)) != ZERO_OK) return s;
-            ZK_TRY(zk::launch_finalize_sqnorm(partials_of(ws), reduce_grid(p->psi), *hp, sc, st));
-            if ((s = run_adam(p, hp, g, mi, m_in, vi, mo, m_out, vo, lp, zk::F_CLIP | guard, sc, st)) != ZERO_OK) return s;
+            if ((s = run_reduce(p, hp, ranks, g, true, ws, sc, st, &n)) != ZERO_OK) return s;
+            if ((s = run_adam(p, hp, g, mi, m_in, vi, mo, m_out, vo, lp, zk::F_CLIP | zk::F_FINALIZE | guard | epi, sc,
+                              st, ws, n)) != ZERO_OK)
+                return s;
         } else {
-            if ((s = run_reduce(p, hp, ranks, nullptr, true, ws, sc, st)) != ZERO_OK) return s;
-            ZK_TRY(zk::launch_finalize_sqnorm(partials_of(ws), reduce_grid(p->psi), *hp, sc, st));
-            if ((s = run_fused(p, hp, ranks, mi, m_in, vi, mo, m_out, vo, lp, zk::F_CLIP | guard | lsf, sc, st)) != ZERO_OK) return s;
+            if ((s = run_reduce(p, hp, ranks, nullptr, true, ws, sc, st, &n)) != ZERO_OK) return s;
+            if ((s = run_fused(p, hp, ranks, mi, m_in, vi, mo, m_out, vo, lp,
+                               zk::F_CLIP | zk::F_FINALIZE | guard | lsf | epi, sc, st, ws, n)) != ZERO_OK)
+                return s;
         }
-        if (ls && !inplace)
-            ZK_TRY(zk::launch_repair(*hp, mi, m_in, vi, mo, m_out, vo, lp, p->param_dtype, p->psi, sc, st));
     }
+    if (!speculative) return ZERO_OK;
+    ZK_TRY(zk::launch_repair(*hp, mi, m_in, vi, mo, m_out, vo, lp, p->param_dtype, p->psi, sc, st));
     return from_cuda(zk::launch_epilogue(*hp, sc, st));
 }
 
@@ -488,9 +509,8 @@ ZERO_API zero_status zero_step_fused_qgather(const zero_plan* p, const zero_hpar
     a.q_codes = codes;
     a.q_scales = scales;
     a.q_gathered = gathered;
-    a.flags = zk::F_QUANT;
-    ZK_TRY(zk::launch_stream(zk::OP_FUSED, p->grad_dtype, p->param_dtype, a, st));
-    return from_cuda(zk::launch_epilogue(*hp, sc, st));
+    a.flags = zk::F_QUANT | zk::F_EPILOGUE;
+    return from_cuda(zk::launch_stream(zk::OP_FUSED, p->grad_dtype, p->param_dtype, a, st));
 }
 
 ZERO_API zero_status zero_debug_wait_timeout(zero_dev_scalars* sc, long long timeout_ns, void* stream)

@@ -39,6 +39,8 @@ enum : int {
     F_CLIP = 1 << 3,    // multiply the gradient by scalars->clip_coef
     F_QUANT = 1 << 4,   // fused block-int8 quantized gather epilogue
     F_LSCALE = 1 << 5,  // divisor includes scalars->loss_scale
+    F_FINALIZE = 1 << 6,  // every CTA sums the reduce pass's partials itself (clip coefficient)
+    F_EPILOGUE = 1 << 7,  // the last CTA to finish commits the step scalars
 };
 
 // ------------------------------------------------------------- PTX wrappers
@@ -262,6 +264,50 @@ __device__ __forceinline__ void sq_accumulate(float g, float& hi, float& lo)
     const float e = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(p, bp));
     hi = s;
     lo = __fadd_rn(lo, __fadd_rn(e, pe));
+}
+
+// Clip coefficient of the clipping reading: max_norm / (norm + 1e-6) when
+// that is below one, else 1 (and 1 when clipping is off).
+__device__ __forceinline__ float clip_coefficient(float max_norm, double sqnorm)
+{
+    if (!(max_norm > 0.0f)) return 1.0f;
+    const double norm = __dsqrt_rn(sqnorm);
+    const float c = __double2float_rn(__ddiv_rn(static_cast<double>(max_norm), __dadd_rn(norm, 1e-6)));
+    return c < 1.0f ? c : 1.0f;
+}
+
+// Commit (or skip) the step, per the loss-scaling reading: a step whose
+// reduced gradient held a non-finite value leaves the state alone, halves
+// the scale (floor min_scale) and resets the good-step count; otherwise t
+// advances, the beta powers take one more factor, and after scale_window
+// good steps the scale doubles.  Clears the step's non-finite flag.
+__device__ __forceinline__ void commit_scalars(const zero_hparams& hp, zero_dev_scalars* sc)
+{
+    const bool skip = hp.loss_scaling && *reinterpret_cast<volatile int*>(&sc->nonfinite) != 0;
+    if (skip) {
+        const float half = __fmul_rn(sc->loss_scale, 0.5f);
+        sc->loss_scale = half > hp.min_scale ? half : hp.min_scale;
+        sc->good_steps = 0;
+        sc->overflow = 1;
+        sc->clip_coef = 1.0f;
+    } else {
+        sc->t += 1;
+        sc->beta1_pow = __dmul_rn(sc->beta1_pow, static_cast<double>(hp.beta1));
+        sc->beta2_pow = __dmul_rn(sc->beta2_pow, static_cast<double>(hp.beta2));
+        sc->overflow = 0;
+        if (hp.loss_scaling) {
+            sc->good_steps += 1;
+            if (sc->good_steps >= hp.scale_window) {
+                sc->loss_scale = __fmul_rn(sc->loss_scale, 2.0f);
+                sc->good_steps = 0;
+            }
+        }
+    }
+    if (!(hp.max_norm > 0.0f)) {
+        sc->sqnorm = 0.0;
+        sc->clip_coef = 1.0f;
+    }
+    sc->nonfinite = 0;
 }
 
 // ------------------------------------------------------------- quantizer

@@ -25,6 +25,8 @@ struct StreamArgs {
     void* q_gathered;
     zero_dev_scalars* sc;
     double* partials;                  // OP_REDUCE + F_SQNORM: one fp64 per CTA
+    const double* fin_partials;        // F_FINALIZE: the reduce pass's partials ...
+    int fin_n;                         // ... and how many
     long long base, seg_stride, seg_len, limit, tiles_per_seg, q_blocks_per_shard;
     int n_seg;
     int n_ranks;                       // rank streams (0 for OP_ADAM)

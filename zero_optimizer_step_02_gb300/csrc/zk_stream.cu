@@ -91,25 +91,44 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
     const int lane = tid & 31;
     const bool quant = (OP == OP_FUSED) && (a.flags & F_QUANT);
 
-    if (tid == 0) {
-        for (int s = 0; s < a.stages; ++s) {
-            mbar_init(&sh->full[s], 1);
-            mbar_init(&sh->empty[s], kConsumerWarps);
-            sh->issued_parity[s] = -1;
+    if (warp == 0) {
+        // F_FINALIZE: the whole warp sums the reduce pass's per-CTA partials in
+        // the order k_finalize uses, so every CTA gets the same bits
+        double sq = 0.0;
+        if (a.flags & F_FINALIZE) {
+            for (int i = lane; i < a.fin_n; i += 32) sq = __dadd_rn(sq, a.fin_partials[i]);
+            sq = warp_sum_f64(sq);
         }
-        sh->abort = 0;
-        StepConsts c = {};
-        const zero_dev_scalars* sc = a.sc;
-        c.skip = (a.flags & F_GUARD) ? (sc->nonfinite != 0) : 0;
-        set_divisor(c, a.n_ranks > 0 ? a.n_ranks : 1, (a.flags & F_LSCALE) ? sc->loss_scale : 1.0f);
-        set_adam(c, a.hp, sc->beta1_pow, sc->beta2_pow);
-        c.clip = (a.flags & F_CLIP) != 0;
-        c.coef = c.clip ? sc->clip_coef : 1.0f;
-        sh->c = c;
-        fence_barrier_init();
+        if (lane == 0) {
+            for (int s = 0; s < a.stages; ++s) {
+                mbar_init(&sh->full[s], 1);
+                mbar_init(&sh->empty[s], kConsumerWarps);
+                sh->issued_parity[s] = -1;
+            }
+            sh->abort = 0;
+            StepConsts c = {};
+            zero_dev_scalars* sc = a.sc;
+            c.skip = (a.flags & F_GUARD) ? (sc->nonfinite != 0) : 0;
+            set_divisor(c, a.n_ranks > 0 ? a.n_ranks : 1, (a.flags & F_LSCALE) ? sc->loss_scale : 1.0f);
+            set_adam(c, a.hp, sc->beta1_pow, sc->beta2_pow);
+            c.clip = (a.flags & F_CLIP) != 0;
+            if (a.flags & F_FINALIZE) {
+                const float coef = clip_coefficient(a.hp.max_norm, sq);
+                c.coef = c.clip ? coef : 1.0f;
+                if (blockIdx.x == 0) {
+                    sc->sqnorm = sq;
+                    sc->clip_coef = coef;
+                }
+            } else {
+                c.coef = c.clip ? sc->clip_coef : 1.0f;
+            }
+            sh->c = c;
+            fence_barrier_init();
+        }
     }
     __syncthreads();
-    if (sh->c.skip) return;  // uniform: a flagged loss-scaling step writes nothing
+    // a flagged loss-scaling step writes nothing (uniform over the CTA)
+    const bool skip = sh->c.skip != 0;
 
     const int n_groups = a.n_ranks > 0 ? (a.n_ranks + kGroupRanks - 1) / kGroupRanks : 1;
     const int rank_slots = a.n_ranks < kGroupRanks ? a.n_ranks : kGroupRanks;
@@ -118,7 +137,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
     bool nonfinite = false;
     float sq_hi = 0.0f, sq_lo = 0.0f;
 
-    if (warp == kConsumerWarps) {
+    if (skip) {
+        // nothing to do; fall through to the end (the epilogue still runs)
+    } else if (warp == kConsumerWarps) {
         // ------------------------------------------------------- producer
         if (lane == 0) {
             const uint64_t pol = l2_policy_evict_first();
@@ -405,6 +426,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
             if (sh->issued_parity[s] >= 0)
                 mbar_wait_bounded(&sh->full[s], static_cast<uint32_t>(sh->issued_parity[s]), nullptr, a.timeout_ns);
         atomicOr(&a.sc->status, ZERO_DEV_TIMEOUT);
+    }
+    if (a.flags & F_EPILOGUE) {
+        // the last CTA to finish commits the step scalars: every CTA read them
+        // in its prologue before taking its ticket (no CTA waits for another)
+        if (tid == 0) {
+            __threadfence();
+            const unsigned done = atomicAdd(&a.sc->ctas_done, 1u);
+            if (done == gridDim.x - 1) {
+                __threadfence();
+                commit_scalars(a.hp, a.sc);
+                a.sc->ctas_done = 0u;
+            }
+        }
     }
 }
 
