@@ -214,7 +214,6 @@ __global__ void __launch_bounds__(kAgThreads) k_all_gather(const __grid_constant
     if (threadIdx.x < 32) {
         if (threadIdx.x == 0 && a.tma_ok) {
             // one thread drives the ring: bulk load tile -> stage, bulk store stage -> gathered
-            const uint64_t pol = l2_policy_evict_first();
             auto next_full = [&](long long t) {
                 for (; t < ntiles; t += gridDim.x) {
                     int r;
@@ -231,8 +230,7 @@ __global__ void __launch_bounds__(kAgThreads) k_all_gather(const __grid_constant
                 int len;
                 ag_span(a, t, r, i0, len);
                 mbar_arrive_expect_tx(&full[s], kAgTile * 2);
-                bulk_load(ring + s * (kAgTile * 2), static_cast<const uint16_t*>(a.shard[r]) + i0, kAgTile * 2,
-                          &full[s], pol);
+                bulk_load(ring + s * (kAgTile * 2), static_cast<const uint16_t*>(a.shard[r]) + i0, kAgTile * 2, &full[s]);
                 issued[s] = static_cast<int>(ph);
             };
             long long load_t = next_full(blockIdx.x);

@@ -478,7 +478,7 @@ ZERO_API zero_status zero_step_fused_qgather(const zero_plan* p, const zero_hpar
     if (p == nullptr) return ZERO_ERR_INVALID_ARG;
     zero_status s;
     if ((s = check_hparams(hp)) != ZERO_OK) return s;
-    if (block != zk::kTile) return ZERO_ERR_UNSUPPORTED;
+    if (block != zk::kQuantBlock) return ZERO_ERR_UNSUPPORTED;
     if (hp->max_norm > 0.0f || hp->loss_scaling) return ZERO_ERR_UNSUPPORTED;
     if (p->param_dtype != ZERO_BF16) return ZERO_ERR_UNSUPPORTED;
     if ((s = check_ranks(p, ranks)) != ZERO_OK) return s;
@@ -497,7 +497,7 @@ ZERO_API zero_status zero_step_fused_qgather(const zero_plan* p, const zero_hpar
     a.limit = p->psi;
     a.n_seg = p->n_d;
     a.tiles_per_seg = tiles_of(p->shard);
-    a.q_blocks_per_shard = a.tiles_per_seg;
+    a.q_blocks_per_shard = (p->shard + zk::kQuantBlock - 1) / zk::kQuantBlock;
     a.tma_ok = (p->shard % 8) == 0 ? 1 : 0;
     a.n_side = 3;
     a.side[0] = mi;
@@ -510,7 +510,7 @@ ZERO_API zero_status zero_step_fused_qgather(const zero_plan* p, const zero_hpar
     a.q_scales = scales;
     a.q_gathered = gathered;
     a.flags = zk::F_QUANT | zk::F_EPILOGUE;
-    return from_cuda(zk::launch_stream(zk::OP_FUSED, p->grad_dtype, p->param_dtype, a, st));
+    return from_cuda(zk::launch_stream(zk::OP_QFUSED, p->grad_dtype, p->param_dtype, a, st));
 }
 
 ZERO_API zero_status zero_debug_wait_timeout(zero_dev_scalars* sc, long long timeout_ns, void* stream)

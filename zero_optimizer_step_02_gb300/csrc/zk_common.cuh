@@ -17,13 +17,14 @@
 namespace zk {
 
 // ------------------------------------------------------------------ geometry
-constexpr int kTile = 2048;                 // elements per tile of the streaming engine
+constexpr int kTile = 4096;                 // elements per tile of the streaming engine
 constexpr int kConsumerWarps = 16;         // one 4-element chunk per consumer thread per tile
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;   // + one producer warp
 constexpr int kChunk = 4;                   // consecutive elements per consumer chunk
 constexpr int kChunksPerThread = kTile / (kChunk * kConsumers);
 static_assert(kChunksPerThread * kChunk * kConsumers == kTile, "tile / consumer mismatch");
+constexpr int kQuantBlock = kChunk * kConsumers;  // fused int8 gather: one block per chunk row (2048)
 constexpr int kGroupRanks = 8;              // rank slices per pipeline stage
 constexpr int kMaxSide = 4;                 // fp32 side streams (g, master, m, v)
 constexpr int kMaxStages = 8;
@@ -113,22 +114,16 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     return false;
 }
 
-__device__ __forceinline__ uint64_t l2_policy_evict_first()
-{
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
 // 1-D bulk copy global -> this CTA's shared memory, completing on `bar`.
-// Both addresses 16-byte aligned, bytes a multiple of 16.
+// Both addresses 16-byte aligned, bytes a multiple of 16.  (An L2
+// evict-first hint on these streamed loads measured no better, or worse.)
 __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src, uint32_t bytes,
-                                          uint64_t* bar, uint64_t policy)
+                                          uint64_t* bar)
 {
     asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(smem_dst)),
-        "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1], %2, [%3];" ::"r"(smem_u32(smem_dst)),
+        "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
 }
 

@@ -7,7 +7,7 @@
 
 namespace zk {
 
-enum { OP_FUSED = 0, OP_REDUCE = 1, OP_ADAM = 2 };
+enum { OP_FUSED = 0, OP_REDUCE = 1, OP_ADAM = 2, OP_QFUSED = 3 /* fused step + int8 gather epilogue */ };
 
 // Arguments of one launch of the streaming engine (kernel parameter space).
 //

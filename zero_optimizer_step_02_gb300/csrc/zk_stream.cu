@@ -29,7 +29,7 @@ struct Shared {
     int abort;
     int pad0;
     StepConsts c;
-    float red_f[2][kConsumerWarps];
+    float red_f[2][kChunksPerThread][kConsumerWarps];
     double red_d[kConsumerWarps + 1];
 };
 static_assert(sizeof(Shared) <= kStageOffset, "shared header too large");
@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    const bool quant = (OP == OP_FUSED) && (a.flags & F_QUANT);
+    constexpr bool quant = OP == OP_QFUSED;
 
     if (warp == 0) {
         // F_FINALIZE: the whole warp sums the reduce pass's per-CTA partials in
@@ -142,7 +142,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
     } else if (warp == kConsumerWarps) {
         // ------------------------------------------------------- producer
         if (lane == 0) {
-            const uint64_t pol = l2_policy_evict_first();
             int s = 0;
             uint32_t ph = 0;
             TileCursor cur;
@@ -165,12 +164,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
                     mbar_arrive_expect_tx(&sh->full[s], bytes);
                     for (int k = 0; k < nr; ++k)
                         bulk_load(st + k * rank_bytes,
-                                  static_cast<const uint16_t*>(a.rank[r0 + k]) + j0, rank_bytes,
-                                  &sh->full[s], pol);
+                                  static_cast<const uint16_t*>(a.rank[r0 + k]) + j0, rank_bytes, &sh->full[s]);
                     if (last)
                         for (int k = 0; k < a.n_side; ++k)
-                            bulk_load(st + side_off + k * kTile * 4u, a.side[k] + j0, kTile * 4u,
-                                      &sh->full[s], pol);
+                            bulk_load(st + side_off + k * kTile * 4u, a.side[k] + j0, kTile * 4u, &sh->full[s]);
                     sh->issued_parity[s] = static_cast<int>(ph);
                     if (++s == a.stages) {
                         s = 0;
@@ -197,7 +194,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
             int len;
             cur.span(a, j0, len);
             if (len <= 0) {
-                if (quant && tid == 0) a.q_scales[cur.seg * a.q_blocks_per_shard + cur.t] = 0.0f;
+                if (quant && tid == 0) {
+                    for (int ch = 0; ch < kChunksPerThread; ++ch) {
+                        const long long blk = cur.t * kChunksPerThread + ch;
+                        if (blk < a.q_blocks_per_shard) a.q_scales[cur.seg * a.q_blocks_per_shard + blk] = 0.0f;
+                    }
+                }
                 continue;
             }
             const bool fast = len == kTile && a.tma_ok;
@@ -346,29 +348,37 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
                 }
             }
 
-            if (quant) {
-                // block = this tile: amax over the consumers, then codes + dequantized bf16
-                float amax = 0.0f;
+            if constexpr (quant) {
+                // one quantization block per chunk row (all consumers x 4 elements):
+                // amax per row over the consumers, then codes + dequantized bf16
+                float amax[kChunksPerThread];
 #pragma unroll
-                for (int ch = 0; ch < kChunksPerThread; ++ch)
+                for (int ch = 0; ch < kChunksPerThread; ++ch) {
+                    amax[ch] = 0.0f;
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        if ((ch * kConsumers + tid) * 4 + e < len) amax = fmaxf(amax, fabsf(xq[ch][e]));
-                amax = warp_max_f32(amax);
+                        if ((ch * kConsumers + tid) * 4 + e < len) amax[ch] = fmaxf(amax[ch], fabsf(xq[ch][e]));
+                    amax[ch] = warp_max_f32(amax[ch]);
+                }
                 // two buffers used alternately: between two uses of one buffer every
                 // consumer has passed the barrier of the other, so reads are done
                 const int par = qiter & 1;
                 ++qiter;
-                if (lane == 0) sh->red_f[par][warp] = amax;
-                named_bar_sync(1, kConsumers);
-                amax = 0.0f;
+                if (lane == 0) {
 #pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) amax = fmaxf(amax, sh->red_f[par][w]);
-                const float scale = __fdiv_rn(amax, 127.0f);
-                if (tid == 0 && alive) a.q_scales[cur.seg * a.q_blocks_per_shard + cur.t] = scale;
-                const float inv_scale = quant_reciprocal(scale);
+                    for (int ch = 0; ch < kChunksPerThread; ++ch) sh->red_f[par][ch][warp] = amax[ch];
+                }
+                named_bar_sync(1, kConsumers);
 #pragma unroll
                 for (int ch = 0; ch < kChunksPerThread; ++ch) {
+                    float m = 0.0f;
+#pragma unroll
+                    for (int w = 0; w < kConsumerWarps; ++w) m = fmaxf(m, sh->red_f[par][ch][w]);
+                    const float scale = __fdiv_rn(m, 127.0f);
+                    const long long blk = cur.t * kChunksPerThread + ch;   // block index within the shard
+                    if (tid == 0 && alive && blk < a.q_blocks_per_shard)
+                        a.q_scales[cur.seg * a.q_blocks_per_shard + blk] = (len > ch * kQuantBlock) ? scale : 0.0f;
+                    const float inv_scale = quant_reciprocal(scale);
                     const int q = ch * kConsumers + tid;
                     const long long jc = j0 + q * 4;
                     int cnt = len - q * 4;
@@ -511,6 +521,9 @@ cudaError_t launch_stream(int op, int grad_dtype, int param_dtype, StreamArgs& a
         return gb ? launch_one<ZERO_BF16, ZERO_BF16, OP_REDUCE>(a, st) : launch_one<ZERO_FP16, ZERO_BF16, OP_REDUCE>(a, st);
     case OP_ADAM:
         return pb ? launch_one<ZERO_BF16, ZERO_BF16, OP_ADAM>(a, st) : launch_one<ZERO_BF16, ZERO_FP16, OP_ADAM>(a, st);
+    case OP_QFUSED:   // the int8 gather reads bf16 parameters only
+        if (!pb) return cudaErrorInvalidValue;
+        return gb ? launch_one<ZERO_BF16, ZERO_BF16, OP_QFUSED>(a, st) : launch_one<ZERO_FP16, ZERO_BF16, OP_QFUSED>(a, st);
     default:
         return cudaErrorInvalidValue;
     }
