@@ -321,6 +321,31 @@ __device__ __forceinline__ float quant_reciprocal(float s)
     return (r < 3.0e38f) ? r : 0.0f;
 }
 
+// Codes of four values at once: the fast products for all four, and one
+// (rarely taken) branch to the exact quotients if any of them is near a tie.
+__device__ __forceinline__ void quant_code4(const float (&x)[4], float s, float inv, int8_t (&q)[4])
+{
+    if (s == 0.0f) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) q[e] = 0;
+        return;
+    }
+    float y[4];
+    bool near = inv == 0.0f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        y[e] = __fmul_rn(x[e], inv);
+        const float d = fabsf(__fsub_rn(__fsub_rn(y[e], floorf(y[e])), 0.5f));
+        near |= d <= 6.103515625e-05f;   // 2^-14
+    }
+    if (near) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) y[e] = __fdiv_rn(x[e], s);
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) q[e] = static_cast<int8_t>(static_cast<int>(fminf(fmaxf(rintf(y[e]), -127.0f), 127.0f)));
+}
+
 __device__ __forceinline__ int8_t quant_code(float x, float s, float inv)
 {
     if (s == 0.0f) return 0;

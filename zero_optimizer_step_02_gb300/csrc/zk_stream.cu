@@ -29,7 +29,7 @@ struct Shared {
     int abort;
     int pad0;
     StepConsts c;
-    float red_f[2][kChunksPerThread][kConsumerWarps];
+    alignas(16) float red_f[2][kChunksPerThread][kConsumerWarps];
     double red_d[kConsumerWarps + 1];
 };
 static_assert(sizeof(Shared) <= kStageOffset, "shared header too large");
@@ -372,8 +372,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
 #pragma unroll
                 for (int ch = 0; ch < kChunksPerThread; ++ch) {
                     float m = 0.0f;
+                    const float4* rv = reinterpret_cast<const float4*>(sh->red_f[par][ch]);
 #pragma unroll
-                    for (int w = 0; w < kConsumerWarps; ++w) m = fmaxf(m, sh->red_f[par][ch][w]);
+                    for (int w = 0; w < kConsumerWarps / 4; ++w) {
+                        const float4 f = rv[w];
+                        m = fmaxf(m, fmaxf(fmaxf(f.x, f.y), fmaxf(f.z, f.w)));
+                    }
                     const float scale = __fdiv_rn(m, 127.0f);
                     const long long blk = cur.t * kChunksPerThread + ch;   // block index within the shard
                     if (tid == 0 && alive && blk < a.q_blocks_per_shard)
@@ -385,11 +389,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
                     cnt = cnt < 0 ? 0 : (cnt > 4 ? 4 : cnt);
                     int8_t code[4];
                     uint16_t dq[4];
+                    quant_code4(xq[ch], scale, inv_scale, code);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        code[e] = quant_code(xq[ch][e], scale, inv_scale);
-                        dq[e] = Lp<ZERO_BF16>::narrow(__fmul_rn(static_cast<float>(code[e]), scale));
-                    }
+                    for (int e = 0; e < 4; ++e) dq[e] = Lp<ZERO_BF16>::narrow(__fmul_rn(static_cast<float>(code[e]), scale));
                     if (!alive) continue;
                     if (fast) {
                         const uint32_t cw = (static_cast<uint32_t>(static_cast<uint8_t>(code[0]))) |
