@@ -81,14 +81,16 @@ typedef struct {
 
 /* Adam hyper-parameters, copied by value at each call.  Adam itself is not
  * printed on the pages (DP-notes "Memory Consumption Analysis" sizes its fp32
- * momentum, variance and master copy); the update is textbook Adam with bias
- * correction and eps outside the square root, with decoupled weight decay
- * (AdamW) when weight_decay > 0:
+ * momentum, variance and master copy); the update is textbook Adam (bias
+ * correction, eps outside the square root) in the efficient order Kingma &
+ * Ba give for their Algorithm 1, with decoupled weight decay (AdamW) when
+ * weight_decay > 0.  With s = sqrt(1-b2^t):
  *     p <- p * (1 - lr*wd)              (only when wd != 0)
  *     m <- b1*m + (1-b1)*g
  *     v <- b2*v + (1-b2)*(g*g)
- *     p <- p - (lr/(1-b1^t)) * (m / (sqrt(v)/sqrt(1-b2^t) + eps))
- * each operation one IEEE fp32 rounding, in this order.                       */
+ *     p <- p - ((lr*s)/(1-b1^t)) * (m / (sqrt(v) + eps*s))
+ * each operation one IEEE fp32 rounding, in this order (equal to Algorithm 1
+ * in exact arithmetic).                                                      */
 typedef struct {
     float lr, beta1, beta2, eps, weight_decay;
     float max_norm;   /* > 0: clip the averaged gradient to this global L2 norm

@@ -39,7 +39,7 @@ class Scalars(ctypes.Structure):
 
 
 class AdamConsts(ctypes.Structure):
-    _fields_ = [("step_size", ctypes.c_float), ("sbc2", ctypes.c_float), ("omb1", ctypes.c_float),
+    _fields_ = [("step_size", ctypes.c_float), ("eps_hat", ctypes.c_float), ("omb1", ctypes.c_float),
                 ("omb2", ctypes.c_float), ("decay", ctypes.c_float)]
 
 

@@ -251,18 +251,24 @@ void zo_all_gather_f32(int n_d, long long psi, long long shard, const float* con
 /* ------------------------------------------------------------------------ */
 /* Adam.  The pages size Adam's state ([DP-notes] "Memory Consumption        */
 /* Analysis": fp32 momentum, variance and master copy) but print no update    */
-/* rule.  Reading: textbook Adam (Kingma & Ba, Algorithm 1) with bias         */
-/* correction and eps outside the square root; weight decay decoupled as in  */
-/* AdamW ([itwiki] "FSDP와의 관계" uses AdamW).  Per committed step t the     */
-/* fp64 products beta^t are extended by one multiplication, never pow().      */
+/* rule.  Reading: textbook Adam (Kingma & Ba, Algorithm 1: bias-corrected    */
+/* moments, eps outside the square root) evaluated in the more efficient      */
+/* order Kingma & Ba give in their Section 2 -- step size                     */
+/* lr * sqrt(1 - beta2^t) / (1 - beta1^t), denominator sqrt(v) + eps_hat --   */
+/* with eps_hat = eps * sqrt(1 - beta2^t), which makes it equal to            */
+/* Algorithm 1 in exact arithmetic.  Weight decay decoupled as in AdamW       */
+/* ([itwiki] "FSDP와의 관계" uses AdamW).  Per committed step t the fp64      */
+/* products beta^t are extended by one multiplication, never pow().           */
 /* ------------------------------------------------------------------------ */
 void zo_adam_consts_for(const zo_hparams* hp, double beta1_pow_t, double beta2_pow_t,
                         zo_adam_consts* c)
 {
     float bc1 = (float)(1.0 - beta1_pow_t);
     float bc2 = (float)(1.0 - beta2_pow_t);
-    c->step_size = hp->lr / bc1;
-    c->sbc2 = sqrtf(bc2);
+    float sbc2 = sqrtf(bc2);
+    float lr_sbc2 = hp->lr * sbc2;
+    c->step_size = lr_sbc2 / bc1;
+    c->eps_hat = hp->eps * sbc2;
     c->omb1 = 1.0f - hp->beta1;
     c->omb2 = 1.0f - hp->beta2;
     float lr_wd = hp->lr * hp->weight_decay;
@@ -279,7 +285,7 @@ void zo_adam_update(const zo_hparams* hp, const zo_adam_consts* c, long long n, 
         float mi = hp->beta1 * m[i] + c->omb1 * gi;          /* no contraction: two roundings, then the add */
         float g2 = gi * gi;
         float vi = hp->beta2 * v[i] + c->omb2 * g2;
-        float denom = sqrtf(vi) / c->sbc2 + hp->eps;
+        float denom = sqrtf(vi) + c->eps_hat;
         float ratio = mi / denom;
         pi = pi - c->step_size * ratio;
         p[i] = pi;

@@ -77,11 +77,11 @@ void zo_all_gather_f32(int n_d, long long psi, long long shard, const float* con
 
 /* ---- Adam (the reading stated in the design notes) ---- */
 typedef struct {
-    float step_size; /* lr / (1 - beta1^t)           */
-    float sbc2;      /* sqrt(1 - beta2^t)            */
-    float omb1;      /* 1 - beta1                    */
-    float omb2;      /* 1 - beta2                    */
-    float decay;     /* 1 - lr * weight_decay        */
+    float step_size; /* lr * sqrt(1 - beta2^t) / (1 - beta1^t) */
+    float eps_hat;   /* eps * sqrt(1 - beta2^t)                */
+    float omb1;      /* 1 - beta1                              */
+    float omb2;      /* 1 - beta2                              */
+    float decay;     /* 1 - lr * weight_decay                  */
 } zo_adam_consts;
 
 void zo_adam_consts_for(const zo_hparams* hp, double beta1_pow_t, double beta2_pow_t,

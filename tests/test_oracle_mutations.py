@@ -16,9 +16,10 @@ PINS = ["tests/test_oracle_accounting.py", "tests/test_oracle_encodings.py",
 
 # (name, text in the oracle source, planted replacement)
 MUTATIONS = [
-    ("no bias correction of m", "c->step_size = hp->lr / bc1;", "c->step_size = hp->lr;"),
-    ("no bias correction of v", "c->sbc2 = sqrtf(bc2);", "c->sbc2 = 1.0f;"),
-    ("eps inside the root", "sqrtf(vi) / c->sbc2 + hp->eps", "sqrtf(vi + hp->eps) / c->sbc2"),
+    ("no bias correction of m", "c->step_size = lr_sbc2 / bc1;", "c->step_size = lr_sbc2;"),
+    ("no bias correction of v", "float sbc2 = sqrtf(bc2);", "float sbc2 = 1.0f;"),
+    ("eps inside the root", "sqrtf(vi) + c->eps_hat", "sqrtf(vi + c->eps_hat)"),
+    ("eps not bias-corrected", "c->eps_hat = hp->eps * sbc2;", "c->eps_hat = hp->eps;"),
     ("update sign flipped", "pi = pi - c->step_size * ratio;", "pi = pi + c->step_size * ratio;"),
     ("ratio transposed", "float ratio = mi / denom;", "float ratio = denom / (mi + 1e-30f);"),
     ("decay dropped", "pi = pi * c->decay;", "pi = pi;"),

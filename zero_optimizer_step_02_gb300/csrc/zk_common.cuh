@@ -194,7 +194,7 @@ __device__ __forceinline__ bool is_finite_f32(float x)
 // Everything a kernel needs from the hyper-parameters and the step scalars,
 // computed once per CTA by one thread.
 struct StepConsts {
-    float b1, b2, omb1, omb2, step, sbc2, eps, decay, coef;
+    float b1, b2, omb1, omb2, step, eps, decay, coef;   // step, eps: bias-corrected (see set_adam)
     float divisor, inv_divisor;
     int wd, clip, div_pow2, skip;
 };
@@ -213,6 +213,10 @@ __device__ __forceinline__ void set_divisor(StepConsts& c, int n_d, float loss_s
 
 // Bias-corrected Adam constants for the step about to be committed: the fp64
 // running products beta^t are extended by one multiplication (never pow).
+// Adam in the order Kingma & Ba give as the efficient form of their
+// Algorithm 1: step = lr * sqrt(1 - beta2^t) / (1 - beta1^t) and
+// eps_hat = eps * sqrt(1 - beta2^t), equal to Algorithm 1 in exact
+// arithmetic, with one division per element instead of two.
 __device__ __forceinline__ void set_adam(StepConsts& c, const zero_hparams& hp, double b1pow,
                                          double b2pow)
 {
@@ -220,13 +224,13 @@ __device__ __forceinline__ void set_adam(StepConsts& c, const zero_hparams& hp, 
     const double b2t = __dmul_rn(b2pow, static_cast<double>(hp.beta2));
     const float bc1 = __double2float_rn(__dsub_rn(1.0, b1t));
     const float bc2 = __double2float_rn(__dsub_rn(1.0, b2t));
+    const float sbc2 = __fsqrt_rn(bc2);
     c.b1 = hp.beta1;
     c.b2 = hp.beta2;
     c.omb1 = __fsub_rn(1.0f, hp.beta1);
     c.omb2 = __fsub_rn(1.0f, hp.beta2);
-    c.step = __fdiv_rn(hp.lr, bc1);
-    c.sbc2 = __fsqrt_rn(bc2);
-    c.eps = hp.eps;
+    c.step = __fdiv_rn(__fmul_rn(hp.lr, sbc2), bc1);
+    c.eps = __fmul_rn(hp.eps, sbc2);
     c.decay = __fsub_rn(1.0f, __fmul_rn(hp.lr, hp.weight_decay));
     c.wd = hp.weight_decay != 0.0f;
 }
@@ -242,7 +246,7 @@ __device__ __forceinline__ void adam_elem(const StepConsts& c, float g, float& p
     if (c.wd) p = __fmul_rn(p, c.decay);
     m = __fadd_rn(__fmul_rn(c.b1, m), __fmul_rn(c.omb1, g));
     v = __fadd_rn(__fmul_rn(c.b2, v), __fmul_rn(c.omb2, __fmul_rn(g, g)));
-    const float denom = __fadd_rn(__fdiv_rn(__fsqrt_rn(v), c.sbc2), c.eps);
+    const float denom = __fadd_rn(__fsqrt_rn(v), c.eps);
     p = __fsub_rn(p, __fmul_rn(c.step, __fdiv_rn(m, denom)));
 }
 
