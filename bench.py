@@ -255,8 +255,10 @@ class Job:
 
 
 def l2_flush(torch, device, buf=[]):
+    """Write 4x the L2 size: evicts the step's inputs, and takes long enough
+    on the GPU that the host has enqueued the step before its start event."""
     if not buf:
-        buf.append(torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device))
+        buf.append(torch.empty(4 * L2_BYTES // 4, dtype=torch.float32, device=device))
     buf[0].fill_(1.0)
 
 
