@@ -414,6 +414,10 @@ int zo_plain_dp_step(int n_d, long long psi, const uint16_t* const* grads, int g
  * shards are all-gathered (stages 1-2) or left sharded (stage 3, gathered
  * per layer before use).  State arrays are n_d * S long; their padding is
  * never touched.  lp_shards (stage 3) is n_d * S long; gathered is psi long. */
+static int step_from_shards(int n_d, long long psi, long long S, int stage, float* shards,
+                            const zo_hparams* hp, zo_scalars* sc, float* master, float* m, float* v,
+                            uint16_t* lp_shards, uint16_t* gathered, int param_dtype);
+
 int zo_zero_step(int n_d, long long psi, int shard_pad, int stage, const uint16_t* const* grads,
                  int grad_dtype, const zo_hparams* hp, zo_scalars* sc, float* master, float* m,
                  float* v, uint16_t* lp_shards, uint16_t* gathered, int param_dtype)
@@ -436,7 +440,18 @@ int zo_zero_step(int n_d, long long psi, int shard_pad, int stage, const uint16_
     } else {
         zo_reduce_scatter(n_d, psi, S, grads, grad_dtype, divisor, shards);
     }
+    return step_from_shards(n_d, psi, S, stage, shards, hp, sc, master, m, v, lp_shards, gathered,
+                            param_dtype);
+}
 
+/* Everything after the reduce: the global checks (one running value across
+ * shards, rank order), the shard Adam, the cast and the gather.  Frees
+ * `shards` (n_d * S reduced gradient, padding +0). */
+static int step_from_shards(int n_d, long long psi, long long S, int stage, float* shards,
+                            const zo_hparams* hp, zo_scalars* sc, float* master, float* m, float* v,
+                            uint16_t* lp_shards, uint16_t* gathered, int param_dtype)
+{
+    long long padded = S * n_d;
     /* scalar all-reduce across shards: one running value, rank order */
     int overflow = 0;
     double sq = 0.0;
@@ -546,4 +561,70 @@ void zo_quant_gather(int n_d, long long psi, long long shard, int block, const u
             zo_quantize_block(hi - lo, shards + off, codes + off, sc, gathered + off);
         }
     }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Quantized gradient exchange.  [itwiki] "후속 기법", ZeRO++ row: gradients  */
+/* are quantized and averaged through an all-to-all (qgZ); bit width and     */
+/* blocking are not given.  Reading: each rank quantizes its own bf16         */
+/* gradient with the block quantizer above (blocks aligned to each           */
+/* destination shard's start), only codes and scales travel, and the shard   */
+/* owner reconstructs every rank's value as (float)code * scale (one fp32    */
+/* rounding) and adds the ranks in order from +0 before dividing once.       */
+/* ------------------------------------------------------------------------ */
+void zo_quantize_ranks(int n_d, long long psi, long long shard, int block, const uint16_t* const* grads,
+                       int8_t* const* codes, float* const* scales)
+{
+    long long blocks_per_shard = (shard + block - 1) / block;
+    uint16_t* deq = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)block);
+    for (int q = 0; q < n_d; ++q) {
+        for (int r = 0; r < n_d; ++r) {
+            long long len = zo_valid_len(psi, shard, r);
+            for (long long b = 0; b < blocks_per_shard; ++b) {
+                long long lo = b * block;
+                long long hi = lo + block < len ? lo + block : len;
+                float* sc = scales[q] + (long long)r * blocks_per_shard + b;
+                if (hi <= lo) {
+                    *sc = 0.0f;
+                    continue;
+                }
+                long long off = (long long)r * shard + lo;
+                zo_quantize_block(hi - lo, grads[q] + off, codes[q] + off, sc, deq);
+            }
+        }
+    }
+    free(deq);
+}
+
+void zo_reduce_scatter_q(int n_d, long long psi, long long shard, int block, const int8_t* const* codes,
+                         const float* const* scales, float divisor, float* shards)
+{
+    long long blocks_per_shard = (shard + block - 1) / block;
+    for (int r = 0; r < n_d; ++r) {
+        long long len = zo_valid_len(psi, shard, r);
+        for (long long i = 0; i < shard; ++i) {
+            long long j = (long long)r * shard + i;
+            if (i >= len) {
+                shards[j] = 0.0f;
+                continue;
+            }
+            long long sidx = (long long)r * blocks_per_shard + i / block;
+            float sum = 0.0f;
+            for (int q = 0; q < n_d; ++q) sum = sum + (float)codes[q][j] * scales[q][sidx];
+            shards[j] = sum / divisor;
+        }
+    }
+}
+
+int zo_zero_step_qgz(int n_d, long long psi, int shard_pad, int stage, int block, const int8_t* const* codes,
+                     const float* const* scales, const zo_hparams* hp, zo_scalars* sc, float* master, float* m,
+                     float* v, uint16_t* lp_shards, uint16_t* gathered, int param_dtype)
+{
+    long long S = zo_shard_size(psi, n_d, shard_pad);
+    long long padded = S * n_d;
+    float divisor = step_divisor(n_d, hp, sc);
+    float* shards = (float*)malloc(sizeof(float) * (size_t)(padded > 0 ? padded : 1));
+    zo_reduce_scatter_q(n_d, psi, S, block, codes, scales, divisor, shards);
+    return step_from_shards(n_d, psi, S, stage, shards, hp, sc, master, m, v, lp_shards, gathered,
+                            param_dtype);
 }

@@ -108,6 +108,15 @@ void zo_quantize_block(long long n, const uint16_t* x_bf16, int8_t* codes, float
 void zo_quant_gather(int n_d, long long psi, long long shard, int block, const uint16_t* shards,
                      int8_t* codes, float* scales, uint16_t* gathered);
 
+/* ---- quantized gradient exchange (ZeRO++ qgZ reading) ---- */
+void zo_quantize_ranks(int n_d, long long psi, long long shard, int block, const uint16_t* const* grads,
+                       int8_t* const* codes, float* const* scales);
+void zo_reduce_scatter_q(int n_d, long long psi, long long shard, int block, const int8_t* const* codes,
+                         const float* const* scales, float divisor, float* shards);
+int zo_zero_step_qgz(int n_d, long long psi, int shard_pad, int stage, int block, const int8_t* const* codes,
+                     const float* const* scales, const zo_hparams* hp, zo_scalars* sc, float* master, float* m,
+                     float* v, uint16_t* lp_shards, uint16_t* gathered, int param_dtype);
+
 #ifdef __cplusplus
 }
 #endif
