@@ -41,7 +41,7 @@ L2_BYTES = 129 * 1024 * 1024
 
 
 # ----------------------------------------------------------------- workloads
-def workload(cfg, nd=None, qgather=False, psi=None):
+def workload(cfg, nd=None, qgather=False, psi=None, qgz=False):
     """Sizes, hyper-parameters and the algorithmic bytes of one step.  psi
     overrides the parameter count (a smaller case of the same workload, for
     profiling)."""
@@ -59,9 +59,9 @@ def workload(cfg, nd=None, qgather=False, psi=None):
                  gdt="bf16", sigma=1e-3, tail=False, lr=1e-3, b2=0.999, wd=0.0, clip=0.0, ls=False, layers=8)
     elif cfg == 5:
         n = nd or 8
-        w = dict(name="zero2_psi2p28_nd%d%s" % (n, "_qgather" if qgather else ""), psi=1 << 28, n_d=n, stage=2,
-                 pad=8, gdt="bf16", sigma=1e-3, tail=False, lr=1e-3, b2=0.999, wd=0.0, clip=0.0, ls=False,
-                 layers=1, qgather=qgather)
+        w = dict(name="zero2_psi2p28_nd%d%s%s" % (n, "_qgather" if qgather else "", "_qgz" if qgz else ""),
+                 psi=1 << 28, n_d=n, stage=2, pad=16 if qgz else 8, gdt="bf16", sigma=1e-3, tail=False, lr=1e-3,
+                 b2=0.999, wd=0.0, clip=0.0, ls=False, layers=1, qgather=qgather, qgz=qgz)
     else:
         raise SystemExit("unknown config %r" % cfg)
     if psi:
@@ -75,6 +75,9 @@ def workload(cfg, nd=None, qgather=False, psi=None):
         w["bytes_per_param"] = 2 * n_d + 30
     elif w.get("qgather"):
         w["bytes_per_param"] = 2 * n_d + 27 + 4.0 / 2048
+    elif w.get("qgz"):
+        # the receiver reads int8 codes + one fp32 scale per 2048 per rank
+        w["bytes_per_param"] = n_d * (1 + 4.0 / 2048) + 26
     else:
         w["bytes_per_param"] = 2 * n_d + 26
     w["psi_total"] = w["psi"] * w["layers"]
@@ -203,10 +206,23 @@ class Job:
             nbs = -(-self.plan.shard // 2048)
             self.codes = torch.zeros(n, dtype=torch.int8, device=device)
             self.scales = torch.zeros(w["n_d"] * nbs, device=device)
+        if w.get("qgz"):
+            # the int8 wire format of every gradient set (sender pass, untimed here)
+            nbs = -(-self.plan.shard // 2048)
+            row16 = (w["psi"] + 15) // 16 * 16
+            self.codes = [torch.empty(w["n_d"], row16, dtype=torch.int8, device=device) for _ in self.grads]
+            self.qscales = [torch.empty(w["n_d"] * w["n_d"] * nbs, device=device) for _ in self.grads]
+            for k in range(len(self.grads)):
+                self.quantize(k)
         self.ws = torch.zeros(max(self.plan.workspace_bytes(self.hp), 256), dtype=torch.uint8, device=device)
         self.scalars = torch.zeros(256, dtype=torch.uint8, device=device)
         z.zero_scalars_init(self.scalars, scale)
         self.k = 0
+
+    def quantize(self, k):
+        """Sender side of the quantized gradient exchange for gradient set k."""
+        self.z.zero_quantize_grads(self.plan.handle, [self.grads[k][r] for r in range(self.w["n_d"])], 2048,
+                                   [self.codes[k][r] for r in range(self.w["n_d"])], self.qscales[k])
 
     def ranks(self, l):
         g = self.grads[l % len(self.grads)]
@@ -223,7 +239,12 @@ class Job:
                 # per-layer gather of the bf16 shards before use (itwiki: ZeRO-3)
                 z.zero_all_gather(h, [self.lp[l][r * S:(r + 1) * S] for r in range(w["n_d"])], self.gathered,
                                   self.scalars)
-            if w.get("qgather"):
+            if w.get("qgz"):
+                k = gsel % len(self.grads)
+                z.zero_step_fused_qgz(h, self.hp, [self.codes[k][r] for r in range(w["n_d"])], self.qscales[k], 2048,
+                                      self.master[l], self.m[l], self.v[l], self.master[l], self.m[l], self.v[l],
+                                      self.lp[l], self.scalars)
+            elif w.get("qgather"):
                 z.zero_step_fused_qgather(h, self.hp, self.ranks(gsel), self.master[l], self.m[l], self.v[l],
                                           self.master[l], self.m[l], self.v[l], 2048, self.codes, self.scales,
                                           self.lp[l], self.scalars, self.ws)
@@ -265,7 +286,7 @@ def l2_flush(torch, device, buf=[]):
 def gpu_arm(args, rank, world, device):
     import torch
     import zero_optimizer_step_02_gb300 as z
-    w = workload(args.config, args.nd, args.qgather, args.psi)
+    w = workload(args.config, args.nd, args.qgather, args.psi, args.qgz)
     torch.cuda.set_device(device)
     job = Job(w, device)
     torch.cuda.synchronize()
@@ -329,7 +350,7 @@ def gpu_arm(args, rank, world, device):
         kernel, kms, kbytes = names[k], dur[k], per_param[k] * w["psi"]
         breakdown = {names[i]: round(dur[i], 4) for i in range(3)}
     else:
-        kernel = "fused_step" if not w.get("qgather") else "fused_step_qgather"
+        kernel = "fused_step_qgather" if w.get("qgather") else ("fused_step_qgz" if w.get("qgz") else "fused_step")
         kms = ms_per_step / w["layers"] if w["stage"] != 3 else None
         if w["stage"] == 3:
             # time the per-layer fused step alone
@@ -355,7 +376,23 @@ def gpu_arm(args, rank, world, device):
                 "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": kernel,
                 "kernel_ms": round(kms, 4), "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)"}
 
-    e2e = None if args.no_e2e else e2e_measure(job, w, args, device, world)
+    e2e = None if args.no_e2e or w.get("qgz") else e2e_measure(job, w, args, device, world)
+    sender = None
+    if w.get("qgz"):
+        # the sender pass (every rank quantizes its bf16 gradient): 2 + 1 + 4/2048 bytes per param per rank
+        evs = []
+        torch.cuda.synchronize()
+        for k in range(max(3, args.steps) + 1):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            job.quantize(k % len(job.grads))
+            b.record()
+            evs.append((a, b))
+        torch.cuda.synchronize()
+        sms = statistics.mean(a.elapsed_time(b) for a, b in evs[1:])
+        sbytes = w["n_d"] * w["psi"] * (3 + 4.0 / 2048)
+        sender = {"ms": round(sms, 4), "gbs": round(sbytes / (sms / 1e3) / 1e9, 1),
+                  "frac": round(sbytes / (sms / 1e3) / 1e9 / peak, 4)}
     out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f32 (state), %s (grads), bf16 (params)" % w["gdt"],
@@ -368,6 +405,8 @@ def gpu_arm(args, rank, world, device):
            "roofline": roofline, "gpu_launches": int(launches), "e2e": e2e, "clocks": clk}
     if breakdown:
         out["kernel_ms"] = breakdown
+    if sender:
+        out["qgz_sender"] = sender
     return out
 
 
@@ -419,7 +458,12 @@ def oracle_sample(w, budget_s, max_steps=None):
     gath = np.zeros(psi, np.uint16)
     steps, t0 = 0, time.perf_counter()
     while True:
-        oracle.zero_step(rows, dt, hp, st, w["pad"], min(w["stage"], 3), lp_shards=lp, gathered=gath)
+        if w.get("qgz"):
+            codes, scales = oracle.quantize_ranks(rows, psi, S, 2048)
+            oracle.zero_step_qgz(codes, scales, 2048, hp, st, w["pad"], min(w["stage"], 3), psi, lp_shards=lp,
+                                 gathered=gath)
+        else:
+            oracle.zero_step(rows, dt, hp, st, w["pad"], min(w["stage"], 3), lp_shards=lp, gathered=gath)
         steps += 1
         el = time.perf_counter() - t0
         if el >= budget_s or (max_steps and steps >= max_steps):
@@ -428,7 +472,7 @@ def oracle_sample(w, budget_s, max_steps=None):
 
 
 def reference_arm(args, rank, world):
-    w = workload(args.config, args.nd, args.qgather, args.psi)
+    w = workload(args.config, args.nd, args.qgather, args.psi, args.qgz)
     if rank != 0:
         return None
     for _ in range(args.warmup):
@@ -485,6 +529,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--psi", type=int, default=None, help="smaller parameter count (profiling)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--qgz", action="store_true", help="quantized gradient exchange (config 5)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -499,7 +544,7 @@ def main():
     out = gpu_arm(args, rank, world, device)
     if rank == 0:
         if not args.no_cpu_baseline and world == 1:
-            w = workload(args.config, args.nd, args.qgather, args.psi)
+            w = workload(args.config, args.nd, args.qgather, args.psi, args.qgz)
             psi, n_d, steps, el = oracle_sample(w, args.cpu_budget)
             out["cpu_baseline"] = {"value": psi * steps / el, "unit": UNIT, "cores": 1, "kind": "oracle",
                                    "sample": "%d of %d params, n_d=%d, %d steps in %.1f s, single-threaded C "

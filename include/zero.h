@@ -263,6 +263,36 @@ ZERO_API zero_status zero_step_fused_qgather(const zero_plan* plan, const zero_h
                                              zero_dev_scalars* scalars_dev, void* ws,
                                              void* stream);
 
+/* ------------------------------------------- quantized gradient exchange --- */
+/* ZeRO++ qgZ (itwiki "후속 기법", ZeRO++ row: gradients are quantized and
+ * averaged through an all-to-all; bit width and blocking not given).  The
+ * reading: every rank quantizes its own gradient with the block quantizer of
+ * zero_quant_gather (int8, absmax/127 scale, blocks aligned to each
+ * destination shard's start), only codes and scales travel, and the shard
+ * owner reconstructs each rank's value as (float)code * scale (one fp32
+ * rounding) before the rank-ordered fp32 sum.
+ *
+ * Sender side: rank q's bf16 gradient (>= Psi elements) -> int8 codes at the
+ * global index j < Psi and fp32 block scales.  rank_codes: host array of n_d
+ * device pointers (>= Psi int8 each, 16-byte aligned).  rank_scales: one
+ * array of n_d * n_d * ceil(S/block) floats, rank q's scales starting at
+ * q * n_d * ceil(S/block), shard-major, 0 for blocks past a shard's valid
+ * length.  Plan gradient dtype bf16; 32 <= block <= 65536, a multiple of 32. */
+ZERO_API zero_status zero_quantize_grads(const zero_plan* plan, const void* const* rank_grads, int block,
+                                         signed char* const* rank_codes, float* rank_scales,
+                                         void* stream);
+
+/* Receiver side, fused: zero_step_fused with the ranks' int8 codes and
+ * scales (layout as above, block 2048) in place of their 16-bit gradients:
+ *   g[j] = (sum over q in order, from +0.0f, of (float)code_q[j] * scale_q(j)) / n_d
+ * then Adam, cast and gather as in zero_step_fused.  No clipping and no loss
+ * scaling in this entry point (ZERO_ERR_UNSUPPORTED).                       */
+ZERO_API zero_status zero_step_fused_qgz(const zero_plan* plan, const zero_hparams* hp,
+                                         const signed char* const* rank_codes, const float* rank_scales,
+                                         int block, const float* master_in, const float* m_in,
+                                         const float* v_in, float* master_out, float* m_out, float* v_out,
+                                         void* lp_out, zero_dev_scalars* scalars_dev, void* stream);
+
 /* ----------------------------------------------------------- diagnostics --- */
 /* Launch one kernel that waits on a barrier nothing completes, with a wait
  * limit of timeout_ns (at most 10 s).  When the limit runs out the kernel sets

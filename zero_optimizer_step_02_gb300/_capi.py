@@ -79,6 +79,8 @@ _SIGS = {
     "zero_debug_wait_timeout": (_i32, [_vp, _ll, _vp]),
     "zero_launch_count": (ctypes.c_ulonglong, []),
     "zero_step_fused_noalloc": (_i32, [_vp, _hp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "zero_quantize_grads": (_i32, [_vp, _vp, _i32, _vp, _vp, _vp]),
+    "zero_step_fused_qgz": (_i32, [_vp, _hp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -221,6 +223,19 @@ def zero_step_fused_qgather(plan, hp, rank_grads, master_in, m_in, v_in, master_
                                         _addr(m_in), _addr(v_in), _addr(master_out), _addr(m_out), _addr(v_out),
                                         block, _addr(codes), _addr(scales), _addr(gathered), _addr(scalars),
                                         _addr(ws), _stream(stream)), "zero_step_fused_qgather")
+
+
+def zero_quantize_grads(plan, rank_grads, block, rank_codes, rank_scales, stream=None):
+    _check(_lib.zero_quantize_grads(plan, _ptr_array(rank_grads), block, _ptr_array(rank_codes),
+                                    _addr(rank_scales), _stream(stream)), "zero_quantize_grads")
+
+
+def zero_step_fused_qgz(plan, hp, rank_codes, rank_scales, block, master_in, m_in, v_in, master_out, m_out, v_out,
+                        lp_out, scalars, stream=None):
+    _check(_lib.zero_step_fused_qgz(plan, ctypes.byref(hp), _ptr_array(rank_codes), _addr(rank_scales), block,
+                                    _addr(master_in), _addr(m_in), _addr(v_in), _addr(master_out), _addr(m_out),
+                                    _addr(v_out), _addr(lp_out), _addr(scalars), _stream(stream)),
+           "zero_step_fused_qgz")
 
 
 def zero_debug_wait_timeout(scalars, timeout_ns, stream=None):

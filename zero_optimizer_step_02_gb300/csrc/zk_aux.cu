@@ -383,6 +383,7 @@ __global__ void __launch_bounds__(256) k_quant_gather(const uint16_t* __restrict
             cq.x = (uint32_t)(uint8_t)q[0] | ((uint32_t)(uint8_t)q[1] << 8) | ((uint32_t)(uint8_t)q[2] << 16) | ((uint32_t)(uint8_t)q[3] << 24);
             cq.y = (uint32_t)(uint8_t)q[4] | ((uint32_t)(uint8_t)q[5] << 8) | ((uint32_t)(uint8_t)q[6] << 16) | ((uint32_t)(uint8_t)q[7] << 24);
             reinterpret_cast<uint2*>(codes + j0)[v] = cq;
+            if (gathered == nullptr) continue;   // codes and scales only (gradient sender)
             uint4 dv;
             dv.x = d[0] | ((uint32_t)d[1] << 16);
             dv.y = d[2] | ((uint32_t)d[3] << 16);
@@ -395,7 +396,7 @@ __global__ void __launch_bounds__(256) k_quant_gather(const uint16_t* __restrict
             uint16_t d;
             quant(Lp<ZERO_BF16>::widen(x[j0 + i]), q, d);
             codes[j0 + i] = q;
-            gathered[j0 + i] = d;
+            if (gathered != nullptr) gathered[j0 + i] = d;
         }
     }
 }
@@ -415,6 +416,20 @@ cudaError_t launch_quant_gather(const void* shards, int n_d, long long shard, lo
                                                                 psi, block, nbs, codes, scales,
                                                                 static_cast<uint16_t*>(gathered));
     return cudaGetLastError();
+}
+
+// Sender side of the quantized gradient exchange: each rank's bf16 gradient
+// through the block quantizer above, codes and scales only.
+cudaError_t launch_quantize_grads(const void* const* ranks, int n_d, long long shard, long long psi, int block,
+                                  signed char* const* codes, float* scales, cudaStream_t st)
+{
+    const long long nbs = (shard + block - 1) / block;
+    for (int q = 0; q < n_d; ++q) {
+        const cudaError_t e = launch_quant_gather(ranks[q], n_d, shard, psi, block, codes[q],
+                                                  scales + static_cast<long long>(q) * n_d * nbs, nullptr, st);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 // ---------------------------------------------------------------- diagnostics

@@ -513,6 +513,60 @@ ZERO_API zero_status zero_step_fused_qgather(const zero_plan* p, const zero_hpar
     return from_cuda(zk::launch_stream(zk::OP_QFUSED, p->grad_dtype, p->param_dtype, a, st));
 }
 
+ZERO_API zero_status zero_quantize_grads(const zero_plan* p, const void* const* ranks, int block,
+                                         signed char* const* codes, float* scales, void* stream)
+{
+    if (p == nullptr || codes == nullptr) return ZERO_ERR_INVALID_ARG;
+    if (block < 32 || block > 65536 || block % 32 != 0) return ZERO_ERR_INVALID_ARG;
+    if (p->grad_dtype != ZERO_BF16) return ZERO_ERR_UNSUPPORTED;
+    zero_status s;
+    if ((s = check_ranks(p, ranks)) != ZERO_OK) return s;
+    if ((s = check_ranks(p, reinterpret_cast<const void* const*>(codes))) != ZERO_OK) return s;
+    if ((s = check_dev(scales)) != ZERO_OK) return s;
+    return from_cuda(zk::launch_quantize_grads(ranks, p->n_d, p->shard, p->psi, block, codes, scales, as_stream(stream)));
+}
+
+ZERO_API zero_status zero_step_fused_qgz(const zero_plan* p, const zero_hparams* hp, const signed char* const* codes,
+                                         const float* scales, int block, const float* mi, const float* m_in,
+                                         const float* vi, float* mo, float* m_out, float* vo, void* lp,
+                                         zero_dev_scalars* sc, void* stream)
+{
+    if (p == nullptr) return ZERO_ERR_INVALID_ARG;
+    zero_status s;
+    if ((s = check_hparams(hp)) != ZERO_OK) return s;
+    if (block != zk::kQuantBlock) return ZERO_ERR_UNSUPPORTED;
+    if (hp->max_norm > 0.0f || hp->loss_scaling) return ZERO_ERR_UNSUPPORTED;
+    if ((s = check_ranks(p, reinterpret_cast<const void* const*>(codes))) != ZERO_OK) return s;
+    if ((s = check_dev(scales)) != ZERO_OK) return s;
+    if ((s = check_dev(sc, 256)) != ZERO_OK) return s;
+    if ((s = check_state(mi, m_in, vi, mo, m_out, vo)) != ZERO_OK) return s;
+    if (lp != nullptr && !aligned(lp, 16)) return ZERO_ERR_MISALIGNED;
+    StreamArgs a = base_args(p, hp, sc);
+    a.n_ranks = p->n_d;
+    for (int r = 0; r < p->n_d; ++r) a.rank[r] = codes[r];
+    // tiles inside shards, so that every 2048-element block of a tile has one scale per rank
+    a.base = 0;
+    a.seg_stride = p->shard;
+    a.seg_len = p->shard;
+    a.limit = p->psi;
+    a.n_seg = p->n_d;
+    a.tiles_per_seg = tiles_of(p->shard);
+    a.q_blocks_per_shard = (p->shard + zk::kQuantBlock - 1) / zk::kQuantBlock;
+    a.q_rank_scales = scales;
+    a.q_rank_scale_stride = a.q_blocks_per_shard * p->n_d;
+    a.tma_ok = (p->shard % 16) == 0 ? 1 : 0;   // int8 slices start 16-byte aligned
+    a.n_side = 3;
+    a.side[0] = mi;
+    a.side[1] = m_in;
+    a.side[2] = vi;
+    a.out_f32[0] = mo;
+    a.out_f32[1] = m_out;
+    a.out_f32[2] = vo;
+    a.out_lp = lp;
+    a.flags = zk::F_EPILOGUE;
+    return from_cuda(zk::launch_stream(zk::OP_FUSED, zk::kGradQ8, p->param_dtype, a, as_stream(stream)));
+}
+
 ZERO_API zero_status zero_debug_wait_timeout(zero_dev_scalars* sc, long long timeout_ns, void* stream)
 {
     const zero_status s = check_dev(sc, 256);

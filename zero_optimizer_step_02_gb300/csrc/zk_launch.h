@@ -9,6 +9,10 @@ namespace zk {
 
 enum { OP_FUSED = 0, OP_REDUCE = 1, OP_ADAM = 2, OP_QFUSED = 3 /* fused step + int8 gather epilogue */ };
 
+// rank streams that carry int8 codes with per-rank fp32 block scales (the
+// quantized gradient exchange) instead of bf16 / fp16 values
+constexpr int kGradQ8 = 2;
+
 // Arguments of one launch of the streaming engine (kernel parameter space).
 //
 // Tiles: element ranges of 2048 laid over "segments".  A flat launch has one
@@ -20,6 +24,8 @@ struct StreamArgs {
     const float* side[4];              // fp32 inputs: OP_FUSED {master, m, v}; OP_ADAM {g, master, m, v}
     float* out_f32[3];                 // OP_FUSED/OP_ADAM {master, m, v}; OP_REDUCE {g or null}
     void* out_lp;                      // 16-bit parameters out (null: none)
+    const float* q_rank_scales;        // kGradQ8 ranks: scales, rank r at r * q_rank_scale_stride,
+    long long q_rank_scale_stride;     //   then shard-major blocks of kQuantBlock
     signed char* q_codes;              // fused quantized gather (F_QUANT)
     float* q_scales;
     void* q_gathered;
@@ -62,6 +68,8 @@ cudaError_t launch_all_gather(const void* const* shards, int n_d, long long shar
 cudaError_t launch_quant_gather(const void* shards, int n_d, long long shard, long long psi,
                                 int block, signed char* codes, float* scales, void* gathered,
                                 cudaStream_t st);
+cudaError_t launch_quantize_grads(const void* const* ranks, int n_d, long long shard, long long psi, int block,
+                                  signed char* const* codes, float* scales, cudaStream_t st);
 cudaError_t launch_debug_wait(zero_dev_scalars* sc, unsigned long long timeout_ns, cudaStream_t st);
 
 }  // namespace zk

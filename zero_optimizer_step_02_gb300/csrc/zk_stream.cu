@@ -71,6 +71,26 @@ struct TileCursor {
     }
 };
 
+// int8 code b of a packed word, as a float (exact)
+__device__ __forceinline__ float code_f32(uint32_t w, int b)
+{
+    return __int2float_rn(static_cast<int>(static_cast<signed char>((w >> (8 * b)) & 0xFFu)));
+}
+
+// scale of rank r's block holding chunk row ch of the current tile
+__device__ __forceinline__ float rank_scale(const StreamArgs& a, int r, long long seg, long long t, int ch)
+{
+    return __ldg(a.q_rank_scales + static_cast<long long>(r) * a.q_rank_scale_stride +
+                 seg * a.q_blocks_per_shard + t * kChunksPerThread + ch);
+}
+
+// rank-ordered add of one rank's dequantized codes: acc += fl(code * scale)
+__device__ __forceinline__ void add_codes(float (&acc)[4], uint32_t w, float s)
+{
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[e] = __fadd_rn(acc[e], __fmul_rn(code_f32(w, e), s));
+}
+
 template <int GT>
 __device__ __forceinline__ void add_slice(float (&acc)[4], uint2 w)
 {
@@ -132,7 +152,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
 
     const int n_groups = a.n_ranks > 0 ? (a.n_ranks + kGroupRanks - 1) / kGroupRanks : 1;
     const int rank_slots = a.n_ranks < kGroupRanks ? a.n_ranks : kGroupRanks;
-    const uint32_t side_off = static_cast<uint32_t>(rank_slots) * kTile * sizeof(uint16_t);
+    constexpr uint32_t kEB = (GT == kGradQ8) ? 1u : 2u;   // bytes per rank element
+    const uint32_t side_off = static_cast<uint32_t>(rank_slots) * kTile * kEB;
 
     bool nonfinite = false;
     float sq_hi = 0.0f, sq_lo = 0.0f;
@@ -158,13 +179,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
                     const int r0 = g * kGroupRanks;
                     const int nr = a.n_ranks - r0 < kGroupRanks ? a.n_ranks - r0 : kGroupRanks;
                     const bool last = g == n_groups - 1;
-                    const uint32_t rank_bytes = kTile * sizeof(uint16_t);
+                    const uint32_t rank_bytes = kTile * kEB;
                     const uint32_t bytes = (nr > 0 ? nr : 0) * rank_bytes + (last ? a.n_side * kTile * 4u : 0u);
                     unsigned char* st = ring + static_cast<size_t>(s) * a.stage_bytes;
                     mbar_arrive_expect_tx(&sh->full[s], bytes);
                     for (int k = 0; k < nr; ++k)
-                        bulk_load(st + k * rank_bytes,
-                                  static_cast<const uint16_t*>(a.rank[r0 + k]) + j0, rank_bytes, &sh->full[s]);
+                        bulk_load(st + k * rank_bytes, static_cast<const unsigned char*>(a.rank[r0 + k]) + j0 * kEB,
+                                  rank_bytes, &sh->full[s]);
                     if (last)
                         for (int k = 0; k < a.n_side; ++k)
                             bulk_load(st + side_off + k * kTile * 4u, a.side[k] + j0, kTile * 4u, &sh->full[s]);
@@ -224,13 +245,31 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
                         const unsigned char* st = ring + static_cast<size_t>(s) * a.stage_bytes;
                         const int r0 = g * kGroupRanks;
                         const int nr = a.n_ranks - r0 < kGroupRanks ? a.n_ranks - r0 : kGroupRanks;
-#pragma unroll
-                        for (int ch = 0; ch < kChunksPerThread; ++ch) {
-                            const int q = ch * kConsumers + tid;  // chunk index within the tile
-#pragma unroll 8
+                        if constexpr (GT == kGradQ8) {
+                            // ranks outer: both chunk rows' block scales of a rank loaded once
+                            const float* sp = a.q_rank_scales + r0 * a.q_rank_scale_stride +
+                                              cur.seg * a.q_blocks_per_shard + cur.t * kChunksPerThread;
+#pragma unroll 4
                             for (int k = 0; k < nr; ++k) {
-                                const uint2 w = reinterpret_cast<const uint2*>(st + k * kTile * 2)[q];
-                                add_slice<GT>(acc[ch], w);
+                                float scl[kChunksPerThread];
+#pragma unroll
+                                for (int ch = 0; ch < kChunksPerThread; ++ch) scl[ch] = __ldg(sp + ch);
+                                sp += a.q_rank_scale_stride;
+#pragma unroll
+                                for (int ch = 0; ch < kChunksPerThread; ++ch) {
+                                    const uint32_t w = reinterpret_cast<const uint32_t*>(st + k * kTile)[ch * kConsumers + tid];
+                                    add_codes(acc[ch], w, scl[ch]);
+                                }
+                            }
+                        } else {
+#pragma unroll
+                            for (int ch = 0; ch < kChunksPerThread; ++ch) {
+                                const int q = ch * kConsumers + tid;  // chunk index within the tile
+#pragma unroll 8
+                                for (int k = 0; k < nr; ++k) {
+                                    const uint2 w = reinterpret_cast<const uint2*>(st + k * kTile * 2)[q];
+                                    add_slice<GT>(acc[ch], w);
+                                }
                             }
                         }
                         if (g == n_groups - 1) {
@@ -268,8 +307,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
                         const int idx = q * 4 + e;
                         if (idx < len) {
                             const long long j = j0 + idx;
-                            for (int r = 0; r < a.n_ranks; ++r)
-                                acc[ch][e] = __fadd_rn(acc[ch][e], Lp<GT>::widen(static_cast<const uint16_t*>(a.rank[r])[j]));
+                            for (int r = 0; r < a.n_ranks; ++r) {
+                                if constexpr (GT == kGradQ8) {
+                                    const float code = static_cast<float>(static_cast<const signed char*>(a.rank[r])[j]);
+                                    acc[ch][e] = __fadd_rn(acc[ch][e], __fmul_rn(code, rank_scale(a, r, cur.seg, cur.t, ch)));
+                                } else {
+                                    acc[ch][e] = __fadd_rn(acc[ch][e], Lp<GT>::widen(static_cast<const uint16_t*>(a.rank[r])[j]));
+                                }
+                            }
 #pragma unroll
                             for (int k = 0; k < kMaxSide; ++k)
                                 if (k < a.n_side) sv[ch][k][e] = a.side[k][j];
@@ -487,7 +532,8 @@ cudaError_t launch_one(StreamArgs& a, cudaStream_t st)
     if (di.sms <= 0) return cudaErrorInvalidDevice;
     // stage size: rank slots + fp32 side streams of one tile
     const int slots = a.n_ranks < kGroupRanks ? a.n_ranks : kGroupRanks;
-    a.stage_bytes = static_cast<unsigned>(slots * kTile * 2 + a.n_side * kTile * 4);
+    const int eb = (GT == kGradQ8) ? 1 : 2;
+    a.stage_bytes = static_cast<unsigned>(slots * kTile * eb + a.n_side * kTile * 4);
     int stages = (di.smem_optin - kStageOffset) / static_cast<int>(a.stage_bytes);
     if (stages > kMaxStages) stages = kMaxStages;
     if (stages < 2) return cudaErrorInvalidConfiguration;
@@ -515,6 +561,10 @@ cudaError_t launch_one(StreamArgs& a, cudaStream_t st)
 cudaError_t launch_stream(int op, int grad_dtype, int param_dtype, StreamArgs& a, cudaStream_t st)
 {
     const bool gb = grad_dtype == ZERO_BF16, pb = param_dtype == ZERO_BF16;
+    if (grad_dtype == kGradQ8) {   // int8 ranks: the fused step only
+        if (op != OP_FUSED) return cudaErrorInvalidValue;
+        return pb ? launch_one<kGradQ8, ZERO_BF16, OP_FUSED>(a, st) : launch_one<kGradQ8, ZERO_FP16, OP_FUSED>(a, st);
+    }
     switch (op) {
     case OP_FUSED:
         if (gb) return pb ? launch_one<ZERO_BF16, ZERO_BF16, OP_FUSED>(a, st) : launch_one<ZERO_BF16, ZERO_FP16, OP_FUSED>(a, st);
