@@ -211,7 +211,8 @@ class Job:
             nbs = -(-self.plan.shard // 2048)
             row16 = (w["psi"] + 15) // 16 * 16
             self.codes = [torch.empty(w["n_d"], row16, dtype=torch.int8, device=device) for _ in self.grads]
-            self.qscales = [torch.empty(w["n_d"] * w["n_d"] * nbs, device=device) for _ in self.grads]
+            n_dp = (w["n_d"] + 3) // 4 * 4
+            self.qscales = [torch.empty(w["n_d"] * nbs * n_dp, device=device) for _ in self.grads]
             for k in range(len(self.grads)):
                 self.quantize(k)
         self.ws = torch.zeros(max(self.plan.workspace_bytes(self.hp), 256), dtype=torch.uint8, device=device)

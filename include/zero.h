@@ -275,9 +275,12 @@ ZERO_API zero_status zero_step_fused_qgather(const zero_plan* plan, const zero_h
  * Sender side: rank q's bf16 gradient (>= Psi elements) -> int8 codes at the
  * global index j < Psi and fp32 block scales.  rank_codes: host array of n_d
  * device pointers (>= Psi int8 each, 16-byte aligned).  rank_scales: one
- * array of n_d * n_d * ceil(S/block) floats, rank q's scales starting at
- * q * n_d * ceil(S/block), shard-major, 0 for blocks past a shard's valid
- * length.  Plan gradient dtype bf16; 32 <= block <= 65536, a multiple of 32. */
+ * array of n_d * ceil(S/block) rows of n_dp = roundup(n_d, 4) floats, block-
+ * major and rank-minor: rank q's scale of block b of shard r at
+ * [(r * ceil(S/block) + b) * n_dp + q] (so one tile's scales of all ranks
+ * are contiguous); 0 for blocks past a shard's valid length and for the
+ * padding columns q >= n_d.  Plan gradient dtype bf16; 32 <= block <= 65536,
+ * a multiple of 32.                                                          */
 ZERO_API zero_status zero_quantize_grads(const zero_plan* plan, const void* const* rank_grads, int block,
                                          signed char* const* rank_codes, float* rank_scales,
                                          void* stream);

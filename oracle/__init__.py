@@ -85,9 +85,10 @@ def lib():
             "zo_scalars_init": (None, [ctypes.POINTER(Scalars), f32]),
             "zo_quantize_block": (None, [ll, _u16p, _i8p, _f32p, _u16p]),
             "zo_quant_gather": (None, [i32, ll, ll, i32, _u16p, _i8p, _f32p, _u16p]),
-            "zo_quantize_ranks": (None, [i32, ll, ll, i32, vp, vp, vp]),
-            "zo_reduce_scatter_q": (None, [i32, ll, ll, i32, vp, vp, f32, _f32p]),
-            "zo_zero_step_qgz": (i32, [i32, ll, i32, i32, i32, vp, vp, ctypes.POINTER(Hparams),
+            "zo_qgz_rank_stride": (ll, [i32]),
+            "zo_quantize_ranks": (None, [i32, ll, ll, i32, vp, vp, _f32p]),
+            "zo_reduce_scatter_q": (None, [i32, ll, ll, i32, vp, _f32p, f32, _f32p]),
+            "zo_zero_step_qgz": (i32, [i32, ll, i32, i32, i32, vp, _f32p, ctypes.POINTER(Hparams),
                                        ctypes.POINTER(Scalars), _f32p, _f32p, _f32p, _u16p, _u16p, i32]),
         }
         for name, (res, args) in sig.items():
@@ -315,22 +316,28 @@ def quant_gather(shards_flat, n_d, psi, shard, block):
 
 
 # ------------------------------------------- quantized gradient exchange --
+def qgz_rank_stride(n_d):
+    return lib().zo_qgz_rank_stride(n_d)
+
+
 def quantize_ranks(grads, psi, shard, block):
-    """Per rank: int8 codes (psi long, global index) and scales
-    (n_d * ceil(S/block), shard-major) of its bf16 gradient."""
+    """Every rank's int8 codes (psi long, global index) and all scales in one
+    array of shape [n_d * nbs, n_dp]: row r * nbs + b, column = rank."""
     rows = [np.ascontiguousarray(g[:psi], dtype=np.uint16) for g in grads]
     n_d = len(rows)
     nbs = (shard + block - 1) // block
+    n_dp = qgz_rank_stride(n_d)
     codes = [np.zeros(max(psi, 1), np.int8) for _ in range(n_d)]
-    scales = [np.zeros(n_d * nbs, np.float32) for _ in range(n_d)]
-    lib().zo_quantize_ranks(n_d, psi, shard, block, _ptr_array(rows), _ptr_array(codes), _ptr_array(scales))
+    scales = np.zeros((n_d * nbs, n_dp), np.float32)
+    lib().zo_quantize_ranks(n_d, psi, shard, block, _ptr_array(rows), _ptr_array(codes), _ptr(scales, ctypes.c_float))
     return codes, scales
 
 
 def reduce_scatter_q(codes, scales, psi, shard, block, divisor):
     n_d = len(codes)
     out = np.empty(n_d * shard, dtype=np.float32)
-    lib().zo_reduce_scatter_q(n_d, psi, shard, block, _ptr_array(codes), _ptr_array(scales), divisor,
+    sc = np.ascontiguousarray(scales, dtype=np.float32)
+    lib().zo_reduce_scatter_q(n_d, psi, shard, block, _ptr_array(codes), _ptr(sc, ctypes.c_float), divisor,
                               _ptr(out, ctypes.c_float))
     return out
 
@@ -339,12 +346,12 @@ def zero_step_qgz(codes, scales, block, hp, state, shard_pad, stage, psi, param_
                   gathered=None):
     """The ZeRO step with the quantized gradient exchange (state n_d*S)."""
     n_d = len(codes)
-    S = shard_size(psi, n_d, shard_pad)
+    sc = np.ascontiguousarray(scales, dtype=np.float32)
     if stage >= 3:
         lp_p, g_p = _ptr(lp_shards, ctypes.c_uint16), None
     else:
         lp_p, g_p = None, _ptr(gathered, ctypes.c_uint16)
-    return bool(lib().zo_zero_step_qgz(n_d, psi, shard_pad, stage, block, _ptr_array(codes), _ptr_array(scales),
+    return bool(lib().zo_zero_step_qgz(n_d, psi, shard_pad, stage, block, _ptr_array(codes), _ptr(sc, ctypes.c_float),
                                        ctypes.byref(hp), ctypes.byref(state.scalars),
                                        _ptr(state.master, ctypes.c_float), _ptr(state.m, ctypes.c_float),
                                        _ptr(state.v, ctypes.c_float), lp_p, g_p, param_dtype))

@@ -571,11 +571,19 @@ void zo_quant_gather(int n_d, long long psi, long long shard, int block, const u
 /* destination shard's start), only codes and scales travel, and the shard   */
 /* owner reconstructs every rank's value as (float)code * scale (one fp32    */
 /* rounding) and adds the ranks in order from +0 before dividing once.       */
+/* Scale layout (a wire-format choice): block-major, rank-minor,             */
+/* scales[(r * nbs + b) * n_dp + q] for rank q's block b of shard r, with    */
+/* nbs = ceil(S / block) and n_dp = n_d rounded up to a multiple of 4 (the   */
+/* entries for q >= n_d are 0).                                               */
 /* ------------------------------------------------------------------------ */
+long long zo_qgz_rank_stride(int n_d) { return ((long long)n_d + 3) / 4 * 4; }
+
 void zo_quantize_ranks(int n_d, long long psi, long long shard, int block, const uint16_t* const* grads,
-                       int8_t* const* codes, float* const* scales)
+                       int8_t* const* codes, float* scales)
 {
     long long blocks_per_shard = (shard + block - 1) / block;
+    long long n_dp = zo_qgz_rank_stride(n_d);
+    for (long long i = 0; i < (long long)n_d * blocks_per_shard * n_dp; ++i) scales[i] = 0.0f;
     uint16_t* deq = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)block);
     for (int q = 0; q < n_d; ++q) {
         for (int r = 0; r < n_d; ++r) {
@@ -583,12 +591,9 @@ void zo_quantize_ranks(int n_d, long long psi, long long shard, int block, const
             for (long long b = 0; b < blocks_per_shard; ++b) {
                 long long lo = b * block;
                 long long hi = lo + block < len ? lo + block : len;
-                float* sc = scales[q] + (long long)r * blocks_per_shard + b;
-                if (hi <= lo) {
-                    *sc = 0.0f;
-                    continue;
-                }
+                if (hi <= lo) continue;
                 long long off = (long long)r * shard + lo;
+                float* sc = scales + ((long long)r * blocks_per_shard + b) * n_dp + q;
                 zo_quantize_block(hi - lo, grads[q] + off, codes[q] + off, sc, deq);
             }
         }
@@ -597,9 +602,10 @@ void zo_quantize_ranks(int n_d, long long psi, long long shard, int block, const
 }
 
 void zo_reduce_scatter_q(int n_d, long long psi, long long shard, int block, const int8_t* const* codes,
-                         const float* const* scales, float divisor, float* shards)
+                         const float* scales, float divisor, float* shards)
 {
     long long blocks_per_shard = (shard + block - 1) / block;
+    long long n_dp = zo_qgz_rank_stride(n_d);
     for (int r = 0; r < n_d; ++r) {
         long long len = zo_valid_len(psi, shard, r);
         for (long long i = 0; i < shard; ++i) {
@@ -608,16 +614,16 @@ void zo_reduce_scatter_q(int n_d, long long psi, long long shard, int block, con
                 shards[j] = 0.0f;
                 continue;
             }
-            long long sidx = (long long)r * blocks_per_shard + i / block;
+            const float* sblk = scales + ((long long)r * blocks_per_shard + i / block) * n_dp;
             float sum = 0.0f;
-            for (int q = 0; q < n_d; ++q) sum = sum + (float)codes[q][j] * scales[q][sidx];
+            for (int q = 0; q < n_d; ++q) sum = sum + (float)codes[q][j] * sblk[q];
             shards[j] = sum / divisor;
         }
     }
 }
 
 int zo_zero_step_qgz(int n_d, long long psi, int shard_pad, int stage, int block, const int8_t* const* codes,
-                     const float* const* scales, const zo_hparams* hp, zo_scalars* sc, float* master, float* m,
+                     const float* scales, const zo_hparams* hp, zo_scalars* sc, float* master, float* m,
                      float* v, uint16_t* lp_shards, uint16_t* gathered, int param_dtype)
 {
     long long S = zo_shard_size(psi, n_d, shard_pad);

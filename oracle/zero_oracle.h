@@ -109,12 +109,13 @@ void zo_quant_gather(int n_d, long long psi, long long shard, int block, const u
                      int8_t* codes, float* scales, uint16_t* gathered);
 
 /* ---- quantized gradient exchange (ZeRO++ qgZ reading) ---- */
+long long zo_qgz_rank_stride(int n_d);
 void zo_quantize_ranks(int n_d, long long psi, long long shard, int block, const uint16_t* const* grads,
-                       int8_t* const* codes, float* const* scales);
+                       int8_t* const* codes, float* scales);
 void zo_reduce_scatter_q(int n_d, long long psi, long long shard, int block, const int8_t* const* codes,
-                         const float* const* scales, float divisor, float* shards);
+                         const float* scales, float divisor, float* shards);
 int zo_zero_step_qgz(int n_d, long long psi, int shard_pad, int stage, int block, const int8_t* const* codes,
-                     const float* const* scales, const zo_hparams* hp, zo_scalars* sc, float* master, float* m,
+                     const float* scales, const zo_hparams* hp, zo_scalars* sc, float* master, float* m,
                      float* v, uint16_t* lp_shards, uint16_t* gathered, int param_dtype);
 
 #ifdef __cplusplus

@@ -45,10 +45,10 @@ MUTATIONS = [
     ("quantizer divides by 128", "float s = amax / 127.0f;", "float s = amax / 128.0f;"),
     ("quantizer truncates", "q = rintf(zo_bf16_to_f32(x_bf16[i]) / s);", "q = truncf(zo_bf16_to_f32(x_bf16[i]) / s);"),
     ("stage 2 keeps full gradients", "    case 2:\n        grads = 2.0 * psi / n_d;", "    case 2:\n        grads = 2.0 * psi;"),
-    ("qgZ scale of the wrong block", "long long sidx = (long long)r * blocks_per_shard + i / block;",
-     "long long sidx = (long long)r * blocks_per_shard + (i + 1) / block;"),
-    ("qgZ ranks summed in reverse", "for (int q = 0; q < n_d; ++q) sum = sum + (float)codes[q][j] * scales[q][sidx];",
-     "for (int q = n_d - 1; q >= 0; --q) sum = sum + (float)codes[q][j] * scales[q][sidx];"),
+    ("qgZ scale of the wrong block", "const float* sblk = scales + ((long long)r * blocks_per_shard + i / block) * n_dp;",
+     "const float* sblk = scales + ((long long)r * blocks_per_shard + (i + 1) / block) * n_dp;"),
+    ("qgZ ranks summed in reverse", "for (int q = 0; q < n_d; ++q) sum = sum + (float)codes[q][j] * sblk[q];",
+     "for (int q = n_d - 1; q >= 0; --q) sum = sum + (float)codes[q][j] * sblk[q];"),
     ("qgZ blocks not aligned to shards", "long long off = (long long)r * shard + lo;\n                zo_quantize_block(hi - lo, grads[q]",
      "long long off = (long long)r * shard + lo + (r > 0);\n                zo_quantize_block(hi - lo, grads[q]"),
     ("stage 3 comm counts one gather", "return reduce_scatter + 2.0 * all_gather;", "return reduce_scatter + all_gather;"),

@@ -37,9 +37,9 @@ def test_lossless_on_grid_equals_the_plain_step(n_d, psi, pad, block, stage):
     for step in range(3):
         rows = _on_grid_grads(n_d, psi, S, block, 10 + step, seed=step)
         codes, scales = oracle.quantize_ranks(rows, psi, S, block)
-        for sc in scales:
-            used = sc[sc != 0]
-            assert np.all(used == np.float32(2.0 ** -(10 + step)))
+        used = scales[:, :n_d][scales[:, :n_d] != 0]
+        assert np.all(used == np.float32(2.0 ** -(10 + step)))
+        assert not scales[:, n_d:].any()          # rank padding of the layout
         bufs_a = dict(lp_shards=np.zeros(n_d * S, np.uint16), gathered=np.zeros(psi, np.uint16))
         bufs_b = dict(lp_shards=np.zeros(n_d * S, np.uint16), gathered=np.zeros(psi, np.uint16))
         oracle.zero_step(rows, BF16, hp, a, pad, stage, **bufs_a)
@@ -61,7 +61,7 @@ def test_codes_are_the_block_quantizers(n_d, psi, pad, block):
         flat[:psi] = rows[q]
         c, s, _ = oracle.quant_gather(flat, n_d, psi, S, block)
         assert np.array_equal(codes[q][:psi], c[:psi])
-        assert np.array_equal(scales[q], s)
+        assert np.array_equal(scales[:, q], s)
 
 
 @pytest.mark.parametrize("n_d", [1, 2, 8])
@@ -76,13 +76,13 @@ def test_reconstruction_error_is_within_half_a_step_per_rank(n_d):
     nbs = -(-S // block)
     j = np.arange(psi)
     sidx = (j // S) * nbs + (j % S) // block
-    half = np.sum([s[sidx] for s in scales], axis=0) / 2.0 / n_d
+    half = np.sum(scales[sidx, :n_d].astype(np.float64), axis=1) / 2.0 / n_d
     err = np.abs(got[:psi].astype(np.float64) - exact)
     # half a step per rank, plus the fp32 roundings of n_d products, n_d sums and one division
     assert np.all(err <= half * (1 + 1e-6) + (2 * n_d + 2) * 2.0 ** -24 * np.abs(exact) + 1e-30)
     if n_d == 1:
         # one rank: the average is exactly the dequantized value code * scale
-        want = np.array([np.float32(codes[0][i]) * scales[0][sidx[i]] for i in range(psi)], np.float32)
+        want = np.array([np.float32(codes[0][i]) * scales[sidx[i], 0] for i in range(psi)], np.float32)
         assert np.array_equal(got[:psi], want)
 
 
@@ -104,5 +104,5 @@ def test_rank_order_decides_the_rounding():
     assert [int(c[1]) for c in codes] == [64, 64, 64]
     got = oracle.reduce_scatter_q(codes, scales, psi, S, block, 3.0)
     assert got[1] == np.float32(1.0) / np.float32(3.0)
-    rev = oracle.reduce_scatter_q(codes[::-1], scales[::-1], psi, S, block, 3.0)
+    rev = oracle.reduce_scatter_q(codes[::-1], np.ascontiguousarray(scales[:, [2, 1, 0, 3]]), psi, S, block, 3.0)
     assert rev[1] == np.float32(1.0 + 2.0 ** -23) / np.float32(3.0)

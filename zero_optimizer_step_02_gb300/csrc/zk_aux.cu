@@ -418,15 +418,99 @@ cudaError_t launch_quant_gather(const void* shards, int n_d, long long shard, lo
     return cudaGetLastError();
 }
 
-// Sender side of the quantized gradient exchange: each rank's bf16 gradient
-// through the block quantizer above, codes and scales only.
+// Sender side of the quantized gradient exchange: rank q's bf16 gradient
+// through the block quantizer (codes at the global index, scales at
+// [(r * nbs + b) * n_dp + q]).  One warp per block.  A full, 16-byte aligned
+// block of 2048 is held in registers (8 x 16 bytes per lane) and quantized in
+// one pass; any other block is read twice (amax, then codes).
+__global__ void __launch_bounds__(256) k_quantize_rank(const uint16_t* __restrict__ x, int n_d, long long shard,
+                                                       long long psi, int block, long long nbs, long long n_dp, int q,
+                                                       signed char* __restrict__ codes, float* __restrict__ scales)
+{
+    const int lane = threadIdx.x & 31;
+    const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+    const long long nblocks = nbs * n_d;
+    const bool vec = (shard % 8) == 0;
+    for (long long bi = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); bi < nblocks;
+         bi += warps) {
+        const int r = static_cast<int>(bi / nbs);
+        const long long b = bi - static_cast<long long>(r) * nbs;
+        float* sc = scales + bi * n_dp + q;
+        if (q == 0 && lane < n_dp - n_d) scales[bi * n_dp + n_d + lane] = 0.0f;   // rank padding of the layout
+        long long valid = psi - static_cast<long long>(r) * shard;
+        valid = valid < 0 ? 0 : (valid > shard ? shard : valid);
+        const long long lo = b * block;
+        const long long hi = lo + block < valid ? lo + block : valid;
+        if (hi <= lo) {
+            if (lane == 0) *sc = 0.0f;
+            continue;
+        }
+        const long long j0 = static_cast<long long>(r) * shard + lo;
+        const int n = static_cast<int>(hi - lo);
+        if (vec && block == 2048 && n == 2048) {
+            uint4 w[8];
+#pragma unroll
+            for (int v = 0; v < 8; ++v) w[v] = reinterpret_cast<const uint4*>(x + j0)[v * 32 + lane];
+            float amax = 0.0f;
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+                const uint32_t ws[4] = {w[v].x, w[v].y, w[v].z, w[v].w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    amax = fmaxf(amax, fmaxf(fabsf(Lp<ZERO_BF16>::lo(ws[k])), fabsf(Lp<ZERO_BF16>::hi(ws[k]))));
+            }
+            amax = warp_max_f32(amax);
+            const float s = __fdiv_rn(amax, 127.0f);
+            if (lane == 0) *sc = s;
+            const float inv = quant_reciprocal(s);
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+                const uint32_t ws[4] = {w[v].x, w[v].y, w[v].z, w[v].w};
+                int8_t c[8];
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const float xs[4] = {Lp<ZERO_BF16>::lo(ws[2 * k]), Lp<ZERO_BF16>::hi(ws[2 * k]),
+                                         Lp<ZERO_BF16>::lo(ws[2 * k + 1]), Lp<ZERO_BF16>::hi(ws[2 * k + 1])};
+                    int8_t c4[4];
+                    quant_code4(xs, s, inv, c4);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) c[4 * k + e] = c4[e];
+                }
+                uint2 cq;
+                cq.x = (uint32_t)(uint8_t)c[0] | ((uint32_t)(uint8_t)c[1] << 8) | ((uint32_t)(uint8_t)c[2] << 16) |
+                       ((uint32_t)(uint8_t)c[3] << 24);
+                cq.y = (uint32_t)(uint8_t)c[4] | ((uint32_t)(uint8_t)c[5] << 8) | ((uint32_t)(uint8_t)c[6] << 16) |
+                       ((uint32_t)(uint8_t)c[7] << 24);
+                reinterpret_cast<uint2*>(codes + j0)[v * 32 + lane] = cq;
+            }
+            continue;
+        }
+        float amax = 0.0f;
+        for (int i = lane; i < n; i += 32) amax = fmaxf(amax, fabsf(Lp<ZERO_BF16>::widen(x[j0 + i])));
+        amax = warp_max_f32(amax);
+        const float s = __fdiv_rn(amax, 127.0f);
+        if (lane == 0) *sc = s;
+        const float inv = quant_reciprocal(s);
+        for (int i = lane; i < n; i += 32) codes[j0 + i] = quant_code(Lp<ZERO_BF16>::widen(x[j0 + i]), s, inv);
+    }
+}
+
 cudaError_t launch_quantize_grads(const void* const* ranks, int n_d, long long shard, long long psi, int block,
                                   signed char* const* codes, float* scales, cudaStream_t st)
 {
+    const int sms = sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
     const long long nbs = (shard + block - 1) / block;
+    const long long n_dp = (n_d + 3) / 4 * 4;
+    const long long nblocks = nbs * n_d;
+    if (nblocks <= 0) return cudaSuccess;
+    long long grid = (nblocks + 7) / 8;
+    if (grid > 16LL * sms) grid = 16LL * sms;
     for (int q = 0; q < n_d; ++q) {
-        const cudaError_t e = launch_quant_gather(ranks[q], n_d, shard, psi, block, codes[q],
-                                                  scales + static_cast<long long>(q) * n_d * nbs, nullptr, st);
+        count_launch();
+        k_quantize_rank<<<static_cast<unsigned>(grid), 256, 0, st>>>(static_cast<const uint16_t*>(ranks[q]), n_d, shard,
+                                                                     psi, block, nbs, n_dp, q, codes[q], scales);
+        const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

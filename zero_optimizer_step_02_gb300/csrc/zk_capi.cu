@@ -553,7 +553,7 @@ ZERO_API zero_status zero_step_fused_qgz(const zero_plan* p, const zero_hparams*
     a.tiles_per_seg = tiles_of(p->shard);
     a.q_blocks_per_shard = (p->shard + zk::kQuantBlock - 1) / zk::kQuantBlock;
     a.q_rank_scales = scales;
-    a.q_rank_scale_stride = a.q_blocks_per_shard * p->n_d;
+    a.q_rank_scale_stride = (p->n_d + 3) / 4 * 4;
     a.tma_ok = (p->shard % 16) == 0 ? 1 : 0;   // int8 slices start 16-byte aligned
     a.n_side = 3;
     a.side[0] = mi;

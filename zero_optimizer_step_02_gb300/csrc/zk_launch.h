@@ -24,8 +24,8 @@ struct StreamArgs {
     const float* side[4];              // fp32 inputs: OP_FUSED {master, m, v}; OP_ADAM {g, master, m, v}
     float* out_f32[3];                 // OP_FUSED/OP_ADAM {master, m, v}; OP_REDUCE {g or null}
     void* out_lp;                      // 16-bit parameters out (null: none)
-    const float* q_rank_scales;        // kGradQ8 ranks: scales, rank r at r * q_rank_scale_stride,
-    long long q_rank_scale_stride;     //   then shard-major blocks of kQuantBlock
+    const float* q_rank_scales;        // kGradQ8 ranks: scales, block-major, rank-minor:
+    long long q_rank_scale_stride;     //   [(shard * blocks_per_shard + block) * stride + rank], stride % 4 == 0
     signed char* q_codes;              // fused quantized gather (F_QUANT)
     float* q_scales;
     void* q_gathered;

@@ -71,24 +71,28 @@ struct TileCursor {
     }
 };
 
-// int8 code b of a packed word, as a float (exact)
-__device__ __forceinline__ float code_f32(uint32_t w, int b)
+// int8 code e of a packed word whose bytes were biased by 0x80 (wb = w ^
+// 0x80808080), as a float: the byte becomes the low mantissa bits of 2^23,
+// so the float is 2^23 + code + 128 exactly, and the subtraction is exact.
+// Full-rate FP ops instead of integer-to-float conversions.
+__device__ __forceinline__ float code_f32(uint32_t wb, int e)
 {
-    return __int2float_rn(static_cast<int>(static_cast<signed char>((w >> (8 * b)) & 0xFFu)));
+    return __fsub_rn(__uint_as_float(__byte_perm(wb, 0x4B000000u, 0x7540u + e)), 8388736.0f);
 }
 
-// scale of rank r's block holding chunk row ch of the current tile
+// scale of rank r's block holding chunk row ch of the current tile (global)
 __device__ __forceinline__ float rank_scale(const StreamArgs& a, int r, long long seg, long long t, int ch)
 {
-    return __ldg(a.q_rank_scales + static_cast<long long>(r) * a.q_rank_scale_stride +
-                 seg * a.q_blocks_per_shard + t * kChunksPerThread + ch);
+    return __ldg(a.q_rank_scales + (seg * a.q_blocks_per_shard + t * kChunksPerThread + ch) * a.q_rank_scale_stride +
+                 r);
 }
 
 // rank-ordered add of one rank's dequantized codes: acc += fl(code * scale)
 __device__ __forceinline__ void add_codes(float (&acc)[4], uint32_t w, float s)
 {
+    const uint32_t wb = w ^ 0x80808080u;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) acc[e] = __fadd_rn(acc[e], __fmul_rn(code_f32(w, e), s));
+    for (int e = 0; e < 4; ++e) acc[e] = __fadd_rn(acc[e], __fmul_rn(code_f32(wb, e), s));
 }
 
 template <int GT>
@@ -100,9 +104,15 @@ __device__ __forceinline__ void add_slice(float (&acc)[4], uint2 w)
     acc[3] = __fadd_rn(acc[3], Lp<GT>::hi(w.y));
 }
 
+// rank slices per pipeline stage: int8 slices are half the bytes of 16-bit
+// ones, so a stage takes twice as many to move the same bytes per barrier
+template <int GT>
+__host__ __device__ constexpr int group_ranks() { return GT == kGradQ8 ? 2 * kGroupRanks : kGroupRanks; }
+
 template <int GT, int PT, int OP>
 __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ StreamArgs a)
 {
+    constexpr int kG = group_ranks<GT>();
     extern __shared__ __align__(1024) unsigned char smem[];
     Shared* sh = reinterpret_cast<Shared*>(smem);
     unsigned char* ring = smem + kStageOffset;
@@ -150,10 +160,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
     // a flagged loss-scaling step writes nothing (uniform over the CTA)
     const bool skip = sh->c.skip != 0;
 
-    const int n_groups = a.n_ranks > 0 ? (a.n_ranks + kGroupRanks - 1) / kGroupRanks : 1;
-    const int rank_slots = a.n_ranks < kGroupRanks ? a.n_ranks : kGroupRanks;
+    const int n_groups = a.n_ranks > 0 ? (a.n_ranks + kG - 1) / kG : 1;
+    const int rank_slots = a.n_ranks < kG ? a.n_ranks : kG;
     constexpr uint32_t kEB = (GT == kGradQ8) ? 1u : 2u;   // bytes per rank element
-    const uint32_t side_off = static_cast<uint32_t>(rank_slots) * kTile * kEB;
+    // int8 ranks: the group's block scales (2 blocks x 8 ranks) follow the rank slices
+    constexpr uint32_t kScaleBytes = (GT == kGradQ8) ? kChunksPerThread * kG * 4u : 0u;
+    const uint32_t scale_off = static_cast<uint32_t>(rank_slots) * kTile * kEB;
+    const uint32_t side_off = scale_off + kScaleBytes;
 
     bool nonfinite = false;
     float sq_hi = 0.0f, sq_lo = 0.0f;
@@ -171,18 +184,32 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
                 int len;
                 cur.span(a, j0, len);
                 if (len != kTile || !a.tma_ok) continue;
+                // int8 ranks: the row of scales of the tile's first block
+                const float* srow = (GT == kGradQ8)
+                                        ? a.q_rank_scales + (cur.seg * a.q_blocks_per_shard + cur.t * kChunksPerThread) *
+                                                                a.q_rank_scale_stride
+                                        : nullptr;
                 for (int g = 0; g < n_groups; ++g) {
                     if (!mbar_wait_bounded(&sh->empty[s], ph ^ 1u, &sh->abort, a.timeout_ns)) {
                         atomicExch(&sh->abort, 1);
                         break;
                     }
-                    const int r0 = g * kGroupRanks;
-                    const int nr = a.n_ranks - r0 < kGroupRanks ? a.n_ranks - r0 : kGroupRanks;
+                    const int r0 = g * kG;
+                    const int nr = a.n_ranks - r0 < kG ? a.n_ranks - r0 : kG;
                     const bool last = g == n_groups - 1;
                     const uint32_t rank_bytes = kTile * kEB;
-                    const uint32_t bytes = (nr > 0 ? nr : 0) * rank_bytes + (last ? a.n_side * kTile * 4u : 0u);
+                    // int8 ranks: this group's scales of the tile's two blocks, rounded up to 4 ranks
+                    // (the wire layout pads ranks to a multiple of 4, so the copy stays in bounds)
+                    const uint32_t nsc = (GT == kGradQ8) ? static_cast<uint32_t>((nr + 3) / 4 * 4) : 0u;
+                    const uint32_t bytes = (nr > 0 ? nr : 0) * rank_bytes + (last ? a.n_side * kTile * 4u : 0u) +
+                                           kChunksPerThread * nsc * 4u;
                     unsigned char* st = ring + static_cast<size_t>(s) * a.stage_bytes;
                     mbar_arrive_expect_tx(&sh->full[s], bytes);
+                    if constexpr (GT == kGradQ8) {
+                        for (int ch = 0; ch < kChunksPerThread; ++ch)
+                            bulk_load(st + scale_off + ch * kG * 4u, srow + ch * a.q_rank_scale_stride + r0,
+                                      nsc * 4u, &sh->full[s]);
+                    }
                     for (int k = 0; k < nr; ++k)
                         bulk_load(st + k * rank_bytes, static_cast<const unsigned char*>(a.rank[r0 + k]) + j0 * kEB,
                                   rank_bytes, &sh->full[s]);
@@ -243,22 +270,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
                     }
                     if (alive) {
                         const unsigned char* st = ring + static_cast<size_t>(s) * a.stage_bytes;
-                        const int r0 = g * kGroupRanks;
-                        const int nr = a.n_ranks - r0 < kGroupRanks ? a.n_ranks - r0 : kGroupRanks;
+                        const int r0 = g * kG;
+                        const int nr = a.n_ranks - r0 < kG ? a.n_ranks - r0 : kG;
                         if constexpr (GT == kGradQ8) {
-                            // ranks outer: both chunk rows' block scales of a rank loaded once
-                            const float* sp = a.q_rank_scales + r0 * a.q_rank_scale_stride +
-                                              cur.seg * a.q_blocks_per_shard + cur.t * kChunksPerThread;
+                            // scales of this group's ranks arrived with the stage (broadcast reads)
+                            const float* ssc = reinterpret_cast<const float*>(st + scale_off);
+#pragma unroll
+                            for (int ch = 0; ch < kChunksPerThread; ++ch) {
+                                const int q = ch * kConsumers + tid;
 #pragma unroll 4
-                            for (int k = 0; k < nr; ++k) {
-                                float scl[kChunksPerThread];
-#pragma unroll
-                                for (int ch = 0; ch < kChunksPerThread; ++ch) scl[ch] = __ldg(sp + ch);
-                                sp += a.q_rank_scale_stride;
-#pragma unroll
-                                for (int ch = 0; ch < kChunksPerThread; ++ch) {
-                                    const uint32_t w = reinterpret_cast<const uint32_t*>(st + k * kTile)[ch * kConsumers + tid];
-                                    add_codes(acc[ch], w, scl[ch]);
+                                for (int k = 0; k < nr; ++k) {
+                                    const uint32_t w = reinterpret_cast<const uint32_t*>(st + k * kTile)[q];
+                                    add_codes(acc[ch], w, ssc[ch * kG + k]);
                                 }
                             }
                         } else {
@@ -531,9 +554,11 @@ cudaError_t launch_one(StreamArgs& a, cudaStream_t st)
     const DevInfo di = device_info(dev);
     if (di.sms <= 0) return cudaErrorInvalidDevice;
     // stage size: rank slots + fp32 side streams of one tile
-    const int slots = a.n_ranks < kGroupRanks ? a.n_ranks : kGroupRanks;
+    constexpr int kG = group_ranks<GT>();
+    const int slots = a.n_ranks < kG ? a.n_ranks : kG;
     const int eb = (GT == kGradQ8) ? 1 : 2;
-    a.stage_bytes = static_cast<unsigned>(slots * kTile * eb + a.n_side * kTile * 4);
+    const int scale_bytes = (GT == kGradQ8) ? kChunksPerThread * kG * 4 : 0;
+    a.stage_bytes = static_cast<unsigned>(slots * kTile * eb + scale_bytes + a.n_side * kTile * 4);
     int stages = (di.smem_optin - kStageOffset) / static_cast<int>(a.stage_bytes);
     if (stages > kMaxStages) stages = kMaxStages;
     if (stages < 2) return cudaErrorInvalidConfiguration;
