@@ -86,6 +86,7 @@ def lib():
             "zo_quantize_block": (None, [ll, _u16p, _i8p, _f32p, _u16p]),
             "zo_quant_gather": (None, [i32, ll, ll, i32, _u16p, _i8p, _f32p, _u16p]),
             "zo_qgz_rank_stride": (ll, [i32]),
+            "zo_reduce_points_q": (None, [i32, ll, vp, vp, f32, _f32p]),
             "zo_quantize_ranks": (None, [i32, ll, ll, i32, vp, vp, _f32p]),
             "zo_reduce_scatter_q": (None, [i32, ll, ll, i32, vp, _f32p, f32, _f32p]),
             "zo_zero_step_qgz": (i32, [i32, ll, i32, i32, i32, vp, _f32p, ctypes.POINTER(Hparams),
@@ -355,3 +356,13 @@ def zero_step_qgz(codes, scales, block, hp, state, shard_pad, stage, psi, param_
                                        ctypes.byref(hp), ctypes.byref(state.scalars),
                                        _ptr(state.master, ctypes.c_float), _ptr(state.m, ctypes.c_float),
                                        _ptr(state.v, ctypes.c_float), lp_p, g_p, param_dtype))
+
+
+def reduce_points_q(codes_at, scales_at, divisor):
+    """Reconstructed average at sampled points: codes_at[q], scales_at[q] are
+    rank q's codes and block scales gathered at the points."""
+    c = [np.ascontiguousarray(x, dtype=np.int8) for x in codes_at]
+    sc = [np.ascontiguousarray(x, dtype=np.float32) for x in scales_at]
+    out = np.empty(c[0].size, dtype=np.float32)
+    lib().zo_reduce_points_q(len(c), c[0].size, _ptr_array(c), _ptr_array(sc), divisor, _ptr(out, ctypes.c_float))
+    return out

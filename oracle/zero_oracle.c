@@ -634,3 +634,16 @@ int zo_zero_step_qgz(int n_d, long long psi, int shard_pad, int stage, int block
     return step_from_shards(n_d, psi, S, stage, shards, hp, sc, master, m, v, lp_shards, gathered,
                             param_dtype);
 }
+
+/* The same reconstruction on sampled points: out[i] = (sum over q in order of
+ * (float)codes[q][i] * scales[q][i]) / divisor, for n points whose codes and
+ * block scales were gathered per rank (full-size checks). */
+void zo_reduce_points_q(int n_d, long long n, const int8_t* const* codes, const float* const* scales,
+                        float divisor, float* out)
+{
+    for (long long i = 0; i < n; ++i) {
+        float sum = 0.0f;
+        for (int q = 0; q < n_d; ++q) sum = sum + (float)codes[q][i] * scales[q][i];
+        out[i] = sum / divisor;
+    }
+}

@@ -114,6 +114,8 @@ void zo_quantize_ranks(int n_d, long long psi, long long shard, int block, const
                        int8_t* const* codes, float* scales);
 void zo_reduce_scatter_q(int n_d, long long psi, long long shard, int block, const int8_t* const* codes,
                          const float* scales, float divisor, float* shards);
+void zo_reduce_points_q(int n_d, long long n, const int8_t* const* codes, const float* const* scales,
+                        float divisor, float* out);
 int zo_zero_step_qgz(int n_d, long long psi, int shard_pad, int stage, int block, const int8_t* const* codes,
                      const float* scales, const zo_hparams* hp, zo_scalars* sc, float* master, float* m,
                      float* v, uint16_t* lp_shards, uint16_t* gathered, int param_dtype);

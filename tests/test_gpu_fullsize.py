@@ -208,3 +208,49 @@ def test_psi_2_28_fused_quantized_gather_full_size():
         c, s, d = oracle.quantize_block(lp[sl])
         assert got_s[k] == np.float32(s)
         assert np.array_equal(got_codes[sl], c) and np.array_equal(got_g[sl], d)
+
+
+@pytest.mark.parametrize("n_d", [8, 64])
+def test_psi_2_28_quantized_gradient_exchange_full_size(n_d):
+    # the bench's qgZ workload: sender on every rank, then the fused receiver
+    # step; sampled elements against the oracle's point-wise reconstruction
+    psi = 1 << 28
+    if _free_gb() < n_d * psi * 3 / 1e9 + 20:
+        pytest.skip("not enough free device memory")
+    hp = z.hparams(lr=1e-3)
+    job = FullJob(psi, n_d, 2, z.ZERO_BF16, hp, seed=707 + n_d)
+    job.plan = z.Plan(psi, n_d, stage=2, grad_dtype=z.ZERO_BF16, shard_pad=16)
+    S = job.plan.shard
+    nbs = -(-S // 2048)
+    n_dp = (n_d + 3) // 4 * 4
+    codes = torch.empty(n_d, (psi + 15) // 16 * 16, dtype=torch.int8, device="cuda")
+    scales = torch.empty(n_d * nbs * n_dp, device="cuda")
+    idx = _sample(psi, 6)
+    job.fill_grads(1, 1e-3)
+    b = job.buf
+    z.zero_quantize_grads(job.plan.handle, b.rank_list(), 2048, [codes[r] for r in range(n_d)], scales)
+    ii = torch.from_numpy(idx).cuda()
+    st = [t[ii].cpu().numpy().copy() for t in (b.master, b.m, b.v)]
+    z.zero_step_fused_qgz(job.plan.handle, hp, [codes[r] for r in range(n_d)], scales, 2048, b.master, b.m, b.v,
+                          b.master, b.m, b.v, b.lp, b.scalars)
+    # the sender's codes at the samples are the oracle's: quantize the sampled
+    # blocks on the CPU from the same bf16 bytes
+    rows = (idx // S) * nbs + (idx % S) // 2048
+    sc_all = scales.view(-1, n_dp).cpu().numpy()
+    c_at = [codes[q][ii].cpu().numpy() for q in range(n_d)]
+    s_at = [sc_all[rows, q] for q in range(n_d)]
+    for blk in np.unique(rows)[:24]:
+        r, bb = divmod(int(blk), nbs)
+        lo = r * S + bb * 2048
+        hi = min(lo + 2048, psi, (r + 1) * S)
+        for q in (0, n_d - 1):
+            x = u16(b.grads[q, lo:hi])
+            oc, osc, _ = oracle.quantize_block(x)
+            assert osc == sc_all[blk, q]
+            assert np.array_equal(codes[q, lo:hi].cpu().numpy(), oc)
+    g = oracle.reduce_points_q(c_at, s_at, float(n_d))
+    hpo = oracle_hp(hp)
+    c = oracle.adam_consts(hpo, float(np.float32(hpo.beta1)), float(np.float32(hpo.beta2)))
+    p, m, v = (a.copy() for a in st)
+    oracle.adam_update(hpo, c, g, p, m, v)
+    job.check(idx, (p, m, v))

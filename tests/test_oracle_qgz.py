@@ -106,3 +106,19 @@ def test_rank_order_decides_the_rounding():
     assert got[1] == np.float32(1.0) / np.float32(3.0)
     rev = oracle.reduce_scatter_q(codes[::-1], np.ascontiguousarray(scales[:, [2, 1, 0, 3]]), psi, S, block, 3.0)
     assert rev[1] == np.float32(1.0 + 2.0 ** -23) / np.float32(3.0)
+
+
+def test_point_reduction_matches_the_shard_reduction():
+    # the sampled-point form used by the full-size checks computes the same
+    # values as the reduce-scatter form at every point
+    psi, n_d, pad, block = 9000, 4, 8, 2048
+    S = oracle.shard_size(psi, n_d, pad)
+    rng = np.random.default_rng(2)
+    rows = [oracle.f32_to_bf16(rng.normal(0, 1e-3, psi).astype(np.float32)) for _ in range(n_d)]
+    codes, scales = oracle.quantize_ranks(rows, psi, S, block)
+    full = oracle.reduce_scatter_q(codes, scales, psi, S, block, float(n_d))
+    nbs = -(-S // block)
+    j = np.arange(psi)
+    row = (j // S) * nbs + (j % S) // block
+    pts = oracle.reduce_points_q([c[:psi] for c in codes], [scales[row, q] for q in range(n_d)], float(n_d))
+    assert np.array_equal(pts.view(np.uint32), full[:psi].view(np.uint32))
