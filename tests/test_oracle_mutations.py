@@ -49,8 +49,9 @@ MUTATIONS = [
      "const float* sblk = scales + ((long long)r * blocks_per_shard + (i + 1) / block) * n_dp;"),
     ("qgZ ranks summed in reverse", "for (int q = 0; q < n_d; ++q) sum = sum + (float)codes[q][j] * sblk[q];",
      "for (int q = n_d - 1; q >= 0; --q) sum = sum + (float)codes[q][j] * sblk[q];"),
-    ("qgZ blocks not aligned to shards", "long long off = (long long)r * shard + lo;\n                zo_quantize_block(hi - lo, grads[q]",
-     "long long off = (long long)r * shard + lo + (r > 0);\n                zo_quantize_block(hi - lo, grads[q]"),
+    ("qgZ blocks not aligned to shards",
+     "long long off = (long long)r * shard + lo;\n                float* sc = scales +",
+     "long long off = (long long)r * shard + lo + (r > 0);\n                float* sc = scales +"),
     ("stage 3 comm counts one gather", "return reduce_scatter + 2.0 * all_gather;", "return reduce_scatter + all_gather;"),
 ]
 
