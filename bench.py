@@ -41,7 +41,7 @@ L2_BYTES = 129 * 1024 * 1024
 
 
 # ----------------------------------------------------------------- workloads
-def workload(cfg, nd=None, qgather=False, psi=None, qgz=False):
+def workload(cfg, nd=None, qgather=False, psi=None, qgz=False, gathers=1):
     """Sizes, hyper-parameters and the algorithmic bytes of one step.  psi
     overrides the parameter count (a smaller case of the same workload, for
     profiling)."""
@@ -55,8 +55,11 @@ def workload(cfg, nd=None, qgather=False, psi=None, qgz=False):
         w = dict(name="zero2_gpt2xl_psi1500000000_nd8_fp16_lossscale", psi=1_500_000_000, n_d=8, stage=2, pad=8,
                  gdt="fp16", sigma=1e-4, tail=False, lr=1e-4, b2=0.999, wd=0.0, clip=0.0, ls=True, layers=1)
     elif cfg == 4:
-        w = dict(name="zero3_llama3_8b_8layers_psil218112000_nd16", psi=218_112_000, n_d=16, stage=3, pad=8,
-                 gdt="bf16", sigma=1e-3, tail=False, lr=1e-3, b2=0.999, wd=0.0, clip=0.0, ls=False, layers=8)
+        # gathers: per layer and step, 1 (the workload as configured) or 2
+        # (forward and backward, the pages' 3-psi communication volume)
+        w = dict(name="zero3_llama3_8b_8layers_psil218112000_nd16" + ("_2gathers" if gathers == 2 else ""),
+                 psi=218_112_000, n_d=16, stage=3, pad=8, gdt="bf16", sigma=1e-3, tail=False, lr=1e-3, b2=0.999,
+                 wd=0.0, clip=0.0, ls=False, layers=8, gathers=gathers)
     elif cfg == 5:
         n = nd or 8
         w = dict(name="zero2_psi2p28_nd%d%s%s" % (n, "_qgather" if qgather else "", "_qgz" if qgz else ""),
@@ -72,7 +75,7 @@ def workload(cfg, nd=None, qgather=False, psi=None, qgz=False):
     if w["clip"] > 0:
         w["bytes_per_param"] = 2 * n_d + 34 if n_d > 4 else 4 * n_d + 26
     elif w["stage"] == 3:
-        w["bytes_per_param"] = 2 * n_d + 30
+        w["bytes_per_param"] = 2 * n_d + 26 + 4 * w.get("gathers", 1)
     elif w.get("qgather"):
         w["bytes_per_param"] = 2 * n_d + 27 + 4.0 / 2048
     elif w.get("qgz"):
@@ -237,9 +240,11 @@ class Job:
             gsel = l if w["layers"] > 1 else self.k
             if w["stage"] == 3:
                 S = self.plan.shard
-                # per-layer gather of the bf16 shards before use (itwiki: ZeRO-3)
-                z.zero_all_gather(h, [self.lp[l][r * S:(r + 1) * S] for r in range(w["n_d"])], self.gathered,
-                                  self.scalars)
+                # per-layer gather of the bf16 shards before use (itwiki: ZeRO-3
+                # gathers each layer for the forward pass and again for the backward)
+                for _ in range(w.get("gathers", 1)):
+                    z.zero_all_gather(h, [self.lp[l][r * S:(r + 1) * S] for r in range(w["n_d"])], self.gathered,
+                                      self.scalars)
             if w.get("qgz"):
                 k = gsel % len(self.grads)
                 z.zero_step_fused_qgz(h, self.hp, [self.codes[k][r] for r in range(w["n_d"])], self.qscales[k], 2048,
@@ -277,17 +282,19 @@ class Job:
 
 
 def l2_flush(torch, device, buf=[]):
-    """Write 4x the L2 size: evicts the step's inputs, and takes long enough
-    on the GPU that the host has enqueued the step before its start event."""
+    """Read 4x the L2 size: evicts the step's inputs with clean lines (a
+    write would leave dirty lines whose write-back the step would pay for),
+    and takes long enough that the host has enqueued the step before its
+    start event."""
     if not buf:
-        buf.append(torch.empty(4 * L2_BYTES // 4, dtype=torch.float32, device=device))
-    buf[0].fill_(1.0)
+        buf.append(torch.ones(4 * L2_BYTES // 4, dtype=torch.float32, device=device))
+    buf[0].sum()
 
 
 def gpu_arm(args, rank, world, device):
     import torch
     import zero_optimizer_step_02_gb300 as z
-    w = workload(args.config, args.nd, args.qgather, args.psi, args.qgz)
+    w = workload(args.config, args.nd, args.qgather, args.psi, args.qgz, args.gathers)
     torch.cuda.set_device(device)
     job = Job(w, device)
     torch.cuda.synchronize()
@@ -473,7 +480,7 @@ def oracle_sample(w, budget_s, max_steps=None):
 
 
 def reference_arm(args, rank, world):
-    w = workload(args.config, args.nd, args.qgather, args.psi, args.qgz)
+    w = workload(args.config, args.nd, args.qgather, args.psi, args.qgz, args.gathers)
     if rank != 0:
         return None
     for _ in range(args.warmup):
@@ -531,6 +538,7 @@ def main():
     ap.add_argument("--psi", type=int, default=None, help="smaller parameter count (profiling)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--qgz", action="store_true", help="quantized gradient exchange (config 5)")
+    ap.add_argument("--gathers", type=int, default=1, choices=[1, 2], help="ZeRO-3 gathers per layer and step")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -545,7 +553,7 @@ def main():
     out = gpu_arm(args, rank, world, device)
     if rank == 0:
         if not args.no_cpu_baseline and world == 1:
-            w = workload(args.config, args.nd, args.qgather, args.psi, args.qgz)
+            w = workload(args.config, args.nd, args.qgather, args.psi, args.qgz, args.gathers)
             psi, n_d, steps, el = oracle_sample(w, args.cpu_budget)
             out["cpu_baseline"] = {"value": psi * steps / el, "unit": UNIT, "cores": 1, "kind": "oracle",
                                    "sample": "%d of %d params, n_d=%d, %d steps in %.1f s, single-threaded C "
