@@ -439,8 +439,10 @@ ZERO_API zero_status zero_step_fused(const zero_plan* p, const zero_hparams* hp,
         if (clip_materialises(p)) {
             float* g = ghat_of(ws);
             if ((s = run_reduce(p, hp, ranks, g, true, ws, sc, st, &n)) != ZERO_OK) return s;
-            if ((s = run_adam(p, hp, g, mi, m_in, vi, mo, m_out, vo, lp, zk::F_CLIP | zk::F_FINALIZE | guard | epi, sc,
-                              st, ws, n)) != ZERO_OK)
+            // the Adam pass walks the tiles from the end: the reduced gradient the
+            // reduce pass wrote last is still in L2
+            if ((s = run_adam(p, hp, g, mi, m_in, vi, mo, m_out, vo, lp,
+                              zk::F_CLIP | zk::F_FINALIZE | guard | epi | zk::F_REVERSE, sc, st, ws, n)) != ZERO_OK)
                 return s;
         } else {
             if ((s = run_reduce(p, hp, ranks, nullptr, true, ws, sc, st, &n)) != ZERO_OK) return s;

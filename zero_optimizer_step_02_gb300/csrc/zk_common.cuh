@@ -42,6 +42,8 @@ enum : int {
     F_LSCALE = 1 << 5,  // divisor includes scalars->loss_scale
     F_FINALIZE = 1 << 6,  // every CTA sums the reduce pass's partials itself (clip coefficient)
     F_EPILOGUE = 1 << 7,  // the last CTA to finish commits the step scalars
+    F_REVERSE = 1 << 8,   // flat launches: walk the tiles from the end (reads what the
+                          // previous pass wrote last first, while it is still in L2)
 };
 
 // ------------------------------------------------------------- PTX wrappers

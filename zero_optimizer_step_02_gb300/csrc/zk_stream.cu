@@ -65,7 +65,8 @@ struct TileCursor {
         const long long lo = a.base + seg * a.seg_stride;
         long long hi = lo + a.seg_len;
         if (hi > a.limit) hi = a.limit;
-        j0 = lo + t * kTile;
+        const long long tt = (a.flags & F_REVERSE) ? a.tiles_per_seg - 1 - t : t;
+        j0 = lo + tt * kTile;
         const long long l = hi - j0;
         len = l <= 0 ? 0 : (l > kTile ? kTile : static_cast<int>(l));
     }
