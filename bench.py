@@ -41,7 +41,7 @@ L2_BYTES = 129 * 1024 * 1024
 
 
 # ----------------------------------------------------------------- workloads
-def workload(cfg, nd=None, qgather=False, psi=None, qgz=False, gathers=1):
+def workload(cfg, nd=None, qgather=False, psi=None, qgz=False, gathers=1, offload=False):
     """Sizes, hyper-parameters and the algorithmic bytes of one step.  psi
     overrides the parameter count (a smaller case of the same workload, for
     profiling)."""
@@ -70,6 +70,10 @@ def workload(cfg, nd=None, qgather=False, psi=None, qgz=False, gathers=1):
     if psi:
         w["psi"] = int(psi)
         w["name"] += "_psi%d" % w["psi"]
+    if offload:
+        # optimizer state in page-locked host memory, read and written over the CPU-GPU link
+        w["offload"] = True
+        w["name"] += "_offload"
     n_d = w["n_d"]
     # algorithmic bytes per parameter of one step (minimum HBM traffic)
     if w["clip"] > 0:
@@ -196,6 +200,11 @@ class Job:
         self.master = [synth.master_init(n, w["psi"], 7 + l, device=device) for l in range(L)]
         self.m = [torch.zeros(n, device=device) for _ in range(L)]
         self.v = [torch.zeros(n, device=device) for _ in range(L)]
+        self.offload = w.get("offload", False)
+        if self.offload:
+            self.master = [x.cpu().pin_memory() for x in self.master]
+            self.m = [torch.zeros(n).pin_memory() for _ in range(L)]
+            self.v = [torch.zeros(n).pin_memory() for _ in range(L)]
         self.pingpong = w["ls"]
         if self.pingpong:
             self.master2 = [torch.zeros(n, device=device) for _ in range(L)]
@@ -261,8 +270,9 @@ class Job:
                 self.m[l], self.m2[l] = self.m2[l], self.m[l]
                 self.v[l], self.v2[l] = self.v2[l], self.v[l]
             else:
-                z.zero_step_fused(h, self.hp, self.ranks(gsel), self.master[l], self.m[l], self.v[l],
-                                  self.master[l], self.m[l], self.v[l], self.lp[l], self.scalars, self.ws)
+                step = z.zero_step_fused_offload if self.offload else z.zero_step_fused
+                step(h, self.hp, self.ranks(gsel), self.master[l], self.m[l], self.v[l], self.master[l], self.m[l],
+                     self.v[l], self.lp[l], self.scalars, self.ws)
         self.k += 1
 
     def parts_step(self, ev):
@@ -294,7 +304,7 @@ def l2_flush(torch, device, buf=[]):
 def gpu_arm(args, rank, world, device):
     import torch
     import zero_optimizer_step_02_gb300 as z
-    w = workload(args.config, args.nd, args.qgather, args.psi, args.qgz, args.gathers)
+    w = workload(args.config, args.nd, args.qgather, args.psi, args.qgz, args.gathers, args.offload)
     torch.cuda.set_device(device)
     job = Job(w, device)
     torch.cuda.synchronize()
@@ -337,7 +347,7 @@ def gpu_arm(args, rank, world, device):
 
     # dominant kernel: per-kernel CUDA events on the launching stream
     peak, peak_kind = measured_hbm_peak()
-    if w["clip"] > 0 and w["n_d"] > 4:
+    if w["clip"] > 0 and w["n_d"] > 4 and not w.get("offload"):
         job.ghat = torch.zeros(job.plan.padded, device=device)
         n_rep = max(3, args.steps)
         dur = [0.0, 0.0, 0.0]
@@ -415,6 +425,9 @@ def gpu_arm(args, rank, world, device):
         out["kernel_ms"] = breakdown
     if sender:
         out["qgz_sender"] = sender
+    if w.get("offload"):
+        # the state's 12 bytes read + 12 written per parameter cross the CPU-GPU link
+        out["offload_link_gbs"] = round(24.0 * w["psi_total"] / (ms_per_step / 1e3) / 1e9, 1)
     return out
 
 
@@ -480,7 +493,7 @@ def oracle_sample(w, budget_s, max_steps=None):
 
 
 def reference_arm(args, rank, world):
-    w = workload(args.config, args.nd, args.qgather, args.psi, args.qgz, args.gathers)
+    w = workload(args.config, args.nd, args.qgather, args.psi, args.qgz, args.gathers, args.offload)
     if rank != 0:
         return None
     for _ in range(args.warmup):
@@ -539,6 +552,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--qgz", action="store_true", help="quantized gradient exchange (config 5)")
     ap.add_argument("--gathers", type=int, default=1, choices=[1, 2], help="ZeRO-3 gathers per layer and step")
+    ap.add_argument("--offload", action="store_true", help="optimizer state in page-locked host memory")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -553,7 +567,7 @@ def main():
     out = gpu_arm(args, rank, world, device)
     if rank == 0:
         if not args.no_cpu_baseline and world == 1:
-            w = workload(args.config, args.nd, args.qgather, args.psi, args.qgz, args.gathers)
+            w = workload(args.config, args.nd, args.qgather, args.psi, args.qgz, args.gathers, args.offload)
             psi, n_d, steps, el = oracle_sample(w, args.cpu_budget)
             out["cpu_baseline"] = {"value": psi * steps / el, "unit": UNIT, "cores": 1, "kind": "oracle",
                                    "sample": "%d of %d params, n_d=%d, %d steps in %.1f s, single-threaded C "

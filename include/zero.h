@@ -236,6 +236,22 @@ ZERO_API zero_status zero_step_fused(const zero_plan* plan, const zero_hparams* 
                                      float* m_out, float* v_out, void* lp_out,
                                      zero_dev_scalars* scalars_dev, void* ws, void* stream);
 
+/* ZeRO-Offload on a Grace-Blackwell node (itwiki "후속 기법", ZeRO-Offload
+ * row: the optimizer state moves to CPU memory).  The same step as
+ * zero_step_fused, with master/m/v (in and out) in page-locked host memory
+ * that the kernels read and write directly over the CPU-GPU link instead of
+ * HBM; gradients, the 16-bit parameters and the workspace stay in device
+ * memory.  The update still runs on the GPU.  Every state pointer must be
+ * page-locked host memory mapped at the same address on the device
+ * (cudaHostAlloc / torch pin_memory); anything else is refused with
+ * ZERO_ERR_INVALID_ARG before a launch.  Saves 12 bytes of HBM per
+ * parameter; the state's 24 bytes per parameter cross the CPU-GPU link.    */
+ZERO_API zero_status zero_step_fused_offload(const zero_plan* plan, const zero_hparams* hp,
+                                             const void* const* rank_grads, const float* master_in,
+                                             const float* m_in, const float* v_in, float* master_out,
+                                             float* m_out, float* v_out, void* lp_out,
+                                             zero_dev_scalars* scalars_dev, void* ws, void* stream);
+
 /* ----------------------------------------------------- quantized gather --- */
 /* ZeRO++ qwZ (itwiki "후속 기법", ZeRO++ row: weights are block-quantized for
  * the all-gather).  Per block of `block` consecutive elements of a shard

@@ -21,7 +21,7 @@ from ._capi import (ZERO_BF16, ZERO_FP16, ZERO_DEV_TIMEOUT, ZeroDevScalars, Zero
                     zero_plan_create_ex, zero_plan_destroy, zero_plan_memory, zero_plan_query, zero_quant_gather,
                     zero_reduce_scatter, zero_scalars_init, zero_status_str, zero_step_fused,
                     zero_step_fused_noalloc, zero_step_fused_qgather, zero_workspace_bytes,
-                    zero_quantize_grads, zero_step_fused_qgz)
+                    zero_quantize_grads, zero_step_fused_qgz, zero_step_fused_offload)
 
 __all__ = ["Plan", "StepBuffers", "read_scalars", "row_len", "hparams", "ZeroError", "ZeroHparams",
            "ZERO_BF16", "ZERO_FP16", "ZERO_DEV_TIMEOUT"] + [n for n in dir(_capi) if n.startswith("zero_")]

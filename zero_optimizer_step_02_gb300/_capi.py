@@ -80,6 +80,7 @@ _SIGS = {
     "zero_launch_count": (ctypes.c_ulonglong, []),
     "zero_step_fused_noalloc": (_i32, [_vp, _hp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "zero_quantize_grads": (_i32, [_vp, _vp, _i32, _vp, _vp, _vp]),
+    "zero_step_fused_offload": (_i32, [_vp, _hp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "zero_step_fused_qgz": (_i32, [_vp, _hp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -210,6 +211,15 @@ def zero_step_fused(plan, hp, rank_grads, master_in, m_in, v_in, master_out, m_o
     _check(_lib.zero_step_fused(plan, ctypes.byref(hp), _ptr_array(rank_grads), _addr(master_in), _addr(m_in),
                                 _addr(v_in), _addr(master_out), _addr(m_out), _addr(v_out), _addr(lp_out),
                                 _addr(scalars), _addr(ws), _stream(stream)), "zero_step_fused")
+
+
+def zero_step_fused_offload(plan, hp, rank_grads, master_in, m_in, v_in, master_out, m_out, v_out, lp_out, scalars,
+                            ws, stream=None):
+    """zero_step_fused with master/m/v in page-locked host memory (pin_memory tensors)."""
+    _check(_lib.zero_step_fused_offload(plan, ctypes.byref(hp), _ptr_array(rank_grads), _addr(master_in),
+                                        _addr(m_in), _addr(v_in), _addr(master_out), _addr(m_out), _addr(v_out),
+                                        _addr(lp_out), _addr(scalars), _addr(ws), _stream(stream)),
+           "zero_step_fused_offload")
 
 
 def zero_quant_gather(plan, shards_bf16, block, codes, scales, gathered, stream=None):

@@ -148,7 +148,8 @@ void set_finalize(StreamArgs& a, void* ws, int n)
 // (fin_ws / fin_n: the partials of the preceding reduce pass)
 zero_status run_fused(const zero_plan* p, const zero_hparams* hp, const void* const* ranks, const float* mi,
                       const float* m_in, const float* vi, float* mo, float* m_out, float* vo, void* lp,
-                      int flags, zero_dev_scalars* sc, cudaStream_t st, void* fin_ws = nullptr, int fin_n = 0)
+                      int flags, zero_dev_scalars* sc, cudaStream_t st, void* fin_ws = nullptr, int fin_n = 0,
+                      bool host_state = false)
 {
     // buckets only when no global check ties the pieces together
     const long long step =
@@ -160,6 +161,7 @@ zero_status run_fused(const zero_plan* p, const zero_hparams* hp, const void* co
         set_ranks(a, p, ranks);
         set_flat(a, lo, hi);
         a.n_side = 3;
+        a.n_side_tma = host_state ? 0 : 3;
         a.side[0] = mi;
         a.side[1] = m_in;
         a.side[2] = vi;
@@ -176,13 +178,15 @@ zero_status run_fused(const zero_plan* p, const zero_hparams* hp, const void* co
 
 zero_status run_adam(const zero_plan* p, const zero_hparams* hp, const float* g, const float* mi,
                      const float* m_in, const float* vi, float* mo, float* m_out, float* vo, void* lp, int flags,
-                     zero_dev_scalars* sc, cudaStream_t st, void* fin_ws = nullptr, int fin_n = 0)
+                     zero_dev_scalars* sc, cudaStream_t st, void* fin_ws = nullptr, int fin_n = 0,
+                     bool host_state = false)
 {
     StreamArgs a = base_args(p, hp, sc);
     if (flags & zk::F_FINALIZE) set_finalize(a, fin_ws, fin_n);
     set_flat(a, 0, p->psi);
     a.n_ranks = 0;
     a.n_side = 4;
+    a.n_side_tma = host_state ? 1 : 4;   // the reduced gradient stays in HBM
     a.side[0] = g;
     a.side[1] = mi;
     a.side[2] = m_in;
@@ -399,9 +403,13 @@ ZERO_API zero_status zero_all_gather(const zero_plan* p, const void* const* shar
     return from_cuda(zk::launch_all_gather(shards, p->n_d, p->shard, p->psi, gathered, sc, as_stream(stream)));
 }
 
-ZERO_API zero_status zero_step_fused(const zero_plan* p, const zero_hparams* hp, const void* const* ranks,
-                                     const float* mi, const float* m_in, const float* vi, float* mo, float* m_out,
-                                     float* vo, void* lp, zero_dev_scalars* sc, void* ws, void* stream)
+namespace {
+
+// The pass schedules of the fused step.  host_state: master/m/v live in
+// page-locked host memory and are read and written directly by the kernels.
+zero_status fused_step(const zero_plan* p, const zero_hparams* hp, const void* const* ranks, const float* mi,
+                       const float* m_in, const float* vi, float* mo, float* m_out, float* vo, void* lp,
+                       zero_dev_scalars* sc, void* ws, void* stream, bool host_state)
 {
     if (p == nullptr) return ZERO_ERR_INVALID_ARG;
     zero_status s;
@@ -423,14 +431,14 @@ ZERO_API zero_status zero_step_fused(const zero_plan* p, const zero_hparams* hp,
 
     if (!clip) {
         if (!ls) {
-            if ((s = run_fused(p, hp, ranks, mi, m_in, vi, mo, m_out, vo, lp, epi, sc, st)) != ZERO_OK) return s;
+            if ((s = run_fused(p, hp, ranks, mi, m_in, vi, mo, m_out, vo, lp, epi, sc, st, nullptr, 0, host_state)) != ZERO_OK) return s;
         } else if (speculative) {
             // update while detecting; undo from the in state if flagged
-            if ((s = run_fused(p, hp, ranks, mi, m_in, vi, mo, m_out, vo, lp, zk::F_DETECT | lsf, sc, st)) != ZERO_OK) return s;
+            if ((s = run_fused(p, hp, ranks, mi, m_in, vi, mo, m_out, vo, lp, zk::F_DETECT | lsf, sc, st, nullptr, 0, host_state)) != ZERO_OK) return s;
         } else {
             // in place: a read-only check pass first, then the guarded update
             if ((s = run_reduce(p, hp, ranks, nullptr, false, ws, sc, st)) != ZERO_OK) return s;
-            if ((s = run_fused(p, hp, ranks, mi, m_in, vi, mo, m_out, vo, lp, zk::F_GUARD | lsf | epi, sc, st)) != ZERO_OK) return s;
+            if ((s = run_fused(p, hp, ranks, mi, m_in, vi, mo, m_out, vo, lp, zk::F_GUARD | lsf | epi, sc, st, nullptr, 0, host_state)) != ZERO_OK) return s;
         }
     } else {
         // the update kernel finishes the reduce pass's norm in its prologue
@@ -442,18 +450,47 @@ ZERO_API zero_status zero_step_fused(const zero_plan* p, const zero_hparams* hp,
             // the Adam pass walks the tiles from the end: the reduced gradient the
             // reduce pass wrote last is still in L2
             if ((s = run_adam(p, hp, g, mi, m_in, vi, mo, m_out, vo, lp,
-                              zk::F_CLIP | zk::F_FINALIZE | guard | epi | zk::F_REVERSE, sc, st, ws, n)) != ZERO_OK)
+                              zk::F_CLIP | zk::F_FINALIZE | guard | epi | zk::F_REVERSE, sc, st, ws, n, host_state)) != ZERO_OK)
                 return s;
         } else {
             if ((s = run_reduce(p, hp, ranks, nullptr, true, ws, sc, st, &n)) != ZERO_OK) return s;
             if ((s = run_fused(p, hp, ranks, mi, m_in, vi, mo, m_out, vo, lp,
-                               zk::F_CLIP | zk::F_FINALIZE | guard | lsf | epi, sc, st, ws, n)) != ZERO_OK)
+                               zk::F_CLIP | zk::F_FINALIZE | guard | lsf | epi, sc, st, ws, n, host_state)) != ZERO_OK)
                 return s;
         }
     }
     if (!speculative) return ZERO_OK;
     ZK_TRY(zk::launch_repair(*hp, mi, m_in, vi, mo, m_out, vo, lp, p->param_dtype, p->psi, sc, st));
     return from_cuda(zk::launch_epilogue(*hp, sc, st));
+}
+
+}  // namespace
+
+ZERO_API zero_status zero_step_fused(const zero_plan* p, const zero_hparams* hp, const void* const* ranks,
+                                     const float* mi, const float* m_in, const float* vi, float* mo, float* m_out,
+                                     float* vo, void* lp, zero_dev_scalars* sc, void* ws, void* stream)
+{
+    return fused_step(p, hp, ranks, mi, m_in, vi, mo, m_out, vo, lp, sc, ws, stream, false);
+}
+
+ZERO_API zero_status zero_step_fused_offload(const zero_plan* p, const zero_hparams* hp, const void* const* ranks,
+                                             const float* mi, const float* m_in, const float* vi, float* mo,
+                                             float* m_out, float* vo, void* lp, zero_dev_scalars* sc, void* ws,
+                                             void* stream)
+{
+    // every state pointer must be page-locked host memory the device reaches
+    // at the same address; anything else is refused before a launch
+    const void* ptrs[] = {mi, m_in, vi, mo, m_out, vo};
+    for (const void* q : ptrs) {
+        if (q == nullptr) return ZERO_ERR_INVALID_ARG;
+        cudaPointerAttributes at;
+        if (cudaPointerGetAttributes(&at, q) != cudaSuccess) {
+            cudaGetLastError();
+            return ZERO_ERR_INVALID_ARG;
+        }
+        if (at.type != cudaMemoryTypeHost || at.devicePointer != q) return ZERO_ERR_INVALID_ARG;
+    }
+    return fused_step(p, hp, ranks, mi, m_in, vi, mo, m_out, vo, lp, sc, ws, stream, true);
 }
 
 ZERO_API zero_status zero_quant_gather(const zero_plan* p, const void* shards, int block, signed char* codes,
@@ -502,6 +539,7 @@ ZERO_API zero_status zero_step_fused_qgather(const zero_plan* p, const zero_hpar
     a.q_blocks_per_shard = (p->shard + zk::kQuantBlock - 1) / zk::kQuantBlock;
     a.tma_ok = (p->shard % 8) == 0 ? 1 : 0;
     a.n_side = 3;
+    a.n_side_tma = 3;
     a.side[0] = mi;
     a.side[1] = m_in;
     a.side[2] = vi;
@@ -558,6 +596,7 @@ ZERO_API zero_status zero_step_fused_qgz(const zero_plan* p, const zero_hparams*
     a.q_rank_scale_stride = (p->n_d + 3) / 4 * 4;
     a.tma_ok = (p->shard % 16) == 0 ? 1 : 0;   // int8 slices start 16-byte aligned
     a.n_side = 3;
+    a.n_side_tma = 3;
     a.side[0] = mi;
     a.side[1] = m_in;
     a.side[2] = vi;

@@ -37,6 +37,8 @@ struct StreamArgs {
     int n_seg;
     int n_ranks;                       // rank streams (0 for OP_ADAM)
     int n_side;                        // fp32 side streams
+    int n_side_tma;                    // the first n_side_tma of them are staged by bulk copies; the
+                                       // rest (state in page-locked host memory) are read directly
     int tma_ok;                        // every full tile is 16-byte aligned in every stream
     int flags;                         // F_* of zk_common.cuh
     int stages;                        // set by the launcher

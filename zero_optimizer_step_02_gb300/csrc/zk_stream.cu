@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
                     // int8 ranks: this group's scales of the tile's two blocks, rounded up to 4 ranks
                     // (the wire layout pads ranks to a multiple of 4, so the copy stays in bounds)
                     const uint32_t nsc = (GT == kGradQ8) ? static_cast<uint32_t>((nr + 3) / 4 * 4) : 0u;
-                    const uint32_t bytes = (nr > 0 ? nr : 0) * rank_bytes + (last ? a.n_side * kTile * 4u : 0u) +
+                    const uint32_t bytes = (nr > 0 ? nr : 0) * rank_bytes + (last ? a.n_side_tma * kTile * 4u : 0u) +
                                            kChunksPerThread * nsc * 4u;
                     unsigned char* st = ring + static_cast<size_t>(s) * a.stage_bytes;
                     mbar_arrive_expect_tx(&sh->full[s], bytes);
@@ -215,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
                         bulk_load(st + k * rank_bytes, static_cast<const unsigned char*>(a.rank[r0 + k]) + j0 * kEB,
                                   rank_bytes, &sh->full[s]);
                     if (last)
-                        for (int k = 0; k < a.n_side; ++k)
+                        for (int k = 0; k < a.n_side_tma; ++k)
                             bulk_load(st + side_off + k * kTile * 4u, a.side[k] + j0, kTile * 4u, &sh->full[s]);
                     sh->issued_parity[s] = static_cast<int>(ph);
                     if (++s == a.stages) {
@@ -264,6 +264,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
                 }
 
             if (fast) {
+                // side streams not staged (state in host memory): 16-byte loads issued
+                // now, before the wait for the gradient stage, so their latency overlaps it
+                if (a.n_side_tma < a.n_side && alive) {
+#pragma unroll
+                    for (int ch = 0; ch < kChunksPerThread; ++ch) {
+                        const long long jc = j0 + (ch * kConsumers + tid) * 4;
+#pragma unroll
+                        for (int k = 0; k < kMaxSide; ++k) {
+                            if (k >= a.n_side_tma && k < a.n_side) {
+                                const float4 f = *reinterpret_cast<const float4*>(a.side[k] + jc);
+                                sv[ch][k][0] = f.x;
+                                sv[ch][k][1] = f.y;
+                                sv[ch][k][2] = f.z;
+                                sv[ch][k][3] = f.w;
+                            }
+                        }
+                    }
+                }
                 for (int g = 0; g < n_groups; ++g) {
                     if (alive && !mbar_wait_bounded(&sh->full[s], ph, &sh->abort, a.timeout_ns)) {
                         alive = false;
@@ -302,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
                                 const int q = ch * kConsumers + tid;
 #pragma unroll
                                 for (int k = 0; k < kMaxSide; ++k) {
-                                    if (k < a.n_side) {
+                                    if (k < a.n_side_tma) {
                                         const float4 f = reinterpret_cast<const float4*>(
                                             st + side_off + k * kTile * 4)[q];
                                         sv[ch][k][0] = f.x;
@@ -559,7 +577,7 @@ cudaError_t launch_one(StreamArgs& a, cudaStream_t st)
     const int slots = a.n_ranks < kG ? a.n_ranks : kG;
     const int eb = (GT == kGradQ8) ? 1 : 2;
     const int scale_bytes = (GT == kGradQ8) ? kChunksPerThread * kG * 4 : 0;
-    a.stage_bytes = static_cast<unsigned>(slots * kTile * eb + scale_bytes + a.n_side * kTile * 4);
+    a.stage_bytes = static_cast<unsigned>(slots * kTile * eb + scale_bytes + a.n_side_tma * kTile * 4);
     int stages = (di.smem_optin - kStageOffset) / static_cast<int>(a.stage_bytes);
     if (stages > kMaxStages) stages = kMaxStages;
     if (stages < 2) return cudaErrorInvalidConfiguration;
