@@ -93,7 +93,8 @@ def workload(cfg, nd=None, qgather=False, psi=None, qgz=False, gathers=1, offloa
 
 # ------------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    """nvidia-smi clocks and throttle reasons, keeping the samples taken while
+    the timed region ran (mark() brackets it)."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -101,12 +102,16 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
-        self.lines = []
+        self.lines = []          # (arrival time, line)
+        self.window = [None, None]
+
+    def mark(self, which):
+        self.window[which] = time.monotonic()
 
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.Q,
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -115,7 +120,7 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
 
     def stop(self):
         if self.proc is None:
@@ -127,7 +132,13 @@ class ClockSampler:
             self.proc.kill()
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        t0, t1 = self.window
+        inside = [ln for t, ln in self.lines if t0 is not None and t1 is not None and t0 <= t <= t1 + 0.05]
+        if not inside and self.lines:
+            # a timed region shorter than the sampling period: the sample nearest to it
+            mid = (t0 + t1) / 2 if t0 is not None and t1 is not None else self.lines[-1][0]
+            inside = [min(self.lines, key=lambda x: abs(x[0] - mid))[1]]
+        for ln in inside:
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
@@ -142,7 +153,7 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples_in_timed_region": len(sm)}
 
 
 # ---------------------------------------------------------------- GPU arm
@@ -318,6 +329,7 @@ def gpu_arm(args, rank, world, device):
     clocks.start()
     time.sleep(0.3)
     n0 = z.zero_launch_count()
+    clocks.mark(0)
     if small:
         total_ms = 0.0
         for _ in range(args.steps):
@@ -339,6 +351,7 @@ def gpu_arm(args, rank, world, device):
         torch.cuda.synchronize()
         total_ms = a.elapsed_time(b)
         launches = z.zero_launch_count() - n0
+    clocks.mark(1)
     clk = clocks.stop()
     total_ms = dist_max(total_ms, world)
     ms_per_step = total_ms / args.steps
@@ -413,8 +426,7 @@ def gpu_arm(args, rank, world, device):
                   "frac": round(sbytes / (sms / 1e3) / 1e9 / peak, 4)}
     out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
-           "scaling": "weak", "vs_baseline": None, "dtype": "f32 (state), %s (grads), bf16 (params)" % w["gdt"],
-           "data": "synthetic", "impl": "gb300",
+           "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic", "impl": "gb300",
            "config": {"workload": w["name"], "psi": w["psi"], "layers": w["layers"], "n_d": w["n_d"],
                       "stage": w["stage"], "grad_dtype": w["gdt"], "clip": w["clip"], "loss_scaling": w["ls"],
                       "bytes_per_param": w["bytes_per_param"], "parallelism": "replicas x%d" % world,
@@ -503,7 +515,7 @@ def reference_arm(args, rank, world):
     sample = "%d of %d params, n_d=%d, %d steps, single-threaded C oracle" % (psi, w["psi"], n_d, steps)
     return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * el / steps, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32 (state), %s (grads)" % w["gdt"], "data": "synthetic",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "impl": "reference", "config": {"workload": w["name"], "psi": w["psi"], "n_d": n_d},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
