@@ -83,6 +83,9 @@ def lib():
                                    ctypes.POINTER(Scalars), _f32p, _f32p, _f32p, _u16p, _u16p,
                                    i32]),
             "zo_scalars_init": (None, [ctypes.POINTER(Scalars), f32]),
+            "zo_accumulate_grads": (None, [i32, ll, vp, i32, _f32p, _f32p]),
+            "zo_zero_step_accum": (i32, [i32, ll, i32, i32, vp, i32, _f32p, i32, ctypes.POINTER(Hparams),
+                                         ctypes.POINTER(Scalars), _f32p, _f32p, _f32p, _u16p, _u16p, i32]),
             "zo_quantize_block": (None, [ll, _u16p, _i8p, _f32p, _u16p]),
             "zo_quant_gather": (None, [i32, ll, ll, i32, _u16p, _i8p, _f32p, _u16p]),
             "zo_qgz_rank_stride": (ll, [i32]),
@@ -290,6 +293,50 @@ def zero_step(grads, grad_dtype, hp, state, shard_pad, stage, param_dtype=BF16, 
                                  ctypes.byref(hp), ctypes.byref(state.scalars),
                                  _ptr(state.master, ctypes.c_float), _ptr(state.m, ctypes.c_float),
                                  _ptr(state.v, ctypes.c_float), lp_p, g_p, param_dtype)
+    return bool(skipped)
+
+
+# ---------------------------------------------------- gradient accumulation --
+def accumulate_grads(grads, dtype, acc_in=None):
+    """acc_out = acc_in (or +0) + the rank-ordered fp32 sum of one
+    micro-batch's gradients (not divided).  Returns acc_out (psi fp32)."""
+    rows = [np.ascontiguousarray(g, dtype=np.uint16) for g in grads]
+    psi = rows[0].size
+    out = np.zeros(psi, dtype=np.float32)
+    a_in = None if acc_in is None else np.ascontiguousarray(acc_in, dtype=np.float32)
+    if a_in is not None:
+        assert a_in.size >= psi
+    lib().zo_accumulate_grads(len(rows), psi, _ptr_array(rows), dtype,
+                              None if a_in is None else _ptr(a_in, ctypes.c_float), _ptr(out, ctypes.c_float))
+    return out
+
+
+def zero_step_accum(grads, grad_dtype, acc, micro, hp, state, shard_pad, stage, param_dtype=BF16,
+                    lp_shards=None, gathered=None):
+    """The step at the micro-th micro-batch: grads are that micro-batch's
+    rank gradients, acc the sum over the earlier ones (None when micro == 1).
+    Same outputs as zero_step.  Returns skipped."""
+    rows = [np.ascontiguousarray(g, dtype=np.uint16) for g in grads]
+    n_d, psi = len(rows), rows[0].size
+    S = shard_size(psi, n_d, shard_pad)
+    for a in (state.master, state.m, state.v):
+        assert a.size == n_d * S
+    assert micro >= 1
+    a_p = None
+    if acc is not None:
+        acc = np.ascontiguousarray(acc, dtype=np.float32)
+        assert acc.size >= psi
+        a_p = _ptr(acc, ctypes.c_float)
+    if stage >= 3:
+        assert lp_shards is not None and lp_shards.size == n_d * S
+        lp_p, g_p = _ptr(lp_shards, ctypes.c_uint16), None
+    else:
+        assert gathered is not None and gathered.size >= psi
+        lp_p, g_p = None, _ptr(gathered, ctypes.c_uint16)
+    skipped = lib().zo_zero_step_accum(n_d, psi, shard_pad, stage, _ptr_array(rows), grad_dtype, a_p, micro,
+                                       ctypes.byref(hp), ctypes.byref(state.scalars),
+                                       _ptr(state.master, ctypes.c_float), _ptr(state.m, ctypes.c_float),
+                                       _ptr(state.v, ctypes.c_float), lp_p, g_p, param_dtype)
     return bool(skipped)
 
 

@@ -199,11 +199,16 @@ double zo_comm_volume(int stage)
 /* to fp32, add ranks in order 0..N-1 starting from +0.0f, divide once by    */
 /* the divisor (N_d times the loss scale).                                    */
 /* ------------------------------------------------------------------------ */
-static float reduce_one(int n_d, const uint16_t* const* grads, int dtype, long long j, float divisor)
+static float rank_sum(int n_d, const uint16_t* const* grads, int dtype, long long j)
 {
     float sum = 0.0f;
     for (int q = 0; q < n_d; ++q) sum = sum + zo_lp_to_f32(grads[q][j], dtype);
-    return sum / divisor;
+    return sum;
+}
+
+static float reduce_one(int n_d, const uint16_t* const* grads, int dtype, long long j, float divisor)
+{
+    return rank_sum(n_d, grads, dtype, j) / divisor;
 }
 
 void zo_all_reduce_mean(int n_d, long long psi, const uint16_t* const* grads, int dtype,
@@ -439,6 +444,48 @@ int zo_zero_step(int n_d, long long psi, int shard_pad, int stage, const uint16_
         free(full);
     } else {
         zo_reduce_scatter(n_d, psi, S, grads, grad_dtype, divisor, shards);
+    }
+    return step_from_shards(n_d, psi, S, stage, shards, hp, sc, master, m, v, lp_shards, gathered,
+                            param_dtype);
+}
+
+/* Gradient accumulation over k micro-batches ([DP-notes] "Connections":
+ * gradient accumulation combined with ZeRO for larger effective batches;
+ * [itwiki] "DeepSpeed에서 쓰기": gradient_accumulation_steps).  The pages
+ * give no arithmetic.  Reading: every micro-batch's gradients are reduced as
+ * in a step (fp32, ranks in order from +0.0f) but not divided, and the rank
+ * sum is added to the owner's fp32 accumulator, micro-batches in order:
+ * acc_mu = acc_(mu-1) + sum_r g_(r,mu), acc_0 = +0.0f.  acc_in may be NULL
+ * (the first micro-batch) or equal to acc_out.  Indices [0, psi). */
+void zo_accumulate_grads(int n_d, long long psi, const uint16_t* const* grads, int dtype,
+                         const float* acc_in, float* acc_out)
+{
+    for (long long j = 0; j < psi; ++j) {
+        float carry = acc_in ? acc_in[j] : 0.0f;
+        acc_out[j] = carry + rank_sum(n_d, grads, dtype, j);
+    }
+}
+
+/* The step at the k-th micro-batch: its gradients are accumulated onto acc
+ * (the sum over micro-batches 1..k-1; NULL when k == 1) and the total is
+ * divided once by n_d * k (times the loss scale): the mean over every rank's
+ * every micro-batch.  The rest is the ZeRO step. */
+int zo_zero_step_accum(int n_d, long long psi, int shard_pad, int stage, const uint16_t* const* grads,
+                       int grad_dtype, const float* acc, int micro, const zo_hparams* hp, zo_scalars* sc,
+                       float* master, float* m, float* v, uint16_t* lp_shards, uint16_t* gathered,
+                       int param_dtype)
+{
+    long long S = zo_shard_size(psi, n_d, shard_pad);
+    long long padded = S * n_d;
+    float divisor = step_divisor(n_d * micro, hp, sc);
+    float* shards = (float*)malloc(sizeof(float) * (size_t)(padded > 0 ? padded : 1));
+    for (long long j = 0; j < padded; ++j) {
+        if (j < psi) {
+            float carry = acc ? acc[j] : 0.0f;
+            shards[j] = (carry + rank_sum(n_d, grads, grad_dtype, j)) / divisor;
+        } else {
+            shards[j] = 0.0f;
+        }
     }
     return step_from_shards(n_d, psi, S, stage, shards, hp, sc, master, m, v, lp_shards, gathered,
                             param_dtype);

@@ -102,6 +102,14 @@ int zo_zero_step(int n_d, long long psi, int shard_pad, int stage, const uint16_
                  float* v, uint16_t* lp_shards, uint16_t* gathered, int param_dtype);
 void zo_scalars_init(zo_scalars* sc, float loss_scale);
 
+/* ---- gradient accumulation ---- */
+void zo_accumulate_grads(int n_d, long long psi, const uint16_t* const* grads, int dtype,
+                         const float* acc_in, float* acc_out);
+int zo_zero_step_accum(int n_d, long long psi, int shard_pad, int stage, const uint16_t* const* grads,
+                       int grad_dtype, const float* acc, int micro, const zo_hparams* hp, zo_scalars* sc,
+                       float* master, float* m, float* v, uint16_t* lp_shards, uint16_t* gathered,
+                       int param_dtype);
+
 /* ---- block-int8 quantized gather ---- */
 void zo_quantize_block(long long n, const uint16_t* x_bf16, int8_t* codes, float* scale,
                        uint16_t* deq_bf16);

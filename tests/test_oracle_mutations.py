@@ -12,7 +12,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "zero_oracle.c")
 PINS = ["tests/test_oracle_accounting.py", "tests/test_oracle_encodings.py",
         "tests/test_oracle_collectives.py", "tests/test_oracle_adam.py",
-        "tests/test_oracle_steps.py", "tests/test_oracle_qgz.py"]
+        "tests/test_oracle_steps.py", "tests/test_oracle_qgz.py", "tests/test_oracle_accum.py"]
 
 # (name, text in the oracle source, planted replacement)
 MUTATIONS = [
@@ -28,7 +28,7 @@ MUTATIONS = [
     ("beta1 power from beta2", "sc->beta1_pow * (double)hp->beta1;\n    sc->beta2_pow",
      "sc->beta1_pow * (double)hp->beta2;\n    sc->beta2_pow"),
     ("ranks summed in reverse", "for (int q = 0; q < n_d; ++q) sum", "for (int q = n_d - 1; q >= 0; --q) sum"),
-    ("sum, not mean", "return sum / divisor;", "return sum;"),
+    ("sum, not mean", "return rank_sum(n_d, grads, dtype, j) / divisor;", "return rank_sum(n_d, grads, dtype, j);"),
     ("loss scale ignored", "float scale = hp->loss_scaling ? sc->loss_scale : 1.0f;", "float scale = 1.0f;"),
     ("bf16 truncates", "return (uint16_t)shift_rne(u, 16);", "return (uint16_t)(u >> 16);"),
     ("fp16 subnormal off by one", "int s = 126 - e;", "int s = 127 - e;"),
@@ -52,6 +52,13 @@ MUTATIONS = [
     ("qgZ blocks not aligned to shards",
      "long long off = (long long)r * shard + lo;\n                float* sc = scales +",
      "long long off = (long long)r * shard + lo + (r > 0);\n                float* sc = scales +"),
+    ("accumulated step divides by n_d only", "float divisor = step_divisor(n_d * micro, hp, sc);",
+     "float divisor = step_divisor(n_d, hp, sc);"),
+    ("accumulated carry dropped at the step", "shards[j] = (carry + rank_sum(n_d, grads, grad_dtype, j)) / divisor;",
+     "shards[j] = rank_sum(n_d, grads, grad_dtype, j) / divisor;"),
+    ("accumulation ignores the accumulator", "float carry = acc_in ? acc_in[j] : 0.0f;", "float carry = 0.0f;"),
+    ("accumulation continues one running sum", "acc_out[j] = carry + rank_sum(n_d, grads, dtype, j);",
+     "for (int q = 0; q < n_d; ++q) carry = carry + zo_lp_to_f32(grads[q][j], dtype);\n        acc_out[j] = carry;"),
     ("stage 3 comm counts one gather", "return reduce_scatter + 2.0 * all_gather;", "return reduce_scatter + all_gather;"),
 ]
 
