@@ -41,7 +41,7 @@ L2_BYTES = 129 * 1024 * 1024
 
 
 # ----------------------------------------------------------------- workloads
-def workload(cfg, nd=None, qgather=False, psi=None, qgz=False, gathers=1, offload=False):
+def workload(cfg, nd=None, qgather=False, psi=None, qgz=False, gathers=1, offload=False, accum=1):
     """Sizes, hyper-parameters and the algorithmic bytes of one step.  psi
     overrides the parameter count (a smaller case of the same workload, for
     profiling)."""
@@ -74,9 +74,24 @@ def workload(cfg, nd=None, qgather=False, psi=None, qgz=False, gathers=1, offloa
         # optimizer state in page-locked host memory, read and written over the CPU-GPU link
         w["offload"] = True
         w["name"] += "_offload"
+    if accum > 1:
+        if w["stage"] == 3 or w.get("qgz") or w.get("qgather") or offload or w["ls"]:
+            raise SystemExit("--accum applies to the plain and clipped ZeRO-2 workloads (configs 1, 2, 5)")
+        w["accum"] = accum
+        w["name"] += "_accum%d" % accum
     n_d = w["n_d"]
     # algorithmic bytes per parameter of one step (minimum HBM traffic)
-    if w["clip"] > 0:
+    if w.get("accum"):
+        # micro-batch 1 writes the fp32 accumulator, 2..k-1 read and write it,
+        # the step at micro-batch k reads it in each pass that reads the ranks
+        k = w["accum"]
+        micro = (2 * n_d + 4) + (k - 2) * (2 * n_d + 8)
+        if w["clip"] > 0:
+            final = 2 * n_d + 38 if n_d > 4 else 4 * n_d + 34
+        else:
+            final = 2 * n_d + 30
+        w["bytes_per_param"] = micro + final
+    elif w["clip"] > 0:
         w["bytes_per_param"] = 2 * n_d + 34 if n_d > 4 else 4 * n_d + 26
     elif w["stage"] == 3:
         w["bytes_per_param"] = 2 * n_d + 26 + 4 * w.get("gathers", 1)
@@ -238,6 +253,8 @@ class Job:
             self.qscales = [torch.empty(w["n_d"] * nbs * n_dp, device=device) for _ in self.grads]
             for k in range(len(self.grads)):
                 self.quantize(k)
+        if w.get("accum"):
+            self.acc = torch.zeros(n, device=device)
         self.ws = torch.zeros(max(self.plan.workspace_bytes(self.hp), 256), dtype=torch.uint8, device=device)
         self.scalars = torch.zeros(256, dtype=torch.uint8, device=device)
         z.zero_scalars_init(self.scalars, scale)
@@ -256,6 +273,9 @@ class Job:
         """One pass of the hot path through the public C ABI."""
         z, w = self.z, self.w
         h = self.plan.handle
+        if w.get("accum"):
+            self.step_accum()
+            return
         for l in range(w["layers"]):
             gsel = l if w["layers"] > 1 else self.k
             if w["stage"] == 3:
@@ -284,6 +304,21 @@ class Job:
                 step = z.zero_step_fused_offload if self.offload else z.zero_step_fused
                 step(h, self.hp, self.ranks(gsel), self.master[l], self.m[l], self.v[l], self.master[l], self.m[l],
                      self.v[l], self.lp[l], self.scalars, self.ws)
+        self.k += 1
+
+    def step_accum(self, sets=None):
+        """One optimizer step over k micro-batches: k - 1 accumulations into
+        the fp32 accumulator, then the step at the k-th."""
+        z, w = self.z, self.w
+        h = self.plan.handle
+        k = w["accum"]
+        for mu in range(k):
+            g = self.ranks(self.k * k + mu if sets is None else sets)
+            if mu < k - 1:
+                z.zero_accumulate_grads(h, g, None if mu == 0 else self.acc, self.acc, self.scalars)
+            else:
+                z.zero_step_fused_accum(h, self.hp, g, self.acc, k, self.master[0], self.m[0], self.v[0],
+                                        self.master[0], self.m[0], self.v[0], self.lp[0], self.scalars, self.ws)
         self.k += 1
 
     def parts_step(self, ev):
@@ -315,7 +350,7 @@ def l2_flush(torch, device, buf=[]):
 def gpu_arm(args, rank, world, device):
     import torch
     import zero_optimizer_step_02_gb300 as z
-    w = workload(args.config, args.nd, args.qgather, args.psi, args.qgz, args.gathers, args.offload)
+    w = workload(args.config, args.nd, args.qgather, args.psi, args.qgz, args.gathers, args.offload, args.accum)
     torch.cuda.set_device(device)
     job = Job(w, device)
     torch.cuda.synchronize()
@@ -360,7 +395,27 @@ def gpu_arm(args, rank, world, device):
 
     # dominant kernel: per-kernel CUDA events on the launching stream
     peak, peak_kind = measured_hbm_peak()
-    if w["clip"] > 0 and w["n_d"] > 4 and not w.get("offload"):
+    if w.get("accum"):
+        # a middle micro-batch (accumulator read and written) and the step at
+        # the last one, each timed alone back to back; the first repetition
+        # is not counted
+        n_rep = max(3, args.steps)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_rep + 1)]
+        torch.cuda.synchronize()
+        for i, ev in enumerate(evs):
+            ev[0].record()
+            z.zero_accumulate_grads(job.plan.handle, job.ranks(i), job.acc, job.acc, job.scalars)
+            ev[1].record()
+            z.zero_step_fused_accum(job.plan.handle, job.hp, job.ranks(i + 1), job.acc, w["accum"], job.master[0],
+                                    job.m[0], job.v[0], job.master[0], job.m[0], job.v[0], job.lp[0], job.scalars,
+                                    job.ws)
+            ev[2].record()
+        torch.cuda.synchronize()
+        t_acc = statistics.mean(ev[0].elapsed_time(ev[1]) for ev in evs[1:])
+        t_fin = statistics.mean(ev[1].elapsed_time(ev[2]) for ev in evs[1:])
+        kernel, kms, kbytes = "accumulate_grads", t_acc, (2 * w["n_d"] + 8) * w["psi"]
+        breakdown = {"accumulate_grads": round(t_acc, 4), "step_accum": round(t_fin, 4)}
+    elif w["clip"] > 0 and w["n_d"] > 4 and not w.get("offload"):
         job.ghat = torch.zeros(job.plan.padded, device=device)
         n_rep = max(3, args.steps)
         dur = [0.0, 0.0, 0.0]
@@ -429,7 +484,8 @@ def gpu_arm(args, rank, world, device):
            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic", "impl": "gb300",
            "config": {"workload": w["name"], "psi": w["psi"], "layers": w["layers"], "n_d": w["n_d"],
                       "stage": w["stage"], "grad_dtype": w["gdt"], "clip": w["clip"], "loss_scaling": w["ls"],
-                      "bytes_per_param": w["bytes_per_param"], "parallelism": "replicas x%d" % world,
+                      "bytes_per_param": w["bytes_per_param"], "micro_batches": w.get("accum", 1),
+                      "parallelism": "replicas x%d" % world,
                       "l2": "flushed between steps" if small else "inputs larger than L2"},
            "step_gbs": round(step_gbs, 1), "step_frac_of_peak": round(step_gbs / peak, 4),
            "roofline": roofline, "gpu_launches": int(launches), "e2e": e2e, "clocks": clk}
@@ -453,19 +509,31 @@ def e2e_measure(job, w, args, device, world):
     host_g.copy_(job.grads[0])
     host_out = torch.empty(job.lp[0].numel(), dtype=torch.bfloat16, pin_memory=True)
     steps = max(1, min(args.steps, 5))
+    k = w.get("accum", 1)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record()
     for _ in range(steps):
-        job.grads[0].copy_(host_g, non_blocking=True)
-        job.k = 0
-        job.step()
+        if k > 1:
+            # every micro-batch's gradients arrive from the host before its pass
+            h = job.plan.handle
+            for mu in range(k):
+                job.grads[0].copy_(host_g, non_blocking=True)
+                if mu < k - 1:
+                    z.zero_accumulate_grads(h, job.ranks(0), None if mu == 0 else job.acc, job.acc, job.scalars)
+                else:
+                    z.zero_step_fused_accum(h, job.hp, job.ranks(0), job.acc, k, job.master[0], job.m[0], job.v[0],
+                                            job.master[0], job.m[0], job.v[0], job.lp[0], job.scalars, job.ws)
+        else:
+            job.grads[0].copy_(host_g, non_blocking=True)
+            job.k = 0
+            job.step()
         host_out.copy_(job.lp[0], non_blocking=True)
     b.record()
     torch.cuda.synchronize()
     ms = dist_max(a.elapsed_time(b), world)
     return {"value": world * w["psi"] * steps / (ms / 1e3), "unit": UNIT,
-            "h2d_bytes_per_step": host_g.numel() * host_g.element_size(),
+            "h2d_bytes_per_step": k * host_g.numel() * host_g.element_size(),
             "d2h_bytes_per_step": host_out.numel() * host_out.element_size(), "steps": steps}
 
 
@@ -491,7 +559,13 @@ def oracle_sample(w, budget_s, max_steps=None):
     gath = np.zeros(psi, np.uint16)
     steps, t0 = 0, time.perf_counter()
     while True:
-        if w.get("qgz"):
+        if w.get("accum"):
+            acc = None
+            for _ in range(w["accum"] - 1):
+                acc = oracle.accumulate_grads(rows, dt, acc)
+            oracle.zero_step_accum(rows, dt, acc, w["accum"], hp, st, w["pad"], min(w["stage"], 3), lp_shards=lp,
+                                   gathered=gath)
+        elif w.get("qgz"):
             codes, scales = oracle.quantize_ranks(rows, psi, S, 2048)
             oracle.zero_step_qgz(codes, scales, 2048, hp, st, w["pad"], min(w["stage"], 3), psi, lp_shards=lp,
                                  gathered=gath)
@@ -505,7 +579,7 @@ def oracle_sample(w, budget_s, max_steps=None):
 
 
 def reference_arm(args, rank, world):
-    w = workload(args.config, args.nd, args.qgather, args.psi, args.qgz, args.gathers, args.offload)
+    w = workload(args.config, args.nd, args.qgather, args.psi, args.qgz, args.gathers, args.offload, args.accum)
     if rank != 0:
         return None
     for _ in range(args.warmup):
@@ -565,6 +639,7 @@ def main():
     ap.add_argument("--qgz", action="store_true", help="quantized gradient exchange (config 5)")
     ap.add_argument("--gathers", type=int, default=1, choices=[1, 2], help="ZeRO-3 gathers per layer and step")
     ap.add_argument("--offload", action="store_true", help="optimizer state in page-locked host memory")
+    ap.add_argument("--accum", type=int, default=1, help="micro-batches per optimizer step (gradient accumulation)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -579,7 +654,7 @@ def main():
     out = gpu_arm(args, rank, world, device)
     if rank == 0:
         if not args.no_cpu_baseline and world == 1:
-            w = workload(args.config, args.nd, args.qgather, args.psi, args.qgz, args.gathers, args.offload)
+            w = workload(args.config, args.nd, args.qgather, args.psi, args.qgz, args.gathers, args.offload, args.accum)
             psi, n_d, steps, el = oracle_sample(w, args.cpu_budget)
             out["cpu_baseline"] = {"value": psi * steps / el, "unit": UNIT, "cores": 1, "kind": "oracle",
                                    "sample": "%d of %d params, n_d=%d, %d steps in %.1f s, single-threaded C "

@@ -52,6 +52,7 @@ extern "C" {
 #define ZERO_ABI_VERSION 1
 #define ZERO_MAX_RANKS 256      /* largest n_d */
 #define ZERO_MAX_SHARD_PAD 4096 /* largest shard_pad */
+#define ZERO_MAX_MICRO_BATCHES 65536 /* largest gradient-accumulation count */
 
 typedef enum {
     ZERO_OK = 0,
@@ -251,6 +252,40 @@ ZERO_API zero_status zero_step_fused_offload(const zero_plan* plan, const zero_h
                                              const float* m_in, const float* v_in, float* master_out,
                                              float* m_out, float* v_out, void* lp_out,
                                              zero_dev_scalars* scalars_dev, void* ws, void* stream);
+
+/* ------------------------------------------------ gradient accumulation --- */
+/* Gradient accumulation over k micro-batches per optimizer step (DP-notes
+ * "Connections": accumulation combined with ZeRO for larger effective
+ * batches; itwiki "DeepSpeed에서 쓰기": gradient_accumulation_steps).  Each
+ * micro-batch is reduce-scattered as it arrives, and its fp32 rank sum is
+ * added to the owners' fp32 accumulator, so no rank keeps more than its
+ * micro-batch gradients; the step at the k-th micro-batch divides once.     */
+
+/* One micro-batch (not the last): acc_out[j] = acc_in[j] + sum_r g_r[j] for
+ * j < Psi, the rank sum in fp32 in rank order from +0.0f, NOT divided.
+ * acc_in NULL means +0.0f (the first micro-batch); acc_in may equal acc_out,
+ * any other overlap is refused (ZERO_ERR_INVALID_ARG).  Both are fp32 device
+ * buffers of at least Psi elements (n_d*S recommended, so that shard r of
+ * the accumulator is [r*S, (r+1)*S)), 16-byte aligned; elements from Psi on
+ * are not touched.  rank_grads as in zero_reduce_scatter.  One kernel.
+ * scalars_dev (may be NULL) only receives ZERO_DEV_TIMEOUT if a wait runs
+ * out; nothing else of it is read or written.                              */
+ZERO_API zero_status zero_accumulate_grads(const zero_plan* plan, const void* const* rank_grads,
+                                           const float* acc_in, float* acc_out,
+                                           zero_dev_scalars* scalars_dev, void* stream);
+
+/* The step at the last (k-th, micro_batches = k) micro-batch: rank_grads are
+ * that micro-batch's gradients, acc the sum zero_accumulate_grads left for
+ * micro-batches 1..k-1 (NULL exactly when k == 1).  The reduced gradient is
+ * (acc[j] + sum_r g_r[j]) / (n_d * k * loss_scale) -- the mean over all
+ * n_d * k rank gradients -- and everything else (clipping, loss-scale skip,
+ * pass schedules, outputs) is zero_step_fused.  acc is read, never written,
+ * and must not overlap an output.  1 <= k <= ZERO_MAX_MICRO_BATCHES.        */
+ZERO_API zero_status zero_step_fused_accum(const zero_plan* plan, const zero_hparams* hp,
+                                           const void* const* rank_grads, const float* acc, int micro_batches,
+                                           const float* master_in, const float* m_in, const float* v_in,
+                                           float* master_out, float* m_out, float* v_out, void* lp_out,
+                                           zero_dev_scalars* scalars_dev, void* ws, void* stream);
 
 /* ----------------------------------------------------- quantized gather --- */
 /* ZeRO++ qwZ (itwiki "후속 기법", ZeRO++ row: weights are block-quantized for

@@ -163,3 +163,21 @@ def test_quantized_gradient_exchange_argument_checks(z):
                 None) == 3
     assert _raw(z, "zero_step_fused_qgz", p.handle, ctypes.byref(clip), ranks, A, 2048, A, A, A, A, A, A, A, A,
                 None) == 3
+
+
+def test_gradient_accumulation_argument_checks(z):
+    A, B = 0x10000, 0x20000
+    p = z.Plan(1000, 2, stage=2)
+    ranks = (ctypes.c_void_p * 2)(A, B)
+    hp = z.hparams()
+    hpp = ctypes.byref(hp)
+    # accumulate: misaligned out / in, partly overlapping in and out, misaligned scalars
+    assert _raw(z, "zero_accumulate_grads", p.handle, ranks, None, A + 4, None, None) == 2
+    assert _raw(z, "zero_accumulate_grads", p.handle, ranks, A + 8, B, None, None) == 2
+    assert _raw(z, "zero_accumulate_grads", p.handle, ranks, A, A + 16, None, None) == 1
+    assert _raw(z, "zero_accumulate_grads", p.handle, ranks, A, B, A + 16, None) == 2
+    assert _raw(z, "zero_accumulate_grads", None, ranks, A, B, None, None) == 1
+    # the accumulated step: micro-batch count in [1, 65536], acc given exactly when k > 1
+    for acc, k in ((A, 1), (None, 2), (A, 0), (A, 65537)):
+        assert _raw(z, "zero_step_fused_accum", p.handle, hpp, ranks, acc, k, A, A, A, A, A, A, A, A, A, None) == 1
+    assert _raw(z, "zero_step_fused_accum", p.handle, hpp, ranks, A + 4, 2, A, A, A, A, A, A, A, A, A, None) == 2

@@ -1,6 +1,6 @@
 """GPU parity: every entry point of libzero.so against the CPU oracle on the
 same seeded bytes, at sizes the oracle finishes in seconds that span many
-2048-element tiles plus ragged tails.
+4096-element tiles plus ragged tails.
 
 Bars: the reduce, Adam and cast use the oracle's IEEE operation order, so
 master/m/v and the 16-bit parameters are compared bit for bit (which implies

@@ -21,7 +21,8 @@ from ._capi import (ZERO_BF16, ZERO_FP16, ZERO_DEV_TIMEOUT, ZeroDevScalars, Zero
                     zero_plan_create_ex, zero_plan_destroy, zero_plan_memory, zero_plan_query, zero_quant_gather,
                     zero_reduce_scatter, zero_scalars_init, zero_status_str, zero_step_fused,
                     zero_step_fused_noalloc, zero_step_fused_qgather, zero_workspace_bytes,
-                    zero_quantize_grads, zero_step_fused_qgz, zero_step_fused_offload)
+                    zero_quantize_grads, zero_step_fused_qgz, zero_step_fused_offload, zero_accumulate_grads,
+                    zero_step_fused_accum)
 
 __all__ = ["Plan", "StepBuffers", "read_scalars", "row_len", "hparams", "ZeroError", "ZeroHparams",
            "ZERO_BF16", "ZERO_FP16", "ZERO_DEV_TIMEOUT"] + [n for n in dir(_capi) if n.startswith("zero_")]
@@ -114,6 +115,22 @@ class StepBuffers:
         else:
             zero_step_fused(self.plan.handle, hp, self.rank_list(), self.master, self.m, self.v, self.master,
                             self.m, self.v, self.lp, self.scalars, self.ws, stream)
+
+    def accumulate(self, first, stream=None):
+        """Add the micro-batch now in grads to the fp32 accumulator `acc`
+        (padded length; started from +0 when first)."""
+        import torch
+        if getattr(self, "acc", None) is None:
+            self.acc = torch.zeros(self.plan.padded, dtype=torch.float32, device=self.master.device)
+        zero_accumulate_grads(self.plan.handle, self.rank_list(), None if first else self.acc, self.acc,
+                              self.scalars, stream)
+
+    def step_accum(self, hp, micro_batches, stream=None):
+        """The step at the last of micro_batches micro-batches (grads holds
+        it; acc the sum of the earlier ones)."""
+        acc = None if micro_batches == 1 else self.acc
+        zero_step_fused_accum(self.plan.handle, hp, self.rank_list(), acc, micro_batches, self.master, self.m,
+                              self.v, self.master, self.m, self.v, self.lp, self.scalars, self.ws, stream)
 
     def scalars_host(self):
         return read_scalars(self.scalars)

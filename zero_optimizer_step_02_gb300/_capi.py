@@ -81,6 +81,8 @@ _SIGS = {
     "zero_step_fused_noalloc": (_i32, [_vp, _hp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "zero_quantize_grads": (_i32, [_vp, _vp, _i32, _vp, _vp, _vp]),
     "zero_step_fused_offload": (_i32, [_vp, _hp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "zero_accumulate_grads": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp]),
+    "zero_step_fused_accum": (_i32, [_vp, _hp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "zero_step_fused_qgz": (_i32, [_vp, _hp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -220,6 +222,21 @@ def zero_step_fused_offload(plan, hp, rank_grads, master_in, m_in, v_in, master_
                                         _addr(m_in), _addr(v_in), _addr(master_out), _addr(m_out), _addr(v_out),
                                         _addr(lp_out), _addr(scalars), _addr(ws), _stream(stream)),
            "zero_step_fused_offload")
+
+
+def zero_accumulate_grads(plan, rank_grads, acc_in, acc_out, scalars=None, stream=None):
+    """acc_out = acc_in (None: +0) + this micro-batch's rank sum (fp32, undivided)."""
+    _check(_lib.zero_accumulate_grads(plan, _ptr_array(rank_grads), _addr(acc_in), _addr(acc_out), _addr(scalars),
+                                      _stream(stream)), "zero_accumulate_grads")
+
+
+def zero_step_fused_accum(plan, hp, rank_grads, acc, micro_batches, master_in, m_in, v_in, master_out, m_out, v_out,
+                          lp_out, scalars, ws, stream=None):
+    """The step at the last of micro_batches micro-batches (acc: sum of the earlier ones, None when 1)."""
+    _check(_lib.zero_step_fused_accum(plan, ctypes.byref(hp), _ptr_array(rank_grads), _addr(acc), micro_batches,
+                                      _addr(master_in), _addr(m_in), _addr(v_in), _addr(master_out), _addr(m_out),
+                                      _addr(v_out), _addr(lp_out), _addr(scalars), _addr(ws), _stream(stream)),
+           "zero_step_fused_accum")
 
 
 def zero_quant_gather(plan, shards_bf16, block, codes, scales, gathered, stream=None):

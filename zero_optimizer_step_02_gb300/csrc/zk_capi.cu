@@ -119,10 +119,28 @@ int reduce_grid(long long n)
     return static_cast<int>(g);
 }
 
+// Gradient accumulation: carry (fp32, indexed like the gradients) is added to
+// the rank sum, and the mean divides by n_d * micro.
+struct Accum {
+    const float* carry;
+    int micro;
+};
+constexpr Accum kNoAccum = {nullptr, 1};
+
+void set_accum(StreamArgs& a, const Accum& acc, int slot)
+{
+    a.micro = acc.micro;
+    if (acc.carry == nullptr) return;
+    a.side[slot] = acc.carry;
+    a.n_side = slot + 1;
+    a.flags |= zk::F_CARRY;
+}
+
 // One reduce pass over [0, psi): optional fp32 output, squared-norm partials,
 // non-finite detection in loss-scaling mode.
 zero_status run_reduce(const zero_plan* p, const zero_hparams* hp, const void* const* ranks, float* out,
-                       bool sqnorm, void* ws, zero_dev_scalars* sc, cudaStream_t st, int* grid_out = nullptr)
+                       bool sqnorm, void* ws, zero_dev_scalars* sc, cudaStream_t st, int* grid_out = nullptr,
+                       const Accum& acc = kNoAccum)
 {
     StreamArgs a = base_args(p, hp, sc);
     set_ranks(a, p, ranks);
@@ -131,6 +149,7 @@ zero_status run_reduce(const zero_plan* p, const zero_hparams* hp, const void* c
     a.out_f32[0] = out;
     a.partials = sqnorm ? partials_of(ws) : nullptr;
     a.flags = (sqnorm ? zk::F_SQNORM : 0) | (hp->loss_scaling ? (zk::F_DETECT | zk::F_LSCALE) : 0);
+    set_accum(a, acc, 0);
     if (out != nullptr && !aligned(out, 16)) a.tma_ok = 0;
     const zero_status s = from_cuda(zk::launch_stream(zk::OP_REDUCE, p->grad_dtype, p->param_dtype, a, st));
     if (grid_out != nullptr) *grid_out = a.grid;
@@ -149,7 +168,7 @@ void set_finalize(StreamArgs& a, void* ws, int n)
 zero_status run_fused(const zero_plan* p, const zero_hparams* hp, const void* const* ranks, const float* mi,
                       const float* m_in, const float* vi, float* mo, float* m_out, float* vo, void* lp,
                       int flags, zero_dev_scalars* sc, cudaStream_t st, void* fin_ws = nullptr, int fin_n = 0,
-                      bool host_state = false)
+                      bool host_state = false, const Accum& acc = kNoAccum)
 {
     // buckets only when no global check ties the pieces together
     const long long step =
@@ -170,6 +189,7 @@ zero_status run_fused(const zero_plan* p, const zero_hparams* hp, const void* co
         a.out_f32[2] = vo;
         a.out_lp = lp;
         a.flags = hi == p->psi ? flags : (flags & ~zk::F_EPILOGUE);
+        set_accum(a, acc, 3);   // the carry is read directly, never staged
         const zero_status s = from_cuda(zk::launch_stream(zk::OP_FUSED, p->grad_dtype, p->param_dtype, a, st));
         if (s != ZERO_OK) return s;
     }
@@ -409,7 +429,7 @@ namespace {
 // page-locked host memory and are read and written directly by the kernels.
 zero_status fused_step(const zero_plan* p, const zero_hparams* hp, const void* const* ranks, const float* mi,
                        const float* m_in, const float* vi, float* mo, float* m_out, float* vo, void* lp,
-                       zero_dev_scalars* sc, void* ws, void* stream, bool host_state)
+                       zero_dev_scalars* sc, void* ws, void* stream, bool host_state, const Accum& acc = kNoAccum)
 {
     if (p == nullptr) return ZERO_ERR_INVALID_ARG;
     zero_status s;
@@ -431,14 +451,14 @@ zero_status fused_step(const zero_plan* p, const zero_hparams* hp, const void* c
 
     if (!clip) {
         if (!ls) {
-            if ((s = run_fused(p, hp, ranks, mi, m_in, vi, mo, m_out, vo, lp, epi, sc, st, nullptr, 0, host_state)) != ZERO_OK) return s;
+            if ((s = run_fused(p, hp, ranks, mi, m_in, vi, mo, m_out, vo, lp, epi, sc, st, nullptr, 0, host_state, acc)) != ZERO_OK) return s;
         } else if (speculative) {
             // update while detecting; undo from the in state if flagged
-            if ((s = run_fused(p, hp, ranks, mi, m_in, vi, mo, m_out, vo, lp, zk::F_DETECT | lsf, sc, st, nullptr, 0, host_state)) != ZERO_OK) return s;
+            if ((s = run_fused(p, hp, ranks, mi, m_in, vi, mo, m_out, vo, lp, zk::F_DETECT | lsf, sc, st, nullptr, 0, host_state, acc)) != ZERO_OK) return s;
         } else {
             // in place: a read-only check pass first, then the guarded update
-            if ((s = run_reduce(p, hp, ranks, nullptr, false, ws, sc, st)) != ZERO_OK) return s;
-            if ((s = run_fused(p, hp, ranks, mi, m_in, vi, mo, m_out, vo, lp, zk::F_GUARD | lsf | epi, sc, st, nullptr, 0, host_state)) != ZERO_OK) return s;
+            if ((s = run_reduce(p, hp, ranks, nullptr, false, ws, sc, st, nullptr, acc)) != ZERO_OK) return s;
+            if ((s = run_fused(p, hp, ranks, mi, m_in, vi, mo, m_out, vo, lp, zk::F_GUARD | lsf | epi, sc, st, nullptr, 0, host_state, acc)) != ZERO_OK) return s;
         }
     } else {
         // the update kernel finishes the reduce pass's norm in its prologue
@@ -446,16 +466,16 @@ zero_status fused_step(const zero_plan* p, const zero_hparams* hp, const void* c
         int n = 0;
         if (clip_materialises(p)) {
             float* g = ghat_of(ws);
-            if ((s = run_reduce(p, hp, ranks, g, true, ws, sc, st, &n)) != ZERO_OK) return s;
+            if ((s = run_reduce(p, hp, ranks, g, true, ws, sc, st, &n, acc)) != ZERO_OK) return s;
             // the Adam pass walks the tiles from the end: the reduced gradient the
             // reduce pass wrote last is still in L2
             if ((s = run_adam(p, hp, g, mi, m_in, vi, mo, m_out, vo, lp,
                               zk::F_CLIP | zk::F_FINALIZE | guard | epi | zk::F_REVERSE, sc, st, ws, n, host_state)) != ZERO_OK)
                 return s;
         } else {
-            if ((s = run_reduce(p, hp, ranks, nullptr, true, ws, sc, st, &n)) != ZERO_OK) return s;
+            if ((s = run_reduce(p, hp, ranks, nullptr, true, ws, sc, st, &n, acc)) != ZERO_OK) return s;
             if ((s = run_fused(p, hp, ranks, mi, m_in, vi, mo, m_out, vo, lp,
-                               zk::F_CLIP | zk::F_FINALIZE | guard | lsf | epi, sc, st, ws, n, host_state)) != ZERO_OK)
+                               zk::F_CLIP | zk::F_FINALIZE | guard | lsf | epi, sc, st, ws, n, host_state, acc)) != ZERO_OK)
                 return s;
         }
     }
@@ -491,6 +511,41 @@ ZERO_API zero_status zero_step_fused_offload(const zero_plan* p, const zero_hpar
         if (at.type != cudaMemoryTypeHost || at.devicePointer != q) return ZERO_ERR_INVALID_ARG;
     }
     return fused_step(p, hp, ranks, mi, m_in, vi, mo, m_out, vo, lp, sc, ws, stream, true);
+}
+
+ZERO_API zero_status zero_accumulate_grads(const zero_plan* p, const void* const* ranks, const float* acc_in,
+                                           float* acc_out, zero_dev_scalars* sc, void* stream)
+{
+    if (p == nullptr) return ZERO_ERR_INVALID_ARG;
+    zero_status s;
+    if ((s = check_ranks(p, ranks)) != ZERO_OK) return s;
+    if ((s = check_dev(acc_out)) != ZERO_OK) return s;
+    if (acc_in != nullptr && !aligned(acc_in, 16)) return ZERO_ERR_MISALIGNED;
+    if (acc_in != nullptr && acc_in != acc_out) {
+        const uintptr_t i0 = reinterpret_cast<uintptr_t>(acc_in), o0 = reinterpret_cast<uintptr_t>(acc_out);
+        const uintptr_t n = sizeof(float) * static_cast<uintptr_t>(p->psi);
+        if (i0 < o0 + n && o0 < i0 + n) return ZERO_ERR_INVALID_ARG;
+    }
+    if (sc != nullptr && !aligned(sc, 256)) return ZERO_ERR_MISALIGNED;
+    // the undivided sum: no loss scale, no guard; sc only reports a timeout
+    StreamArgs a = base_args(p, nullptr, sc);
+    set_ranks(a, p, ranks);
+    set_flat(a, 0, p->psi);
+    a.out_f32[0] = acc_out;
+    a.flags = zk::F_RAW;
+    set_accum(a, Accum{acc_in, 1}, 0);
+    return from_cuda(zk::launch_stream(zk::OP_REDUCE, p->grad_dtype, p->param_dtype, a, as_stream(stream)));
+}
+
+ZERO_API zero_status zero_step_fused_accum(const zero_plan* p, const zero_hparams* hp, const void* const* ranks,
+                                           const float* acc, int micro_batches, const float* mi, const float* m_in,
+                                           const float* vi, float* mo, float* m_out, float* vo, void* lp,
+                                           zero_dev_scalars* sc, void* ws, void* stream)
+{
+    if (micro_batches < 1 || micro_batches > ZERO_MAX_MICRO_BATCHES) return ZERO_ERR_INVALID_ARG;
+    if ((acc == nullptr) != (micro_batches == 1)) return ZERO_ERR_INVALID_ARG;
+    if (acc != nullptr && !aligned(acc, 16)) return ZERO_ERR_MISALIGNED;
+    return fused_step(p, hp, ranks, mi, m_in, vi, mo, m_out, vo, lp, sc, ws, stream, false, Accum{acc, micro_batches});
 }
 
 ZERO_API zero_status zero_quant_gather(const zero_plan* p, const void* shards, int block, signed char* codes,

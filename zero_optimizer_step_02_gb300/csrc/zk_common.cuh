@@ -44,6 +44,9 @@ enum : int {
     F_EPILOGUE = 1 << 7,  // the last CTA to finish commits the step scalars
     F_REVERSE = 1 << 8,   // flat launches: walk the tiles from the end (reads what the
                           // previous pass wrote last first, while it is still in L2)
+    F_CARRY = 1 << 9,     // gradient accumulation: the rank sum is added to an fp32 carry
+                          // stream (side 0 of OP_REDUCE, side 3 of OP_FUSED) before the mean
+    F_RAW = 1 << 10,      // OP_REDUCE: store the sum itself, no division
 };
 
 // ------------------------------------------------------------- PTX wrappers

@@ -21,7 +21,8 @@ constexpr int kGradQ8 = 2;
 // at limit (= Psi), so that no tile crosses a shard boundary.
 struct StreamArgs {
     const void* rank[ZERO_MAX_RANKS];  // 16-bit gradient buffers, rank order
-    const float* side[4];              // fp32 inputs: OP_FUSED {master, m, v}; OP_ADAM {g, master, m, v}
+    const float* side[4];              // fp32 inputs: OP_FUSED {master, m, v, carry}; OP_ADAM {g, master, m, v};
+                                       // OP_REDUCE {carry}  (carry: F_CARRY only)
     float* out_f32[3];                 // OP_FUSED/OP_ADAM {master, m, v}; OP_REDUCE {g or null}
     void* out_lp;                      // 16-bit parameters out (null: none)
     const float* q_rank_scales;        // kGradQ8 ranks: scales, block-major, rank-minor:
@@ -36,6 +37,7 @@ struct StreamArgs {
     long long base, seg_stride, seg_len, limit, tiles_per_seg, q_blocks_per_shard;
     int n_seg;
     int n_ranks;                       // rank streams (0 for OP_ADAM)
+    int micro;                         // micro-batches in the mean (divisor n_ranks * micro); 0 reads as 1
     int n_side;                        // fp32 side streams
     int n_side_tma;                    // the first n_side_tma of them are staged by bulk copies; the
                                        // rest (state in page-locked host memory) are read directly

@@ -1,17 +1,21 @@
 // zk_stream.cu -- the streaming engine of the ZeRO-DP step and its three ops.
 //
-// One persistent CTA per SM.  Warp 8 is the producer: one thread issues 1-D
-// bulk (TMA) copies of 2048-element tiles into a ring of shared-memory stages,
-// each stage holding up to 8 ranks' gradient slices plus, with the last rank
-// group of a tile, the fp32 side streams (reduced gradient / master / m / v).
-// Warps 0-7 are consumers: they add the rank slices in rank order into fp32
-// registers, release the stage, then apply the op and store the results with
-// 16-byte coalesced stores.  Tiles shorter than 2048 (the ragged tail, a
-// shard's last tile) or not 16-byte aligned take a plain-load path.
+// One persistent CTA per SM.  Warp 16 is the producer: one thread issues 1-D
+// bulk (TMA) copies of 4096-element tiles into a ring of shared-memory stages,
+// each stage holding up to 8 ranks' gradient slices (16 for int8 codes) plus,
+// with the last rank group of a tile, the staged fp32 side streams (reduced
+// gradient / master / m / v).  Warps 0-15 are consumers: they add the rank
+// slices in rank order into fp32 registers, release the stage, then apply the
+// op and store the results with 16-byte coalesced stores.  Side streams that
+// are not staged (state in host memory, an accumulation carry) are read with
+// 16-byte loads issued before the stage wait.  Tiles shorter than 4096 (the
+// ragged tail, a shard's last tile) or not 16-byte aligned take a plain-load
+// path.
 //
 //   OP_FUSED  : reduce-scatter + Adam + 16-bit cast (or fused int8 gather)
 //   OP_REDUCE : reduce-scatter alone (optional fp32 output, squared-norm
-//               partials, non-finite detection)
+//               partials, non-finite detection), or one micro-batch's
+//               undivided rank sum added to an fp32 accumulator
 //   OP_ADAM   : Adam from an fp32 reduced gradient + 16-bit cast
 //
 // Sources: DP-notes "ZeRO-2: Gradient Partitioning" (reduce-scatter, then
@@ -140,8 +144,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
             StepConsts c = {};
             zero_dev_scalars* sc = a.sc;
             c.skip = (a.flags & F_GUARD) ? (sc->nonfinite != 0) : 0;
-            set_divisor(c, a.n_ranks > 0 ? a.n_ranks : 1, (a.flags & F_LSCALE) ? sc->loss_scale : 1.0f);
-            set_adam(c, a.hp, sc->beta1_pow, sc->beta2_pow);
+            set_divisor(c, (a.n_ranks > 0 ? a.n_ranks : 1) * (a.micro > 0 ? a.micro : 1),
+                        (a.flags & F_LSCALE) ? sc->loss_scale : 1.0f);
+            if (sc != nullptr) set_adam(c, a.hp, sc->beta1_pow, sc->beta2_pow);   // null: plain sums only
             c.clip = (a.flags & F_CLIP) != 0;
             if (a.flags & F_FINALIZE) {
                 const float coef = clip_coefficient(a.hp.max_norm, sq);
@@ -237,6 +242,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
         const StepConsts c = sh->c;
         const bool detect = (a.flags & (F_DETECT | F_SQNORM)) != 0;
         const bool want_sq = (a.flags & F_SQNORM) != 0;
+        const bool carry = (a.flags & F_CARRY) != 0;
+        const bool raw = (a.flags & F_RAW) != 0;
+        constexpr int kCarry = (OP == OP_REDUCE) ? 0 : 3;   // side slot of the carry stream
         TileCursor cur;
         for (cur.start(a); cur.valid(a); cur.next(a)) {
             long long j0;
@@ -377,7 +385,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
                     float gv[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        gv[e] = mean_of(c, acc[ch][e]);
+                        const float sum = carry ? __fadd_rn(sv[ch][kCarry][e], acc[ch][e]) : acc[ch][e];
+                        gv[e] = raw ? sum : mean_of(c, sum);
                         if (e < cnt) {
                             if (detect && !is_finite_f32(gv[e])) nonfinite = true;
                             if (want_sq) sq_accumulate(gv[e], sq_hi, sq_lo);
@@ -393,13 +402,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
                         }
                     }
                 } else {
-                    // OP_FUSED: side = {master, m, v}; OP_ADAM: side = {g, master, m, v}
+                    // OP_FUSED: side = {master, m, v[, carry]}; OP_ADAM: side = {g, master, m, v}
                     constexpr int P = (OP == OP_ADAM) ? 1 : 0;
                     float pv[4], mv[4], vv[4];
                     uint16_t lp[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        float g = (OP == OP_ADAM) ? sv[ch][0][e] : mean_of(c, acc[ch][e]);
+                        float g = (OP == OP_ADAM)
+                                      ? sv[ch][0][e]
+                                      : mean_of(c, carry ? __fadd_rn(sv[ch][kCarry][e], acc[ch][e]) : acc[ch][e]);
                         if (detect && e < cnt && !is_finite_f32(g)) nonfinite = true;
                         if (c.clip) g = __fmul_rn(g, c.coef);
                         pv[e] = sv[ch][P + 0][e];
@@ -524,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
         for (int s = 0; s < a.stages; ++s)
             if (sh->issued_parity[s] >= 0)
                 mbar_wait_bounded(&sh->full[s], static_cast<uint32_t>(sh->issued_parity[s]), nullptr, a.timeout_ns);
-        atomicOr(&a.sc->status, ZERO_DEV_TIMEOUT);
+        if (a.sc != nullptr) atomicOr(&a.sc->status, ZERO_DEV_TIMEOUT);
     }
     if (a.flags & F_EPILOGUE) {
         // the last CTA to finish commits the step scalars: every CTA read them
