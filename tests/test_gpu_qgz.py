@@ -24,7 +24,10 @@ def _codes_buffers(n_d, psi, S, block):
 
 
 @pytest.mark.parametrize("n_d,psi,pad,block", [(2, 1 << 20, 8, 2048), (4, 1_000_003, 8, 2048),
-                                               (3, 100_001, 1, 256), (8, 70_000, 64, 2048), (16, 5000, 8, 32)])
+                                               (3, 100_001, 1, 256), (8, 70_000, 64, 2048), (16, 5000, 8, 32),
+                                               (1, 123_457, 8, 2048), (5, 4097 * 3, 1, 2048),
+                                               (3, 100_001, 1, 2048), (64, 40_000, 16, 2048),
+                                               (7, 6, 8, 2048), (2, 2 * 4096 * 37, 4096, 2048)])
 def test_sender_codes_and_scales(n_d, psi, pad, block):
     plan = z.Plan(psi, n_d, stage=2, shard_pad=pad)
     S = plan.shard

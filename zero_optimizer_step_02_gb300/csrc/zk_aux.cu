@@ -11,6 +11,8 @@
 //   k_epilogue       commits the step scalars (t, beta powers, loss scale)
 //   k_repair         restores a speculative step that turned out to overflow
 //   k_scalars_init, k_debug_wait
+#include <cstring>
+
 #include "zk_common.cuh"
 #include "zk_launch.h"
 
@@ -366,22 +368,25 @@ __global__ void __launch_bounds__(256) k_quant_gather(const uint16_t* __restrict
         if (lane == 0) scales[bi] = s;
         const float inv = quant_reciprocal(s);
         auto quant = [&](float xv, signed char& q, uint16_t& d) {
-            q = quant_code(xv, s, inv);
-            d = Lp<ZERO_BF16>::narrow(__fmul_rn(static_cast<float>(q), s));
+            const float cf = quant_code_f(xv, s, inv);
+            q = static_cast<signed char>(static_cast<uint8_t>(code_bits(cf)));
+            d = Lp<ZERO_BF16>::narrow(__fmul_rn(cf, s));
         };
         for (int v = lane; v < nv; v += 32) {
             const uint4 w = reinterpret_cast<const uint4*>(x + j0)[v];
             const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-            signed char q[8];
             uint16_t d[8];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                quant(Lp<ZERO_BF16>::lo(ws[k]), q[2 * k], d[2 * k]);
-                quant(Lp<ZERO_BF16>::hi(ws[k]), q[2 * k + 1], d[2 * k + 1]);
-            }
             uint2 cq;
-            cq.x = (uint32_t)(uint8_t)q[0] | ((uint32_t)(uint8_t)q[1] << 8) | ((uint32_t)(uint8_t)q[2] << 16) | ((uint32_t)(uint8_t)q[3] << 24);
-            cq.y = (uint32_t)(uint8_t)q[4] | ((uint32_t)(uint8_t)q[5] << 8) | ((uint32_t)(uint8_t)q[6] << 16) | ((uint32_t)(uint8_t)q[7] << 24);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const float xs[4] = {Lp<ZERO_BF16>::lo(ws[2 * h]), Lp<ZERO_BF16>::hi(ws[2 * h]),
+                                     Lp<ZERO_BF16>::lo(ws[2 * h + 1]), Lp<ZERO_BF16>::hi(ws[2 * h + 1])};
+                float cf[4];
+                const uint32_t c4 = quant_code4(xs, s, inv, cf);
+                if (h == 0) cq.x = c4; else cq.y = c4;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) d[4 * h + e] = Lp<ZERO_BF16>::narrow(__fmul_rn(cf[e], s));
+            }
             reinterpret_cast<uint2*>(codes + j0)[v] = cq;
             if (gathered == nullptr) continue;   // codes and scales only (gradient sender)
             uint4 dv;
@@ -418,80 +423,161 @@ cudaError_t launch_quant_gather(const void* shards, int n_d, long long shard, lo
     return cudaGetLastError();
 }
 
-// Sender side of the quantized gradient exchange: rank q's bf16 gradient
-// through the block quantizer (codes at the global index, scales at
-// [(r * nbs + b) * n_dp + q]).  One warp per block.  A full, 16-byte aligned
-// block of 2048 is held in registers (8 x 16 bytes per lane) and quantized in
-// one pass; any other block is read twice (amax, then codes).
-__global__ void __launch_bounds__(256) k_quantize_rank(const uint16_t* __restrict__ x, int n_d, long long shard,
-                                                       long long psi, int block, long long nbs, long long n_dp, int q,
-                                                       signed char* __restrict__ codes, float* __restrict__ scales)
+// Sender side of the quantized gradient exchange: every rank q's bf16
+// gradient through the block quantizer, codes at the global index of rank
+// q's code buffer, scales at [(r * nbs + b) * n_dp + q] (block b of shard r).
+// All ranks in one launch.  One warp per block at a time, no block-wide
+// barrier: each warp owns kQsSlots shared-memory slots of one 2048-element
+// block that its lane 0 fills with 1-D bulk copies kQsSlots blocks ahead, so
+// ~192 KB per SM are in flight while the warps quantize.  Blocks that are not
+// full, 16-byte aligned 2048-element blocks (ragged shard ends, other block
+// sizes) are read from global memory twice (amax, then codes).
+constexpr int kQsWarps = 16;
+constexpr int kQsSlots = 3;
+constexpr int kQsSlotBytes = kQuantBlock * 2;
+
+struct QsArgs {
+    const uint16_t* rank[ZERO_MAX_RANKS];
+    signed char* codes[ZERO_MAX_RANKS];
+    float* scales;
+    long long shard, psi, nbs, n_dp, total;   // total = n_d * n_d * nbs blocks
+    int n_d, block, ring_ok;                   // ring_ok: block == 2048 and shard % 8 == 0
+    unsigned long long timeout_ns;
+};
+
+struct QsBlock {
+    int q;           // rank whose gradient it is
+    long long row;   // scale row r * nbs + b
+    long long j0;    // first element (global index)
+    int n;           // valid elements (0: past psi)
+};
+
+__device__ __forceinline__ QsBlock qs_block(const QsArgs& a, long long bi)
 {
+    QsBlock k;
+    const long long per_rank = static_cast<long long>(a.n_d) * a.nbs;
+    k.q = static_cast<int>(bi / per_rank);
+    k.row = bi - static_cast<long long>(k.q) * per_rank;
+    const long long r = k.row / a.nbs;
+    const long long b = k.row - r * a.nbs;
+    long long valid = a.psi - r * a.shard;
+    valid = valid < 0 ? 0 : (valid > a.shard ? a.shard : valid);
+    const long long lo = b * a.block;
+    const long long hi = lo + a.block < valid ? lo + a.block : valid;
+    k.j0 = r * a.shard + lo;
+    k.n = hi > lo ? static_cast<int>(hi - lo) : 0;
+    return k;
+}
+
+__device__ __forceinline__ bool qs_ring(const QsArgs& a, const QsBlock& k) { return a.ring_ok && k.n == kQuantBlock; }
+
+__global__ void __launch_bounds__(kQsWarps * 32, 1) k_quantize_ranks(const __grid_constant__ QsArgs a)
+{
+    extern __shared__ __align__(1024) unsigned char smem[];
+    const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
-    const long long nblocks = nbs * n_d;
-    const bool vec = (shard % 8) == 0;
-    for (long long bi = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); bi < nblocks;
-         bi += warps) {
-        const int r = static_cast<int>(bi / nbs);
-        const long long b = bi - static_cast<long long>(r) * nbs;
-        float* sc = scales + bi * n_dp + q;
-        if (q == 0 && lane < n_dp - n_d) scales[bi * n_dp + n_d + lane] = 0.0f;   // rank padding of the layout
-        long long valid = psi - static_cast<long long>(r) * shard;
-        valid = valid < 0 ? 0 : (valid > shard ? shard : valid);
-        const long long lo = b * block;
-        const long long hi = lo + block < valid ? lo + block : valid;
-        if (hi <= lo) {
-            if (lane == 0) *sc = 0.0f;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem) + warp * kQsSlots;
+    unsigned char* slot0 = smem + 1024 + static_cast<size_t>(warp) * kQsSlots * kQsSlotBytes;
+    const long long step = static_cast<long long>(gridDim.x) * kQsWarps;
+    const long long first = static_cast<long long>(blockIdx.x) * kQsWarps + warp;
+    const int pad = static_cast<int>(a.n_dp) - a.n_d;
+
+    if (lane == 0) {
+        for (int s = 0; s < kQsSlots; ++s) mbar_init(&bar[s], 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+
+    // lane 0 issues block number kk of this warp's sequence into its slot
+    uint32_t pending = 0;   // lane 0: slots with a copy in flight
+    auto issue = [&](long long kk) {
+        const long long bi = first + kk * step;
+        if (bi >= a.total) return;
+        const QsBlock k = qs_block(a, bi);
+        if (!qs_ring(a, k)) return;
+        const int s = static_cast<int>(kk % kQsSlots);
+        if (lane == 0) {
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(&bar[s], kQsSlotBytes);
+            bulk_load(slot0 + s * kQsSlotBytes, a.rank[k.q] + k.j0, kQsSlotBytes, &bar[s]);
+            pending |= 1u << s;
+        }
+    };
+    for (int kk = 0; kk < kQsSlots; ++kk) issue(kk);
+
+    uint32_t phase = 0;     // per slot: parity of its next completion
+    bool ok = true;
+    for (long long kk = 0;; ++kk) {
+        const long long bi = first + kk * step;
+        if (bi >= a.total) break;
+        const QsBlock k = qs_block(a, bi);
+        const int s = static_cast<int>(kk % kQsSlots);
+        float* srow = a.scales + k.row * a.n_dp;
+        if (k.q == a.n_d - 1 && lane >= 1 && lane <= pad) srow[a.n_d - 1 + lane] = 0.0f;   // layout padding
+        if (k.n <= 0) {
+            if (lane == 0) srow[k.q] = 0.0f;
+            issue(kk + kQsSlots);
             continue;
         }
-        const long long j0 = static_cast<long long>(r) * shard + lo;
-        const int n = static_cast<int>(hi - lo);
-        if (vec && block == 2048 && n == 2048) {
+        if (qs_ring(a, k)) {
+            const bool got = mbar_wait_bounded(&bar[s], (phase >> s) & 1u, nullptr, a.timeout_ns);
+            if (!__all_sync(0xffffffffu, got)) {
+                ok = false;
+                break;
+            }
+            phase ^= 1u << s;
+            if (lane == 0) pending &= ~(1u << s);
+            const uint4* src = reinterpret_cast<const uint4*>(slot0 + s * kQsSlotBytes);
             uint4 w[8];
 #pragma unroll
-            for (int v = 0; v < 8; ++v) w[v] = reinterpret_cast<const uint4*>(x + j0)[v * 32 + lane];
-            float amax = 0.0f;
+            for (int v = 0; v < 8; ++v) w[v] = src[v * 32 + lane];
+            float am[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
             for (int v = 0; v < 8; ++v) {
                 const uint32_t ws[4] = {w[v].x, w[v].y, w[v].z, w[v].w};
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    amax = fmaxf(amax, fmaxf(fabsf(Lp<ZERO_BF16>::lo(ws[k])), fabsf(Lp<ZERO_BF16>::hi(ws[k]))));
+                for (int e = 0; e < 4; ++e)
+                    am[e] = fmaxf(am[e], fmaxf(fabsf(Lp<ZERO_BF16>::lo(ws[e])), fabsf(Lp<ZERO_BF16>::hi(ws[e]))));
             }
-            amax = warp_max_f32(amax);
-            const float s = __fdiv_rn(amax, 127.0f);
-            if (lane == 0) *sc = s;
-            const float inv = quant_reciprocal(s);
+            const float amax = warp_max_f32(fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3])));
+            // every lane's reads of the slot are complete (their values were used): refill it
+            __syncwarp();
+            issue(kk + kQsSlots);
+            const float sc = __fdiv_rn(amax, 127.0f);
+            if (lane == 0) srow[k.q] = sc;
+            const float inv = quant_reciprocal(sc);
+            uint2* dst = reinterpret_cast<uint2*>(a.codes[k.q] + k.j0);
 #pragma unroll
             for (int v = 0; v < 8; ++v) {
                 const uint32_t ws[4] = {w[v].x, w[v].y, w[v].z, w[v].w};
-                int8_t c[8];
+                uint32_t packed[2];
 #pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    const float xs[4] = {Lp<ZERO_BF16>::lo(ws[2 * k]), Lp<ZERO_BF16>::hi(ws[2 * k]),
-                                         Lp<ZERO_BF16>::lo(ws[2 * k + 1]), Lp<ZERO_BF16>::hi(ws[2 * k + 1])};
-                    int8_t c4[4];
-                    quant_code4(xs, s, inv, c4);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) c[4 * k + e] = c4[e];
+                for (int h = 0; h < 2; ++h) {
+                    const float xs[4] = {Lp<ZERO_BF16>::lo(ws[2 * h]), Lp<ZERO_BF16>::hi(ws[2 * h]),
+                                         Lp<ZERO_BF16>::lo(ws[2 * h + 1]), Lp<ZERO_BF16>::hi(ws[2 * h + 1])};
+                    float cf[4];
+                    packed[h] = quant_code4(xs, sc, inv, cf);
                 }
-                uint2 cq;
-                cq.x = (uint32_t)(uint8_t)c[0] | ((uint32_t)(uint8_t)c[1] << 8) | ((uint32_t)(uint8_t)c[2] << 16) |
-                       ((uint32_t)(uint8_t)c[3] << 24);
-                cq.y = (uint32_t)(uint8_t)c[4] | ((uint32_t)(uint8_t)c[5] << 8) | ((uint32_t)(uint8_t)c[6] << 16) |
-                       ((uint32_t)(uint8_t)c[7] << 24);
-                reinterpret_cast<uint2*>(codes + j0)[v * 32 + lane] = cq;
+                dst[v * 32 + lane] = make_uint2(packed[0], packed[1]);
             }
-            continue;
+        } else {
+            issue(kk + kQsSlots);
+            const uint16_t* x = a.rank[k.q] + k.j0;
+            float amax = 0.0f;
+            for (int i = lane; i < k.n; i += 32) amax = fmaxf(amax, fabsf(Lp<ZERO_BF16>::widen(x[i])));
+            amax = warp_max_f32(amax);
+            const float sc = __fdiv_rn(amax, 127.0f);
+            if (lane == 0) srow[k.q] = sc;
+            const float inv = quant_reciprocal(sc);
+            signed char* c = a.codes[k.q] + k.j0;
+            for (int i = lane; i < k.n; i += 32) c[i] = quant_code(Lp<ZERO_BF16>::widen(x[i]), sc, inv);
         }
-        float amax = 0.0f;
-        for (int i = lane; i < n; i += 32) amax = fmaxf(amax, fabsf(Lp<ZERO_BF16>::widen(x[j0 + i])));
-        amax = warp_max_f32(amax);
-        const float s = __fdiv_rn(amax, 127.0f);
-        if (lane == 0) *sc = s;
-        const float inv = quant_reciprocal(s);
-        for (int i = lane; i < n; i += 32) codes[j0 + i] = quant_code(Lp<ZERO_BF16>::widen(x[j0 + i]), s, inv);
+    }
+    if (!ok && lane == 0) {
+        // a wait ran out: let the copies in flight land before the CTA's
+        // shared memory is released
+        for (int s = 0; s < kQsSlots; ++s)
+            if (pending & (1u << s)) mbar_wait_bounded(&bar[s], (phase >> s) & 1u, nullptr, a.timeout_ns);
     }
 }
 
@@ -500,20 +586,41 @@ cudaError_t launch_quantize_grads(const void* const* ranks, int n_d, long long s
 {
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
-    const long long nbs = (shard + block - 1) / block;
-    const long long n_dp = (n_d + 3) / 4 * 4;
-    const long long nblocks = nbs * n_d;
-    if (nblocks <= 0) return cudaSuccess;
-    long long grid = (nblocks + 7) / 8;
-    if (grid > 16LL * sms) grid = 16LL * sms;
+    QsArgs a;
+    std::memset(&a, 0, sizeof(a));
+    bool aligned = true;
     for (int q = 0; q < n_d; ++q) {
-        count_launch();
-        k_quantize_rank<<<static_cast<unsigned>(grid), 256, 0, st>>>(static_cast<const uint16_t*>(ranks[q]), n_d, shard,
-                                                                     psi, block, nbs, n_dp, q, codes[q], scales);
-        const cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
+        a.rank[q] = static_cast<const uint16_t*>(ranks[q]);
+        a.codes[q] = codes[q];
+        aligned = aligned && (reinterpret_cast<uintptr_t>(ranks[q]) & 15) == 0 &&
+                  (reinterpret_cast<uintptr_t>(codes[q]) & 15) == 0;
     }
-    return cudaSuccess;
+    a.scales = scales;
+    a.shard = shard;
+    a.psi = psi;
+    a.block = block;
+    a.n_d = n_d;
+    a.nbs = (shard + block - 1) / block;
+    a.n_dp = (n_d + 3) / 4 * 4;
+    a.total = static_cast<long long>(n_d) * n_d * a.nbs;
+    a.ring_ok = (block == kQuantBlock && shard % 8 == 0 && aligned) ? 1 : 0;
+    a.timeout_ns = kDefaultTimeoutNs;
+    if (a.total <= 0) return cudaSuccess;
+    const size_t smem = 1024 + static_cast<size_t>(kQsWarps) * kQsSlots * kQsSlotBytes;
+    static int attr_done[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !__atomic_load_n(&attr_done[dev], __ATOMIC_ACQUIRE)) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(k_quantize_ranks, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        __atomic_store_n(&attr_done[dev], 1, __ATOMIC_RELEASE);
+    }
+    long long grid = (a.total + kQsWarps - 1) / kQsWarps;
+    if (grid > sms) grid = sms;
+    count_launch();
+    k_quantize_ranks<<<static_cast<unsigned>(grid), kQsWarps * 32, smem, st>>>(a);
+    return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------- diagnostics

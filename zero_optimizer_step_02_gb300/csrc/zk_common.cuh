@@ -68,6 +68,12 @@ __device__ __forceinline__ void fence_barrier_init()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// order this thread's earlier shared-memory accesses before later bulk copies
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes)
 {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
@@ -174,6 +180,12 @@ struct Lp<ZERO_BF16> {
     {
         return __bfloat16_as_ushort(__float2bfloat16_rn(x));
     }
+    // two values in one conversion, a in the low half (each rounded as narrow)
+    __device__ static __forceinline__ uint32_t narrow2(float a, float b)
+    {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    }
 };
 
 template <>
@@ -188,6 +200,11 @@ struct Lp<ZERO_FP16> {
     }
     __device__ static __forceinline__ float widen(uint16_t h) { return __half2float(__ushort_as_half(h)); }
     __device__ static __forceinline__ uint16_t narrow(float x) { return __half_as_ushort(__float2half_rn(x)); }
+    __device__ static __forceinline__ uint32_t narrow2(float a, float b)
+    {
+        const __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    }
 };
 
 __device__ __forceinline__ bool is_finite_f32(float x)
@@ -321,53 +338,83 @@ __device__ __forceinline__ void commit_scalars(const zero_hparams& hp, zero_dev_
 // quotient only when that product lies within 2^-14 of a half-integer: the
 // product and the quotient differ by a few ulp of a value below 128 (an ulp
 // there is at most 2^-17), so away from a tie both round to the same integer.
-// inv = quant_reciprocal(s); 0 when 1/s is not a normal float (then every
-// code takes the exact quotient).
+// inv = quant_reciprocal(s); 0 unless s is a positive normal float below
+// 3e38 (then every code takes the exact quotient).  With a normal s,
+// |x * inv| <= 127 (1 + 2^-22) for every |x| <= amax, so the fast codes
+// never need the clamp.
 __device__ __forceinline__ float quant_reciprocal(float s)
 {
-    if (!(s > 0.0f)) return 0.0f;
-    const float r = __frcp_rn(s);
-    return (r < 3.0e38f) ? r : 0.0f;
+    if (!(s >= 1.17549435e-38f) || !(s < 3.0e38f)) return 0.0f;
+    return __frcp_rn(s);
 }
+
+// Round to nearest, ties to even, with one addition: for |y| < 2^22,
+// y + 1.5 * 2^23 keeps no fraction bits, so the sum is rint(y) + 1.5 * 2^23
+// exactly and subtracting the constant gives rint(y); the sum's low byte is
+// the two's-complement low byte of rint(y) (the constant's low 22 bits are
+// zero).  Larger |y| are not rounded exactly but stay beyond +-127.5, which
+// the clamp below maps to +-127 as it would rint(y); NaN clamps to -127 as
+// fmaxf(rintf(NaN), -127) does.  Full-rate FP adds instead of the conversion
+// unit's rint / floor / float-to-int.
+constexpr float kRintShift = 12582912.0f;
+// |y - rint(y)| at or above this: y lies within 2^-14 of a half-integer
+constexpr float kTieBand = 0.49993896484375f;   // 0.5 - 2^-14
+
+__device__ __forceinline__ float rint_shift(float y) { return __fsub_rn(__fadd_rn(y, kRintShift), kRintShift); }
+
+__device__ __forceinline__ float clamp127(float r) { return fminf(fmaxf(r, -127.0f), 127.0f); }
+
+// the int8 bits of an integer-valued float in [-127, 127], in the low byte
+__device__ __forceinline__ uint32_t code_bits(float cf) { return __float_as_uint(__fadd_rn(cf, kRintShift)); }
 
 // Codes of four values at once: the fast products for all four, and one
 // (rarely taken) branch to the exact quotients if any of them is near a tie.
-__device__ __forceinline__ void quant_code4(const float (&x)[4], float s, float inv, int8_t (&q)[4])
+// cf receives the codes as floats (for dequantization); the return value
+// packs the four int8 codes, code e in byte e.
+__device__ __forceinline__ uint32_t quant_code4(const float (&x)[4], float s, float inv, float (&cf)[4])
 {
     if (s == 0.0f) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) q[e] = 0;
-        return;
+        for (int e = 0; e < 4; ++e) cf[e] = 0.0f;
+        return 0u;
     }
-    float y[4];
+    // fast: t = rint(x * inv) + 1.5 * 2^23 (its low byte is the code), no
+    // clamp needed (see quant_reciprocal); a NaN product fails the test below
+    float t[4];
     bool near = inv == 0.0f;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-        y[e] = __fmul_rn(x[e], inv);
-        const float d = fabsf(__fsub_rn(__fsub_rn(y[e], floorf(y[e])), 0.5f));
-        near |= d <= 6.103515625e-05f;   // 2^-14
+        const float y = __fmul_rn(x[e], inv);
+        t[e] = __fadd_rn(y, kRintShift);
+        cf[e] = __fsub_rn(t[e], kRintShift);
+        near |= !(fabsf(__fsub_rn(y, cf[e])) < kTieBand);
     }
     if (near) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) y[e] = __fdiv_rn(x[e], s);
+        for (int e = 0; e < 4; ++e) {
+            cf[e] = clamp127(rint_shift(__fdiv_rn(x[e], s)));
+            t[e] = __fadd_rn(cf[e], kRintShift);
+        }
     }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) q[e] = static_cast<int8_t>(static_cast<int>(fminf(fmaxf(rintf(y[e]), -127.0f), 127.0f)));
+    const uint32_t u[4] = {__float_as_uint(t[0]), __float_as_uint(t[1]), __float_as_uint(t[2]), __float_as_uint(t[3])};
+    return __byte_perm(__byte_perm(u[0], u[1], 0x0040u), __byte_perm(u[2], u[3], 0x0040u), 0x5410u);
+}
+
+// One code, as a float (see quant_code4).
+__device__ __forceinline__ float quant_code_f(float x, float s, float inv)
+{
+    if (s == 0.0f) return 0.0f;
+    if (inv != 0.0f) {
+        const float y = __fmul_rn(x, inv);
+        const float r = rint_shift(y);
+        if (fabsf(__fsub_rn(y, r)) < kTieBand) return r;   // else near a tie (or NaN): decide exactly
+    }
+    return clamp127(rint_shift(__fdiv_rn(x, s)));
 }
 
 __device__ __forceinline__ int8_t quant_code(float x, float s, float inv)
 {
-    if (s == 0.0f) return 0;
-    float y;
-    if (inv != 0.0f) {
-        y = __fmul_rn(x, inv);
-        const float d = fabsf(__fsub_rn(__fsub_rn(y, floorf(y)), 0.5f));
-        if (d <= 6.103515625e-05f) y = __fdiv_rn(x, s);   // 2^-14: near a tie, decide exactly
-    } else {
-        y = __fdiv_rn(x, s);
-    }
-    const float q = fminf(fmaxf(rintf(y), -127.0f), 127.0f);
-    return static_cast<int8_t>(static_cast<int>(q));
+    return static_cast<int8_t>(static_cast<uint8_t>(code_bits(quant_code_f(x, s, inv))));
 }
 
 __device__ __forceinline__ double warp_sum_f64(double x)

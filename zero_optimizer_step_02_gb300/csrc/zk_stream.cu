@@ -114,6 +114,8 @@ __device__ __forceinline__ void add_slice(float (&acc)[4], uint2 w)
 template <int GT>
 __host__ __device__ constexpr int group_ranks() { return GT == kGradQ8 ? 2 * kGroupRanks : kGroupRanks; }
 
+// 17 warps spread over an SM's 4 sub-partitions put 5 on one of them, whose
+// 16K registers then allow 96 per thread: the bound ptxas works to here.
 template <int GT, int PT, int OP>
 __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ StreamArgs a)
 {
@@ -485,27 +487,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
                     const long long jc = j0 + q * 4;
                     int cnt = len - q * 4;
                     cnt = cnt < 0 ? 0 : (cnt > 4 ? 4 : cnt);
-                    int8_t code[4];
-                    uint16_t dq[4];
-                    quant_code4(xq[ch], scale, inv_scale, code);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) dq[e] = Lp<ZERO_BF16>::narrow(__fmul_rn(static_cast<float>(code[e]), scale));
+                    float cf[4];
+                    const uint32_t cw = quant_code4(xq[ch], scale, inv_scale, cf);
+                    const uint32_t d01 = Lp<ZERO_BF16>::narrow2(__fmul_rn(cf[0], scale), __fmul_rn(cf[1], scale));
+                    const uint32_t d23 = Lp<ZERO_BF16>::narrow2(__fmul_rn(cf[2], scale), __fmul_rn(cf[3], scale));
+                    const uint16_t dq[4] = {static_cast<uint16_t>(d01), static_cast<uint16_t>(d01 >> 16),
+                                            static_cast<uint16_t>(d23), static_cast<uint16_t>(d23 >> 16)};
                     if (!alive) continue;
                     if (fast) {
-                        const uint32_t cw = (static_cast<uint32_t>(static_cast<uint8_t>(code[0]))) |
-                                            (static_cast<uint32_t>(static_cast<uint8_t>(code[1])) << 8) |
-                                            (static_cast<uint32_t>(static_cast<uint8_t>(code[2])) << 16) |
-                                            (static_cast<uint32_t>(static_cast<uint8_t>(code[3])) << 24);
                         *reinterpret_cast<uint32_t*>(a.q_codes + jc) = cw;
-                        uint2 w;
-                        w.x = static_cast<uint32_t>(dq[0]) | (static_cast<uint32_t>(dq[1]) << 16);
-                        w.y = static_cast<uint32_t>(dq[2]) | (static_cast<uint32_t>(dq[3]) << 16);
-                        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.q_gathered) + jc) = w;
+                        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.q_gathered) + jc) = make_uint2(d01, d23);
                     } else {
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             if (e < cnt) {
-                                a.q_codes[jc + e] = code[e];
+                                a.q_codes[jc + e] = static_cast<signed char>(static_cast<uint8_t>(cw >> (8 * e)));
                                 static_cast<uint16_t*>(a.q_gathered)[jc + e] = dq[e];
                             }
                         }
