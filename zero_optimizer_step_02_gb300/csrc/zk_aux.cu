@@ -432,8 +432,8 @@ cudaError_t launch_quant_gather(const void* shards, int n_d, long long shard, lo
 // ~192 KB per SM are in flight while the warps quantize.  Blocks that are not
 // full, 16-byte aligned 2048-element blocks (ragged shard ends, other block
 // sizes) are read from global memory twice (amax, then codes).
-constexpr int kQsWarps = 16;
-constexpr int kQsSlots = 3;
+constexpr int kQsWarps = 28;
+constexpr int kQsSlots = 2;
 constexpr int kQsSlotBytes = kQuantBlock * 2;
 
 struct QsArgs {
@@ -452,22 +452,56 @@ struct QsBlock {
     int n;           // valid elements (0: past psi)
 };
 
-__device__ __forceinline__ QsBlock qs_block(const QsArgs& a, long long bi)
-{
-    QsBlock k;
-    const long long per_rank = static_cast<long long>(a.n_d) * a.nbs;
-    k.q = static_cast<int>(bi / per_rank);
-    k.row = bi - static_cast<long long>(k.q) * per_rank;
-    const long long r = k.row / a.nbs;
-    const long long b = k.row - r * a.nbs;
-    long long valid = a.psi - r * a.shard;
-    valid = valid < 0 ? 0 : (valid > a.shard ? a.shard : valid);
-    const long long lo = b * a.block;
-    const long long hi = lo + a.block < valid ? lo + a.block : valid;
-    k.j0 = r * a.shard + lo;
-    k.n = hi > lo ? static_cast<int>(hi - lo) : 0;
-    return k;
-}
+// Walks one warp's blocks bi = first, first + step, ... as (q, r, b) with
+// bi = (q * n_d + r) * nbs + b: divisions once, then add-and-carry.
+struct QsCursor {
+    int q, r, b;      // current block (nbs < 2^31: checked at launch)
+    int dq, dr, db;   // step split the same way
+
+    __device__ static __forceinline__ void split(const QsArgs& a, long long x, int& q, int& r, int& b)
+    {
+        const long long per_rank = static_cast<long long>(a.n_d) * a.nbs;
+        const long long qq = x / per_rank;
+        const long long row = x - qq * per_rank;
+        const long long rr = row / a.nbs;
+        q = static_cast<int>(qq);   // x < grid * warps per CTA: fits
+        r = static_cast<int>(rr);
+        b = static_cast<int>(row - rr * a.nbs);
+    }
+    __device__ __forceinline__ void start(const QsArgs& a, long long first, long long step)
+    {
+        split(a, first, q, r, b);
+        split(a, step, dq, dr, db);
+    }
+    __device__ __forceinline__ void next(const QsArgs& a)
+    {
+        b += db;
+        if (b >= a.nbs) {
+            b -= a.nbs;
+            ++r;
+        }
+        r += dr;
+        if (r >= a.n_d) {
+            r -= a.n_d;
+            ++q;
+        }
+        q += dq;
+    }
+    __device__ __forceinline__ bool valid(const QsArgs& a) const { return q < a.n_d; }
+    __device__ __forceinline__ QsBlock block(const QsArgs& a) const
+    {
+        QsBlock k;
+        k.q = q;
+        k.row = static_cast<long long>(r) * a.nbs + b;
+        long long valid = a.psi - static_cast<long long>(r) * a.shard;
+        valid = valid < 0 ? 0 : (valid > a.shard ? a.shard : valid);
+        const long long lo = static_cast<long long>(b) * a.block;
+        const long long hi = lo + a.block < valid ? lo + a.block : valid;
+        k.j0 = static_cast<long long>(r) * a.shard + lo;
+        k.n = hi > lo ? static_cast<int>(hi - lo) : 0;
+        return k;
+    }
+};
 
 __device__ __forceinline__ bool qs_ring(const QsArgs& a, const QsBlock& k) { return a.ring_ok && k.n == kQuantBlock; }
 
@@ -488,35 +522,36 @@ __global__ void __launch_bounds__(kQsWarps * 32, 1) k_quantize_ranks(const __gri
     }
     __syncwarp();
 
-    // lane 0 issues block number kk of this warp's sequence into its slot
+    // lane 0 issues the block under the issue cursor, kQsSlots blocks ahead
+    // of the work cursor, into slot s
     uint32_t pending = 0;   // lane 0: slots with a copy in flight
-    auto issue = [&](long long kk) {
-        const long long bi = first + kk * step;
-        if (bi >= a.total) return;
-        const QsBlock k = qs_block(a, bi);
-        if (!qs_ring(a, k)) return;
-        const int s = static_cast<int>(kk % kQsSlots);
-        if (lane == 0) {
-            fence_proxy_async_smem();
-            mbar_arrive_expect_tx(&bar[s], kQsSlotBytes);
-            bulk_load(slot0 + s * kQsSlotBytes, a.rank[k.q] + k.j0, kQsSlotBytes, &bar[s]);
-            pending |= 1u << s;
+    QsCursor ic;
+    ic.start(a, first, step);
+    auto issue = [&](int s) {
+        if (ic.valid(a)) {
+            const QsBlock k = ic.block(a);
+            if (qs_ring(a, k) && lane == 0) {
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(&bar[s], kQsSlotBytes);
+                bulk_load(slot0 + s * kQsSlotBytes, a.rank[k.q] + k.j0, kQsSlotBytes, &bar[s]);
+                pending |= 1u << s;
+            }
         }
+        ic.next(a);
     };
-    for (int kk = 0; kk < kQsSlots; ++kk) issue(kk);
+    for (int s = 0; s < kQsSlots; ++s) issue(s);
 
     uint32_t phase = 0;     // per slot: parity of its next completion
     bool ok = true;
-    for (long long kk = 0;; ++kk) {
-        const long long bi = first + kk * step;
-        if (bi >= a.total) break;
-        const QsBlock k = qs_block(a, bi);
-        const int s = static_cast<int>(kk % kQsSlots);
+    QsCursor wc;
+    wc.start(a, first, step);
+    for (int s = 0; wc.valid(a); wc.next(a), s = (s + 1 == kQsSlots) ? 0 : s + 1) {
+        const QsBlock k = wc.block(a);
         float* srow = a.scales + k.row * a.n_dp;
         if (k.q == a.n_d - 1 && lane >= 1 && lane <= pad) srow[a.n_d - 1 + lane] = 0.0f;   // layout padding
         if (k.n <= 0) {
             if (lane == 0) srow[k.q] = 0.0f;
-            issue(kk + kQsSlots);
+            issue(s);
             continue;
         }
         if (qs_ring(a, k)) {
@@ -527,29 +562,31 @@ __global__ void __launch_bounds__(kQsWarps * 32, 1) k_quantize_ranks(const __gri
             }
             phase ^= 1u << s;
             if (lane == 0) pending &= ~(1u << s);
+            // the block is read from its slot twice (amax, then codes) so that a
+            // lane holds 16 bytes of it at a time
             const uint4* src = reinterpret_cast<const uint4*>(slot0 + s * kQsSlotBytes);
-            uint4 w[8];
+            // |x| maxima on bf16 pairs (a max picks one of its inputs, so it is
+            // exact in bf16; a NaN input is passed over as fmaxf does)
+            __nv_bfloat162 am[4];
 #pragma unroll
-            for (int v = 0; v < 8; ++v) w[v] = src[v * 32 + lane];
-            float am[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            for (int e = 0; e < 4; ++e) am[e] = __float2bfloat162_rn(0.0f);
 #pragma unroll
             for (int v = 0; v < 8; ++v) {
-                const uint32_t ws[4] = {w[v].x, w[v].y, w[v].z, w[v].w};
+                const uint4 wv = src[v * 32 + lane];
+                const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    am[e] = fmaxf(am[e], fmaxf(fabsf(Lp<ZERO_BF16>::lo(ws[e])), fabsf(Lp<ZERO_BF16>::hi(ws[e]))));
+                for (int e = 0; e < 4; ++e) am[e] = __hmax2(am[e], __habs2(*reinterpret_cast<const __nv_bfloat162*>(&ws[e])));
             }
-            const float amax = warp_max_f32(fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3])));
-            // every lane's reads of the slot are complete (their values were used): refill it
-            __syncwarp();
-            issue(kk + kQsSlots);
+            const __nv_bfloat162 m2 = __hmax2(__hmax2(am[0], am[1]), __hmax2(am[2], am[3]));
+            const float amax = warp_max_f32(fmaxf(__low2float(m2), __high2float(m2)));
             const float sc = __fdiv_rn(amax, 127.0f);
             if (lane == 0) srow[k.q] = sc;
             const float inv = quant_reciprocal(sc);
             uint2* dst = reinterpret_cast<uint2*>(a.codes[k.q] + k.j0);
 #pragma unroll
             for (int v = 0; v < 8; ++v) {
-                const uint32_t ws[4] = {w[v].x, w[v].y, w[v].z, w[v].w};
+                const uint4 wv = src[v * 32 + lane];
+                const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
                 uint32_t packed[2];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
@@ -560,8 +597,11 @@ __global__ void __launch_bounds__(kQsWarps * 32, 1) k_quantize_ranks(const __gri
                 }
                 dst[v * 32 + lane] = make_uint2(packed[0], packed[1]);
             }
+            // every lane's reads of the slot are complete (their values were used): refill it
+            __syncwarp();
+            issue(s);
         } else {
-            issue(kk + kQsSlots);
+            issue(s);
             const uint16_t* x = a.rank[k.q] + k.j0;
             float amax = 0.0f;
             for (int i = lane; i < k.n; i += 32) amax = fmaxf(amax, fabsf(Lp<ZERO_BF16>::widen(x[i])));
@@ -603,6 +643,7 @@ cudaError_t launch_quantize_grads(const void* const* ranks, int n_d, long long s
     a.nbs = (shard + block - 1) / block;
     a.n_dp = (n_d + 3) / 4 * 4;
     a.total = static_cast<long long>(n_d) * n_d * a.nbs;
+    if (a.nbs > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
     a.ring_ok = (block == kQuantBlock && shard % 8 == 0 && aligned) ? 1 : 0;
     a.timeout_ns = kDefaultTimeoutNs;
     if (a.total <= 0) return cudaSuccess;
