@@ -214,7 +214,7 @@ class Job:
                             max_norm=w["clip"], loss_scaling=w["ls"])
         self.plan = z.Plan(w["psi"], w["n_d"], stage=w["stage"], grad_dtype=gdt, shard_pad=w["pad"])
         tdt = torch.float16 if gdt == z.ZERO_FP16 else torch.bfloat16
-        row = z.row_len(w["psi"])
+        row = z.row_len(w["psi"], w.get("row_pad", 0))
         scale = 1024.0 if w["ls"] else 1.0
         # gradient sets: one per layer for ZeRO-3, else a small pool used in turn
         nsets = w["layers"] if w["layers"] > 1 else pool
@@ -354,6 +354,9 @@ def gpu_arm(args, rank, world, device):
     import torch
     import zero_optimizer_step_02_gb300 as z
     w = workload(args.config, args.nd, args.qgather, args.psi, args.qgz, args.gathers, args.offload, args.accum)
+    if args.row_pad:
+        w["row_pad"] = args.row_pad
+        w["name"] += "_rowpad%d" % args.row_pad
     torch.cuda.set_device(device)
     job = Job(w, device)
     torch.cuda.synchronize()
@@ -488,6 +491,7 @@ def gpu_arm(args, rank, world, device):
            "config": {"workload": w["name"], "psi": w["psi"], "layers": w["layers"], "n_d": w["n_d"],
                       "stage": w["stage"], "grad_dtype": w["gdt"], "clip": w["clip"], "loss_scaling": w["ls"],
                       "bytes_per_param": w["bytes_per_param"], "micro_batches": w.get("accum", 1),
+                      "rank_row_pad": w.get("row_pad", 0),
                       "parallelism": "replicas x%d" % world,
                       "l2": "flushed between steps" if small else "inputs larger than L2"},
            "step_gbs": round(step_gbs, 1), "step_frac_of_peak": round(step_gbs / peak, 4),
@@ -643,6 +647,8 @@ def main():
     ap.add_argument("--gathers", type=int, default=1, choices=[1, 2], help="ZeRO-3 gathers per layer and step")
     ap.add_argument("--offload", action="store_true", help="optimizer state in page-locked host memory")
     ap.add_argument("--accum", type=int, default=1, help="micro-batches per optimizer step (gradient accumulation)")
+    ap.add_argument("--row-pad", type=int, default=0,
+                    help="extra elements between rank rows (breaks power-of-two rank strides)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

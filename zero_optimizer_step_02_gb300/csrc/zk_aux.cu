@@ -432,7 +432,7 @@ cudaError_t launch_quant_gather(const void* shards, int n_d, long long shard, lo
 // ~192 KB per SM are in flight while the warps quantize.  Blocks that are not
 // full, 16-byte aligned 2048-element blocks (ragged shard ends, other block
 // sizes) are read from global memory twice (amax, then codes).
-constexpr int kQsWarps = 28;
+constexpr int kQsWarps = 24;
 constexpr int kQsSlots = 2;
 constexpr int kQsSlotBytes = kQuantBlock * 2;
 

@@ -170,8 +170,61 @@ __device__ __forceinline__ void named_bar_sync(int id, int count)
 template <int DT>
 struct Lp;
 
+// ------------------------------------------- packed and mixed fp32 arithmetic
+// sm_100-family instructions that do what several scalar ones do, with the
+// same IEEE round-to-nearest results (subnormals kept): an fp32 add of a
+// 16-bit operand (the widening is exact, so this is fadd(widen(h), acc)),
+// and fp32 operations on register pairs.
+__device__ __forceinline__ void halves(uint32_t w, unsigned short& lo, unsigned short& hi)
+{
+    asm("mov.b32 {%0, %1}, %2;" : "=h"(lo), "=h"(hi) : "r"(w));
+}
+__device__ __forceinline__ float add_bf16_f32(unsigned short h, float acc)
+{
+    float d;
+    asm("add.rn.f32.bf16 %0, %1, %2;" : "=f"(d) : "h"(h), "f"(acc));
+    return d;
+}
+__device__ __forceinline__ float add_f16_f32(unsigned short h, float acc)
+{
+    float d;
+    asm("add.rn.f32.f16 %0, %1, %2;" : "=f"(d) : "h"(h), "f"(acc));
+    return d;
+}
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 pack2(float a, float b)
+{
+    f32x2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void unpack2(f32x2 v, float& a, float& b)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b)
+{
+    f32x2 d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f32x2 sub2(f32x2 a, f32x2 b)
+{
+    f32x2 d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b)
+{
+    f32x2 d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 template <>
 struct Lp<ZERO_BF16> {
+    // acc + the 16-bit value h, one rounding
+    __device__ static __forceinline__ float add(float acc, unsigned short h) { return add_bf16_f32(h, acc); }
     // a 32-bit word holds two consecutive elements, the first in the low half
     __device__ static __forceinline__ float lo(uint32_t w) { return __uint_as_float(w << 16); }
     __device__ static __forceinline__ float hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -190,6 +243,7 @@ struct Lp<ZERO_BF16> {
 
 template <>
 struct Lp<ZERO_FP16> {
+    __device__ static __forceinline__ float add(float acc, unsigned short h) { return add_f16_f32(h, acc); }
     __device__ static __forceinline__ float lo(uint32_t w)
     {
         return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xFFFFu)));
@@ -380,15 +434,22 @@ __device__ __forceinline__ uint32_t quant_code4(const float (&x)[4], float s, fl
     }
     // fast: t = rint(x * inv) + 1.5 * 2^23 (its low byte is the code), no
     // clamp needed (see quant_reciprocal); a NaN product fails the test below
-    float t[4];
+    float t[4], d[4];
+    {
+        const f32x2 inv2 = pack2(inv, inv), m2 = pack2(kRintShift, kRintShift);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const f32x2 y = mul2(pack2(x[2 * h], x[2 * h + 1]), inv2);
+            const f32x2 tt = add2(y, m2);
+            const f32x2 c = sub2(tt, m2);
+            unpack2(tt, t[2 * h], t[2 * h + 1]);
+            unpack2(c, cf[2 * h], cf[2 * h + 1]);
+            unpack2(sub2(y, c), d[2 * h], d[2 * h + 1]);
+        }
+    }
     bool near = inv == 0.0f;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const float y = __fmul_rn(x[e], inv);
-        t[e] = __fadd_rn(y, kRintShift);
-        cf[e] = __fsub_rn(t[e], kRintShift);
-        near |= !(fabsf(__fsub_rn(y, cf[e])) < kTieBand);
-    }
+    for (int e = 0; e < 4; ++e) near |= !(fabsf(d[e]) < kTieBand);
     if (near) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {

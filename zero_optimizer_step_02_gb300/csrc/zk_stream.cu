@@ -103,10 +103,11 @@ __device__ __forceinline__ void add_codes(float (&acc)[4], uint32_t w, float s)
 template <int GT>
 __device__ __forceinline__ void add_slice(float (&acc)[4], uint2 w)
 {
-    acc[0] = __fadd_rn(acc[0], Lp<GT>::lo(w.x));
-    acc[1] = __fadd_rn(acc[1], Lp<GT>::hi(w.x));
-    acc[2] = __fadd_rn(acc[2], Lp<GT>::lo(w.y));
-    acc[3] = __fadd_rn(acc[3], Lp<GT>::hi(w.y));
+    unsigned short h[4];
+    halves(w.x, h[0], h[1]);
+    halves(w.y, h[2], h[3]);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[e] = Lp<GT>::add(acc[e], h[e]);
 }
 
 // rank slices per pipeline stage: int8 slices are half the bytes of 16-bit
@@ -364,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
                                     const float code = static_cast<float>(static_cast<const signed char*>(a.rank[r])[j]);
                                     acc[ch][e] = __fadd_rn(acc[ch][e], __fmul_rn(code, rank_scale(a, r, cur.seg, cur.t, ch)));
                                 } else {
-                                    acc[ch][e] = __fadd_rn(acc[ch][e], Lp<GT>::widen(static_cast<const uint16_t*>(a.rank[r])[j]));
+                                    acc[ch][e] = Lp<GT>::add(acc[ch][e], static_cast<const uint16_t*>(a.rank[r])[j]);
                                 }
                             }
 #pragma unroll
