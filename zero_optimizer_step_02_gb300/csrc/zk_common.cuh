@@ -174,7 +174,10 @@ struct Lp;
 // sm_100-family instructions that do what several scalar ones do, with the
 // same IEEE round-to-nearest results (subnormals kept): an fp32 add of a
 // 16-bit operand (the widening is exact, so this is fadd(widen(h), acc)),
-// and fp32 operations on register pairs.
+// and fp32 operations on register pairs.  Caution: ptxas fuses a packed
+// multiply that feeds a packed add or subtract into one rounding, whatever
+// the rounding modifier or -fmad setting; packed multiplies are used only
+// where that cannot change a result (the quantizer's fast path).
 __device__ __forceinline__ void halves(uint32_t w, unsigned short& lo, unsigned short& hi)
 {
     asm("mov.b32 {%0, %1}, %2;" : "=h"(lo), "=h"(hi) : "r"(w));
@@ -433,7 +436,11 @@ __device__ __forceinline__ uint32_t quant_code4(const float (&x)[4], float s, fl
         return 0u;
     }
     // fast: t = rint(x * inv) + 1.5 * 2^23 (its low byte is the code), no
-    // clamp needed (see quant_reciprocal); a NaN product fails the test below
+    // clamp needed (see quant_reciprocal); a NaN product fails the test below.
+    // The packed multiply may be fused into the adds (one rounding of the
+    // exact product P): away from the tie band rint(P) is still the integer
+    // the exact quotient rounds to (|P - x/s| < 2^-17, band 2^-14), and in
+    // it the exact quotient decides.
     float t[4], d[4];
     {
         const f32x2 inv2 = pack2(inv, inv), m2 = pack2(kRintShift, kRintShift);
