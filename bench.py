@@ -184,12 +184,12 @@ def measured_hbm_peak():
 # kernel and workload, with a hash of the kernel sources they were taken on;
 # reported as null once the sources change.
 TRAFFIC = {
-    ("adam_shard", "zero2_gpt2small_psi124439808_nd8_adamw_clip1"): {"bytes": 3.625e9, "src": "7b7becb7e853"},
-    ("fused_step", "zero2_psi2p28_nd8"): {"bytes": 11.110e9, "src": "7b7becb7e853"},
-    ("fused_step_qgather", "zero2_psi2p28_nd2_qgather"): {"bytes": 8.081e9, "src": "7b7becb7e853"},
-    ("fused_step_qgz", "zero2_psi2p28_nd8_qgz"): {"bytes": 8.918e9, "src": "7b7becb7e853"},
+    ("adam_shard", "zero2_gpt2small_psi124439808_nd8_adamw_clip1"): {"bytes": 3.625e9, "src": "aa5b7efe0553"},
+    ("fused_step", "zero2_psi2p28_nd8"): {"bytes": 11.112e9, "src": "aa5b7efe0553"},
+    ("fused_step_qgather", "zero2_psi2p28_nd2_qgather"): {"bytes": 8.082e9, "src": "aa5b7efe0553"},
+    ("fused_step_qgz", "zero2_psi2p28_nd8_qgz"): {"bytes": 8.919e9, "src": "aa5b7efe0553"},
     ("accumulate_grads", "zero2_gpt2small_psi124439808_nd8_adamw_clip1_accum4"): {"bytes": 2.950e9,
-                                                                                   "src": "7b7becb7e853"},
+                                                                                   "src": "aa5b7efe0553"},
 }
 
 
