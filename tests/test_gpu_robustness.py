@@ -125,3 +125,49 @@ def test_zero3_layerwise_loop_matches_the_oracle():
             job.gpu_step()
             job.oracle_step()
             job.assert_bit_exact()
+
+
+@pytest.mark.parametrize("n_d,psi,pad,clip", [(4, 1_000_003, 8, 0.0), (8, 123_457, 1, 1.0), (3, 70_001, 16, 0.0),
+                                              (16, 8193, 8, 1.0), (5, 4097 * 3, 64, 0.0)])
+def test_newer_kernels_write_only_their_buffers(n_d, psi, pad, clip):
+    # the gradient sender (all ranks in one launch), the quantized-exchange
+    # receiver, and gradient accumulation with the step at the last micro-batch
+    hp = z.hparams(lr=1e-3, max_norm=clip)
+    plan = z.Plan(psi, n_d, stage=2, shard_pad=pad)
+    n, S = plan.padded, plan.shard
+    row = z.row_len(psi)
+    row16 = (psi + 15) // 16 * 16
+    nbs = -(-S // 2048)
+    n_dp = (n_d + 3) // 4 * 4
+    sizes = {"grads": n_d * row * 2, "master": 4 * n, "m": 4 * n, "v": 4 * n, "lp": 2 * psi,
+             "ws": plan.workspace_bytes(hp), "scalars": 256, "acc": 4 * n, "qscales": 4 * n_d * nbs * n_dp,
+             "qscales256": 4 * n_d * -(-S // 256) * n_dp}
+    for r in range(n_d):
+        sizes["codes%d" % r] = row16
+    bufs = {k: _guarded(v) for k, v in sizes.items()}
+    inner = {k: v[1] for k, v in bufs.items()}
+    grads = inner["grads"].view(torch.bfloat16).view(n_d, row)
+    grads.copy_(synth.rank_grads(n_d, psi, 1e-2, seed=4, step=1, row_pad=row - psi).cuda())
+    master, m, v = (inner[k].view(torch.float32) for k in ("master", "m", "v"))
+    master.copy_(synth.master_init(n, psi, seed=4).cuda())
+    m.zero_()
+    v.zero_()
+    sc = inner["scalars"]
+    z.zero_scalars_init(sc)
+    ranks = [grads[r] for r in range(n_d)]
+    lp = inner["lp"].view(torch.bfloat16)
+    acc = inner["acc"].view(torch.float32)
+    codes = [inner["codes%d" % r].view(torch.int8) for r in range(n_d)]
+    qscales = inner["qscales"].view(torch.float32)
+    z.zero_accumulate_grads(plan.handle, ranks, None, acc, sc)
+    z.zero_accumulate_grads(plan.handle, ranks, acc, acc, sc)
+    z.zero_step_fused_accum(plan.handle, hp, ranks, acc, 3, master, m, v, master, m, v, lp, sc, inner["ws"])
+    z.zero_quantize_grads(plan.handle, ranks, 2048, codes, qscales)
+    z.zero_quantize_grads(plan.handle, ranks, 256, codes, inner["qscales256"].view(torch.float32))
+    z.zero_quantize_grads(plan.handle, ranks, 2048, codes, qscales)
+    if clip == 0.0:
+        z.zero_step_fused_qgz(plan.handle, hp, codes, qscales, 2048, master, m, v, master, m, v, lp, sc)
+    torch.cuda.synchronize()
+    for name, (whole, _) in bufs.items():
+        assert _intact(whole), "a kernel wrote outside the %s buffer" % name
+    assert z.read_scalars(sc).status == 0
