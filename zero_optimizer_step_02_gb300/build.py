@@ -65,7 +65,7 @@ def build(force=False, verbose_ptxas=False):
                 raise RuntimeError("nvcc failed: " + " ".join(cmd))
     if force or jobs or _stale(LIB, objs):
         tmp = LIB + ".tmp.%d" % os.getpid()
-        cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
+        cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-ldl"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             sys.stderr.write(r.stdout + r.stderr)

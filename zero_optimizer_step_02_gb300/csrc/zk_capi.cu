@@ -6,6 +6,8 @@
 #include <cstring>
 #include <new>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "zk_common.cuh"
 #include "zk_launch.h"
 
@@ -24,6 +26,17 @@ struct zero_plan {
 namespace {
 
 using zk::StreamArgs;
+
+// An NVTX range named after the entry point around each call that launches
+// work, so that profilers (nsys, ncu --nvtx) group its kernels; with no tool
+// attached it costs a branch.
+struct CallRange {
+    explicit CallRange(const char* name) { nvtxRangePushA(name); }
+    ~CallRange() { nvtxRangePop(); }
+    CallRange(const CallRange&) = delete;
+    CallRange& operator=(const CallRange&) = delete;
+};
+#define ZK_CALL_RANGE() const CallRange zk_call_range_(__func__)
 
 constexpr size_t kPartialBytes = sizeof(double) * zk::kMaxPartials;  // 32 KB, 256-aligned
 
@@ -346,6 +359,7 @@ ZERO_API size_t zero_workspace_bytes(const zero_plan* p, const zero_hparams* hp)
 
 ZERO_API zero_status zero_scalars_init(zero_dev_scalars* sc, float loss_scale, void* stream)
 {
+    ZK_CALL_RANGE();
     const zero_status s = check_dev(sc, 256);
     if (s != ZERO_OK) return s;
     if (!(loss_scale > 0.0f) || std::isinf(loss_scale)) return ZERO_ERR_INVALID_ARG;
@@ -355,6 +369,7 @@ ZERO_API zero_status zero_scalars_init(zero_dev_scalars* sc, float loss_scale, v
 ZERO_API zero_status zero_reduce_scatter(const zero_plan* p, const void* const* ranks, const zero_hparams* hp,
                                          zero_dev_scalars* sc, float* grad_shards, void* ws, void* stream)
 {
+    ZK_CALL_RANGE();
     if (p == nullptr) return ZERO_ERR_INVALID_ARG;
     zero_status s;
     if ((s = check_hparams(hp)) != ZERO_OK) return s;
@@ -372,6 +387,7 @@ ZERO_API zero_status zero_reduce_scatter(const zero_plan* p, const void* const* 
 ZERO_API zero_status zero_grad_sqnorm(const zero_plan* p, const float* grad_shards, const zero_hparams* hp,
                                       zero_dev_scalars* sc, void* ws, void* stream)
 {
+    ZK_CALL_RANGE();
     if (p == nullptr) return ZERO_ERR_INVALID_ARG;
     zero_status s;
     if ((s = check_hparams(hp)) != ZERO_OK) return s;
@@ -393,6 +409,7 @@ ZERO_API zero_status zero_adam_shard_step(const zero_plan* p, const zero_hparams
                                           float* master, float* m, float* v, void* lp_out, zero_dev_scalars* sc,
                                           void* stream)
 {
+    ZK_CALL_RANGE();
     if (p == nullptr) return ZERO_ERR_INVALID_ARG;
     zero_status s;
     if ((s = check_hparams(hp)) != ZERO_OK) return s;
@@ -409,6 +426,7 @@ ZERO_API zero_status zero_adam_shard_step(const zero_plan* p, const zero_hparams
 ZERO_API zero_status zero_all_gather(const zero_plan* p, const void* const* shards, void* gathered,
                                      zero_dev_scalars* sc, void* stream)
 {
+    ZK_CALL_RANGE();
     if (p == nullptr || shards == nullptr) return ZERO_ERR_INVALID_ARG;
     // shard pointers need only element (2-byte) alignment: shards cut from one
     // flat buffer at an odd S are legal; the bulk-copy ring is used when all
@@ -490,6 +508,7 @@ ZERO_API zero_status zero_step_fused(const zero_plan* p, const zero_hparams* hp,
                                      const float* mi, const float* m_in, const float* vi, float* mo, float* m_out,
                                      float* vo, void* lp, zero_dev_scalars* sc, void* ws, void* stream)
 {
+    ZK_CALL_RANGE();
     return fused_step(p, hp, ranks, mi, m_in, vi, mo, m_out, vo, lp, sc, ws, stream, false);
 }
 
@@ -498,6 +517,7 @@ ZERO_API zero_status zero_step_fused_offload(const zero_plan* p, const zero_hpar
                                              float* m_out, float* vo, void* lp, zero_dev_scalars* sc, void* ws,
                                              void* stream)
 {
+    ZK_CALL_RANGE();
     // every state pointer must be page-locked host memory the device reaches
     // at the same address; anything else is refused before a launch
     const void* ptrs[] = {mi, m_in, vi, mo, m_out, vo};
@@ -516,6 +536,7 @@ ZERO_API zero_status zero_step_fused_offload(const zero_plan* p, const zero_hpar
 ZERO_API zero_status zero_accumulate_grads(const zero_plan* p, const void* const* ranks, const float* acc_in,
                                            float* acc_out, zero_dev_scalars* sc, void* stream)
 {
+    ZK_CALL_RANGE();
     if (p == nullptr) return ZERO_ERR_INVALID_ARG;
     zero_status s;
     if ((s = check_ranks(p, ranks)) != ZERO_OK) return s;
@@ -542,6 +563,7 @@ ZERO_API zero_status zero_step_fused_accum(const zero_plan* p, const zero_hparam
                                            const float* vi, float* mo, float* m_out, float* vo, void* lp,
                                            zero_dev_scalars* sc, void* ws, void* stream)
 {
+    ZK_CALL_RANGE();
     if (micro_batches < 1 || micro_batches > ZERO_MAX_MICRO_BATCHES) return ZERO_ERR_INVALID_ARG;
     if ((acc == nullptr) != (micro_batches == 1)) return ZERO_ERR_INVALID_ARG;
     if (acc != nullptr && !aligned(acc, 16)) return ZERO_ERR_MISALIGNED;
@@ -551,6 +573,7 @@ ZERO_API zero_status zero_step_fused_accum(const zero_plan* p, const zero_hparam
 ZERO_API zero_status zero_quant_gather(const zero_plan* p, const void* shards, int block, signed char* codes,
                                        float* scales, void* gathered, void* stream)
 {
+    ZK_CALL_RANGE();
     if (p == nullptr) return ZERO_ERR_INVALID_ARG;
     if (block < 32 || block > 65536 || block % 32 != 0) return ZERO_ERR_INVALID_ARG;
     if (p->param_dtype != ZERO_BF16) return ZERO_ERR_UNSUPPORTED;
@@ -568,6 +591,7 @@ ZERO_API zero_status zero_step_fused_qgather(const zero_plan* p, const zero_hpar
                                              float* m_out, float* vo, int block, signed char* codes, float* scales,
                                              void* gathered, zero_dev_scalars* sc, void* ws, void* stream)
 {
+    ZK_CALL_RANGE();
     (void)ws;
     if (p == nullptr) return ZERO_ERR_INVALID_ARG;
     zero_status s;
@@ -611,6 +635,7 @@ ZERO_API zero_status zero_step_fused_qgather(const zero_plan* p, const zero_hpar
 ZERO_API zero_status zero_quantize_grads(const zero_plan* p, const void* const* ranks, int block,
                                          signed char* const* codes, float* scales, void* stream)
 {
+    ZK_CALL_RANGE();
     if (p == nullptr || codes == nullptr) return ZERO_ERR_INVALID_ARG;
     if (block < 32 || block > 65536 || block % 32 != 0) return ZERO_ERR_INVALID_ARG;
     if (p->grad_dtype != ZERO_BF16) return ZERO_ERR_UNSUPPORTED;
@@ -626,6 +651,7 @@ ZERO_API zero_status zero_step_fused_qgz(const zero_plan* p, const zero_hparams*
                                          const float* vi, float* mo, float* m_out, float* vo, void* lp,
                                          zero_dev_scalars* sc, void* stream)
 {
+    ZK_CALL_RANGE();
     if (p == nullptr) return ZERO_ERR_INVALID_ARG;
     zero_status s;
     if ((s = check_hparams(hp)) != ZERO_OK) return s;
@@ -665,6 +691,7 @@ ZERO_API zero_status zero_step_fused_qgz(const zero_plan* p, const zero_hparams*
 
 ZERO_API zero_status zero_debug_wait_timeout(zero_dev_scalars* sc, long long timeout_ns, void* stream)
 {
+    ZK_CALL_RANGE();
     const zero_status s = check_dev(sc, 256);
     if (s != ZERO_OK) return s;
     if (timeout_ns < 1 || timeout_ns > 10000000000LL) return ZERO_ERR_INVALID_ARG;
