@@ -41,7 +41,7 @@ L2_BYTES = 129 * 1024 * 1024
 
 
 # ----------------------------------------------------------------- workloads
-def workload(cfg, nd=None, qgather=False, psi=None, qgz=False, gathers=1, offload=False, accum=1):
+def workload(cfg, nd=None, qgather=False, psi=None, qgz=False, gathers=1, offload=False, accum=1, overlap=False):
     """Sizes, hyper-parameters and the algorithmic bytes of one step.  psi
     overrides the parameter count (a smaller case of the same workload, for
     profiling)."""
@@ -74,6 +74,12 @@ def workload(cfg, nd=None, qgather=False, psi=None, qgz=False, gathers=1, offloa
         # optimizer state in page-locked host memory, read and written over the CPU-GPU link
         w["offload"] = True
         w["name"] += "_offload"
+    if overlap:
+        if w["stage"] != 3:
+            raise SystemExit("--overlap applies to the ZeRO-3 layer loop (config 4)")
+        # the next layer's gather on a second stream while this layer's step runs
+        w["overlap"] = True
+        w["name"] += "_overlap"
     if accum > 1:
         if w["stage"] == 3 or w.get("qgz") or w.get("qgather") or offload or w["ls"]:
             raise SystemExit("--accum applies to the plain and clipped ZeRO-2 workloads (configs 1, 2, 5)")
@@ -245,6 +251,11 @@ class Job:
         self.lp = [torch.zeros(lp_n, dtype=torch.bfloat16, device=device) for _ in range(L)]
         if w["stage"] == 3:
             self.gathered = torch.zeros(w["psi"], dtype=torch.bfloat16, device=device)
+        if w.get("overlap"):
+            self.gathered2 = torch.zeros(w["psi"], dtype=torch.bfloat16, device=device)
+            self.gather_stream = torch.cuda.Stream(device=device)
+            self.ev_gathered = [torch.cuda.Event() for _ in range(w["layers"])]
+            self.ev_stepped = [None] * w["layers"]
         if w.get("qgather"):
             nbs = -(-self.plan.shard // 2048)
             self.codes = torch.zeros(n, dtype=torch.int8, device=device)
@@ -281,6 +292,9 @@ class Job:
         if w.get("accum"):
             self.step_accum()
             return
+        if w.get("overlap"):
+            self.step_zero3_overlap()
+            return
         for l in range(w["layers"]):
             gsel = l if w["layers"] > 1 else self.k
             if w["stage"] == 3:
@@ -309,6 +323,40 @@ class Job:
                 step = z.zero_step_fused_offload if self.offload else z.zero_step_fused
                 step(h, self.hp, self.ranks(gsel), self.master[l], self.m[l], self.v[l], self.master[l], self.m[l],
                      self.v[l], self.lp[l], self.scalars, self.ws)
+        self.k += 1
+
+    def step_zero3_overlap(self):
+        """The ZeRO-3 layer loop with layer l+1's gather(s) issued on a second
+        stream while layer l's reduce-scatter + Adam runs.  A gather waits for
+        the step that last wrote its layer's shards; a step waits for its
+        layer's gather (which reads the shards the step overwrites)."""
+        torch, z, w = self.torch, self.z, self.w
+        h = self.plan.handle
+        S = self.plan.shard
+        comp = torch.cuda.current_stream()
+        gs = self.gather_stream
+        bufs = (self.gathered, self.gathered2)
+
+        def gather(l):
+            if self.ev_stepped[l] is not None:
+                gs.wait_event(self.ev_stepped[l])
+            for _ in range(w.get("gathers", 1)):
+                z.zero_all_gather(h, [self.lp[l][r * S:(r + 1) * S] for r in range(w["n_d"])], bufs[l % 2],
+                                  self.scalars, gs)
+            self.ev_gathered[l].record(gs)
+
+        gs.wait_stream(comp)
+        gather(0)
+        for l in range(w["layers"]):
+            if l + 1 < w["layers"]:
+                gather(l + 1)
+            comp.wait_event(self.ev_gathered[l])
+            z.zero_step_fused(h, self.hp, self.ranks(l), self.master[l], self.m[l], self.v[l], self.master[l],
+                              self.m[l], self.v[l], self.lp[l], self.scalars, self.ws)
+            ev = torch.cuda.Event()
+            ev.record(comp)
+            self.ev_stepped[l] = ev
+        comp.wait_stream(gs)
         self.k += 1
 
     def step_accum(self, sets=None):
@@ -355,7 +403,8 @@ def l2_flush(torch, device, buf=[]):
 def gpu_arm(args, rank, world, device):
     import torch
     import zero_optimizer_step_02_gb300 as z
-    w = workload(args.config, args.nd, args.qgather, args.psi, args.qgz, args.gathers, args.offload, args.accum)
+    w = workload(args.config, args.nd, args.qgather, args.psi, args.qgz, args.gathers, args.offload, args.accum,
+                 args.overlap)
     if args.row_pad:
         w["row_pad"] = args.row_pad
         w["name"] += "_rowpad%d" % args.row_pad
@@ -610,7 +659,8 @@ def oracle_sample(w, budget_s, max_steps=None):
 
 
 def reference_arm(args, rank, world):
-    w = workload(args.config, args.nd, args.qgather, args.psi, args.qgz, args.gathers, args.offload, args.accum)
+    w = workload(args.config, args.nd, args.qgather, args.psi, args.qgz, args.gathers, args.offload, args.accum,
+                 args.overlap)
     if rank != 0:
         return None
     for _ in range(args.warmup):
@@ -671,6 +721,8 @@ def main():
     ap.add_argument("--gathers", type=int, default=1, choices=[1, 2], help="ZeRO-3 gathers per layer and step")
     ap.add_argument("--offload", action="store_true", help="optimizer state in page-locked host memory")
     ap.add_argument("--accum", type=int, default=1, help="micro-batches per optimizer step (gradient accumulation)")
+    ap.add_argument("--overlap", action="store_true",
+                    help="ZeRO-3: next layer's gather on a second stream during this layer's step")
     ap.add_argument("--row-pad", type=int, default=0,
                     help="extra elements between rank rows (breaks power-of-two rank strides)")
     args = ap.parse_args()
@@ -687,7 +739,8 @@ def main():
     out = gpu_arm(args, rank, world, device)
     if rank == 0:
         if not args.no_cpu_baseline and world == 1:
-            w = workload(args.config, args.nd, args.qgather, args.psi, args.qgz, args.gathers, args.offload, args.accum)
+            w = workload(args.config, args.nd, args.qgather, args.psi, args.qgz, args.gathers, args.offload, args.accum,
+                 args.overlap)
             psi, n_d, steps, el = oracle_sample(w, args.cpu_budget)
             out["cpu_baseline"] = {"value": psi * steps / el, "unit": UNIT, "cores": 1, "kind": "oracle",
                                    "sample": "%d of %d params, n_d=%d, %d steps in %.1f s, single-threaded C "

@@ -24,7 +24,7 @@ def _worker(rank, world, port, q):
     mx = bench.dist_max(10.0 * (rank + 1), w)
 
     class A:  # arguments of the reference arm
-        config, nd, qgather, steps, warmup, psi, qgz, gathers, offload, accum, row_pad = 1, None, False, 1, 0, None, False, 1, False, 1, 0
+        config, nd, qgather, steps, warmup, psi, qgz, gathers, offload, accum, row_pad, overlap = 1, None, False, 1, 0, None, False, 1, False, 1, 0, False
     ref = bench.reference_arm(A, r, w)
     q.put((rank, mx, ref is None))
     import torch.distributed as dist
