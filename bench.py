@@ -552,9 +552,44 @@ def gpu_arm(args, rank, world, device):
     if sender:
         out["qgz_sender"] = sender
     if w.get("offload"):
-        # the state's 12 bytes read + 12 written per parameter cross the CPU-GPU link
-        out["offload_link_gbs"] = round(24.0 * w["psi_total"] / (ms_per_step / 1e3) / 1e9, 1)
+        # the state's 12 bytes read + 12 written per parameter cross the CPU-GPU
+        # link: against that link's duplex rate measured in this run
+        link = host_link_gbs(torch, device)
+        gbs = 24.0 * w["psi_total"] / (ms_per_step / 1e3) / 1e9
+        out["offload_link_gbs"] = round(gbs, 1)
+        out["host_link_gbs"] = link
+        out["offload_link_frac"] = round(gbs / link["duplex"], 4)
     return out
+
+
+def host_link_gbs(torch, device, nbytes=1 << 30, reps=3):
+    """The CPU-GPU link measured here: pinned-host-to-device, device-to-host,
+    and both at once on two streams (GB/s, both directions counted)."""
+    h_in = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    h_out = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d_in = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    d_out = torch.ones(nbytes, dtype=torch.uint8, device=device)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def timed(fn):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            fn()
+        torch.cuda.synchronize()
+        return (time.perf_counter() - t0) / reps
+
+    def both():
+        with torch.cuda.stream(s1):
+            d_in.copy_(h_in, non_blocking=True)
+        with torch.cuda.stream(s2):
+            h_out.copy_(d_out, non_blocking=True)
+
+    timed(both)
+    h2d = nbytes / timed(lambda: d_in.copy_(h_in, non_blocking=True)) / 1e9
+    d2h = nbytes / timed(lambda: h_out.copy_(d_out, non_blocking=True)) / 1e9
+    duplex = 2 * nbytes / timed(both) / 1e9
+    return {"h2d": round(h2d, 1), "d2h": round(d2h, 1), "duplex": round(duplex, 1)}
 
 
 def e2e_measure(job, w, args, device, world):
