@@ -331,7 +331,10 @@ ZERO_API zero_status zero_step_fused_qgather(const zero_plan* plan, const zero_h
  * [(r * ceil(S/block) + b) * n_dp + q] (so one tile's scales of all ranks
  * are contiguous); 0 for blocks past a shard's valid length and for the
  * padding columns q >= n_d.  Plan gradient dtype bf16; 32 <= block <= 65536,
- * a multiple of 32.                                                          */
+ * a multiple of 32.  One kernel for all ranks; with block 2048 and a shard
+ * size that is a multiple of 8, full blocks are staged by 1-D bulk copies.
+ * Its waits are bounded; a wait that runs out ends the kernel early (there
+ * is no scalars block to report it in).                                     */
 ZERO_API zero_status zero_quantize_grads(const zero_plan* plan, const void* const* rank_grads, int block,
                                          signed char* const* rank_codes, float* rank_scales,
                                          void* stream);

@@ -6,6 +6,8 @@
 //                    partitions; itwiki: ZeRO-3 gathers each layer before use)
 //   k_quant_gather   block-int8 quantize + dequantize (itwiki "후속 기법",
 //                    ZeRO++ qwZ), one warp per block
+//   k_quantize_ranks every rank's gradient through the block quantizer in one
+//                    launch (ZeRO++ qgZ sender), per-warp bulk-copy slots
 //   k_sqnorm_f32     per-CTA partial sums of g^2 of an fp32 array
 //   k_finalize       fixed-order fp64 sum of the partials, clip coefficient
 //   k_epilogue       commits the step scalars (t, beta powers, loss scale)
