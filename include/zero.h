@@ -333,11 +333,12 @@ ZERO_API zero_status zero_step_fused_qgather(const zero_plan* plan, const zero_h
  * padding columns q >= n_d.  Plan gradient dtype bf16; 32 <= block <= 65536,
  * a multiple of 32.  One kernel for all ranks; with block 2048 and a shard
  * size that is a multiple of 8, full blocks are staged by 1-D bulk copies.
- * Its waits are bounded; a wait that runs out ends the kernel early (there
- * is no scalars block to report it in).                                     */
+ * scalars_dev (may be NULL, else 256-byte aligned) only receives
+ * ZERO_DEV_TIMEOUT if a bounded wait runs out; nothing else of it is read or
+ * written.                                                                  */
 ZERO_API zero_status zero_quantize_grads(const zero_plan* plan, const void* const* rank_grads, int block,
                                          signed char* const* rank_codes, float* rank_scales,
-                                         void* stream);
+                                         zero_dev_scalars* scalars_dev, void* stream);
 
 /* Receiver side, fused: zero_step_fused with the ranks' int8 codes and
  * scales (layout as above, block 2048) in place of their 16-bit gradients:

@@ -155,10 +155,11 @@ def test_quantized_gradient_exchange_argument_checks(z):
     ranks = (ctypes.c_void_p * 2)(A, A)
     hp = z.hparams()
     clip = z.hparams(max_norm=1.0)
-    assert _raw(z, "zero_quantize_grads", p.handle, ranks, 31, ranks, A, None) == 1
-    assert _raw(z, "zero_quantize_grads", p.handle, ranks, 2048, (ctypes.c_void_p * 2)(A, A + 8), A, None) == 2
+    assert _raw(z, "zero_quantize_grads", p.handle, ranks, 31, ranks, A, None, None) == 1
+    assert _raw(z, "zero_quantize_grads", p.handle, ranks, 2048, (ctypes.c_void_p * 2)(A, A + 8), A, None, None) == 2
+    assert _raw(z, "zero_quantize_grads", p.handle, ranks, 2048, ranks, A, A + 16, None) == 2
     p16 = z.Plan(1000, 2, stage=2, grad_dtype=z.ZERO_FP16)
-    assert _raw(z, "zero_quantize_grads", p16.handle, ranks, 2048, ranks, A, None) == 3
+    assert _raw(z, "zero_quantize_grads", p16.handle, ranks, 2048, ranks, A, None, None) == 3
     assert _raw(z, "zero_step_fused_qgz", p.handle, ctypes.byref(hp), ranks, A, 1024, A, A, A, A, A, A, A, A,
                 None) == 3
     assert _raw(z, "zero_step_fused_qgz", p.handle, ctypes.byref(clip), ranks, A, 2048, A, A, A, A, A, A, A, A,

@@ -79,7 +79,7 @@ _SIGS = {
     "zero_debug_wait_timeout": (_i32, [_vp, _ll, _vp]),
     "zero_launch_count": (ctypes.c_ulonglong, []),
     "zero_step_fused_noalloc": (_i32, [_vp, _hp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
-    "zero_quantize_grads": (_i32, [_vp, _vp, _i32, _vp, _vp, _vp]),
+    "zero_quantize_grads": (_i32, [_vp, _vp, _i32, _vp, _vp, _vp, _vp]),
     "zero_step_fused_offload": (_i32, [_vp, _hp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "zero_accumulate_grads": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp]),
     "zero_step_fused_accum": (_i32, [_vp, _hp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
@@ -252,9 +252,9 @@ def zero_step_fused_qgather(plan, hp, rank_grads, master_in, m_in, v_in, master_
                                         _addr(ws), _stream(stream)), "zero_step_fused_qgather")
 
 
-def zero_quantize_grads(plan, rank_grads, block, rank_codes, rank_scales, stream=None):
+def zero_quantize_grads(plan, rank_grads, block, rank_codes, rank_scales, scalars=None, stream=None):
     _check(_lib.zero_quantize_grads(plan, _ptr_array(rank_grads), block, _ptr_array(rank_codes),
-                                    _addr(rank_scales), _stream(stream)), "zero_quantize_grads")
+                                    _addr(rank_scales), _addr(scalars), _stream(stream)), "zero_quantize_grads")
 
 
 def zero_step_fused_qgz(plan, hp, rank_codes, rank_scales, block, master_in, m_in, v_in, master_out, m_out, v_out,

@@ -442,6 +442,7 @@ struct QsArgs {
     const uint16_t* rank[ZERO_MAX_RANKS];
     signed char* codes[ZERO_MAX_RANKS];
     float* scales;
+    zero_dev_scalars* sc;                     // may be null: receives ZERO_DEV_TIMEOUT
     long long shard, psi, nbs, n_dp, total;   // total = n_d * n_d * nbs blocks
     int n_d, block, ring_ok;                   // ring_ok: block == 2048 and shard % 8 == 0
     unsigned long long timeout_ns;
@@ -617,14 +618,15 @@ __global__ void __launch_bounds__(kQsWarps * 32, 1) k_quantize_ranks(const __gri
     }
     if (!ok && lane == 0) {
         // a wait ran out: let the copies in flight land before the CTA's
-        // shared memory is released
+        // shared memory is released, then report
         for (int s = 0; s < kQsSlots; ++s)
             if (pending & (1u << s)) mbar_wait_bounded(&bar[s], (phase >> s) & 1u, nullptr, a.timeout_ns);
+        if (a.sc != nullptr) atomicOr(&a.sc->status, ZERO_DEV_TIMEOUT);
     }
 }
 
 cudaError_t launch_quantize_grads(const void* const* ranks, int n_d, long long shard, long long psi, int block,
-                                  signed char* const* codes, float* scales, cudaStream_t st)
+                                  signed char* const* codes, float* scales, zero_dev_scalars* sc, cudaStream_t st)
 {
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
@@ -638,6 +640,7 @@ cudaError_t launch_quantize_grads(const void* const* ranks, int n_d, long long s
                   (reinterpret_cast<uintptr_t>(codes[q]) & 15) == 0;
     }
     a.scales = scales;
+    a.sc = sc;
     a.shard = shard;
     a.psi = psi;
     a.block = block;

@@ -633,7 +633,8 @@ ZERO_API zero_status zero_step_fused_qgather(const zero_plan* p, const zero_hpar
 }
 
 ZERO_API zero_status zero_quantize_grads(const zero_plan* p, const void* const* ranks, int block,
-                                         signed char* const* codes, float* scales, void* stream)
+                                         signed char* const* codes, float* scales, zero_dev_scalars* sc,
+                                         void* stream)
 {
     ZK_CALL_RANGE();
     if (p == nullptr || codes == nullptr) return ZERO_ERR_INVALID_ARG;
@@ -643,7 +644,9 @@ ZERO_API zero_status zero_quantize_grads(const zero_plan* p, const void* const* 
     if ((s = check_ranks(p, ranks)) != ZERO_OK) return s;
     if ((s = check_ranks(p, reinterpret_cast<const void* const*>(codes))) != ZERO_OK) return s;
     if ((s = check_dev(scales)) != ZERO_OK) return s;
-    return from_cuda(zk::launch_quantize_grads(ranks, p->n_d, p->shard, p->psi, block, codes, scales, as_stream(stream)));
+    if (sc != nullptr && !aligned(sc, 256)) return ZERO_ERR_MISALIGNED;
+    return from_cuda(
+        zk::launch_quantize_grads(ranks, p->n_d, p->shard, p->psi, block, codes, scales, sc, as_stream(stream)));
 }
 
 ZERO_API zero_status zero_step_fused_qgz(const zero_plan* p, const zero_hparams* hp, const signed char* const* codes,

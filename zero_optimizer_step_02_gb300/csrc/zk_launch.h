@@ -73,7 +73,7 @@ cudaError_t launch_quant_gather(const void* shards, int n_d, long long shard, lo
                                 int block, signed char* codes, float* scales, void* gathered,
                                 cudaStream_t st);
 cudaError_t launch_quantize_grads(const void* const* ranks, int n_d, long long shard, long long psi, int block,
-                                  signed char* const* codes, float* scales, cudaStream_t st);
+                                  signed char* const* codes, float* scales, zero_dev_scalars* sc, cudaStream_t st);
 cudaError_t launch_debug_wait(zero_dev_scalars* sc, unsigned long long timeout_ns, cudaStream_t st);
 
 }  // namespace zk
