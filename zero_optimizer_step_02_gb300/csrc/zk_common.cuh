@@ -86,15 +86,20 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// One test of the phase; while it is incomplete the thread is suspended in
+// hardware until it completes or kWaitHintNs pass, so a waiting warp does not
+// spin on issue slots the working warps need.
+constexpr uint32_t kWaitHintNs = 10000000u;
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kWaitHintNs)
         : "memory");
     return ok != 0;
 }
@@ -117,10 +122,9 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1; it < (1u << 28); ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0) {
-            if (abort != nullptr && *abort) return false;
-            if (globaltimer_ns() - t0 > timeout_ns) return false;
-        }
+        // each test may have slept up to kWaitHintNs: check every time
+        if (abort != nullptr && *abort) return false;
+        if (globaltimer_ns() - t0 > timeout_ns) return false;
     }
     return false;
 }
