@@ -349,3 +349,85 @@ def test_quant_codes_at_and_near_ties():
     oc, osc, og = oracle.quant_gather(xb, n_d, psi, S, block)
     assert np.all(osc == np.float32(2.0 ** -10))
     assert np.array_equal(codes.cpu().numpy(), oc) and np.array_equal(u16(gathered), og)
+
+
+@pytest.mark.parametrize("n_d,psi", [(3, 5), (4, 50_001), (2, 8192 * 3 + 1)])
+def test_largest_shard_pad(n_d, psi):
+    # shard_pad 4096: shards padded to a whole tile, trailing shards empty or short
+    job = Job(psi, n_d, pad=4096, hp=z.hparams(lr=1e-3, weight_decay=0.1, max_norm=0.5), seed=17)
+    for step in (1, 2):
+        job.new_grads(step)
+        job.gpu_step()
+        job.oracle_step()
+        sc = job.scalars()
+        o = np.float32(job.ost.scalars.clip_coef)
+        assert abs(int(np.float32(sc.clip_coef).view(np.int32)) - int(o.view(np.int32))) <= 1
+        if np.float32(sc.clip_coef) == o:
+            job.assert_bit_exact()
+        else:
+            job.assert_within_tolerance()
+
+
+def _with_subnormals(g, rng, frac=0.05):
+    """Replace a fraction of a [n_d, row] bf16 tensor's entries by bf16
+    subnormals (exponent field zero) of random sign and mantissa."""
+    bits = g.view(torch.int16).numpy()
+    mask = rng.random(bits.shape) < frac
+    sub = (rng.integers(1, 128, size=bits.shape) | (rng.integers(0, 2, size=bits.shape) << 15)).astype(np.int16)
+    bits[mask] = sub[mask]
+    return g
+
+
+@pytest.mark.parametrize("stage", [2, 3])
+def test_subnormal_gradients(stage):
+    # bf16 subnormals in every rank: the rank sums (mixed-precision adds)
+    # and Adam must keep them as the oracle's IEEE arithmetic does
+    n_d, psi = 4, 300_007
+    job = Job(psi, n_d, stage=stage, pad=8, hp=z.hparams(lr=1e-3), seed=23)
+    rng = np.random.default_rng(5)
+    for step in (1, 2):
+        g = synth.rank_grads(n_d, psi, 1e-36, 23, step, row_pad=job.buf.grads.shape[1] - psi)
+        g = _with_subnormals(g, rng)
+        job.buf.grads.copy_(g.cuda())
+        job.rows = [u16(g[r, :psi]) for r in range(n_d)]
+        assert any((np.asarray(r) & 0x7F80 == 0).any() and (np.asarray(r) & 0x7F).any() for r in job.rows)
+        job.gpu_step()
+        job.oracle_step()
+        job.assert_bit_exact()
+
+
+def test_subnormal_values_through_the_quantizers():
+    # blocks whose values are bf16 subnormals (scale itself subnormal: the
+    # exact path) next to blocks with a normal maximum and subnormal members
+    n_d, psi = 2, 2048 * 8
+    plan = z.Plan(psi, n_d, stage=2, shard_pad=8)
+    S = plan.shard
+    rng = np.random.default_rng(9)
+    g = torch.zeros(n_d, z.row_len(psi), dtype=torch.bfloat16)
+    g[:, :psi] = torch.from_numpy(rng.normal(0, 1e-37, size=(n_d, psi)).astype(np.float32)).to(torch.bfloat16)
+    g = _with_subnormals(g, rng, frac=0.5)
+    g[:, 2048 * 2:2048 * 3] = torch.from_numpy(rng.normal(0, 1e-3, size=(n_d, 2048)).astype(np.float32)).to(
+        torch.bfloat16)
+    g[:, 2048 * 2 + 7] = 3e-36   # a normal block maximum small enough that members may round to code 1
+    gd = g.cuda()
+    nbs = -(-S // 2048)
+    n_dp = (n_d + 3) // 4 * 4
+    codes = torch.zeros(n_d, (psi + 15) // 16 * 16, dtype=torch.int8, device="cuda")
+    scales = torch.zeros(n_d * nbs * n_dp, device="cuda")
+    z.zero_quantize_grads(plan.handle, [gd[r] for r in range(n_d)], 2048, [codes[r] for r in range(n_d)], scales)
+    rows = [u16(g[r, :psi]) for r in range(n_d)]
+    oc, osc = oracle.quantize_ranks(rows, psi, S, 2048)
+    got_c = codes.cpu().numpy()
+    for q in range(n_d):
+        assert np.array_equal(got_c[q, :psi], oc[q][:psi])
+    assert np.array_equal(u32(scales.cpu().numpy().reshape(osc.shape)), u32(osc))
+    # the standalone quantized gather of the same values as one shard set
+    x = gd[0, :psi].contiguous()
+    qc = torch.zeros(psi, dtype=torch.int8, device="cuda")
+    qs = torch.zeros(n_d * nbs, device="cuda")
+    qg = torch.zeros(psi, dtype=torch.bfloat16, device="cuda")
+    z.zero_quant_gather(plan.handle, x, 2048, qc, qs, qg)
+    wc, ws, wg = oracle.quant_gather(u16(x), n_d, psi, S, 2048)
+    assert np.array_equal(qc.cpu().numpy(), wc)
+    assert np.array_equal(u32(qs.cpu().numpy()), u32(ws))
+    assert np.array_equal(u16(qg), wg)
