@@ -38,6 +38,9 @@ struct Shared {
 };
 static_assert(sizeof(Shared) <= kStageOffset, "shared header too large");
 
+// rank-group shapes of a launch (the FULL parameter of k_stream)
+enum { kPartial = 0, kFullOne = 1, kFullMulti = 2 };
+
 // Walks this CTA's tiles (blockIdx.x, + gridDim.x, ...) as (segment, tile in
 // segment) without a 64-bit division per tile: one division at the start,
 // then an add-and-carry per step.
@@ -117,7 +120,7 @@ __host__ __device__ constexpr int group_ranks() { return GT == kGradQ8 ? 2 * kGr
 
 // 17 warps spread over an SM's 4 sub-partitions put 5 on one of them, whose
 // 16K registers then allow 96 per thread: the bound ptxas works to here.
-template <int GT, int PT, int OP>
+template <int GT, int PT, int OP, int FULL>
 __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ StreamArgs a)
 {
     constexpr int kG = group_ranks<GT>();
@@ -302,26 +305,53 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
                         const unsigned char* st = ring + static_cast<size_t>(s) * a.stage_bytes;
                         const int r0 = g * kG;
                         const int nr = a.n_ranks - r0 < kG ? a.n_ranks - r0 : kG;
+                        // Every group full (N_d a multiple of the group size): a loop
+                        // of constant trip count, constant shared-memory offsets and no
+                        // loop tests; otherwise one bounded at run time.  How far it is
+                        // unrolled was measured per case (int8 ranks: fully when a tile
+                        // has several groups, by 8 when it has one).
                         if constexpr (GT == kGradQ8) {
                             // scales of this group's ranks arrived with the stage (broadcast reads)
                             const float* ssc = reinterpret_cast<const float*>(st + scale_off);
 #pragma unroll
                             for (int ch = 0; ch < kChunksPerThread; ++ch) {
                                 const int q = ch * kConsumers + tid;
+                                if constexpr (FULL == kFullMulti) {
+                                    const uint32_t* cw = reinterpret_cast<const uint32_t*>(st) + q;
+#pragma unroll
+                                    for (int k = 0; k < kG; ++k) add_codes(acc[ch], cw[k * (kTile / 4)], ssc[ch * kG + k]);
+                                } else if constexpr (FULL == kFullOne) {
+                                    const uint32_t* cw = reinterpret_cast<const uint32_t*>(st) + q;
+#pragma unroll 8
+                                    for (int k = 0; k < kG; ++k) add_codes(acc[ch], cw[k * (kTile / 4)], ssc[ch * kG + k]);
+                                } else {
 #pragma unroll 4
-                                for (int k = 0; k < nr; ++k) {
-                                    const uint32_t w = reinterpret_cast<const uint32_t*>(st + k * kTile)[q];
-                                    add_codes(acc[ch], w, ssc[ch * kG + k]);
+                                    for (int k = 0; k < nr; ++k) {
+                                        const uint32_t w = reinterpret_cast<const uint32_t*>(st + k * kTile)[q];
+                                        add_codes(acc[ch], w, ssc[ch * kG + k]);
+                                    }
                                 }
                             }
                         } else {
 #pragma unroll
                             for (int ch = 0; ch < kChunksPerThread; ++ch) {
                                 const int q = ch * kConsumers + tid;  // chunk index within the tile
+                                const uint2* rw = reinterpret_cast<const uint2*>(st) + q;
+                                if constexpr (FULL != kPartial && OP == OP_QFUSED) {
+                                    // the int8-gather step measured fastest in this form
+                                    if (nr == kG) {
+#pragma unroll
+                                        for (int k = 0; k < kG; ++k) add_slice<GT>(acc[ch], rw[k * (kTile / 4)]);
+                                    } else {
 #pragma unroll 8
-                                for (int k = 0; k < nr; ++k) {
-                                    const uint2 w = reinterpret_cast<const uint2*>(st + k * kTile * 2)[q];
-                                    add_slice<GT>(acc[ch], w);
+                                        for (int k = 0; k < nr; ++k) add_slice<GT>(acc[ch], rw[k * (kTile / 4)]);
+                                    }
+                                } else if constexpr (FULL != kPartial) {
+#pragma unroll
+                                    for (int k = 0; k < kG; ++k) add_slice<GT>(acc[ch], rw[k * (kTile / 4)]);
+                                } else {
+#pragma unroll 8
+                                    for (int k = 0; k < nr; ++k) add_slice<GT>(acc[ch], rw[k * (kTile / 4)]);
                                 }
                             }
                         }
@@ -572,8 +602,8 @@ DevInfo device_info(int dev)
     return cache[dev];
 }
 
-template <int GT, int PT, int OP>
-cudaError_t launch_one(StreamArgs& a, cudaStream_t st)
+template <int GT, int PT, int OP, int FULL>
+cudaError_t launch_one_k(StreamArgs& a, cudaStream_t st)
 {
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
@@ -593,7 +623,7 @@ cudaError_t launch_one(StreamArgs& a, cudaStream_t st)
     const size_t smem = kStageOffset + static_cast<size_t>(stages) * a.stage_bytes;
     static int attr_done[64];
     if (dev < 64 && !__atomic_load_n(&attr_done[dev], __ATOMIC_ACQUIRE)) {
-        err = cudaFuncSetAttribute(k_stream<GT, PT, OP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        err = cudaFuncSetAttribute(k_stream<GT, PT, OP, FULL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    di.smem_optin);
         if (err != cudaSuccess) return err;
         __atomic_store_n(&attr_done[dev], 1, __ATOMIC_RELEASE);
@@ -604,8 +634,24 @@ cudaError_t launch_one(StreamArgs& a, cudaStream_t st)
     if (grid <= 0) return cudaSuccess;
     a.grid = static_cast<int>(grid);
     count_launch();
-    k_stream<GT, PT, OP><<<static_cast<unsigned>(grid), kThreads, smem, st>>>(a);
+    k_stream<GT, PT, OP, FULL><<<static_cast<unsigned>(grid), kThreads, smem, st>>>(a);
     return cudaGetLastError();
+}
+
+// picks the rank-loop shape from the launch's rank count
+template <int GT, int PT, int OP>
+cudaError_t launch_one(StreamArgs& a, cudaStream_t st)
+{
+    constexpr int kG = group_ranks<GT>();
+    if constexpr (OP == OP_ADAM) {
+        return launch_one_k<GT, PT, OP, kPartial>(a, st);
+    } else {
+        if (a.n_ranks <= 0 || a.n_ranks % kG != 0) return launch_one_k<GT, PT, OP, kPartial>(a, st);
+        if constexpr (GT == kGradQ8) {
+            if (a.n_ranks > kG) return launch_one_k<GT, PT, OP, kFullMulti>(a, st);
+        }
+        return launch_one_k<GT, PT, OP, kFullOne>(a, st);
+    }
 }
 
 }  // namespace
