@@ -526,7 +526,7 @@ def gpu_arm(args, rank, world, device):
                 "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": kernel,
                 "kernel_ms": round(kms, 4), "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)"}
 
-    e2e = None if args.no_e2e or w.get("qgz") else e2e_measure(job, w, args, device, world)
+    e2e = None if args.no_e2e else e2e_measure(job, w, args, device, world)
     sender = None
     if w.get("qgz"):
         # the sender pass (every rank quantizes its bf16 gradient): 2 + 1 + 4/2048 bytes per param per rank
@@ -611,8 +611,18 @@ def e2e_measure(job, w, args, device, world):
         return None
     z = job.z
     h = job.plan.handle
-    host_g = torch.empty(job.grads[0].shape, dtype=job.grads[0].dtype, pin_memory=True)
-    host_g.copy_(job.grads[0])
+    qgz = bool(w.get("qgz"))
+    if qgz:
+        # the quantized exchange's wire format crosses the link: every rank's
+        # int8 codes and fp32 block scales (the sender ran where the gradients are)
+        dev_sets = [(job.codes[i], job.qscales[i]) for i in range(2)]
+    else:
+        dev_sets = [(job.grads[i],) for i in range(2)]
+    host_in = []
+    for t in dev_sets[0]:
+        ht = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        ht.copy_(t)
+        host_in.append(ht)
     host_out = torch.empty(job.lp[0].numel(), dtype=torch.bfloat16, pin_memory=True)
     steps = max(1, min(args.steps, 10))
     k = w.get("accum", 1)
@@ -627,7 +637,8 @@ def e2e_measure(job, w, args, device, world):
         with torch.cuda.stream(copy_s):
             if i >= 2:
                 copy_s.wait_event(used[i % 2])   # the pass that read this buffer is done
-            job.grads[i % 2].copy_(host_g, non_blocking=True)
+            for dst, src in zip(dev_sets[i % 2], host_in):
+                dst.copy_(src, non_blocking=True)
             copied[i % 2].record(copy_s)
 
     torch.cuda.synchronize()
@@ -639,7 +650,11 @@ def e2e_measure(job, w, args, device, world):
             issue_copy(i + 1)
         comp.wait_event(copied[i % 2])
         mu = i % k
-        if k > 1 and mu < k - 1:
+        if qgz:
+            codes, scales = dev_sets[i % 2]
+            z.zero_step_fused_qgz(h, job.hp, [codes[r] for r in range(w["n_d"])], scales, 2048, job.master[0],
+                                  job.m[0], job.v[0], job.master[0], job.m[0], job.v[0], job.lp[0], job.scalars)
+        elif k > 1 and mu < k - 1:
             z.zero_accumulate_grads(h, job.ranks(i % 2), None if mu == 0 else job.acc, job.acc, job.scalars)
         elif k > 1:
             z.zero_step_fused_accum(h, job.hp, job.ranks(i % 2), job.acc, k, job.master[0], job.m[0], job.v[0],
@@ -654,9 +669,10 @@ def e2e_measure(job, w, args, device, world):
     torch.cuda.synchronize()
     ms = dist_max(a.elapsed_time(b), world)
     return {"value": world * w["psi"] * steps / (ms / 1e3), "unit": UNIT,
-            "h2d_bytes_per_step": k * host_g.numel() * host_g.element_size(),
+            "h2d_bytes_per_step": k * sum(t.numel() * t.element_size() for t in host_in),
             "d2h_bytes_per_step": host_out.numel() * host_out.element_size(), "steps": steps,
-            "overlap": "next gradient copy on a second stream"}
+            "overlap": "next gradient copy on a second stream",
+            "inputs": "int8 codes + fp32 block scales of every rank" if qgz else "16-bit gradients of every rank"}
 
 
 # ------------------------------------------------------------- CPU oracle arm
