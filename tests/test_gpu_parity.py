@@ -289,6 +289,23 @@ def test_fused_quantized_gather(n_d, psi, pad):
 
 
 # -------------------------------------------------------- bounded waits
+def test_engine_timeout_path_reports_and_context_survives():
+    # a streaming-engine launch whose producer never fills a stage: every
+    # consumer wait runs out, the launch reports and returns
+    sc = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    scratch = torch.zeros(8192, dtype=torch.uint8, device="cuda")
+    z.zero_scalars_init(sc)
+    z.zero_debug_stream_timeout(scratch, sc, 2_000_000)
+    s = z.read_scalars(sc)
+    assert s.status & z.ZERO_DEV_TIMEOUT
+    assert torch.count_nonzero(scratch).item() == 0
+    job = Job(10_000, 2, hp=z.hparams(), seed=72)
+    job.new_grads(1)
+    job.gpu_step()
+    job.oracle_step()
+    job.assert_bit_exact()
+
+
 def test_bounded_wait_reports_timeout_and_context_survives():
     sc = torch.zeros(256, dtype=torch.uint8, device="cuda")
     z.zero_scalars_init(sc)

@@ -77,6 +77,7 @@ _SIGS = {
     "zero_step_fused_qgather": (_i32, [_vp, _hp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp,
                                        _vp, _vp, _vp]),
     "zero_debug_wait_timeout": (_i32, [_vp, _ll, _vp]),
+    "zero_debug_stream_timeout": (_i32, [_vp, _vp, _ll, _vp]),
     "zero_launch_count": (ctypes.c_ulonglong, []),
     "zero_step_fused_noalloc": (_i32, [_vp, _hp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "zero_quantize_grads": (_i32, [_vp, _vp, _i32, _vp, _vp, _vp, _vp]),
@@ -267,6 +268,12 @@ def zero_step_fused_qgz(plan, hp, rank_codes, rank_scales, block, master_in, m_i
 
 def zero_debug_wait_timeout(scalars, timeout_ns, stream=None):
     _check(_lib.zero_debug_wait_timeout(_addr(scalars), timeout_ns, _stream(stream)), "zero_debug_wait_timeout")
+
+
+def zero_debug_stream_timeout(scratch, scalars, timeout_ns, stream=None):
+    """One streaming-engine launch whose waits all run out (tests the timeout path)."""
+    _check(_lib.zero_debug_stream_timeout(_addr(scratch), _addr(scalars), timeout_ns, _stream(stream)),
+           "zero_debug_stream_timeout")
 
 
 def zero_step_fused_noalloc(plan, hp, rank_grads, master_in, m_in, v_in, master_out, m_out, v_out, lp_out,

@@ -701,6 +701,24 @@ ZERO_API zero_status zero_debug_wait_timeout(zero_dev_scalars* sc, long long tim
     return from_cuda(zk::launch_debug_wait(sc, static_cast<unsigned long long>(timeout_ns), as_stream(stream)));
 }
 
+ZERO_API zero_status zero_debug_stream_timeout(void* scratch, zero_dev_scalars* sc, long long timeout_ns, void* stream)
+{
+    ZK_CALL_RANGE();
+    zero_status s;
+    if ((s = check_dev(scratch)) != ZERO_OK) return s;
+    if ((s = check_dev(sc, 256)) != ZERO_OK) return s;
+    if (timeout_ns < 1 || timeout_ns > 10000000000LL) return ZERO_ERR_INVALID_ARG;
+    // one full tile of one bf16 rank: the consumers wait for a stage the
+    // producer never fills
+    StreamArgs a = base_args(nullptr, nullptr, sc);
+    a.n_ranks = 1;
+    a.rank[0] = scratch;
+    set_flat(a, 0, zk::kTile);
+    a.flags = zk::F_DEBUG_STARVE;
+    a.timeout_ns = static_cast<unsigned long long>(timeout_ns);
+    return from_cuda(zk::launch_stream(zk::OP_REDUCE, ZERO_BF16, ZERO_BF16, a, as_stream(stream)));
+}
+
 ZERO_API unsigned long long zero_launch_count(void) { return zk::launch_count(); }
 
 }  // extern "C"

@@ -47,6 +47,8 @@ enum : int {
     F_CARRY = 1 << 9,     // gradient accumulation: the rank sum is added to an fp32 carry
                           // stream (side 0 of OP_REDUCE, side 3 of OP_FUSED) before the mean
     F_RAW = 1 << 10,      // OP_REDUCE: store the sum itself, no division
+    F_DEBUG_STARVE = 1 << 11,   // the producer issues no copy, so every consumer wait
+                                // runs out (tests the timeout path; nothing is read)
 };
 
 // ------------------------------------------------------------- PTX wrappers

@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
         // nothing to do; fall through to the end (the epilogue still runs)
     } else if (warp == kConsumerWarps) {
         // ------------------------------------------------------- producer
-        if (lane == 0) {
+        if (lane == 0 && !(a.flags & F_DEBUG_STARVE)) {
             int s = 0;
             uint32_t ph = 0;
             TileCursor cur;
