@@ -356,15 +356,19 @@ ZERO_API zero_status zero_step_fused_qgz(const zero_plan* plan, const zero_hpara
  * limit of timeout_ns (at most 10 s).  When the limit runs out the kernel sets
  * ZERO_DEV_TIMEOUT in scalars->status and returns, leaving the context usable.
  * Exists so that the bounded-wait path can be tested.                       */
-/* The streaming engine's own timeout path: one launch of the reduce kernel
- * over one 4096-element tile whose producer issues no copy, so every
- * consumer's bounded wait runs out after timeout_ns (at most 10 s).  The
- * kernel raises its abort flag, lets nothing in flight land (nothing was
- * issued), sets ZERO_DEV_TIMEOUT in scalars->status and returns.  scratch:
- * any 16-byte aligned device buffer of at least 8 KB, never read.  Exists so
- * that the engine's timeout handling can be tested.                         */
-ZERO_API zero_status zero_debug_stream_timeout(void* scratch, zero_dev_scalars* scalars_dev, long long timeout_ns,
-                                               void* stream);
+/* A pipelined kernel's own timeout path: one small launch of
+ *   kernel 0: the streaming engine (reduce op, one 4096-element tile),
+ *   kernel 1: the all-gather ring (one 8192-element shard),
+ *   kernel 2: the gradient sender (one 2048-element block),
+ * whose bulk copies are never issued, so every bounded wait runs out (after
+ * timeout_ns for kernel 0, at most 10 s; after 2 ms for kernels 1 and 2).
+ * The kernel gives up, lets nothing in flight land (nothing was issued), sets
+ * ZERO_DEV_TIMEOUT in scalars->status and returns.  scratch: a 16-byte
+ * aligned device buffer of at least 32 KB; the gradient or shard region (its
+ * first 16 KB) is never read; kernel 2 may write its scale row (16 bytes at
+ * offset 8 KB).  Exists so that the timeout handling can be tested.         */
+ZERO_API zero_status zero_debug_stream_timeout(int kernel, void* scratch, zero_dev_scalars* scalars_dev,
+                                               long long timeout_ns, void* stream);
 
 ZERO_API zero_status zero_debug_wait_timeout(zero_dev_scalars* scalars_dev, long long timeout_ns,
                                              void* stream);

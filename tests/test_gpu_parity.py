@@ -289,16 +289,17 @@ def test_fused_quantized_gather(n_d, psi, pad):
 
 
 # -------------------------------------------------------- bounded waits
-def test_engine_timeout_path_reports_and_context_survives():
-    # a streaming-engine launch whose producer never fills a stage: every
-    # consumer wait runs out, the launch reports and returns
+@pytest.mark.parametrize("kernel", [0, 1, 2])   # streaming engine, all-gather ring, gradient sender
+def test_pipelined_kernel_timeout_path_reports_and_context_survives(kernel):
+    # a launch whose bulk copies are never issued: every wait runs out, the
+    # launch reports and returns
     sc = torch.zeros(256, dtype=torch.uint8, device="cuda")
-    scratch = torch.zeros(8192, dtype=torch.uint8, device="cuda")
+    scratch = torch.zeros(32768, dtype=torch.uint8, device="cuda")
     z.zero_scalars_init(sc)
-    z.zero_debug_stream_timeout(scratch, sc, 2_000_000)
+    z.zero_debug_stream_timeout(kernel, scratch, sc, 2_000_000)
     s = z.read_scalars(sc)
     assert s.status & z.ZERO_DEV_TIMEOUT
-    assert torch.count_nonzero(scratch).item() == 0
+    assert torch.count_nonzero(scratch[:8192]).item() == 0      # the input region is never touched
     job = Job(10_000, 2, hp=z.hparams(), seed=72)
     job.new_grads(1)
     job.gpu_step()

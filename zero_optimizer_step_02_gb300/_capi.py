@@ -77,7 +77,7 @@ _SIGS = {
     "zero_step_fused_qgather": (_i32, [_vp, _hp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp,
                                        _vp, _vp, _vp]),
     "zero_debug_wait_timeout": (_i32, [_vp, _ll, _vp]),
-    "zero_debug_stream_timeout": (_i32, [_vp, _vp, _ll, _vp]),
+    "zero_debug_stream_timeout": (_i32, [_i32, _vp, _vp, _ll, _vp]),
     "zero_launch_count": (ctypes.c_ulonglong, []),
     "zero_step_fused_noalloc": (_i32, [_vp, _hp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "zero_quantize_grads": (_i32, [_vp, _vp, _i32, _vp, _vp, _vp, _vp]),
@@ -270,9 +270,10 @@ def zero_debug_wait_timeout(scalars, timeout_ns, stream=None):
     _check(_lib.zero_debug_wait_timeout(_addr(scalars), timeout_ns, _stream(stream)), "zero_debug_wait_timeout")
 
 
-def zero_debug_stream_timeout(scratch, scalars, timeout_ns, stream=None):
-    """One streaming-engine launch whose waits all run out (tests the timeout path)."""
-    _check(_lib.zero_debug_stream_timeout(_addr(scratch), _addr(scalars), timeout_ns, _stream(stream)),
+def zero_debug_stream_timeout(kernel, scratch, scalars, timeout_ns, stream=None):
+    """One launch of a pipelined kernel (0 engine, 1 all-gather, 2 sender)
+    whose bulk copies are never issued: every wait runs out (tests the timeout path)."""
+    _check(_lib.zero_debug_stream_timeout(kernel, _addr(scratch), _addr(scalars), timeout_ns, _stream(stream)),
            "zero_debug_stream_timeout")
 
 

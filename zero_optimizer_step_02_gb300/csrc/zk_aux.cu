@@ -183,6 +183,7 @@ struct AgArgs {
     long long tiles_per_shard;    // ceil(S / kAgTile)
     int n_d;
     int tma_ok;                   // S % 8 == 0 (every tile 16-byte aligned at both ends)
+    int starve;                   // issue no copy: every wait runs out (tests the timeout path)
     unsigned long long timeout_ns;
     zero_dev_scalars* sc;
 };
@@ -229,6 +230,7 @@ __global__ void __launch_bounds__(kAgThreads) k_all_gather(const __grid_constant
                 return ntiles;
             };
             auto issue_load = [&](long long t, int s, uint32_t ph) {
+                if (a.starve) return;
                 int r;
                 long long i0;
                 int len;
@@ -295,7 +297,7 @@ __global__ void __launch_bounds__(kAgThreads) k_all_gather(const __grid_constant
 }
 
 cudaError_t launch_all_gather(const void* const* shards, int n_d, long long shard, long long psi,
-                              void* gathered, zero_dev_scalars* sc, cudaStream_t st)
+                              void* gathered, zero_dev_scalars* sc, cudaStream_t st, bool starve)
 {
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
@@ -309,7 +311,8 @@ cudaError_t launch_all_gather(const void* const* shards, int n_d, long long shar
     bool aligned = shard % 8 == 0 && (reinterpret_cast<uintptr_t>(gathered) & 15) == 0;
     for (int r = 0; r < n_d; ++r) aligned = aligned && (reinterpret_cast<uintptr_t>(shards[r]) & 15) == 0;
     a.tma_ok = aligned ? 1 : 0;
-    a.timeout_ns = kDefaultTimeoutNs;
+    a.timeout_ns = starve ? 2000000ull : kDefaultTimeoutNs;
+    a.starve = starve ? 1 : 0;
     a.sc = sc;
     const long long ntiles = a.tiles_per_shard * n_d;
     if (ntiles <= 0) return cudaSuccess;
@@ -445,6 +448,7 @@ struct QsArgs {
     zero_dev_scalars* sc;                     // may be null: receives ZERO_DEV_TIMEOUT
     long long shard, psi, nbs, n_dp, total;   // total = n_d * n_d * nbs blocks
     int n_d, block, ring_ok;                   // ring_ok: block == 2048 and shard % 8 == 0
+    int starve;                                // issue no copy: every wait runs out (tests the timeout path)
     unsigned long long timeout_ns;
 };
 
@@ -533,7 +537,7 @@ __global__ void __launch_bounds__(kQsWarps * 32, 1) k_quantize_ranks(const __gri
     auto issue = [&](int s) {
         if (ic.valid(a)) {
             const QsBlock k = ic.block(a);
-            if (qs_ring(a, k) && lane == 0) {
+            if (qs_ring(a, k) && lane == 0 && !a.starve) {
                 fence_proxy_async_smem();
                 mbar_arrive_expect_tx(&bar[s], kQsSlotBytes);
                 bulk_load(slot0 + s * kQsSlotBytes, a.rank[k.q] + k.j0, kQsSlotBytes, &bar[s]);
@@ -626,7 +630,8 @@ __global__ void __launch_bounds__(kQsWarps * 32, 1) k_quantize_ranks(const __gri
 }
 
 cudaError_t launch_quantize_grads(const void* const* ranks, int n_d, long long shard, long long psi, int block,
-                                  signed char* const* codes, float* scales, zero_dev_scalars* sc, cudaStream_t st)
+                                  signed char* const* codes, float* scales, zero_dev_scalars* sc, cudaStream_t st,
+                                  bool starve)
 {
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
@@ -650,7 +655,8 @@ cudaError_t launch_quantize_grads(const void* const* ranks, int n_d, long long s
     a.total = static_cast<long long>(n_d) * n_d * a.nbs;
     if (a.nbs > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
     a.ring_ok = (block == kQuantBlock && shard % 8 == 0 && aligned) ? 1 : 0;
-    a.timeout_ns = kDefaultTimeoutNs;
+    a.timeout_ns = starve ? 2000000ull : kDefaultTimeoutNs;
+    a.starve = starve ? 1 : 0;
     if (a.total <= 0) return cudaSuccess;
     const size_t smem = 1024 + static_cast<size_t>(kQsWarps) * kQsSlots * kQsSlotBytes;
     static int attr_done[64];

@@ -701,13 +701,29 @@ ZERO_API zero_status zero_debug_wait_timeout(zero_dev_scalars* sc, long long tim
     return from_cuda(zk::launch_debug_wait(sc, static_cast<unsigned long long>(timeout_ns), as_stream(stream)));
 }
 
-ZERO_API zero_status zero_debug_stream_timeout(void* scratch, zero_dev_scalars* sc, long long timeout_ns, void* stream)
+ZERO_API zero_status zero_debug_stream_timeout(int kernel, void* scratch, zero_dev_scalars* sc, long long timeout_ns,
+                                               void* stream)
 {
     ZK_CALL_RANGE();
     zero_status s;
     if ((s = check_dev(scratch)) != ZERO_OK) return s;
     if ((s = check_dev(sc, 256)) != ZERO_OK) return s;
     if (timeout_ns < 1 || timeout_ns > 10000000000LL) return ZERO_ERR_INVALID_ARG;
+    unsigned char* buf = static_cast<unsigned char*>(scratch);
+    if (kernel == 1) {
+        // one 8192-element shard gathered from the first 16 KB into the next 16 KB
+        const void* shards[1] = {buf};
+        return from_cuda(zk::launch_all_gather(shards, 1, 8192, 8192, buf + 16384, sc, as_stream(stream), true));
+    }
+    if (kernel == 2) {
+        // one rank, one 2048-element block: gradient in the first 4 KB, codes
+        // in the next 2 KB, the scale row (4 floats) after them
+        const void* ranks[1] = {buf};
+        signed char* codes[1] = {reinterpret_cast<signed char*>(buf + 4096)};
+        return from_cuda(zk::launch_quantize_grads(ranks, 1, 2048, 2048, zk::kQuantBlock, codes,
+                                                   reinterpret_cast<float*>(buf + 8192), sc, as_stream(stream), true));
+    }
+    if (kernel != 0) return ZERO_ERR_INVALID_ARG;
     // one full tile of one bf16 rank: the consumers wait for a stage the
     // producer never fills
     StreamArgs a = base_args(nullptr, nullptr, sc);

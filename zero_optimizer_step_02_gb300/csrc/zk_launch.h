@@ -67,13 +67,15 @@ cudaError_t launch_repair(const zero_hparams& hp, const float* master_in, const 
                           const float* v_in, float* master_out, float* m_out, float* v_out,
                           void* lp_out, int param_dtype, long long psi, zero_dev_scalars* sc,
                           cudaStream_t st);
+// starve: issue no copy, so every wait runs out (tests the timeout path)
 cudaError_t launch_all_gather(const void* const* shards, int n_d, long long shard, long long psi,
-                              void* gathered, zero_dev_scalars* sc, cudaStream_t st);
+                              void* gathered, zero_dev_scalars* sc, cudaStream_t st, bool starve = false);
 cudaError_t launch_quant_gather(const void* shards, int n_d, long long shard, long long psi,
                                 int block, signed char* codes, float* scales, void* gathered,
                                 cudaStream_t st);
 cudaError_t launch_quantize_grads(const void* const* ranks, int n_d, long long shard, long long psi, int block,
-                                  signed char* const* codes, float* scales, zero_dev_scalars* sc, cudaStream_t st);
+                                  signed char* const* codes, float* scales, zero_dev_scalars* sc, cudaStream_t st,
+                                  bool starve = false);
 cudaError_t launch_debug_wait(zero_dev_scalars* sc, unsigned long long timeout_ns, cudaStream_t st);
 
 }  // namespace zk
