@@ -463,7 +463,7 @@ def gpu_arm(args, rank, world, device):
         # a middle micro-batch (accumulator read and written) and the step at
         # the last one, each timed alone back to back; the first repetition
         # is not counted
-        n_rep = max(3, args.steps)
+        n_rep = min(max(3, args.steps), 50)
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_rep + 1)]
         torch.cuda.synchronize()
         for i, ev in enumerate(evs):
@@ -481,7 +481,7 @@ def gpu_arm(args, rank, world, device):
         breakdown = {"accumulate_grads": round(t_acc, 4), "step_accum": round(t_fin, 4)}
     elif w["clip"] > 0 and w["n_d"] > 4 and not w.get("offload"):
         job.ghat = torch.zeros(job.plan.padded, device=device)
-        n_rep = max(3, args.steps)
+        n_rep = min(max(3, args.steps), 50)
         dur = [0.0, 0.0, 0.0]
         # enqueue every repetition back to back (one sync at the end) so the
         # host's launch latency never sits inside an interval; the first
@@ -506,7 +506,7 @@ def gpu_arm(args, rank, world, device):
             # time the per-layer fused step alone
             evs = []
             torch.cuda.synchronize()
-            for _ in range(max(3, args.steps) + 1):
+            for _ in range(min(max(3, args.steps), 50) + 1):
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record()
                 z.zero_step_fused(job.plan.handle, job.hp, job.ranks(0), job.master[0], job.m[0], job.v[0],
@@ -532,7 +532,7 @@ def gpu_arm(args, rank, world, device):
         # the sender pass (every rank quantizes its bf16 gradient): 2 + 1 + 4/2048 bytes per param per rank
         evs = []
         torch.cuda.synchronize()
-        for k in range(max(3, args.steps) + 1):
+        for k in range(min(max(3, args.steps), 50) + 1):
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             job.quantize(k % len(job.grads))
@@ -765,7 +765,8 @@ def dist_max(x, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200,
+                    help="timed steps (the default makes the timed region long enough for several clock samples)")
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--config", type=int, default=2)
