@@ -325,6 +325,36 @@ __device__ __forceinline__ float mean_of(const StepConsts& c, float sum)
     return c.div_pow2 ? __fmul_rn(sum, c.inv_divisor) : __fdiv_rn(sum, c.divisor);
 }
 
+// The mean of four sums: the divisor's form is tested once for the four.
+__device__ __forceinline__ void mean_of4(const StepConsts& c, const float (&sum)[4], float (&g)[4])
+{
+    if (c.div_pow2) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) g[e] = __fmul_rn(sum[e], c.inv_divisor);
+    } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) g[e] = __fdiv_rn(sum[e], c.divisor);
+    }
+}
+
+// Four Adam/AdamW element updates, each in adam_elem's operation order; the
+// weight-decay test is made once for the four.
+__device__ __forceinline__ void adam_elem4(const StepConsts& c, const float (&g)[4], float (&p)[4], float (&m)[4],
+                                           float (&v)[4])
+{
+    if (c.wd) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) p[e] = __fmul_rn(p[e], c.decay);
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        m[e] = __fadd_rn(__fmul_rn(c.b1, m[e]), __fmul_rn(c.omb1, g[e]));
+        v[e] = __fadd_rn(__fmul_rn(c.b2, v[e]), __fmul_rn(c.omb2, __fmul_rn(g[e], g[e])));
+        const float denom = __fadd_rn(__fsqrt_rn(v[e]), c.eps);
+        p[e] = __fsub_rn(p[e], __fmul_rn(c.step, __fdiv_rn(m[e], denom)));
+    }
+}
+
 // One Adam/AdamW element update in the fixed operation order.
 __device__ __forceinline__ void adam_elem(const StepConsts& c, float g, float& p, float& m, float& v)
 {

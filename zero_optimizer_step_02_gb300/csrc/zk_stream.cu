@@ -437,21 +437,61 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
                 } else {
                     // OP_FUSED: side = {master, m, v[, carry]}; OP_ADAM: side = {g, master, m, v}
                     constexpr int P = (OP == OP_ADAM) ? 1 : 0;
-                    float pv[4], mv[4], vv[4];
+                    // uniform tests (divisor form, carry, detection, clip, decay)
+                    // made once per chunk, not once per element -- except in the
+                    // int8-gather step and with int8 ranks, whose register budget
+                    // measured faster with the per-element form
+                    float pv[4], mv[4], vv[4], gv[4];
                     uint16_t lp[4];
+                    if constexpr (OP == OP_QFUSED || GT == kGradQ8) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            float g = mean_of(c, carry ? __fadd_rn(sv[ch][kCarry][e], acc[ch][e]) : acc[ch][e]);
+                            if (detect && e < cnt && !is_finite_f32(g)) nonfinite = true;
+                            if (c.clip) g = __fmul_rn(g, c.coef);
+                            pv[e] = sv[ch][P + 0][e];
+                            mv[e] = sv[ch][P + 1][e];
+                            vv[e] = sv[ch][P + 2][e];
+                            adam_elem(c, g, pv[e], mv[e], vv[e]);
+                            lp[e] = Lp<PT>::narrow(pv[e]);
+                            xq[ch][e] = Lp<PT>::widen(lp[e]);
+                        }
+                    } else {
+                    if constexpr (OP == OP_ADAM) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) gv[e] = sv[ch][0][e];
+                    } else {
+                        float sum[4];
+                        if (carry) {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) sum[e] = __fadd_rn(sv[ch][kCarry][e], acc[ch][e]);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) sum[e] = acc[ch][e];
+                        }
+                        mean_of4(c, sum, gv);
+                    }
+                    if (detect) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if (e < cnt && !is_finite_f32(gv[e])) nonfinite = true;
+                    }
+                    if (c.clip) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) gv[e] = __fmul_rn(gv[e], c.coef);
+                    }
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        float g = (OP == OP_ADAM)
-                                      ? sv[ch][0][e]
-                                      : mean_of(c, carry ? __fadd_rn(sv[ch][kCarry][e], acc[ch][e]) : acc[ch][e]);
-                        if (detect && e < cnt && !is_finite_f32(g)) nonfinite = true;
-                        if (c.clip) g = __fmul_rn(g, c.coef);
                         pv[e] = sv[ch][P + 0][e];
                         mv[e] = sv[ch][P + 1][e];
                         vv[e] = sv[ch][P + 2][e];
-                        adam_elem(c, g, pv[e], mv[e], vv[e]);
+                    }
+                    adam_elem4(c, gv, pv, mv, vv);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
                         lp[e] = Lp<PT>::narrow(pv[e]);
                         xq[ch][e] = Lp<PT>::widen(lp[e]);
+                    }
                     }
                     if (alive) {
                         if (fast) {
