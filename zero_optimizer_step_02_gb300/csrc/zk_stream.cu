@@ -415,15 +415,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
                 int cnt = len - q * 4;
                 cnt = cnt < 0 ? 0 : (cnt > 4 ? 4 : cnt);
                 if (OP == OP_REDUCE) {
-                    float gv[4];
+                    // uniform tests once per chunk; the squares are still added in element order
+                    float gv[4], sum[4];
+                    if (carry) {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float sum = carry ? __fadd_rn(sv[ch][kCarry][e], acc[ch][e]) : acc[ch][e];
-                        gv[e] = raw ? sum : mean_of(c, sum);
-                        if (e < cnt) {
-                            if (detect && !is_finite_f32(gv[e])) nonfinite = true;
-                            if (want_sq) sq_accumulate(gv[e], sq_hi, sq_lo);
-                        }
+                        for (int e = 0; e < 4; ++e) sum[e] = __fadd_rn(sv[ch][kCarry][e], acc[ch][e]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) sum[e] = acc[ch][e];
+                    }
+                    if (raw) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) gv[e] = sum[e];
+                    } else {
+                        mean_of4(c, sum, gv);
+                    }
+                    if (detect) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if (e < cnt && !is_finite_f32(gv[e])) nonfinite = true;
+                    }
+                    if (want_sq) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if (e < cnt) sq_accumulate(gv[e], sq_hi, sq_lo);
                     }
                     if (alive && a.out_f32[0] != nullptr) {
                         if (fast) {
