@@ -190,12 +190,12 @@ def measured_hbm_peak():
 # kernel and workload, with a hash of the kernel sources they were taken on;
 # reported as null once the sources change.
 TRAFFIC = {
-    ("adam_shard", "zero2_gpt2small_psi124439808_nd8_adamw_clip1"): {"bytes": 3.625e9, "src": "31bdb03d33dd"},
-    ("fused_step", "zero2_psi2p28_nd8"): {"bytes": 11.110e9, "src": "31bdb03d33dd"},
-    ("fused_step_qgather", "zero2_psi2p28_nd2_qgather"): {"bytes": 8.080e9, "src": "31bdb03d33dd"},
-    ("fused_step_qgz", "zero2_psi2p28_nd8_qgz"): {"bytes": 8.923e9, "src": "31bdb03d33dd"},
-    ("accumulate_grads", "zero2_gpt2small_psi124439808_nd8_adamw_clip1_accum4"): {"bytes": 2.951e9,
-                                                                                   "src": "31bdb03d33dd"},
+    ("adam_shard", "zero2_gpt2small_psi124439808_nd8_adamw_clip1"): {"bytes": 3.627e9, "src": "102303894aae"},
+    ("fused_step", "zero2_psi2p28_nd8"): {"bytes": 11.106e9, "src": "102303894aae"},
+    ("fused_step_qgather", "zero2_psi2p28_nd2_qgather"): {"bytes": 8.080e9, "src": "102303894aae"},
+    ("fused_step_qgz", "zero2_psi2p28_nd8_qgz"): {"bytes": 8.918e9, "src": "102303894aae"},
+    ("accumulate_grads", "zero2_gpt2small_psi124439808_nd8_adamw_clip1_accum4"): {"bytes": 2.950e9,
+                                                                                   "src": "102303894aae"},
 }
 
 
