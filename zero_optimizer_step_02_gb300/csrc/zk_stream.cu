@@ -321,9 +321,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
 #pragma unroll
                                     for (int k = 0; k < kG; ++k) add_codes(acc[ch], cw[k * (kTile / 4)], ssc[ch * kG + k]);
                                 } else if constexpr (FULL == kFullOne) {
+                                    // four ranks' scales per 16-byte shared load
                                     const uint32_t* cw = reinterpret_cast<const uint32_t*>(st) + q;
-#pragma unroll 8
-                                    for (int k = 0; k < kG; ++k) add_codes(acc[ch], cw[k * (kTile / 4)], ssc[ch * kG + k]);
+                                    const float4* s4 = reinterpret_cast<const float4*>(ssc + ch * kG);
+                                    auto four = [&](int k4) {
+                                        const float4 sc4 = s4[k4];
+                                        add_codes(acc[ch], cw[(4 * k4 + 0) * (kTile / 4)], sc4.x);
+                                        add_codes(acc[ch], cw[(4 * k4 + 1) * (kTile / 4)], sc4.y);
+                                        add_codes(acc[ch], cw[(4 * k4 + 2) * (kTile / 4)], sc4.z);
+                                        add_codes(acc[ch], cw[(4 * k4 + 3) * (kTile / 4)], sc4.w);
+                                    };
+#pragma unroll 2
+                                    for (int k4 = 0; k4 < kG / 4; ++k4) four(k4);
                                 } else {
 #pragma unroll 4
                                     for (int k = 0; k < nr; ++k) {
