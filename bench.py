@@ -190,12 +190,12 @@ def measured_hbm_peak():
 # kernel and workload, with a hash of the kernel sources they were taken on;
 # reported as null once the sources change.
 TRAFFIC = {
-    ("adam_shard", "zero2_gpt2small_psi124439808_nd8_adamw_clip1"): {"bytes": 3.627e9, "src": "102303894aae"},
-    ("fused_step", "zero2_psi2p28_nd8"): {"bytes": 11.106e9, "src": "102303894aae"},
-    ("fused_step_qgather", "zero2_psi2p28_nd2_qgather"): {"bytes": 8.080e9, "src": "102303894aae"},
-    ("fused_step_qgz", "zero2_psi2p28_nd8_qgz"): {"bytes": 8.918e9, "src": "102303894aae"},
+    ("adam_shard", "zero2_gpt2small_psi124439808_nd8_adamw_clip1"): {"bytes": 3.628e9, "src": "c4265dd9bcab"},
+    ("fused_step", "zero2_psi2p28_nd8"): {"bytes": 11.109e9, "src": "c4265dd9bcab"},
+    ("fused_step_qgather", "zero2_psi2p28_nd2_qgather"): {"bytes": 8.080e9, "src": "c4265dd9bcab"},
+    ("fused_step_qgz", "zero2_psi2p28_nd8_qgz"): {"bytes": 8.918e9, "src": "c4265dd9bcab"},
     ("accumulate_grads", "zero2_gpt2small_psi124439808_nd8_adamw_clip1_accum4"): {"bytes": 2.950e9,
-                                                                                   "src": "102303894aae"},
+                                                                                   "src": "c4265dd9bcab"},
 }
 
 
@@ -718,8 +718,9 @@ def oracle_sample(w, budget_s, max_steps=None):
     workload: the same n_d, dtype and hyper-parameters on fewer parameters."""
     import numpy as np
     import oracle
-    psi = min(w["psi"], 4_000_000)
     n_d = w["n_d"]
+    # ~4M parameters at N_d = 8; fewer when a step reads more rank gradients
+    psi = min(w["psi"], 4_000_000 * 8 // max(8, n_d * w.get("accum", 1)))
     rng = np.random.default_rng(1)
     dt = oracle.FP16 if w["gdt"] == "fp16" else oracle.BF16
     scale = 1024.0 if w["ls"] else 1.0
@@ -760,7 +761,8 @@ def reference_arm(args, rank, world):
         return None
     for _ in range(args.warmup):
         oracle_sample(w, 0.0, max_steps=1)
-    psi, n_d, steps, el = oracle_sample(w, 0.0, max_steps=args.steps)
+    # exactly K steps of the sample (no time budget)
+    psi, n_d, steps, el = oracle_sample(w, float("inf"), max_steps=args.steps)
     value = psi * steps / el
     sample = "%d of %d params, n_d=%d, %d steps, single-threaded C oracle" % (psi, w["psi"], n_d, steps)
     return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
