@@ -1,0 +1,60 @@
+"""The benchmark's algorithmic bytes per parameter (the numerator of every
+roofline fraction it reports) against the closed forms of the method's
+minimum HBM traffic, workload by workload."""
+import os
+import sys
+
+import pytest
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+import bench  # noqa: E402
+
+
+def test_headline_clipped_step():
+    # reduce pass 2N_d + 4 (fp32 reduced gradient written), Adam pass 30
+    w = bench.workload(2)
+    assert (w["psi"], w["n_d"], w["clip"]) == (124_439_808, 8, 1.0)
+    assert w["bytes_per_param"] == (2 * 8 + 4) + 30 == 50
+
+
+@pytest.mark.parametrize("cfg,n_d,want", [(1, 4, 2 * 4 + 26), (3, 8, 2 * 8 + 26)])
+def test_fused_step(cfg, n_d, want):
+    w = bench.workload(cfg)
+    assert w["n_d"] == n_d and w["bytes_per_param"] == want
+
+
+@pytest.mark.parametrize("n_d", [2, 4, 8, 16, 64])
+def test_sweep_and_quantized_variants(n_d):
+    assert bench.workload(5, nd=n_d)["bytes_per_param"] == 2 * n_d + 26
+    # int8 gather: codes (1) + dequantized bf16 (2) instead of the plain param (2), one scale per 2048
+    assert bench.workload(5, nd=n_d, qgather=True)["bytes_per_param"] == 2 * n_d + 27 + 4.0 / 2048
+    # qgZ receiver: one int8 code and one fp32 scale per 2048 per rank
+    assert bench.workload(5, nd=n_d, qgz=True)["bytes_per_param"] == n_d * (1 + 4.0 / 2048) + 26
+
+
+@pytest.mark.parametrize("gathers", [1, 2])
+def test_zero3_layer(gathers):
+    w = bench.workload(4, gathers=gathers)
+    assert w["layers"] == 8 and w["psi"] == 218_112_000
+    # each gather reads a 16-bit shard and writes the gathered layer
+    assert w["bytes_per_param"] == 2 * 16 + 26 + 4 * gathers
+    assert w["psi_total"] == 8 * 218_112_000
+
+
+@pytest.mark.parametrize("k", [2, 4, 8])
+def test_accumulation(k):
+    # micro-batch 1 writes the fp32 accumulator, 2..k-1 read and write it,
+    # the clipped step at micro-batch k reads it in its reduce pass
+    w = bench.workload(2, accum=k)
+    n = w["n_d"]
+    assert w["bytes_per_param"] == (2 * n + 4) + (k - 2) * (2 * n + 8) + (2 * n + 38)
+    assert w["bytes_per_param"] == 2 * n * k + 8 * (k - 1) + 34
+    w1 = bench.workload(1, accum=k)
+    assert w1["bytes_per_param"] == 2 * 4 * k + 8 * (k - 1) + 26
+
+
+def test_variants_that_do_not_apply_are_refused():
+    with pytest.raises(SystemExit):
+        bench.workload(4, accum=2)
+    with pytest.raises(SystemExit):
+        bench.workload(2, overlap=True)
