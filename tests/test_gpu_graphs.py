@@ -1,6 +1,7 @@
-"""The fused step captured into a CUDA graph (after one eager call on the
-device, which caches the device attributes and kernel settings) replays with
-the same bits as eager calls."""
+"""The step's entry points captured into a CUDA graph (after one eager call
+on the device, which caches the device attributes and kernel settings) replay
+with the same bits as eager calls: the fused step, gradient accumulation, and
+the quantized gradient exchange (sender and receiver)."""
 import pytest
 import torch
 
@@ -41,3 +42,85 @@ def test_graph_replay_equals_eager(hp_kw):
     for a, b in ((eager.master, graphed.master), (eager.m, graphed.m), (eager.v, graphed.v), (eager.lp, graphed.lp)):
         assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
     assert eager.scalars_host().t == graphed.scalars_host().t == 4
+
+
+def _pair(psi, n_d, hp, stage=2):
+    plan = z.Plan(psi, n_d, stage=stage, shard_pad=8)
+    bufs = []
+    for _ in range(2):
+        b = z.StepBuffers(plan, hp, device="cuda")
+        b.master.copy_(synth.master_init(plan.padded, psi, seed=3, device="cuda"))
+        b.grads.copy_(synth.rank_grads(n_d, psi, 1e-2, seed=5, step=1, device="cuda",
+                                       row_pad=b.grads.shape[1] - psi))
+        b.init_scalars()
+        bufs.append(b)
+    return plan, bufs
+
+
+def _capture(fn):
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+    torch.cuda.current_stream().wait_stream(stream)
+    return g
+
+
+def _same(a, b):
+    for x, y in ((a.master, b.master), (a.m, b.m), (a.v, b.v), (a.lp, b.lp)):
+        assert torch.equal(x.view(torch.uint8), y.view(torch.uint8))
+
+
+def test_accumulation_in_a_graph():
+    # three micro-batches per step (two accumulations, then the step), twice
+    hp = z.hparams(lr=1e-3, weight_decay=0.1, max_norm=1.0)
+    plan, (eager, graphed) = _pair(300_007, 8, hp)
+
+    def one_step(b):
+        b.accumulate(first=True)
+        b.accumulate(first=False)
+        b.step_accum(hp, 3)
+
+    for b in (eager, graphed):
+        one_step(b)                                   # eager first calls
+    g = _capture(lambda: [one_step(graphed) for _ in range(2)])
+    for _ in range(2):
+        one_step(eager)
+    g.replay()
+    torch.cuda.synchronize()
+    _same(eager, graphed)
+    assert torch.equal(eager.acc, graphed.acc)
+    assert eager.scalars_host().t == graphed.scalars_host().t == 3
+
+
+def test_quantized_exchange_in_a_graph():
+    # sender and receiver of the int8 gradient exchange, twice per graph
+    hp = z.hparams(lr=1e-3)
+    n_d, psi = 8, 300_007
+    plan, (eager, graphed) = _pair(psi, n_d, hp)
+    nbs = -(-plan.shard // 2048)
+    wire = []
+    for _ in range(2):
+        codes = torch.zeros(n_d, (psi + 15) // 16 * 16, dtype=torch.int8, device="cuda")
+        scales = torch.zeros(n_d * nbs * ((n_d + 3) // 4 * 4), device="cuda")
+        wire.append((codes, scales))
+
+    def one_step(b, w):
+        codes, scales = w
+        z.zero_quantize_grads(plan.handle, b.rank_list(), 2048, [codes[r] for r in range(n_d)], scales, b.scalars)
+        z.zero_step_fused_qgz(plan.handle, hp, [codes[r] for r in range(n_d)], scales, 2048, b.master, b.m, b.v,
+                              b.master, b.m, b.v, b.lp, b.scalars)
+
+    one_step(eager, wire[0])
+    one_step(graphed, wire[1])
+    g = _capture(lambda: [one_step(graphed, wire[1]) for _ in range(2)])
+    for _ in range(2):
+        one_step(eager, wire[0])
+    g.replay()
+    torch.cuda.synchronize()
+    _same(eager, graphed)
+    assert torch.equal(wire[0][0], wire[1][0]) and torch.equal(wire[0][1], wire[1][1])
+    assert eager.scalars_host().t == graphed.scalars_host().t == 3
