@@ -681,7 +681,7 @@ cudaError_t launch_one_k(StreamArgs& a, cudaStream_t st)
     const int scale_bytes = (GT == kGradQ8) ? kChunksPerThread * kG * 4 : 0;
     a.stage_bytes = static_cast<unsigned>(slots * kTile * eb + scale_bytes + a.n_side_tma * kTile * 4);
     int stages = (di.smem_optin - kStageOffset) / static_cast<int>(a.stage_bytes);
-    if (stages > kMaxStages) stages = kMaxStages;
+    if (stages > kRingStages) stages = kRingStages;
     if (stages < 2) return cudaErrorInvalidConfiguration;
     a.stages = stages;
     const size_t smem = kStageOffset + static_cast<size_t>(stages) * a.stage_bytes;
