@@ -201,7 +201,7 @@ zero_status run_fused(const zero_plan* p, const zero_hparams* hp, const void* co
         a.out_f32[1] = m_out;
         a.out_f32[2] = vo;
         a.out_lp = lp;
-        a.flags = hi == p->psi ? flags : (flags & ~zk::F_EPILOGUE);
+        a.flags = (hi == p->psi ? flags : (flags & ~zk::F_EPILOGUE)) | (host_state ? zk::F_HOST_STATE : 0);
         set_accum(a, acc, 3);   // the carry is read directly, never staged
         const zero_status s = from_cuda(zk::launch_stream(zk::OP_FUSED, p->grad_dtype, p->param_dtype, a, st));
         if (s != ZERO_OK) return s;
@@ -228,7 +228,7 @@ zero_status run_adam(const zero_plan* p, const zero_hparams* hp, const float* g,
     a.out_f32[1] = m_out;
     a.out_f32[2] = vo;
     a.out_lp = lp;
-    a.flags = flags;
+    a.flags = flags | (host_state ? zk::F_HOST_STATE : 0);
     return from_cuda(zk::launch_stream(zk::OP_ADAM, p->grad_dtype, p->param_dtype, a, st));
 }
 

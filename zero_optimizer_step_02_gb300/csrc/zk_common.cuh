@@ -28,10 +28,12 @@ constexpr int kQuantBlock = kChunk * kConsumers;  // fused int8 gather: one bloc
 constexpr int kGroupRanks = 8;              // rank slices per pipeline stage
 constexpr int kMaxSide = 4;                 // fp32 side streams (g, master, m, v)
 constexpr int kMaxStages = 8;
-// Ring depth the engine uses: two stages measured faster than three for every
-// op (e.g. the clipped GPT-2-small step 95% -> 99.6% of the copy bandwidth);
-// 152 SMs x 2 stages already keep ~13 MB in flight, and more only adds L2 and
-// DRAM contention.
+// Ring depth the engine uses with its state in HBM: two stages measured
+// faster than three for every op (the clipped GPT-2-small step 0.980 ->
+// 0.940 ms); 152 SMs x 2 stages of up to 112 KB already keep ~20-34 MB in
+// flight, and more only adds L2 and DRAM contention.  With the state in host
+// memory the ring stages only the small reduced-gradient tiles and keeps the
+// deeper ring (up to kMaxStages), which that path measured faster with.
 constexpr int kRingStages = 2;
 constexpr int kStageOffset = 1024;          // dynamic smem bytes before the stage ring
 constexpr int kMaxPartials = 4096;          // per-CTA partial sums kept in the workspace
@@ -54,6 +56,7 @@ enum : int {
     F_RAW = 1 << 10,      // OP_REDUCE: store the sum itself, no division
     F_DEBUG_STARVE = 1 << 11,   // the producer issues no copy, so every consumer wait
                                 // runs out (tests the timeout path; nothing is read)
+    F_HOST_STATE = 1 << 12,     // master/m/v in page-locked host memory (launch shape only)
 };
 
 // ------------------------------------------------------------- PTX wrappers
