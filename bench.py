@@ -190,12 +190,12 @@ def measured_hbm_peak():
 # kernel and workload, with a hash of the kernel sources they were taken on;
 # reported as null once the sources change.
 TRAFFIC = {
-    ("adam_shard", "zero2_gpt2small_psi124439808_nd8_adamw_clip1"): {"bytes": 3.628e9, "src": "c4265dd9bcab"},
-    ("fused_step", "zero2_psi2p28_nd8"): {"bytes": 11.109e9, "src": "c4265dd9bcab"},
-    ("fused_step_qgather", "zero2_psi2p28_nd2_qgather"): {"bytes": 8.080e9, "src": "c4265dd9bcab"},
-    ("fused_step_qgz", "zero2_psi2p28_nd8_qgz"): {"bytes": 8.918e9, "src": "c4265dd9bcab"},
-    ("accumulate_grads", "zero2_gpt2small_psi124439808_nd8_adamw_clip1_accum4"): {"bytes": 2.950e9,
-                                                                                   "src": "c4265dd9bcab"},
+    ("adam_shard", "zero2_gpt2small_psi124439808_nd8_adamw_clip1"): {"bytes": 3.625e9, "src": "5245f4e1cfd2"},
+    ("fused_step", "zero2_psi2p28_nd8"): {"bytes": 11.102e9, "src": "5245f4e1cfd2"},
+    ("fused_step_qgather", "zero2_psi2p28_nd2_qgather"): {"bytes": 8.083e9, "src": "5245f4e1cfd2"},
+    ("fused_step_qgz", "zero2_psi2p28_nd8_qgz"): {"bytes": 8.917e9, "src": "5245f4e1cfd2"},
+    ("accumulate_grads", "zero2_gpt2small_psi124439808_nd8_adamw_clip1_accum4"): {"bytes": 2.952e9,
+                                                                                   "src": "5245f4e1cfd2"},
 }
 
 
