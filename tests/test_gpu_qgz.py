@@ -106,3 +106,40 @@ def test_receiver_on_grid_equals_the_plain_fused_step():
     torch.cuda.synchronize()
     assert torch.equal(a.master.view(torch.int32), b.master.view(torch.int32))
     assert torch.equal(a.lp.view(torch.int16), b.lp.view(torch.int16))
+
+
+@pytest.mark.parametrize("n_d,psi,pad", [(3, 50_001, 1), (16, 200_003, 16), (17, 70_001, 8), (64, 300_000, 16)])
+def test_receiver_decodes_every_byte(n_d, psi, pad):
+    # codes drawn over all 256 byte values (the sender never writes -128, but
+    # the receiver takes any int8 as its value) with random positive and zero
+    # scales: the decode of each byte and each scale product, bit for bit
+    hp = z.hparams(lr=1e-3)
+    plan = z.Plan(psi, n_d, stage=2, shard_pad=pad)
+    S = plan.shard
+    buf = z.StepBuffers(plan, hp, device="cuda")
+    master = synth.master_init(plan.padded, psi, seed=3)
+    buf.master.copy_(master.cuda())
+    buf.init_scalars()
+    st = oracle.State(master.numpy().copy(), np.zeros(plan.padded, np.float32), np.zeros(plan.padded, np.float32),
+                      oracle.new_scalars())
+    o_g = np.zeros(psi, np.uint16)
+    codes, scales, nbs = _codes_buffers(n_d, psi, S, 2048)
+    rng = np.random.default_rng(n_d * 1000 + psi)
+    oc = [rng.integers(-128, 128, size=psi).astype(np.int8) for _ in range(n_d)]
+    oc[0][:256] = np.arange(-128, 128, dtype=np.int8)
+    n_dp = oracle.qgz_rank_stride(n_d)
+    osc = np.zeros((n_d * nbs, n_dp), np.float32)
+    osc[:, :n_d] = np.exp(rng.uniform(-14.0, -6.0, size=(n_d * nbs, n_d))).astype(np.float32)
+    osc[:, :n_d][rng.random((n_d * nbs, n_d)) < 0.05] = 0.0
+    for q in range(n_d):
+        codes[q, :psi] = torch.from_numpy(oc[q]).cuda()
+    scales.copy_(torch.from_numpy(osc.reshape(-1)).cuda())
+    z.zero_step_fused_qgz(plan.handle, hp, [codes[r] for r in range(n_d)], scales, 2048, buf.master, buf.m, buf.v,
+                          buf.master, buf.m, buf.v, buf.lp, buf.scalars)
+    oracle.zero_step_qgz(oc, osc, 2048, oracle_hp(hp), st, pad, 2, psi, gathered=o_g)
+    torch.cuda.synchronize()
+    for a, b in ((buf.master, st.master), (buf.m, st.m), (buf.v, st.v)):
+        bad = np.flatnonzero(u32(a.cpu().numpy()) != u32(b))
+        assert bad.size == 0, "%d elements differ, first %s" % (bad.size, bad[:5])
+    assert np.array_equal(u16(buf.lp[:psi]), o_g)
+    assert buf.scalars_host().status == 0
