@@ -289,8 +289,25 @@ class Job:
                                    [self.codes[k][r] for r in range(self.w["n_d"])], self.qscales[k])
 
     def ranks(self, l):
-        g = self.grads[l % len(self.grads)]
-        return [g[r] for r in range(self.w["n_d"])]
+        """Gradient set l's rank rows as the pointer array the library reads
+        (built once: the sets never move)."""
+        if not hasattr(self, "_rank_ptrs"):
+            n_d = self.w["n_d"]
+            self._rank_ptrs = [self.z.rank_ptrs([g[r] for r in range(n_d)]) for g in self.grads]
+        return self._rank_ptrs[l % len(self.grads)]
+
+    def shard_ptrs(self, l):
+        """Layer l's 16-bit shards (ZeRO-3) as a pointer array, built once."""
+        if not hasattr(self, "_shard_ptrs"):
+            S, n_d = self.plan.shard, self.w["n_d"]
+            self._shard_ptrs = [self.z.rank_ptrs([x[r * S:(r + 1) * S] for r in range(n_d)]) for x in self.lp]
+        return self._shard_ptrs[l]
+
+    def code_ptrs(self, k):
+        if not hasattr(self, "_code_ptrs"):
+            n_d = self.w["n_d"]
+            self._code_ptrs = [self.z.rank_ptrs([c[r] for r in range(n_d)]) for c in self.codes]
+        return self._code_ptrs[k]
 
     def step(self):
         """One pass of the hot path through the public C ABI."""
@@ -305,15 +322,13 @@ class Job:
         for l in range(w["layers"]):
             gsel = l if w["layers"] > 1 else self.k
             if w["stage"] == 3:
-                S = self.plan.shard
                 # per-layer gather of the bf16 shards before use (itwiki: ZeRO-3
                 # gathers each layer for the forward pass and again for the backward)
                 for _ in range(w.get("gathers", 1)):
-                    z.zero_all_gather(h, [self.lp[l][r * S:(r + 1) * S] for r in range(w["n_d"])], self.gathered,
-                                      self.scalars)
+                    z.zero_all_gather(h, self.shard_ptrs(l), self.gathered, self.scalars)
             if w.get("qgz"):
                 k = gsel % len(self.grads)
-                z.zero_step_fused_qgz(h, self.hp, [self.codes[k][r] for r in range(w["n_d"])], self.qscales[k], 2048,
+                z.zero_step_fused_qgz(h, self.hp, self.code_ptrs(k), self.qscales[k], 2048,
                                       self.master[l], self.m[l], self.v[l], self.master[l], self.m[l], self.v[l],
                                       self.lp[l], self.scalars)
             elif w.get("qgather"):
@@ -339,7 +354,6 @@ class Job:
         layer's gather (which reads the shards the step overwrites)."""
         torch, z, w = self.torch, self.z, self.w
         h = self.plan.handle
-        S = self.plan.shard
         comp = torch.cuda.current_stream()
         gs = self.gather_stream
         bufs = (self.gathered, self.gathered2)
@@ -348,8 +362,7 @@ class Job:
             if self.ev_stepped[l] is not None:
                 gs.wait_event(self.ev_stepped[l])
             for _ in range(w.get("gathers", 1)):
-                z.zero_all_gather(h, [self.lp[l][r * S:(r + 1) * S] for r in range(w["n_d"])], bufs[l % 2],
-                                  self.scalars, gs)
+                z.zero_all_gather(h, self.shard_ptrs(l), bufs[l % 2], self.scalars, gs)
             self.ev_gathered[l].record(gs)
 
         gs.wait_stream(comp)

@@ -186,3 +186,19 @@ def test_gradient_accumulation_argument_checks(z):
     for acc, k in ((A, 1), (None, 2), (A, 0), (A, 65537)):
         assert _raw(z, "zero_step_fused_accum", p.handle, hpp, ranks, acc, k, A, A, A, A, A, A, A, A, A, None) == 1
     assert _raw(z, "zero_step_fused_accum", p.handle, hpp, ranks, A + 4, 2, A, A, A, A, A, A, A, A, A, None) == 2
+
+
+def test_prebuilt_rank_pointer_arrays(z):
+    # a pointer array built once by rank_ptrs goes through unchanged and
+    # reaches the same argument checks as a list of addresses
+    hp = z.hparams()
+    plan = z.Plan(1000, 2, stage=2)     # kept alive: its handle is freed with it
+    h = plan.handle
+    A, B = 0x10000, 0x20000
+    arr = z.rank_ptrs([A, B + 2])
+    assert list(arr) == [A, B + 2]
+    assert z._capi._ptr_array(arr) is arr
+    for ranks in (arr, [A, B + 2]):
+        with pytest.raises(z.ZeroError) as e:
+            z.zero_step_fused(h, hp, ranks, A, A, A, A, A, A, A, A, A, stream=0)
+        assert e.value.status == 2

@@ -22,9 +22,9 @@ from ._capi import (ZERO_BF16, ZERO_FP16, ZERO_DEV_TIMEOUT, ZeroDevScalars, Zero
                     zero_reduce_scatter, zero_scalars_init, zero_status_str, zero_step_fused,
                     zero_step_fused_noalloc, zero_step_fused_qgather, zero_workspace_bytes,
                     zero_quantize_grads, zero_step_fused_qgz, zero_step_fused_offload, zero_accumulate_grads,
-                    zero_step_fused_accum, zero_debug_stream_timeout)
+                    zero_step_fused_accum, zero_debug_stream_timeout, rank_ptrs)
 
-__all__ = ["Plan", "StepBuffers", "read_scalars", "row_len", "hparams", "ZeroError", "ZeroHparams",
+__all__ = ["Plan", "StepBuffers", "read_scalars", "row_len", "hparams", "rank_ptrs", "ZeroError", "ZeroHparams",
            "ZERO_BF16", "ZERO_FP16", "ZERO_DEV_TIMEOUT"] + [n for n in dir(_capi) if n.startswith("zero_")]
 
 
@@ -101,19 +101,27 @@ class StepBuffers:
     def rank_list(self):
         return [self.grads[r] for r in range(self.plan.n_d)]
 
+    def rank_ptrs(self):
+        """The ranks' rows as the pointer array the entry points read, built
+        once per grads tensor (again if grads is replaced)."""
+        key = (self.grads.data_ptr(), self.grads.stride(0))
+        if getattr(self, "_rank_key", None) != key:
+            self._rank_arr, self._rank_key = rank_ptrs(self.rank_list()), key
+        return self._rank_arr
+
     def init_scalars(self, loss_scale=1.0):
         zero_scalars_init(self.scalars, loss_scale)
 
     def step(self, hp, stream=None):
         """One fused step; with pingpong the state alternates between the two sets."""
         if self.pingpong:
-            zero_step_fused(self.plan.handle, hp, self.rank_list(), self.master, self.m, self.v, self.master2,
+            zero_step_fused(self.plan.handle, hp, self.rank_ptrs(), self.master, self.m, self.v, self.master2,
                             self.m2, self.v2, self.lp, self.scalars, self.ws, stream)
             self.master, self.master2 = self.master2, self.master
             self.m, self.m2 = self.m2, self.m
             self.v, self.v2 = self.v2, self.v
         else:
-            zero_step_fused(self.plan.handle, hp, self.rank_list(), self.master, self.m, self.v, self.master,
+            zero_step_fused(self.plan.handle, hp, self.rank_ptrs(), self.master, self.m, self.v, self.master,
                             self.m, self.v, self.lp, self.scalars, self.ws, stream)
 
     def accumulate(self, first, stream=None):
@@ -122,14 +130,14 @@ class StepBuffers:
         import torch
         if getattr(self, "acc", None) is None:
             self.acc = torch.zeros(self.plan.padded, dtype=torch.float32, device=self.master.device)
-        zero_accumulate_grads(self.plan.handle, self.rank_list(), None if first else self.acc, self.acc,
+        zero_accumulate_grads(self.plan.handle, self.rank_ptrs(), None if first else self.acc, self.acc,
                               self.scalars, stream)
 
     def step_accum(self, hp, micro_batches, stream=None):
         """The step at the last of micro_batches micro-batches (grads holds
         it; acc the sum of the earlier ones)."""
         acc = None if micro_batches == 1 else self.acc
-        zero_step_fused_accum(self.plan.handle, hp, self.rank_list(), acc, micro_batches, self.master, self.m,
+        zero_step_fused_accum(self.plan.handle, hp, self.rank_ptrs(), acc, micro_batches, self.master, self.m,
                               self.v, self.master, self.m, self.v, self.lp, self.scalars, self.ws, stream)
 
     def scalars_host(self):
