@@ -186,6 +186,11 @@ def measured_hbm_peak():
         return 6800.0, "fallback"
 
 
+# nominal HBM3e bandwidth of the part: a second denominator for the step's
+# fraction, beside the measured copy bandwidth that the roofline uses
+NOMINAL_HBM_GBS = 8000.0
+
+
 # ncu DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum), per
 # kernel and workload, with a hash of the kernel sources they were taken on;
 # reported as null once the sources change.
@@ -599,6 +604,7 @@ def gpu_arm(args, rank, world, device):
                       "parallelism": "replicas x%d" % world,
                       "l2": "flushed between steps" if small else "inputs larger than L2"},
            "step_gbs": round(step_gbs, 1), "step_frac_of_peak": round(step_gbs / peak, 4),
+           "step_frac_of_nominal": round(step_gbs / NOMINAL_HBM_GBS, 4),
            "roofline": roofline, "gpu_launches": int(launches), "e2e": e2e, "clocks": clk}
     if breakdown:
         out["kernel_ms"] = breakdown

@@ -41,6 +41,7 @@ def test_gpu_arm_line():
     r = d["roofline"]
     assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] > 0
     assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-3
+    assert abs(d["step_frac_of_nominal"] - d["step_gbs"] / 8000.0) < 1e-3
     assert d["config"]["l2"] == "flushed between steps"
     e = d["e2e"]
     assert e["value"] > 0 and e["h2d_bytes_per_step"] == 4 * 2 * 1_000_008 and e["d2h_bytes_per_step"] == 2 * 1_000_003
