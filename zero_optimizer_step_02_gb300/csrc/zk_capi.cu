@@ -95,14 +95,13 @@ void set_flat(StreamArgs& a, long long lo, long long hi)
     a.tma_ok = (lo % 8) == 0 ? 1 : 0;
 }
 
-StreamArgs base_args(const zero_plan* p, const zero_hparams* hp, zero_dev_scalars* sc)
+StreamArgs base_args(const zero_hparams* hp, zero_dev_scalars* sc)
 {
     StreamArgs a;
     std::memset(&a, 0, sizeof(a));
     a.sc = sc;
     a.timeout_ns = zk::kDefaultTimeoutNs;
     if (hp != nullptr) a.hp = *hp;
-    (void)p;
     return a;
 }
 
@@ -155,7 +154,7 @@ zero_status run_reduce(const zero_plan* p, const zero_hparams* hp, const void* c
                        bool sqnorm, void* ws, zero_dev_scalars* sc, cudaStream_t st, int* grid_out = nullptr,
                        const Accum& acc = kNoAccum)
 {
-    StreamArgs a = base_args(p, hp, sc);
+    StreamArgs a = base_args(hp, sc);
     set_ranks(a, p, ranks);
     set_flat(a, 0, p->psi);
     a.n_side = 0;
@@ -188,7 +187,7 @@ zero_status run_fused(const zero_plan* p, const zero_hparams* hp, const void* co
         (flags & (zk::F_CLIP | zk::F_GUARD | zk::F_DETECT | zk::F_FINALIZE)) ? p->psi : p->bucket;
     for (long long lo = 0; lo < p->psi; lo += step) {
         const long long hi = lo + step < p->psi ? lo + step : p->psi;
-        StreamArgs a = base_args(p, hp, sc);
+        StreamArgs a = base_args(hp, sc);
         if (flags & zk::F_FINALIZE) set_finalize(a, fin_ws, fin_n);
         set_ranks(a, p, ranks);
         set_flat(a, lo, hi);
@@ -214,7 +213,7 @@ zero_status run_adam(const zero_plan* p, const zero_hparams* hp, const float* g,
                      zero_dev_scalars* sc, cudaStream_t st, void* fin_ws = nullptr, int fin_n = 0,
                      bool host_state = false)
 {
-    StreamArgs a = base_args(p, hp, sc);
+    StreamArgs a = base_args(hp, sc);
     if (flags & zk::F_FINALIZE) set_finalize(a, fin_ws, fin_n);
     set_flat(a, 0, p->psi);
     a.n_ranks = 0;
@@ -549,7 +548,7 @@ ZERO_API zero_status zero_accumulate_grads(const zero_plan* p, const void* const
     }
     if (sc != nullptr && !aligned(sc, 256)) return ZERO_ERR_MISALIGNED;
     // the undivided sum: no loss scale, no guard; sc only reports a timeout
-    StreamArgs a = base_args(p, nullptr, sc);
+    StreamArgs a = base_args(nullptr, sc);
     set_ranks(a, p, ranks);
     set_flat(a, 0, p->psi);
     a.out_f32[0] = acc_out;
@@ -606,7 +605,7 @@ ZERO_API zero_status zero_step_fused_qgather(const zero_plan* p, const zero_hpar
     if ((s = check_dev(scales)) != ZERO_OK) return s;
     if ((s = check_dev(gathered)) != ZERO_OK) return s;
     const cudaStream_t st = as_stream(stream);
-    StreamArgs a = base_args(p, hp, sc);
+    StreamArgs a = base_args(hp, sc);
     set_ranks(a, p, ranks);
     // one tile per quantization block, blocks starting at each shard's first element
     a.base = 0;
@@ -665,7 +664,7 @@ ZERO_API zero_status zero_step_fused_qgz(const zero_plan* p, const zero_hparams*
     if ((s = check_dev(sc, 256)) != ZERO_OK) return s;
     if ((s = check_state(mi, m_in, vi, mo, m_out, vo)) != ZERO_OK) return s;
     if (lp != nullptr && !aligned(lp, 16)) return ZERO_ERR_MISALIGNED;
-    StreamArgs a = base_args(p, hp, sc);
+    StreamArgs a = base_args(hp, sc);
     a.n_ranks = p->n_d;
     for (int r = 0; r < p->n_d; ++r) a.rank[r] = codes[r];
     // tiles inside shards, so that every 2048-element block of a tile has one scale per rank
@@ -726,7 +725,7 @@ ZERO_API zero_status zero_debug_stream_timeout(int kernel, void* scratch, zero_d
     if (kernel != 0) return ZERO_ERR_INVALID_ARG;
     // one full tile of one bf16 rank: the consumers wait for a stage the
     // producer never fills
-    StreamArgs a = base_args(nullptr, nullptr, sc);
+    StreamArgs a = base_args(nullptr, sc);
     a.n_ranks = 1;
     a.rank[0] = scratch;
     set_flat(a, 0, zk::kTile);
