@@ -62,11 +62,19 @@ def workload(cfg, nd=None, qgather=False, psi=None, qgz=False, gathers=1, offloa
                  wd=0.0, clip=0.0, ls=False, layers=8, gathers=gathers)
     elif cfg == 5:
         n = nd or 8
-        w = dict(name="zero2_psi2p28_nd%d%s%s" % (n, "_qgather" if qgather else "", "_qgz" if qgz else ""),
-                 psi=1 << 28, n_d=n, stage=2, pad=16 if qgz else 8, gdt="bf16", sigma=1e-3, tail=False, lr=1e-3,
-                 b2=0.999, wd=0.0, clip=0.0, ls=False, layers=1, qgather=qgather, qgz=qgz)
+        w = dict(name="zero2_psi2p28_nd%d" % n, psi=1 << 28, n_d=n, stage=2, pad=8, gdt="bf16", sigma=1e-3,
+                 tail=False, lr=1e-3, b2=0.999, wd=0.0, clip=0.0, ls=False, layers=1)
     else:
         raise SystemExit("unknown config %r" % cfg)
+    if qgather or qgz:
+        # the ZeRO++ variants of the bf16 ZeRO-2 workloads: the int8 gather
+        # epilogue, or int8 codes + block scales as the ranks' gradients
+        if w["stage"] == 3 or w["gdt"] != "bf16" or (qgather and qgz):
+            raise SystemExit("--qgather or --qgz (one of them) applies to the bf16 ZeRO-2 workloads (configs 1, 2, 5)")
+        w["qgather"], w["qgz"] = qgather, qgz
+        w["name"] += "_qgather" if qgather else "_qgz"
+        if qgz:
+            w["pad"] = 16     # int8 shard slices start 16-byte aligned
     if psi:
         w["psi"] = int(psi)
         w["name"] += "_psi%d" % w["psi"]
@@ -97,15 +105,22 @@ def workload(cfg, nd=None, qgather=False, psi=None, qgz=False, gathers=1, offloa
         else:
             final = 2 * n_d + 30
         w["bytes_per_param"] = micro + final
+    elif w.get("qgz"):
+        # the receiver reads int8 codes + one fp32 scale per 2048 per rank;
+        # clipped, the reduce pass over them comes first, writing the fp32
+        # reduced gradient for the Adam pass when n_d > 4
+        q = n_d * (1 + 4.0 / 2048)
+        if w["clip"] > 0:
+            w["bytes_per_param"] = q + 34 if n_d > 4 else 2 * q + 26
+        else:
+            w["bytes_per_param"] = q + 26
+    elif w.get("qgather"):
+        # clipped: a read-only reduce pass, then the fused step re-reads the ranks
+        w["bytes_per_param"] = 2 * n_d + 27 + 4.0 / 2048 + (2 * n_d if w["clip"] > 0 else 0)
     elif w["clip"] > 0:
         w["bytes_per_param"] = 2 * n_d + 34 if n_d > 4 else 4 * n_d + 26
     elif w["stage"] == 3:
         w["bytes_per_param"] = 2 * n_d + 26 + 4 * w.get("gathers", 1)
-    elif w.get("qgather"):
-        w["bytes_per_param"] = 2 * n_d + 27 + 4.0 / 2048
-    elif w.get("qgz"):
-        # the receiver reads int8 codes + one fp32 scale per 2048 per rank
-        w["bytes_per_param"] = n_d * (1 + 4.0 / 2048) + 26
     else:
         w["bytes_per_param"] = 2 * n_d + 26
     w["psi_total"] = w["psi"] * w["layers"]
@@ -335,7 +350,7 @@ class Job:
                 k = gsel % len(self.grads)
                 z.zero_step_fused_qgz(h, self.hp, self.code_ptrs(k), self.qscales[k], 2048,
                                       self.master[l], self.m[l], self.v[l], self.master[l], self.m[l], self.v[l],
-                                      self.lp[l], self.scalars)
+                                      self.lp[l], self.scalars, self.ws)
             elif w.get("qgather"):
                 z.zero_step_fused_qgather(h, self.hp, self.ranks(gsel), self.master[l], self.m[l], self.v[l],
                                           self.master[l], self.m[l], self.v[l], 2048, self.codes, self.scales,
@@ -530,7 +545,7 @@ def gpu_arm(args, rank, world, device):
         t_fin = statistics.mean(ev[1].elapsed_time(ev[2]) for ev in evs[1:])
         kernel, kms, kbytes = "accumulate_grads", t_acc, (2 * w["n_d"] + 8) * w["psi"]
         breakdown = {"accumulate_grads": round(t_acc, 4), "step_accum": round(t_fin, 4)}
-    elif w["clip"] > 0 and w["n_d"] > 4 and not w.get("offload"):
+    elif w["clip"] > 0 and w["n_d"] > 4 and not (w.get("offload") or w.get("qgz") or w.get("qgather")):
         job.ghat = torch.zeros(job.plan.padded, device=device)
         n_rep = min(max(3, args.steps), 50)
         dur = [0.0, 0.0, 0.0]
@@ -552,6 +567,8 @@ def gpu_arm(args, rank, world, device):
         breakdown = {names[i]: round(dur[i], 4) for i in range(3)}
     else:
         kernel = "fused_step_qgather" if w.get("qgather") else ("fused_step_qgz" if w.get("qgz") else "fused_step")
+        if w["clip"] > 0:
+            kernel = "clipped_" + kernel     # both passes of the clipped step
         kms = ms_per_step / w["layers"] if w["stage"] != 3 else None
         if w["stage"] == 3:
             # time the per-layer fused step alone
@@ -709,7 +726,8 @@ def e2e_measure(job, w, args, device, world):
         if qgz:
             codes, scales = dev_sets[i % 2]
             z.zero_step_fused_qgz(h, job.hp, [codes[r] for r in range(w["n_d"])], scales, 2048, job.master[0],
-                                  job.m[0], job.v[0], job.master[0], job.m[0], job.v[0], job.lp[0], job.scalars)
+                                  job.m[0], job.v[0], job.master[0], job.m[0], job.v[0], job.lp[0], job.scalars,
+                                  job.ws)
         elif k > 1 and mu < k - 1:
             z.zero_accumulate_grads(h, job.ranks(i % 2), None if mu == 0 else job.acc, job.acc, job.scalars)
         elif k > 1:
@@ -760,6 +778,10 @@ def oracle_sample(w, budget_s, max_steps=None):
                 acc = oracle.accumulate_grads(rows, dt, acc)
             oracle.zero_step_accum(rows, dt, acc, w["accum"], hp, st, w["pad"], min(w["stage"], 3), lp_shards=lp,
                                    gathered=gath)
+        elif w.get("qgather"):
+            # the step with its 16-bit output sharded, then the block-int8 gather of the shards
+            oracle.zero_step(rows, dt, hp, st, w["pad"], 3, lp_shards=lp, gathered=gath)
+            oracle.quant_gather(lp, n_d, psi, S, 2048)
         elif w.get("qgz"):
             codes, scales = oracle.quantize_ranks(rows, psi, S, 2048)
             oracle.zero_step_qgz(codes, scales, 2048, hp, st, w["pad"], min(w["stage"], 3), psi, lp_shards=lp,

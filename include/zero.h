@@ -49,7 +49,7 @@
 extern "C" {
 #endif
 
-#define ZERO_ABI_VERSION 1
+#define ZERO_ABI_VERSION 2
 #define ZERO_MAX_RANKS 256      /* largest n_d */
 #define ZERO_MAX_SHARD_PAD 4096 /* largest shard_pad */
 #define ZERO_MAX_MICRO_BATCHES 65536 /* largest gradient-accumulation count */
@@ -301,10 +301,17 @@ ZERO_API zero_status zero_quant_gather(const zero_plan* plan, const void* shards
                                        signed char* codes_out, float* scales_out,
                                        void* gathered_bf16, void* stream);
 
-/* The fused step of zero_step_fused (no clipping, no loss scaling) whose
- * epilogue is the quantized gather above instead of the plain 16-bit write:
- * codes, scales and dequantized bf16 gathered values come from the updated
- * master of each block (block must be 2048; parameter dtype bf16).           */
+/* The fused step of zero_step_fused whose epilogue is the quantized gather
+ * above instead of the plain 16-bit write: codes, scales and dequantized bf16
+ * gathered values come from the updated master of each block (block must be
+ * 2048; parameter dtype bf16).  With clipping or loss scaling a read-only
+ * reduce pass comes first (squared-norm partials and the non-finite flag, in
+ * ws: zero_workspace_bytes(plan, hp) bytes, 256-byte aligned); the update
+ * pass then re-reads the rank gradients, finishes the norm in its prologue,
+ * and with the flag set writes nothing (state, codes, scales and gathered
+ * values keep the last step's) while the scalar epilogue halves the scale.
+ * Loss scaling needs the state in place (master_out == master_in, likewise
+ * m, v), else ZERO_ERR_UNSUPPORTED.  ws may be NULL with neither.           */
 ZERO_API zero_status zero_step_fused_qgather(const zero_plan* plan, const zero_hparams* hp,
                                              const void* const* rank_grads,
                                              const float* master_in, const float* m_in,
@@ -343,13 +350,19 @@ ZERO_API zero_status zero_quantize_grads(const zero_plan* plan, const void* cons
 /* Receiver side, fused: zero_step_fused with the ranks' int8 codes and
  * scales (layout as above, block 2048) in place of their 16-bit gradients:
  *   g[j] = (sum over q in order, from +0.0f, of (float)code_q[j] * scale_q(j)) / n_d
- * then Adam, cast and gather as in zero_step_fused.  No clipping and no loss
- * scaling in this entry point (ZERO_ERR_UNSUPPORTED).                       */
+ * then Adam, cast and gather as in zero_step_fused.  With clipping
+ * (hp->max_norm > 0) the schedule is zero_step_fused's: a reduce pass over the
+ * codes writes the squared-norm partials (and, for n_d > 4, the reduced
+ * gradient) into ws, and the update pass finishes the norm in its prologue.
+ * ws: zero_workspace_bytes(plan, hp) bytes, 256-byte aligned, required with
+ * clipping, unused (may be NULL) without.  Loss scaling is refused
+ * (ZERO_ERR_UNSUPPORTED): the sender takes bf16 gradients, which need none. */
 ZERO_API zero_status zero_step_fused_qgz(const zero_plan* plan, const zero_hparams* hp,
                                          const signed char* const* rank_codes, const float* rank_scales,
                                          int block, const float* master_in, const float* m_in,
                                          const float* v_in, float* master_out, float* m_out, float* v_out,
-                                         void* lp_out, zero_dev_scalars* scalars_dev, void* stream);
+                                         void* lp_out, zero_dev_scalars* scalars_dev, void* ws,
+                                         void* stream);
 
 /* ----------------------------------------------------------- diagnostics --- */
 /* Launch one kernel that waits on a barrier nothing completes, with a wait

@@ -74,24 +74,30 @@ class Job:
     def oracle_lp(self):
         return self.o_lp_shards if self.stage == 3 else self.o_gathered
 
-    def assert_bit_exact(self):
+    def assert_bit_exact(self, lp=True):
+        """master/m/v bit for bit, and the 16-bit parameters unless lp=False
+        (a step whose epilogue writes another output)."""
         gm, gmm, gv, glp = self.gpu_state()
         for name, a, b in (("master", gm, self.ost.master), ("m", gmm, self.ost.m), ("v", gv, self.ost.v)):
             bad = np.flatnonzero(u32(a) != u32(b))
             assert bad.size == 0, "%s differs at %d places, first %s: gpu %r oracle %r" % (
                 name, bad.size, bad[:5], a[bad[:5]], b[bad[:5]])
+        if not lp:
+            return
         olp = self.oracle_lp()
         bad = np.flatnonzero(glp != olp[: glp.size])
         assert bad.size == 0, "16-bit params differ at %d places, first %s" % (bad.size, bad[:5])
 
-    def assert_within_tolerance(self, rel=1e-6, lp_ulp=1):
+    def assert_within_tolerance(self, rel=1e-6, lp_ulp=1, lp=True):
         """The stated tolerance: per array max|gpu - cpu| / max|cpu| <= rel,
-        16-bit parameters within lp_ulp units in the last place."""
+        16-bit parameters (unless lp=False) within lp_ulp units in the last place."""
         gm, gmm, gv, glp = self.gpu_state()
         for name, a, b in (("master", gm, self.ost.master), ("m", gmm, self.ost.m), ("v", gv, self.ost.v)):
             denom = max(float(np.max(np.abs(b))), 1e-30)
             err = float(np.max(np.abs(a.astype(np.float64) - b.astype(np.float64)))) / denom
             assert err <= rel, "%s relative error %.3g > %.1g" % (name, err, rel)
+        if not lp:
+            return
         olp = self.oracle_lp()[: glp.size]
         # 16-bit patterns of same-sign values are ordered like the values
         d = np.abs(glp.astype(np.int64) - olp.astype(np.int64))

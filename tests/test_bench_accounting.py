@@ -53,7 +53,28 @@ def test_accumulation(k):
     assert w1["bytes_per_param"] == 2 * 4 * k + 8 * (k - 1) + 26
 
 
+@pytest.mark.parametrize("cfg,n_d,clip", [(2, 8, True), (1, 4, False)])
+def test_quantized_variants_of_the_other_zero2_workloads(cfg, n_d, clip):
+    q = n_d * (1 + 4.0 / 2048)
+    # clipped qgZ with n_d > 4: reduce pass over codes + scales writing the fp32
+    # reduced gradient (4), then the Adam pass (30)
+    assert bench.workload(cfg, qgz=True)["bytes_per_param"] == (q + 34 if clip else q + 26)
+    # clipped int8 gather: a read-only reduce pass (2 n_d) before the fused step
+    want = 2 * n_d + 27 + 4.0 / 2048 + (2 * n_d if clip else 0)
+    assert bench.workload(cfg, qgather=True)["bytes_per_param"] == want
+
+
+def test_quantized_variant_names():
+    # the names key the stored ncu traffic of the N_d sweep
+    assert bench.workload(5, nd=2, qgather=True)["name"] == "zero2_psi2p28_nd2_qgather"
+    assert bench.workload(5, nd=8, qgz=True)["name"] == "zero2_psi2p28_nd8_qgz"
+    assert bench.workload(2, qgz=True)["name"] == "zero2_gpt2small_psi124439808_nd8_adamw_clip1_qgz"
+
+
 def test_variants_that_do_not_apply_are_refused():
+    for cfg, kw in ((3, dict(qgz=True)), (4, dict(qgather=True)), (5, dict(qgz=True, qgather=True))):
+        with pytest.raises(SystemExit):
+            bench.workload(cfg, **kw)
     with pytest.raises(SystemExit):
         bench.workload(4, accum=2)
     with pytest.raises(SystemExit):

@@ -39,7 +39,7 @@ def test_every_declared_symbol_is_exported(z):
 
 
 def test_abi_and_struct_layout(z):
-    assert z.zero_abi_version() == 1
+    assert z.zero_abi_version() == 2
     assert z.zero_dev_scalars_size() == ctypes.sizeof(z.ZeroDevScalars) == 64
     assert z.zero_status_str(0) == "ok"
     assert "misaligned" in z.zero_status_str(2)
@@ -135,7 +135,11 @@ def test_calls_check_arguments_before_touching_the_device(z):
     assert _raw(z, "zero_quant_gather", h, A, 31, A, A, A, None) == 1
     assert _raw(z, "zero_quant_gather", h, A, 70000, A, A, A, None) == 1
     assert _raw(z, "zero_step_fused_qgather", h, hpp, ranks_ok, A, A, A, A, A, A, 1024, A, A, A, A, A, None) == 3
+    # clipping or loss scaling need the workspace; loss scaling needs the state in place
     assert _raw(z, "zero_step_fused_qgather", h, ctypes.byref(clip), ranks_ok, A, A, A, A, A, A, 2048, A, A, A,
+                A, None, None) == 1
+    lsc = z.hparams(loss_scaling=True)
+    assert _raw(z, "zero_step_fused_qgather", h, ctypes.byref(lsc), ranks_ok, A, A, A, B, B, B, 2048, A, A, A,
                 A, A, None) == 3
     # the timeout probe rejects limits outside (0, 10 s]
     assert _raw(z, "zero_debug_wait_timeout", A, 0, None) == 1
@@ -165,9 +169,15 @@ def test_quantized_gradient_exchange_argument_checks(z):
     p16 = z.Plan(1000, 2, stage=2, grad_dtype=z.ZERO_FP16)
     assert _raw(z, "zero_quantize_grads", p16.handle, ranks, 2048, ranks, A, None, None) == 3
     assert _raw(z, "zero_step_fused_qgz", p.handle, ctypes.byref(hp), ranks, A, 1024, A, A, A, A, A, A, A, A,
-                None) == 3
+                None, None) == 3
+    # clipping needs the workspace; bf16 gradients take no loss scaling
     assert _raw(z, "zero_step_fused_qgz", p.handle, ctypes.byref(clip), ranks, A, 2048, A, A, A, A, A, A, A, A,
-                None) == 3
+                None, None) == 1
+    assert _raw(z, "zero_step_fused_qgz", p.handle, ctypes.byref(clip), ranks, A, 2048, A, A, A, A, A, A, A, A,
+                A + 16, None) == 2
+    lsc = z.hparams(loss_scaling=True)
+    assert _raw(z, "zero_step_fused_qgz", p.handle, ctypes.byref(lsc), ranks, A, 2048, A, A, A, A, A, A, A, A,
+                A, None) == 3
 
 
 def test_gradient_accumulation_argument_checks(z):

@@ -84,7 +84,7 @@ _SIGS = {
     "zero_step_fused_offload": (_i32, [_vp, _hp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "zero_accumulate_grads": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp]),
     "zero_step_fused_accum": (_i32, [_vp, _hp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
-    "zero_step_fused_qgz": (_i32, [_vp, _hp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "zero_step_fused_qgz": (_i32, [_vp, _hp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -270,10 +270,11 @@ def zero_quantize_grads(plan, rank_grads, block, rank_codes, rank_scales, scalar
 
 
 def zero_step_fused_qgz(plan, hp, rank_codes, rank_scales, block, master_in, m_in, v_in, master_out, m_out, v_out,
-                        lp_out, scalars, stream=None):
+                        lp_out, scalars, ws=None, stream=None):
+    """ws: the workspace, needed with clipping (None otherwise)."""
     _check(_lib.zero_step_fused_qgz(plan, ctypes.byref(hp), _ptr_array(rank_codes), _addr(rank_scales), block,
                                     _addr(master_in), _addr(m_in), _addr(v_in), _addr(master_out), _addr(m_out),
-                                    _addr(v_out), _addr(lp_out), _addr(scalars), _stream(stream)),
+                                    _addr(v_out), _addr(lp_out), _addr(scalars), _addr(ws), _stream(stream)),
            "zero_step_fused_qgz")
 
 

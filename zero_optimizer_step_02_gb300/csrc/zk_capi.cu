@@ -231,6 +231,63 @@ zero_status run_adam(const zero_plan* p, const zero_hparams* hp, const float* g,
     return from_cuda(zk::launch_stream(zk::OP_ADAM, p->grad_dtype, p->param_dtype, a, st));
 }
 
+// int8 rank streams (the quantized gradient exchange): tiles inside shards,
+// so that every 2048-element block of a tile has one scale per rank
+void set_q8_ranks(StreamArgs& a, const zero_plan* p, const signed char* const* codes, const float* scales)
+{
+    a.n_ranks = p->n_d;
+    for (int r = 0; r < p->n_d; ++r) a.rank[r] = codes[r];
+    a.base = 0;
+    a.seg_stride = p->shard;
+    a.seg_len = p->shard;
+    a.limit = p->psi;
+    a.n_seg = p->n_d;
+    a.tiles_per_seg = tiles_of(p->shard);
+    a.q_blocks_per_shard = (p->shard + zk::kQuantBlock - 1) / zk::kQuantBlock;
+    a.q_rank_scales = scales;
+    a.q_rank_scale_stride = (p->n_d + 3) / 4 * 4;
+    a.tma_ok = (p->shard % 16) == 0 ? 1 : 0;   // int8 slices start 16-byte aligned
+}
+
+// reduce pass over int8 ranks: squared-norm partials, optional fp32 output
+zero_status run_reduce_q8(const zero_plan* p, const zero_hparams* hp, const signed char* const* codes,
+                          const float* scales, float* out, void* ws, zero_dev_scalars* sc, cudaStream_t st,
+                          int* grid_out)
+{
+    StreamArgs a = base_args(hp, sc);
+    set_q8_ranks(a, p, codes, scales);
+    a.n_side = 0;
+    a.out_f32[0] = out;
+    a.partials = partials_of(ws);
+    a.flags = zk::F_SQNORM;
+    const zero_status s = from_cuda(zk::launch_stream(zk::OP_REDUCE, zk::kGradQ8, p->param_dtype, a, st));
+    *grid_out = a.grid;
+    return s;
+}
+
+// the fused step over int8 ranks (flags: F_EPILOGUE, and F_CLIP | F_FINALIZE
+// after a reduce pass whose partials are in ws)
+zero_status run_fused_q8(const zero_plan* p, const zero_hparams* hp, const signed char* const* codes,
+                         const float* scales, const float* mi, const float* m_in, const float* vi, float* mo,
+                         float* m_out, float* vo, void* lp, int flags, zero_dev_scalars* sc, cudaStream_t st,
+                         void* fin_ws = nullptr, int fin_n = 0)
+{
+    StreamArgs a = base_args(hp, sc);
+    if (flags & zk::F_FINALIZE) set_finalize(a, fin_ws, fin_n);
+    set_q8_ranks(a, p, codes, scales);
+    a.n_side = 3;
+    a.n_side_tma = 3;
+    a.side[0] = mi;
+    a.side[1] = m_in;
+    a.side[2] = vi;
+    a.out_f32[0] = mo;
+    a.out_f32[1] = m_out;
+    a.out_f32[2] = vo;
+    a.out_lp = lp;
+    a.flags = flags;
+    return from_cuda(zk::launch_stream(zk::OP_FUSED, zk::kGradQ8, p->param_dtype, a, st));
+}
+
 zero_status check_state(const float* mi, const float* m_in, const float* vi, float* mo, float* m_out, float* vo)
 {
     const void* ptrs[] = {mi, m_in, vi, mo, m_out, vo};
@@ -591,21 +648,37 @@ ZERO_API zero_status zero_step_fused_qgather(const zero_plan* p, const zero_hpar
                                              void* gathered, zero_dev_scalars* sc, void* ws, void* stream)
 {
     ZK_CALL_RANGE();
-    (void)ws;
     if (p == nullptr) return ZERO_ERR_INVALID_ARG;
     zero_status s;
     if ((s = check_hparams(hp)) != ZERO_OK) return s;
     if (block != zk::kQuantBlock) return ZERO_ERR_UNSUPPORTED;
-    if (hp->max_norm > 0.0f || hp->loss_scaling) return ZERO_ERR_UNSUPPORTED;
     if (p->param_dtype != ZERO_BF16) return ZERO_ERR_UNSUPPORTED;
+    const bool clip = hp->max_norm > 0.0f;
+    const bool ls = hp->loss_scaling != 0;
+    // loss scaling takes the guarded schedule, which leaves a skipped step's
+    // state where it is: in place only
+    if (ls && mo != mi) return ZERO_ERR_UNSUPPORTED;
     if ((s = check_ranks(p, ranks)) != ZERO_OK) return s;
     if ((s = check_dev(sc, 256)) != ZERO_OK) return s;
     if ((s = check_state(mi, m_in, vi, mo, m_out, vo)) != ZERO_OK) return s;
     if ((s = check_dev(codes)) != ZERO_OK) return s;
     if ((s = check_dev(scales)) != ZERO_OK) return s;
     if ((s = check_dev(gathered)) != ZERO_OK) return s;
+    if ((clip || ls) && (s = check_dev(ws, 256)) != ZERO_OK) return s;
     const cudaStream_t st = as_stream(stream);
+    int flags = zk::F_QUANT | zk::F_EPILOGUE;
+    int n = 0;
+    if (clip || ls) {
+        // a read-only reduce pass first: the squared-norm partials (clipping)
+        // and the non-finite flag (loss scaling); the update pass re-reads the
+        // rank gradients, finishes the norm in its prologue and writes nothing
+        // when the flag is set
+        if ((s = run_reduce(p, hp, ranks, nullptr, clip, ws, sc, st, &n)) != ZERO_OK) return s;
+        if (clip) flags |= zk::F_CLIP | zk::F_FINALIZE;
+        if (ls) flags |= zk::F_GUARD | zk::F_LSCALE;
+    }
     StreamArgs a = base_args(hp, sc);
+    if (flags & zk::F_FINALIZE) set_finalize(a, ws, n);
     set_ranks(a, p, ranks);
     // one tile per quantization block, blocks starting at each shard's first element
     a.base = 0;
@@ -627,7 +700,7 @@ ZERO_API zero_status zero_step_fused_qgather(const zero_plan* p, const zero_hpar
     a.q_codes = codes;
     a.q_scales = scales;
     a.q_gathered = gathered;
-    a.flags = zk::F_QUANT | zk::F_EPILOGUE;
+    a.flags = flags;
     return from_cuda(zk::launch_stream(zk::OP_QFUSED, p->grad_dtype, p->param_dtype, a, st));
 }
 
@@ -651,44 +724,34 @@ ZERO_API zero_status zero_quantize_grads(const zero_plan* p, const void* const* 
 ZERO_API zero_status zero_step_fused_qgz(const zero_plan* p, const zero_hparams* hp, const signed char* const* codes,
                                          const float* scales, int block, const float* mi, const float* m_in,
                                          const float* vi, float* mo, float* m_out, float* vo, void* lp,
-                                         zero_dev_scalars* sc, void* stream)
+                                         zero_dev_scalars* sc, void* ws, void* stream)
 {
     ZK_CALL_RANGE();
     if (p == nullptr) return ZERO_ERR_INVALID_ARG;
     zero_status s;
     if ((s = check_hparams(hp)) != ZERO_OK) return s;
     if (block != zk::kQuantBlock) return ZERO_ERR_UNSUPPORTED;
-    if (hp->max_norm > 0.0f || hp->loss_scaling) return ZERO_ERR_UNSUPPORTED;
+    if (hp->loss_scaling) return ZERO_ERR_UNSUPPORTED;
     if ((s = check_ranks(p, reinterpret_cast<const void* const*>(codes))) != ZERO_OK) return s;
     if ((s = check_dev(scales)) != ZERO_OK) return s;
     if ((s = check_dev(sc, 256)) != ZERO_OK) return s;
     if ((s = check_state(mi, m_in, vi, mo, m_out, vo)) != ZERO_OK) return s;
     if (lp != nullptr && !aligned(lp, 16)) return ZERO_ERR_MISALIGNED;
-    StreamArgs a = base_args(hp, sc);
-    a.n_ranks = p->n_d;
-    for (int r = 0; r < p->n_d; ++r) a.rank[r] = codes[r];
-    // tiles inside shards, so that every 2048-element block of a tile has one scale per rank
-    a.base = 0;
-    a.seg_stride = p->shard;
-    a.seg_len = p->shard;
-    a.limit = p->psi;
-    a.n_seg = p->n_d;
-    a.tiles_per_seg = tiles_of(p->shard);
-    a.q_blocks_per_shard = (p->shard + zk::kQuantBlock - 1) / zk::kQuantBlock;
-    a.q_rank_scales = scales;
-    a.q_rank_scale_stride = (p->n_d + 3) / 4 * 4;
-    a.tma_ok = (p->shard % 16) == 0 ? 1 : 0;   // int8 slices start 16-byte aligned
-    a.n_side = 3;
-    a.n_side_tma = 3;
-    a.side[0] = mi;
-    a.side[1] = m_in;
-    a.side[2] = vi;
-    a.out_f32[0] = mo;
-    a.out_f32[1] = m_out;
-    a.out_f32[2] = vo;
-    a.out_lp = lp;
-    a.flags = zk::F_EPILOGUE;
-    return from_cuda(zk::launch_stream(zk::OP_FUSED, zk::kGradQ8, p->param_dtype, a, as_stream(stream)));
+    const bool clip = hp->max_norm > 0.0f;
+    if (clip && (s = check_dev(ws, 256)) != ZERO_OK) return s;
+    const cudaStream_t st = as_stream(stream);
+    if (!clip) return run_fused_q8(p, hp, codes, scales, mi, m_in, vi, mo, m_out, vo, lp, zk::F_EPILOGUE, sc, st);
+    // clipped: the schedule of zero_step_fused, its reduce pass over the codes
+    int n = 0;
+    if (clip_materialises(p)) {
+        float* g = ghat_of(ws);
+        if ((s = run_reduce_q8(p, hp, codes, scales, g, ws, sc, st, &n)) != ZERO_OK) return s;
+        return run_adam(p, hp, g, mi, m_in, vi, mo, m_out, vo, lp,
+                        zk::F_CLIP | zk::F_FINALIZE | zk::F_EPILOGUE | zk::F_REVERSE, sc, st, ws, n);
+    }
+    if ((s = run_reduce_q8(p, hp, codes, scales, nullptr, ws, sc, st, &n)) != ZERO_OK) return s;
+    return run_fused_q8(p, hp, codes, scales, mi, m_in, vi, mo, m_out, vo, lp,
+                        zk::F_CLIP | zk::F_FINALIZE | zk::F_EPILOGUE, sc, st, ws, n);
 }
 
 ZERO_API zero_status zero_debug_wait_timeout(zero_dev_scalars* sc, long long timeout_ns, void* stream)
