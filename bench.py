@@ -68,11 +68,11 @@ def workload(cfg, nd=None, qgather=False, psi=None, qgz=False, gathers=1, offloa
         raise SystemExit("unknown config %r" % cfg)
     if qgather or qgz:
         # the ZeRO++ variants of the bf16 ZeRO-2 workloads: the int8 gather
-        # epilogue, or int8 codes + block scales as the ranks' gradients
-        if w["stage"] == 3 or w["gdt"] != "bf16" or (qgather and qgz):
-            raise SystemExit("--qgather or --qgz (one of them) applies to the bf16 ZeRO-2 workloads (configs 1, 2, 5)")
+        # epilogue, int8 codes + block scales as the ranks' gradients, or both
+        if w["stage"] == 3 or w["gdt"] != "bf16":
+            raise SystemExit("--qgather and --qgz apply to the bf16 ZeRO-2 workloads (configs 1, 2, 5)")
         w["qgather"], w["qgz"] = qgather, qgz
-        w["name"] += "_qgather" if qgather else "_qgz"
+        w["name"] += ("_qgz" if qgz else "") + ("_qgather" if qgather else "")
         if qgz:
             w["pad"] = 16     # int8 shard slices start 16-byte aligned
     if psi:
@@ -105,6 +105,11 @@ def workload(cfg, nd=None, qgather=False, psi=None, qgz=False, gathers=1, offloa
         else:
             final = 2 * n_d + 30
         w["bytes_per_param"] = micro + final
+    elif w.get("qgz") and w.get("qgather"):
+        # int8 codes in, int8 gather out; clipped, a read-only reduce pass
+        # over the codes first
+        q = n_d * (1 + 4.0 / 2048)
+        w["bytes_per_param"] = q + 27 + 4.0 / 2048 + (q if w["clip"] > 0 else 0)
     elif w.get("qgz"):
         # the receiver reads int8 codes + one fp32 scale per 2048 per rank;
         # clipped, the reduce pass over them comes first, writing the fp32
@@ -285,8 +290,8 @@ class Job:
             self.ev_stepped = [None] * w["layers"]
         if w.get("qgather"):
             nbs = -(-self.plan.shard // 2048)
-            self.codes = torch.zeros(n, dtype=torch.int8, device=device)
-            self.scales = torch.zeros(w["n_d"] * nbs, device=device)
+            self.gq_codes = torch.zeros(n, dtype=torch.int8, device=device)
+            self.gq_scales = torch.zeros(w["n_d"] * nbs, device=device)
         if w.get("qgz"):
             # the int8 wire format of every gradient set (sender pass, untimed here)
             nbs = -(-self.plan.shard // 2048)
@@ -346,14 +351,19 @@ class Job:
                 # gathers each layer for the forward pass and again for the backward)
                 for _ in range(w.get("gathers", 1)):
                     z.zero_all_gather(h, self.shard_ptrs(l), self.gathered, self.scalars)
-            if w.get("qgz"):
+            if w.get("qgz") and w.get("qgather"):
+                k = gsel % len(self.grads)
+                z.zero_step_fused_qgz_qgather(h, self.hp, self.code_ptrs(k), self.qscales[k], 2048, self.master[l],
+                                              self.m[l], self.v[l], self.master[l], self.m[l], self.v[l],
+                                              self.gq_codes, self.gq_scales, self.lp[l], self.scalars, self.ws)
+            elif w.get("qgz"):
                 k = gsel % len(self.grads)
                 z.zero_step_fused_qgz(h, self.hp, self.code_ptrs(k), self.qscales[k], 2048,
                                       self.master[l], self.m[l], self.v[l], self.master[l], self.m[l], self.v[l],
                                       self.lp[l], self.scalars, self.ws)
             elif w.get("qgather"):
                 z.zero_step_fused_qgather(h, self.hp, self.ranks(gsel), self.master[l], self.m[l], self.v[l],
-                                          self.master[l], self.m[l], self.v[l], 2048, self.codes, self.scales,
+                                          self.master[l], self.m[l], self.v[l], 2048, self.gq_codes, self.gq_scales,
                                           self.lp[l], self.scalars, self.ws)
             elif self.pingpong:
                 z.zero_step_fused(h, self.hp, self.ranks(gsel), self.master[l], self.m[l], self.v[l],
@@ -566,7 +576,7 @@ def gpu_arm(args, rank, world, device):
         kernel, kms, kbytes = names[k], dur[k], per_param[k] * w["psi"]
         breakdown = {names[i]: round(dur[i], 4) for i in range(3)}
     else:
-        kernel = "fused_step_qgather" if w.get("qgather") else ("fused_step_qgz" if w.get("qgz") else "fused_step")
+        kernel = "fused_step" + ("_qgz" if w.get("qgz") else "") + ("_qgather" if w.get("qgather") else "")
         if w["clip"] > 0:
             kernel = "clipped_" + kernel     # both passes of the clipped step
         kms = ms_per_step / w["layers"] if w["stage"] != 3 else None
@@ -724,10 +734,8 @@ def e2e_measure(job, w, args, device, world):
         comp.wait_event(copied[i % 2])
         mu = i % k
         if qgz:
-            codes, scales = dev_sets[i % 2]
-            z.zero_step_fused_qgz(h, job.hp, [codes[r] for r in range(w["n_d"])], scales, 2048, job.master[0],
-                                  job.m[0], job.v[0], job.master[0], job.m[0], job.v[0], job.lp[0], job.scalars,
-                                  job.ws)
+            job.k = i % 2
+            job.step()
         elif k > 1 and mu < k - 1:
             z.zero_accumulate_grads(h, job.ranks(i % 2), None if mu == 0 else job.acc, job.acc, job.scalars)
         elif k > 1:
@@ -778,14 +786,18 @@ def oracle_sample(w, budget_s, max_steps=None):
                 acc = oracle.accumulate_grads(rows, dt, acc)
             oracle.zero_step_accum(rows, dt, acc, w["accum"], hp, st, w["pad"], min(w["stage"], 3), lp_shards=lp,
                                    gathered=gath)
+        elif w.get("qgz"):
+            codes, scales = oracle.quantize_ranks(rows, psi, S, 2048)
+            if w.get("qgather"):
+                oracle.zero_step_qgz(codes, scales, 2048, hp, st, w["pad"], 3, psi, lp_shards=lp)
+                oracle.quant_gather(lp, n_d, psi, S, 2048)
+            else:
+                oracle.zero_step_qgz(codes, scales, 2048, hp, st, w["pad"], min(w["stage"], 3), psi, lp_shards=lp,
+                                     gathered=gath)
         elif w.get("qgather"):
             # the step with its 16-bit output sharded, then the block-int8 gather of the shards
             oracle.zero_step(rows, dt, hp, st, w["pad"], 3, lp_shards=lp, gathered=gath)
             oracle.quant_gather(lp, n_d, psi, S, 2048)
-        elif w.get("qgz"):
-            codes, scales = oracle.quantize_ranks(rows, psi, S, 2048)
-            oracle.zero_step_qgz(codes, scales, 2048, hp, st, w["pad"], min(w["stage"], 3), psi, lp_shards=lp,
-                                 gathered=gath)
         else:
             oracle.zero_step(rows, dt, hp, st, w["pad"], min(w["stage"], 3), lp_shards=lp, gathered=gath)
         steps += 1

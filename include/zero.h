@@ -364,6 +364,24 @@ ZERO_API zero_status zero_step_fused_qgz(const zero_plan* plan, const zero_hpara
                                          void* lp_out, zero_dev_scalars* scalars_dev, void* ws,
                                          void* stream);
 
+/* The ZeRO++ step with both quantized collectives: the receiver of
+ * zero_step_fused_qgz (the ranks' int8 codes and scales in, dequantized and
+ * summed in rank order, Adam) whose epilogue is the quantized gather of
+ * zero_step_fused_qgather (codes_out, scales_out and the dequantized bf16
+ * gathered values from the updated master, blocks of 2048 from each shard's
+ * first element).  Layouts as in those two entry points.  With clipping a
+ * read-only reduce pass over the codes comes first (norm partials in ws:
+ * zero_workspace_bytes(plan, hp) bytes, 256-byte aligned; ws may be NULL
+ * without clipping) and the update pass re-reads them.  block must be 2048,
+ * the parameter dtype bf16; no loss scaling (ZERO_ERR_UNSUPPORTED).         */
+ZERO_API zero_status zero_step_fused_qgz_qgather(const zero_plan* plan, const zero_hparams* hp,
+                                                 const signed char* const* rank_codes, const float* rank_scales,
+                                                 int block, const float* master_in, const float* m_in,
+                                                 const float* v_in, float* master_out, float* m_out,
+                                                 float* v_out, signed char* codes_out, float* scales_out,
+                                                 void* gathered_bf16, zero_dev_scalars* scalars_dev, void* ws,
+                                                 void* stream);
+
 /* ----------------------------------------------------------- diagnostics --- */
 /* Launch one kernel that waits on a barrier nothing completes, with a wait
  * limit of timeout_ns (at most 10 s).  When the limit runs out the kernel sets

@@ -71,8 +71,18 @@ def test_quantized_variant_names():
     assert bench.workload(2, qgz=True)["name"] == "zero2_gpt2small_psi124439808_nd8_adamw_clip1_qgz"
 
 
+@pytest.mark.parametrize("cfg,n_d,clip", [(5, 8, False), (2, 8, True)])
+def test_both_quantized_exchanges(cfg, n_d, clip):
+    # int8 codes + scales in, int8 codes + scale + dequantized bf16 out; clipped,
+    # a read-only reduce pass over the codes first
+    q = n_d * (1 + 4.0 / 2048)
+    w = bench.workload(cfg, qgz=True, qgather=True)
+    assert w["bytes_per_param"] == q + 27 + 4.0 / 2048 + (q if clip else 0)
+    assert w["name"].endswith("_qgz_qgather") and w["pad"] == 16
+
+
 def test_variants_that_do_not_apply_are_refused():
-    for cfg, kw in ((3, dict(qgz=True)), (4, dict(qgather=True)), (5, dict(qgz=True, qgather=True))):
+    for cfg, kw in ((3, dict(qgz=True)), (4, dict(qgather=True)), (4, dict(qgz=True, qgather=True))):
         with pytest.raises(SystemExit):
             bench.workload(cfg, **kw)
     with pytest.raises(SystemExit):

@@ -212,3 +212,20 @@ def test_prebuilt_rank_pointer_arrays(z):
         with pytest.raises(z.ZeroError) as e:
             z.zero_step_fused(h, hp, ranks, A, A, A, A, A, A, A, A, A, stream=0)
         assert e.value.status == 2
+
+
+def test_two_exchange_step_argument_checks(z):
+    # every case fails its checks before anything is launched
+    A = 0x10000
+    p = z.Plan(1000, 2, stage=2)
+    ranks = (ctypes.c_void_p * 2)(A, A)
+    f = "zero_step_fused_qgz_qgather"
+    hp, clip, lsc = z.hparams(), z.hparams(max_norm=1.0), z.hparams(loss_scaling=True)
+    assert _raw(z, f, p.handle, ctypes.byref(hp), ranks, A, 1024, A, A, A, A, A, A, A, A, A, A, None, None) == 3
+    assert _raw(z, f, p.handle, ctypes.byref(lsc), ranks, A, 2048, A, A, A, A, A, A, A, A, A, A, A, None) == 3
+    assert _raw(z, f, p.handle, ctypes.byref(clip), ranks, A, 2048, A, A, A, A, A, A, A, A, A, A, None, None) == 1
+    assert _raw(z, f, p.handle, ctypes.byref(hp), ranks, A, 2048, A, A, A, A, A, A, A + 4, A, A, A, None, None) == 2
+    assert _raw(z, f, p.handle, ctypes.byref(hp), ranks, A, 2048, A, A, A, A, A, A, A, A, A, A + 16, None,
+                None) == 2
+    p16 = z.Plan(1000, 2, stage=2, param_dtype=z.ZERO_FP16)
+    assert _raw(z, f, p16.handle, ctypes.byref(hp), ranks, A, 2048, A, A, A, A, A, A, A, A, A, A, None, None) == 3

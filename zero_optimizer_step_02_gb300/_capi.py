@@ -85,6 +85,8 @@ _SIGS = {
     "zero_accumulate_grads": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp]),
     "zero_step_fused_accum": (_i32, [_vp, _hp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "zero_step_fused_qgz": (_i32, [_vp, _hp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "zero_step_fused_qgz_qgather": (_i32, [_vp, _hp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                           _vp, _vp, _vp]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -276,6 +278,17 @@ def zero_step_fused_qgz(plan, hp, rank_codes, rank_scales, block, master_in, m_i
                                     _addr(master_in), _addr(m_in), _addr(v_in), _addr(master_out), _addr(m_out),
                                     _addr(v_out), _addr(lp_out), _addr(scalars), _addr(ws), _stream(stream)),
            "zero_step_fused_qgz")
+
+
+def zero_step_fused_qgz_qgather(plan, hp, rank_codes, rank_scales, block, master_in, m_in, v_in, master_out, m_out,
+                                v_out, codes_out, scales_out, gathered, scalars, ws=None, stream=None):
+    """Both ZeRO++ exchanges in one step: int8 rank codes in, int8 gather out
+    (ws: the workspace, needed with clipping)."""
+    _check(_lib.zero_step_fused_qgz_qgather(plan, ctypes.byref(hp), _ptr_array(rank_codes), _addr(rank_scales),
+                                            block, _addr(master_in), _addr(m_in), _addr(v_in), _addr(master_out),
+                                            _addr(m_out), _addr(v_out), _addr(codes_out), _addr(scales_out),
+                                            _addr(gathered), _addr(scalars), _addr(ws), _stream(stream)),
+           "zero_step_fused_qgz_qgather")
 
 
 def zero_debug_wait_timeout(scalars, timeout_ns, stream=None):

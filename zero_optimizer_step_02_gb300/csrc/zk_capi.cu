@@ -754,6 +754,53 @@ ZERO_API zero_status zero_step_fused_qgz(const zero_plan* p, const zero_hparams*
                         zk::F_CLIP | zk::F_FINALIZE | zk::F_EPILOGUE, sc, st, ws, n);
 }
 
+ZERO_API zero_status zero_step_fused_qgz_qgather(const zero_plan* p, const zero_hparams* hp,
+                                                 const signed char* const* codes, const float* scales, int block,
+                                                 const float* mi, const float* m_in, const float* vi, float* mo,
+                                                 float* m_out, float* vo, signed char* codes_out, float* scales_out,
+                                                 void* gathered, zero_dev_scalars* sc, void* ws, void* stream)
+{
+    ZK_CALL_RANGE();
+    if (p == nullptr) return ZERO_ERR_INVALID_ARG;
+    zero_status s;
+    if ((s = check_hparams(hp)) != ZERO_OK) return s;
+    if (block != zk::kQuantBlock) return ZERO_ERR_UNSUPPORTED;
+    if (hp->loss_scaling || p->param_dtype != ZERO_BF16) return ZERO_ERR_UNSUPPORTED;
+    if ((s = check_ranks(p, reinterpret_cast<const void* const*>(codes))) != ZERO_OK) return s;
+    if ((s = check_dev(scales)) != ZERO_OK) return s;
+    if ((s = check_dev(sc, 256)) != ZERO_OK) return s;
+    if ((s = check_state(mi, m_in, vi, mo, m_out, vo)) != ZERO_OK) return s;
+    if ((s = check_dev(codes_out)) != ZERO_OK) return s;
+    if ((s = check_dev(scales_out)) != ZERO_OK) return s;
+    if ((s = check_dev(gathered)) != ZERO_OK) return s;
+    const bool clip = hp->max_norm > 0.0f;
+    if (clip && (s = check_dev(ws, 256)) != ZERO_OK) return s;
+    const cudaStream_t st = as_stream(stream);
+    int flags = zk::F_QUANT | zk::F_EPILOGUE;
+    int n = 0;
+    if (clip) {
+        // a read-only reduce pass over the codes; the update pass re-reads them
+        if ((s = run_reduce_q8(p, hp, codes, scales, nullptr, ws, sc, st, &n)) != ZERO_OK) return s;
+        flags |= zk::F_CLIP | zk::F_FINALIZE;
+    }
+    StreamArgs a = base_args(hp, sc);
+    if (clip) set_finalize(a, ws, n);
+    set_q8_ranks(a, p, codes, scales);
+    a.n_side = 3;
+    a.n_side_tma = 3;
+    a.side[0] = mi;
+    a.side[1] = m_in;
+    a.side[2] = vi;
+    a.out_f32[0] = mo;
+    a.out_f32[1] = m_out;
+    a.out_f32[2] = vo;
+    a.q_codes = codes_out;
+    a.q_scales = scales_out;
+    a.q_gathered = gathered;
+    a.flags = flags;
+    return from_cuda(zk::launch_stream(zk::OP_QFUSED, zk::kGradQ8, p->param_dtype, a, st));
+}
+
 ZERO_API zero_status zero_debug_wait_timeout(zero_dev_scalars* sc, long long timeout_ns, void* stream)
 {
     ZK_CALL_RANGE();

@@ -748,8 +748,9 @@ cudaError_t launch_one(StreamArgs& a, cudaStream_t st)
 cudaError_t launch_stream(int op, int grad_dtype, int param_dtype, StreamArgs& a, cudaStream_t st)
 {
     const bool gb = grad_dtype == ZERO_BF16, pb = param_dtype == ZERO_BF16;
-    if (grad_dtype == kGradQ8) {   // int8 ranks: the fused step and the reduce pass
+    if (grad_dtype == kGradQ8) {   // int8 ranks: the fused step (plain or int8 gather) and the reduce pass
         if (op == OP_REDUCE) return launch_one<kGradQ8, ZERO_BF16, OP_REDUCE>(a, st);
+        if (op == OP_QFUSED) return pb ? launch_one<kGradQ8, ZERO_BF16, OP_QFUSED>(a, st) : cudaErrorInvalidValue;
         if (op != OP_FUSED) return cudaErrorInvalidValue;
         return pb ? launch_one<kGradQ8, ZERO_BF16, OP_FUSED>(a, st) : launch_one<kGradQ8, ZERO_FP16, OP_FUSED>(a, st);
     }
