@@ -51,7 +51,7 @@ class QGather:
         assert np.array_equal(u16(self.gathered), og)
 
 
-@pytest.mark.parametrize("n_d,psi,pad", [(2, 300_001, 8), (8, 400_003, 8), (5, 123_457, 1)])
+@pytest.mark.parametrize("n_d,psi,pad", [(2, 300_001, 8), (8, 400_003, 8), (5, 123_457, 1), (8, 7, 8)])
 def test_quantized_gather_with_clipping(n_d, psi, pad):
     hp = z.hparams(lr=3e-4, beta2=0.95, weight_decay=0.1, max_norm=1.0)
     job = Job(psi, n_d, pad=pad, hp=hp, seed=81 + n_d)
@@ -60,7 +60,8 @@ def test_quantized_gather_with_clipping(n_d, psi, pad):
         job.new_grads(step, sigma=1e-2, heavy_tail=True)
         q.gpu_step()
         job.oracle_step()
-        assert np.float32(job.ost.scalars.clip_coef) < 1.0      # the clip is active
+        if psi >= 1000:
+            assert np.float32(job.ost.scalars.clip_coef) < 1.0      # the clip is active
         if _coef_check(job):
             job.assert_bit_exact(lp=False)
             q.assert_outputs()
@@ -93,7 +94,8 @@ def test_quantized_gather_overflow_skip(max_norm):
             job.assert_within_tolerance(lp=False)
 
 
-@pytest.mark.parametrize("n_d,psi,pad", [(2, 300_001, 16), (8, 400_003, 16), (17, 70_001, 1), (4, 5_000, 16)])
+@pytest.mark.parametrize("n_d,psi,pad", [(2, 300_001, 16), (8, 400_003, 16), (17, 70_001, 1), (4, 5_000, 16),
+                                         (8, 7, 16), (3, 1, 1)])
 @pytest.mark.parametrize("stage", [2, 3])
 def test_quantized_exchange_with_clipping(n_d, psi, pad, stage):
     # n_d <= 4: reduce pass over the codes, then the fused step re-reads them;
@@ -114,7 +116,8 @@ def test_quantized_exchange_with_clipping(n_d, psi, pad, stage):
         oc, osc = oracle.quantize_ranks(job.rows, psi, S, 2048)
         oracle.zero_step_qgz(oc, osc, 2048, oracle_hp(hp), job.ost, pad, stage, psi, lp_shards=job.o_lp_shards,
                              gathered=job.o_gathered)
-        assert np.float32(job.ost.scalars.clip_coef) < 1.0
+        if psi >= 1000:
+            assert np.float32(job.ost.scalars.clip_coef) < 1.0
         sc = job.scalars()
         assert sc.sqnorm == pytest.approx(job.ost.scalars.sqnorm, rel=2 * psi * 2.0 ** -53)
         if _coef_check(job):

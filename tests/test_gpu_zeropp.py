@@ -15,7 +15,8 @@ pytestmark = pytest.mark.gpu
 
 @pytest.mark.parametrize("n_d,psi,pad,clip", [(2, 300_001, 16, False), (8, 400_003, 16, True),
                                               (16, 200_003, 16, False), (17, 70_001, 1, True),
-                                              (8, 100_000, 16, False), (32, 4097 * 7, 16, True)])
+                                              (8, 100_000, 16, False), (32, 4097 * 7, 16, True),
+                                              (8, 7, 16, True), (4, 2, 1, False)])
 def test_two_exchange_step(n_d, psi, pad, clip):
     hp = z.hparams(lr=3e-4, beta2=0.95, weight_decay=0.1, max_norm=1.0 if clip else 0.0)
     job = Job(psi, n_d, pad=pad, hp=hp, seed=101 + n_d)
