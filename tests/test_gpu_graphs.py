@@ -1,7 +1,8 @@
 """The step's entry points captured into a CUDA graph (after one eager call
 on the device, which caches the device attributes and kernel settings) replay
 with the same bits as eager calls: the fused step, gradient accumulation, and
-the quantized gradient exchange (sender and receiver)."""
+the quantized gradient exchange (sender and receiver; plain, clipped, and
+with the int8 gather epilogue)."""
 import pytest
 import torch
 
@@ -96,31 +97,46 @@ def test_accumulation_in_a_graph():
     assert eager.scalars_host().t == graphed.scalars_host().t == 3
 
 
-def test_quantized_exchange_in_a_graph():
-    # sender and receiver of the int8 gradient exchange, twice per graph
-    hp = z.hparams(lr=1e-3)
+@pytest.mark.parametrize("mode", ["plain", "clip", "both", "both_clip"])
+def test_quantized_exchange_in_a_graph(mode):
+    # sender and receiver of the int8 gradient exchange, twice per graph;
+    # clipped (reduce pass over the codes first) and with the int8 gather
+    # epilogue of the two-exchange step
+    hp = z.hparams(lr=1e-3, max_norm=1.0 if mode.endswith("clip") else 0.0)
     n_d, psi = 8, 300_007
     plan, (eager, graphed) = _pair(psi, n_d, hp)
     nbs = -(-plan.shard // 2048)
-    wire = []
+    wire, outs = [], []
     for _ in range(2):
         codes = torch.zeros(n_d, (psi + 15) // 16 * 16, dtype=torch.int8, device="cuda")
         scales = torch.zeros(n_d * nbs * ((n_d + 3) // 4 * 4), device="cuda")
         wire.append((codes, scales))
+        outs.append((torch.zeros(plan.padded, dtype=torch.int8, device="cuda"),
+                     torch.zeros(n_d * nbs, device="cuda"), torch.zeros(psi, dtype=torch.bfloat16, device="cuda")))
 
-    def one_step(b, w):
+    def one_step(b, w, o):
         codes, scales = w
-        z.zero_quantize_grads(plan.handle, b.rank_list(), 2048, [codes[r] for r in range(n_d)], scales, b.scalars)
-        z.zero_step_fused_qgz(plan.handle, hp, [codes[r] for r in range(n_d)], scales, 2048, b.master, b.m, b.v,
-                              b.master, b.m, b.v, b.lp, b.scalars)
+        rows = [codes[r] for r in range(n_d)]
+        z.zero_quantize_grads(plan.handle, b.rank_list(), 2048, rows, scales, b.scalars)
+        if mode.startswith("both"):
+            z.zero_step_fused_qgz_qgather(plan.handle, hp, rows, scales, 2048, b.master, b.m, b.v, b.master, b.m,
+                                          b.v, o[0], o[1], o[2], b.scalars, b.ws)
+        else:
+            z.zero_step_fused_qgz(plan.handle, hp, rows, scales, 2048, b.master, b.m, b.v, b.master, b.m, b.v,
+                                  b.lp, b.scalars, b.ws)
 
-    one_step(eager, wire[0])
-    one_step(graphed, wire[1])
-    g = _capture(lambda: [one_step(graphed, wire[1]) for _ in range(2)])
+    one_step(eager, wire[0], outs[0])
+    one_step(graphed, wire[1], outs[1])
+    g = _capture(lambda: [one_step(graphed, wire[1], outs[1]) for _ in range(2)])
     for _ in range(2):
-        one_step(eager, wire[0])
+        one_step(eager, wire[0], outs[0])
     g.replay()
     torch.cuda.synchronize()
     _same(eager, graphed)
     assert torch.equal(wire[0][0], wire[1][0]) and torch.equal(wire[0][1], wire[1][1])
-    assert eager.scalars_host().t == graphed.scalars_host().t == 3
+    for x, y in zip(outs[0], outs[1]):
+        assert torch.equal(x.view(torch.uint8), y.view(torch.uint8))
+    se, sg = eager.scalars_host(), graphed.scalars_host()
+    assert se.t == sg.t == 3 and se.clip_coef == sg.clip_coef
+    if mode.endswith("clip"):
+        assert se.clip_coef < 1.0
