@@ -48,7 +48,7 @@ def test_layout_is_the_minimal_padded_contiguous_split(psi, n_d, pad):
         assert r * S + i == j and i < lens[r]
 
 
-def test_survey_config_layout():
+def test_small_workload_shard_layout():
     # Psi = 1,000,003 over 4 ranks: pad 8 -> S = 250,008; pad 1 -> S = 250,001
     S = oracle.shard_size(1_000_003, 4, 8)
     assert S == 250_008 and oracle.valid_len(1_000_003, S, 3) == 249_979
