@@ -58,7 +58,7 @@ typedef enum {
     ZERO_OK = 0,
     ZERO_ERR_INVALID_ARG = 1, /* a size, a dtype, a stage or a NULL pointer is wrong  */
     ZERO_ERR_MISALIGNED = 2,  /* a device pointer breaks the alignment rule above     */
-    ZERO_ERR_UNSUPPORTED = 3, /* a valid request this build does not implement        */
+    ZERO_ERR_UNSUPPORTED = 3, /* a valid request the library does not implement       */
     ZERO_ERR_CUDA = 4,        /* the CUDA runtime reported an error at launch         */
     ZERO_ERR_TIMEOUT = 5,     /* a bounded device wait ran out (see ZERO_DEV_TIMEOUT) */
     ZERO_ERR_BOUNDS = 6       /* a request exceeds a fixed capacity of the library   */
