@@ -295,7 +295,8 @@ class Job:
         if w.get("qgz"):
             # the int8 wire format of every gradient set (sender pass, untimed here)
             nbs = -(-self.plan.shard // 2048)
-            row16 = (w["psi"] + 15) // 16 * 16
+            # --row-pad applies to the int8 rows too (rounded to keep them 16-byte aligned)
+            row16 = (w["psi"] + 15) // 16 * 16 + (w.get("row_pad", 0) + 15) // 16 * 16
             self.codes = [torch.empty(w["n_d"], row16, dtype=torch.int8, device=device) for _ in self.grads]
             n_dp = (w["n_d"] + 3) // 4 * 4
             self.qscales = [torch.empty(w["n_d"] * nbs * n_dp, device=device) for _ in self.grads]
