@@ -150,12 +150,10 @@ __global__ void k_repair(const float* __restrict__ mi, const float* __restrict__
     }
 }
 
-cudaError_t launch_repair(const zero_hparams& hp, const float* master_in, const float* m_in,
-                          const float* v_in, float* master_out, float* m_out, float* v_out,
-                          void* lp_out, int param_dtype, long long psi, zero_dev_scalars* sc,
+cudaError_t launch_repair(const float* master_in, const float* m_in, const float* v_in, float* master_out,
+                          float* m_out, float* v_out, void* lp_out, int param_dtype, long long psi, zero_dev_scalars* sc,
                           cudaStream_t st)
 {
-    (void)hp;
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
     long long blocks = (psi + 255) / 256;

@@ -554,7 +554,7 @@ zero_status fused_step(const zero_plan* p, const zero_hparams* hp, const void* c
         }
     }
     if (!speculative) return ZERO_OK;
-    ZK_TRY(zk::launch_repair(*hp, mi, m_in, vi, mo, m_out, vo, lp, p->param_dtype, p->psi, sc, st));
+    ZK_TRY(zk::launch_repair(mi, m_in, vi, mo, m_out, vo, lp, p->param_dtype, p->psi, sc, st));
     return from_cuda(zk::launch_epilogue(*hp, sc, st));
 }
 

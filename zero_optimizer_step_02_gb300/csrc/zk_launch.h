@@ -63,9 +63,8 @@ cudaError_t launch_finalize_sqnorm(const double* partials, int n, const zero_hpa
 cudaError_t launch_sqnorm_f32(const float* g, long long n, double* partials, int* n_partials,
                               cudaStream_t st);
 cudaError_t launch_epilogue(const zero_hparams& hp, zero_dev_scalars* sc, cudaStream_t st);
-cudaError_t launch_repair(const zero_hparams& hp, const float* master_in, const float* m_in,
-                          const float* v_in, float* master_out, float* m_out, float* v_out,
-                          void* lp_out, int param_dtype, long long psi, zero_dev_scalars* sc,
+cudaError_t launch_repair(const float* master_in, const float* m_in, const float* v_in, float* master_out,
+                          float* m_out, float* v_out, void* lp_out, int param_dtype, long long psi, zero_dev_scalars* sc,
                           cudaStream_t st);
 // starve: issue no copy, so every wait runs out (tests the timeout path)
 cudaError_t launch_all_gather(const void* const* shards, int n_d, long long shard, long long psi,
