@@ -215,12 +215,12 @@ NOMINAL_HBM_GBS = 8000.0
 # kernel and workload, with a hash of the kernel sources they were taken on;
 # reported as null once the sources change.
 TRAFFIC = {
-    ("adam_shard", "zero2_gpt2small_psi124439808_nd8_adamw_clip1"): {"bytes": 3.625e9, "src": "9e92db8df40c"},
-    ("fused_step", "zero2_psi2p28_nd8"): {"bytes": 11.105e9, "src": "9e92db8df40c"},
-    ("fused_step_qgather", "zero2_psi2p28_nd2_qgather"): {"bytes": 8.080e9, "src": "9e92db8df40c"},
-    ("fused_step_qgz", "zero2_psi2p28_nd8_qgz"): {"bytes": 8.922e9, "src": "9e92db8df40c"},
+    ("adam_shard", "zero2_gpt2small_psi124439808_nd8_adamw_clip1"): {"bytes": 3.623e9, "src": "e92f70f96686"},
+    ("fused_step", "zero2_psi2p28_nd8"): {"bytes": 11.106e9, "src": "e92f70f96686"},
+    ("fused_step_qgather", "zero2_psi2p28_nd2_qgather"): {"bytes": 8.081e9, "src": "e92f70f96686"},
+    ("fused_step_qgz", "zero2_psi2p28_nd8_qgz"): {"bytes": 8.917e9, "src": "e92f70f96686"},
     ("accumulate_grads", "zero2_gpt2small_psi124439808_nd8_adamw_clip1_accum4"): {"bytes": 2.952e9,
-                                                                                   "src": "9e92db8df40c"},
+                                                                                   "src": "e92f70f96686"},
 }
 
 

@@ -248,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
         // constants in registers: a reference into shared memory would be
         // re-read for every element (the stores in the loop may alias it)
         const StepConsts c = sh->c;
-        const bool detect = (a.flags & (F_DETECT | F_SQNORM)) != 0;
+        const bool detect = (a.flags & F_DETECT) != 0;   // recorded only under loss scaling
         const bool want_sq = (a.flags & F_SQNORM) != 0;
         const bool carry = (a.flags & F_CARRY) != 0;
         const bool raw = (a.flags & F_RAW) != 0;
