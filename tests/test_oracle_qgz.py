@@ -27,9 +27,10 @@ def _on_grid_grads(n_d, psi, S, block, e, seed):
 @pytest.mark.parametrize("n_d,psi,pad,block", [(2, 5000, 8, 2048), (4, 1003, 1, 256), (8, 7000, 64, 2048),
                                                (3, 4096 * 3 + 5, 8, 2048)])
 @pytest.mark.parametrize("stage", [2, 3])
-def test_lossless_on_grid_equals_the_plain_step(n_d, psi, pad, block, stage):
+@pytest.mark.parametrize("max_norm", [0.0, 0.05])      # plain, and clipped (active on these inputs)
+def test_lossless_on_grid_equals_the_plain_step(n_d, psi, pad, block, stage, max_norm):
     S = oracle.shard_size(psi, n_d, pad)
-    hp = oracle.hparams(lr=1e-3, weight_decay=0.01)
+    hp = oracle.hparams(lr=1e-3, weight_decay=0.01, max_norm=max_norm)
     a = oracle.State(np.zeros(n_d * S, np.float32), np.zeros(n_d * S, np.float32),
                      np.zeros(n_d * S, np.float32), oracle.new_scalars())
     a.master[:psi] = np.random.default_rng(1).normal(0, 0.02, psi).astype(np.float32)
@@ -46,6 +47,8 @@ def test_lossless_on_grid_equals_the_plain_step(n_d, psi, pad, block, stage):
         oracle.zero_step_qgz(codes, scales, block, hp, b, pad, stage, psi, **bufs_b)
         for x, y in ((a.master, b.master), (a.m, b.m), (a.v, b.v)):
             assert np.array_equal(x.view(np.uint32), y.view(np.uint32))
+        if max_norm > 0:
+            assert a.scalars.clip_coef < 1.0 and a.scalars.clip_coef == b.scalars.clip_coef
         key = "lp_shards" if stage == 3 else "gathered"
         assert np.array_equal(bufs_a[key], bufs_b[key])
 
