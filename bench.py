@@ -1,7 +1,9 @@
 """Benchmark of the GB300 ZeRO-DP optimizer step.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
-                    [--config 1..5] [--nd N] [--qgather] [--no-cpu-baseline]
+                    [--config 1..5] [--nd N] [--qgather] [--qgz] [--accum K]
+                    [--offload] [--overlap] [--gathers 1|2] [--row-pad N]
+                    [--psi N] [--no-cpu-baseline] [--no-e2e]
 
 A step is one pass of the whole hot path (reduce-scatter of the simulated
 ranks' gradients, global checks, Adam on every shard, 16-bit cast and gather)
