@@ -218,8 +218,9 @@ ZERO_API zero_status zero_all_gather(const zero_plan* plan, const void* const* s
 /* The whole step in as few passes as the global checks allow: reduce-scatter,
  * Adam and the 16-bit cast written straight to lp_out (gathered buffer for
  * stages 1-2, sharded buffer for stage 3), the reduced gradient kept in
- * registers.  State is read from *_in and written to *_out (each n_d*S); an
- * *_out may equal its *_in.  Passes:
+ * registers.  State is read from *_in and written to *_out (each n_d*S); the
+ * *_out may equal their *_in (all three or none); otherwise no *_out may
+ * share a byte with another state array (ZERO_ERR_INVALID_ARG).  Passes:
  *   no clipping, no loss scaling : 1 pass
  *   loss scaling, out != in      : 1 pass, speculative; on overflow the out
  *                                  state is restored from in and lp_out is

@@ -106,6 +106,7 @@ def test_calls_check_arguments_before_touching_the_device(z):
     h = p.handle
     A = 0x10000          # 16- and 256-byte aligned fake addresses: never dereferenced,
     B = 0x20000          # every call below fails its checks first
+    S1, S2, S3 = 0x100000, 0x200000, 0x300000   # distinct state arrays
     ranks_ok = (ctypes.c_void_p * 2)(A, B)
     ranks_bad = (ctypes.c_void_p * 2)(A, B + 2)
     ranks_null = (ctypes.c_void_p * 2)(A, None)
@@ -130,16 +131,18 @@ def test_calls_check_arguments_before_touching_the_device(z):
     assert _raw(z, "zero_reduce_scatter", h, ranks_ok, ctypes.byref(ls), A, A, A, None) == 1
     # workspace required with clipping
     clip = z.hparams(max_norm=1.0)
-    assert _raw(z, "zero_step_fused", h, ctypes.byref(clip), ranks_ok, A, A, A, A, A, A, A, A, None, None) == 1
+    assert _raw(z, "zero_step_fused", h, ctypes.byref(clip), ranks_ok, S1, S2, S3, S1, S2, S3, A, A, None,
+                None) == 1
     # quantized gather: block limits, fused variant only with block 2048 and no clipping
     assert _raw(z, "zero_quant_gather", h, A, 31, A, A, A, None) == 1
     assert _raw(z, "zero_quant_gather", h, A, 70000, A, A, A, None) == 1
     assert _raw(z, "zero_step_fused_qgather", h, hpp, ranks_ok, A, A, A, A, A, A, 1024, A, A, A, A, A, None) == 3
     # clipping or loss scaling need the workspace; loss scaling needs the state in place
-    assert _raw(z, "zero_step_fused_qgather", h, ctypes.byref(clip), ranks_ok, A, A, A, A, A, A, 2048, A, A, A,
+    assert _raw(z, "zero_step_fused_qgather", h, ctypes.byref(clip), ranks_ok, S1, S2, S3, S1, S2, S3, 2048, A, A, A,
                 A, None, None) == 1
     lsc = z.hparams(loss_scaling=True)
-    assert _raw(z, "zero_step_fused_qgather", h, ctypes.byref(lsc), ranks_ok, A, A, A, B, B, B, 2048, A, A, A,
+    assert _raw(z, "zero_step_fused_qgather", h, ctypes.byref(lsc), ranks_ok, S1, S2, S3, B, B + 0x4000, B + 0x8000,
+                2048, A, A, A,
                 A, A, None) == 3
     # the timeout probe rejects limits outside (0, 10 s]
     assert _raw(z, "zero_debug_wait_timeout", A, 0, None) == 1
@@ -159,6 +162,7 @@ def test_library_is_built_in_tree(z):
 
 def test_quantized_gradient_exchange_argument_checks(z):
     A = 0x10000
+    S1, S2, S3 = 0x100000, 0x200000, 0x300000   # distinct state arrays (updated in place)
     p = z.Plan(1000, 2, stage=2)
     ranks = (ctypes.c_void_p * 2)(A, A)
     hp = z.hparams()
@@ -168,15 +172,15 @@ def test_quantized_gradient_exchange_argument_checks(z):
     assert _raw(z, "zero_quantize_grads", p.handle, ranks, 2048, ranks, A, A + 16, None) == 2
     p16 = z.Plan(1000, 2, stage=2, grad_dtype=z.ZERO_FP16)
     assert _raw(z, "zero_quantize_grads", p16.handle, ranks, 2048, ranks, A, None, None) == 3
-    assert _raw(z, "zero_step_fused_qgz", p.handle, ctypes.byref(hp), ranks, A, 1024, A, A, A, A, A, A, A, A,
+    assert _raw(z, "zero_step_fused_qgz", p.handle, ctypes.byref(hp), ranks, A, 1024, S1, S2, S3, S1, S2, S3, A, A,
                 None, None) == 3
     # clipping needs the workspace; bf16 gradients take no loss scaling
-    assert _raw(z, "zero_step_fused_qgz", p.handle, ctypes.byref(clip), ranks, A, 2048, A, A, A, A, A, A, A, A,
+    assert _raw(z, "zero_step_fused_qgz", p.handle, ctypes.byref(clip), ranks, A, 2048, S1, S2, S3, S1, S2, S3, A, A,
                 None, None) == 1
-    assert _raw(z, "zero_step_fused_qgz", p.handle, ctypes.byref(clip), ranks, A, 2048, A, A, A, A, A, A, A, A,
+    assert _raw(z, "zero_step_fused_qgz", p.handle, ctypes.byref(clip), ranks, A, 2048, S1, S2, S3, S1, S2, S3, A, A,
                 A + 16, None) == 2
     lsc = z.hparams(loss_scaling=True)
-    assert _raw(z, "zero_step_fused_qgz", p.handle, ctypes.byref(lsc), ranks, A, 2048, A, A, A, A, A, A, A, A,
+    assert _raw(z, "zero_step_fused_qgz", p.handle, ctypes.byref(lsc), ranks, A, 2048, S1, S2, S3, S1, S2, S3, A, A,
                 A, None) == 3
 
 
@@ -217,15 +221,36 @@ def test_prebuilt_rank_pointer_arrays(z):
 def test_two_exchange_step_argument_checks(z):
     # every case fails its checks before anything is launched
     A = 0x10000
+    S1, S2, S3 = 0x100000, 0x200000, 0x300000   # distinct state arrays (updated in place)
     p = z.Plan(1000, 2, stage=2)
     ranks = (ctypes.c_void_p * 2)(A, A)
     f = "zero_step_fused_qgz_qgather"
     hp, clip, lsc = z.hparams(), z.hparams(max_norm=1.0), z.hparams(loss_scaling=True)
-    assert _raw(z, f, p.handle, ctypes.byref(hp), ranks, A, 1024, A, A, A, A, A, A, A, A, A, A, None, None) == 3
-    assert _raw(z, f, p.handle, ctypes.byref(lsc), ranks, A, 2048, A, A, A, A, A, A, A, A, A, A, A, None) == 3
-    assert _raw(z, f, p.handle, ctypes.byref(clip), ranks, A, 2048, A, A, A, A, A, A, A, A, A, A, None, None) == 1
-    assert _raw(z, f, p.handle, ctypes.byref(hp), ranks, A, 2048, A, A, A, A, A, A, A + 4, A, A, A, None, None) == 2
-    assert _raw(z, f, p.handle, ctypes.byref(hp), ranks, A, 2048, A, A, A, A, A, A, A, A, A, A + 16, None,
+    assert _raw(z, f, p.handle, ctypes.byref(hp), ranks, A, 1024, S1, S2, S3, S1, S2, S3, A, A, A, A, None, None) == 3
+    assert _raw(z, f, p.handle, ctypes.byref(lsc), ranks, A, 2048, S1, S2, S3, S1, S2, S3, A, A, A, A, A, None) == 3
+    assert _raw(z, f, p.handle, ctypes.byref(clip), ranks, A, 2048, S1, S2, S3, S1, S2, S3, A, A, A, A, None, None) == 1
+    assert _raw(z, f, p.handle, ctypes.byref(hp), ranks, A, 2048, S1, S2, S3, S1, S2, S3, A + 4, A, A, A, None, None) == 2
+    assert _raw(z, f, p.handle, ctypes.byref(hp), ranks, A, 2048, S1, S2, S3, S1, S2, S3, A, A, A, A + 16, None,
                 None) == 2
     p16 = z.Plan(1000, 2, stage=2, param_dtype=z.ZERO_FP16)
-    assert _raw(z, f, p16.handle, ctypes.byref(hp), ranks, A, 2048, A, A, A, A, A, A, A, A, A, A, None, None) == 3
+    assert _raw(z, f, p16.handle, ctypes.byref(hp), ranks, A, 2048, S1, S2, S3, S1, S2, S3, A, A, A, A, None, None) == 3
+
+
+def test_overlapping_state_arrays_are_refused(z):
+    # master/m/v (n_d*S floats each) may be updated in place, array by array;
+    # any other shared byte between an output and another state array is refused
+    hp = z.hparams()
+    plan = z.Plan(1000, 2, stage=2)          # n_d*S = 1008 floats = 4032 bytes
+    h, hpp = plan.handle, ctypes.byref(hp)
+    A = 0x10000
+    ranks = (ctypes.c_void_p * 2)(A, A)
+    S1, S2, S3 = 0x100000, 0x200000, 0x300000
+    T1, T2, T3 = 0x400000, 0x500000, 0x600000
+
+    def step(*state):
+        return _raw(z, "zero_step_fused", h, hpp, ranks, *state, A, A, A, None)
+    assert step(S1, S2, S3, S1, S2, S3 + 4096) == 1           # partly in place
+    assert step(S1, S2, S3, T1, T1 + 1024, T3) == 1            # two outputs share bytes
+    assert step(S1, S2, S3, T1, T2, S1 + 2048) == 1            # an output overlaps another input
+    assert step(S1, S1 + 2048, S3, S1, S1 + 2048, S3) == 1     # in place, but m overlaps master
+    assert _raw(z, "zero_adam_shard_step", h, hpp, A, S1, S1 + 16, S3, None, A, None) == 1   # m overlaps master

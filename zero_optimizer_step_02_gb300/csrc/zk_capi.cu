@@ -288,16 +288,34 @@ zero_status run_fused_q8(const zero_plan* p, const zero_hparams* hp, const signe
     return from_cuda(zk::launch_stream(zk::OP_FUSED, zk::kGradQ8, p->param_dtype, a, st));
 }
 
-zero_status check_state(const float* mi, const float* m_in, const float* vi, float* mo, float* m_out, float* vo)
+// two arrays of n bytes share a byte
+bool overlaps(const void* a, const void* b, uintptr_t n)
+{
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + n && y < x + n;
+}
+
+// master/m/v in and out, n_d*S floats each: out may equal in, array by array,
+// but all three or none; no output shares a byte with another output, nor
+// with an input other than its own
+zero_status check_state(const zero_plan* p, const float* mi, const float* m_in, const float* vi, float* mo,
+                        float* m_out, float* vo)
 {
     const void* ptrs[] = {mi, m_in, vi, mo, m_out, vo};
     for (const void* q : ptrs) {
         const zero_status s = check_dev(q);
         if (s != ZERO_OK) return s;
     }
-    // out may alias in, array by array, but all three or none
     const int alias = (mo == mi) + (m_out == m_in) + (vo == vi);
     if (alias != 0 && alias != 3) return ZERO_ERR_INVALID_ARG;
+    const uintptr_t n = sizeof(float) * static_cast<uintptr_t>(p->padded);
+    const void* outs[3] = {mo, m_out, vo};
+    const void* ins[3] = {mi, m_in, vi};
+    for (int i = 0; i < 3; ++i)
+        for (int j = 0; j < 3; ++j) {
+            if (i != j && overlaps(outs[i], outs[j], n)) return ZERO_ERR_INVALID_ARG;
+            if ((i != j || alias == 0) && overlaps(outs[i], ins[j], n)) return ZERO_ERR_INVALID_ARG;
+        }
     return ZERO_OK;
 }
 
@@ -471,7 +489,7 @@ ZERO_API zero_status zero_adam_shard_step(const zero_plan* p, const zero_hparams
     if ((s = check_hparams(hp)) != ZERO_OK) return s;
     if ((s = check_dev(sc, 256)) != ZERO_OK) return s;
     if ((s = check_dev(grad_shards)) != ZERO_OK) return s;
-    if ((s = check_state(master, m, v, master, m, v)) != ZERO_OK) return s;
+    if ((s = check_state(p, master, m, v, master, m, v)) != ZERO_OK) return s;
     if (lp_out != nullptr && !aligned(lp_out, 16)) return ZERO_ERR_MISALIGNED;
     const cudaStream_t st = as_stream(stream);
     const int flags =
@@ -510,7 +528,7 @@ zero_status fused_step(const zero_plan* p, const zero_hparams* hp, const void* c
     if ((s = check_hparams(hp)) != ZERO_OK) return s;
     if ((s = check_ranks(p, ranks)) != ZERO_OK) return s;
     if ((s = check_dev(sc, 256)) != ZERO_OK) return s;
-    if ((s = check_state(mi, m_in, vi, mo, m_out, vo)) != ZERO_OK) return s;
+    if ((s = check_state(p, mi, m_in, vi, mo, m_out, vo)) != ZERO_OK) return s;
     if (lp != nullptr && !aligned(lp, 16)) return ZERO_ERR_MISALIGNED;
     const bool clip = hp->max_norm > 0.0f;
     const bool ls = hp->loss_scaling != 0;
@@ -660,7 +678,7 @@ ZERO_API zero_status zero_step_fused_qgather(const zero_plan* p, const zero_hpar
     if (ls && mo != mi) return ZERO_ERR_UNSUPPORTED;
     if ((s = check_ranks(p, ranks)) != ZERO_OK) return s;
     if ((s = check_dev(sc, 256)) != ZERO_OK) return s;
-    if ((s = check_state(mi, m_in, vi, mo, m_out, vo)) != ZERO_OK) return s;
+    if ((s = check_state(p, mi, m_in, vi, mo, m_out, vo)) != ZERO_OK) return s;
     if ((s = check_dev(codes)) != ZERO_OK) return s;
     if ((s = check_dev(scales)) != ZERO_OK) return s;
     if ((s = check_dev(gathered)) != ZERO_OK) return s;
@@ -735,7 +753,7 @@ ZERO_API zero_status zero_step_fused_qgz(const zero_plan* p, const zero_hparams*
     if ((s = check_ranks(p, reinterpret_cast<const void* const*>(codes))) != ZERO_OK) return s;
     if ((s = check_dev(scales)) != ZERO_OK) return s;
     if ((s = check_dev(sc, 256)) != ZERO_OK) return s;
-    if ((s = check_state(mi, m_in, vi, mo, m_out, vo)) != ZERO_OK) return s;
+    if ((s = check_state(p, mi, m_in, vi, mo, m_out, vo)) != ZERO_OK) return s;
     if (lp != nullptr && !aligned(lp, 16)) return ZERO_ERR_MISALIGNED;
     const bool clip = hp->max_norm > 0.0f;
     if (clip && (s = check_dev(ws, 256)) != ZERO_OK) return s;
@@ -769,7 +787,7 @@ ZERO_API zero_status zero_step_fused_qgz_qgather(const zero_plan* p, const zero_
     if ((s = check_ranks(p, reinterpret_cast<const void* const*>(codes))) != ZERO_OK) return s;
     if ((s = check_dev(scales)) != ZERO_OK) return s;
     if ((s = check_dev(sc, 256)) != ZERO_OK) return s;
-    if ((s = check_state(mi, m_in, vi, mo, m_out, vo)) != ZERO_OK) return s;
+    if ((s = check_state(p, mi, m_in, vi, mo, m_out, vo)) != ZERO_OK) return s;
     if ((s = check_dev(codes_out)) != ZERO_OK) return s;
     if ((s = check_dev(scales_out)) != ZERO_OK) return s;
     if ((s = check_dev(gathered)) != ZERO_OK) return s;
