@@ -47,6 +47,9 @@ MUTATIONS = [
     ("stage 2 keeps full gradients", "    case 2:\n        grads = 2.0 * psi / n_d;", "    case 2:\n        grads = 2.0 * psi;"),
     ("qgZ scale of the wrong block", "const float* sblk = scales + ((long long)r * blocks_per_shard + i / block) * n_dp;",
      "const float* sblk = scales + ((long long)r * blocks_per_shard + (i + 1) / block) * n_dp;"),
+    ("qgZ step ignores clipping",
+     "zo_reduce_scatter_q(n_d, psi, S, block, codes, scales, divisor, shards);\n    return step_from_shards(n_d, psi, S, stage, shards, hp,",
+     "zo_reduce_scatter_q(n_d, psi, S, block, codes, scales, divisor, shards);\n    zo_hparams nc = *hp;\n    nc.max_norm = 0.0f;\n    return step_from_shards(n_d, psi, S, stage, shards, &nc,"),
     ("qgZ ranks summed in reverse", "for (int q = 0; q < n_d; ++q) sum = sum + (float)codes[q][j] * sblk[q];",
      "for (int q = n_d - 1; q >= 0; --q) sum = sum + (float)codes[q][j] * sblk[q];"),
     ("qgZ blocks not aligned to shards",
