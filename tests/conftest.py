@@ -30,3 +30,20 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter):
+    # how often a clipped GPU step's clip coefficient came out one fp32 ulp
+    # from the oracle's (checked then against the oracle's update with the
+    # GPU's coefficient, bit for bit): per test and in total
+    helpers = sys.modules.get("gpu_helpers")
+    counts = getattr(helpers, "ULP_BRANCH", None)
+    if not counts:
+        return
+    taken = sum(v[0] for v in counts.values())
+    total = sum(v[1] for v in counts.values())
+    terminalreporter.write_line("clipped GPU steps whose clip coefficient was one ulp off the oracle's: "
+                                "%d of %d" % (taken, total))
+    for name, (t, n) in sorted(counts.items()):
+        if t:
+            terminalreporter.write_line("  %s: %d of %d steps" % (name, t, n))

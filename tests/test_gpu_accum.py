@@ -10,7 +10,7 @@ import torch
 
 import oracle
 import zero_optimizer_step_02_gb300 as z
-from gpu_helpers import ORACLE_DT, Job, oracle_hp, u16, u32
+from gpu_helpers import ORACLE_DT, Job, accum_ghat, oracle_hp, u16, u32
 from zero_optimizer_step_02_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -31,6 +31,7 @@ class AccumJob(Job):
             self.buf.accumulate(first=mu == 1)
             acc = oracle.accumulate_grads(self.rows, ORACLE_DT[self.gdt], acc)
         self.micro_rows(step, k, **kw)
+        self.acc_k = (acc, k)
         if self.buf.pingpong:
             a = None if k == 1 else self.buf.acc
             b = self.buf
@@ -41,22 +42,16 @@ class AccumJob(Job):
             b.v, b.v2 = b.v2, b.v
         else:
             self.buf.step_accum(self.hp, k)
+        self.snapshot()
         return oracle.zero_step_accum(self.rows, ORACLE_DT[self.gdt], acc, k, oracle_hp(self.hp), self.ost,
                                       self.pad, self.stage, param_dtype=ORACLE_DT[self.pdt],
                                       lp_shards=self.o_lp_shards, gathered=self.o_gathered), acc
 
-    def assert_step(self):
-        """Bit-exact, or (clipping: the norm's summation order differs, so the
-        coefficient may be an ulp off) exact whenever the coefficients agree
-        and within the stated tolerance otherwise."""
-        if self.hp.max_norm > 0.0:
-            sc = self.scalars()
-            o = np.float32(self.ost.scalars.clip_coef)
-            assert abs(int(np.float32(sc.clip_coef).view(np.int32)) - int(o.view(np.int32))) <= 1
-            if np.float32(sc.clip_coef) != o:
-                self.assert_within_tolerance()
-                return
-        self.assert_bit_exact()
+    def assert_step(self, skipped=False):
+        """Bit-exact; with clipping, against the oracle's update with the GPU's
+        coefficient when the two coefficients are one ulp apart (Job.settle)."""
+        acc, k = self.acc_k
+        self.settle(ghat=lambda: accum_ghat(self, acc, k), skipped=skipped)
 
 
 CASES = [  # (n_d, k, psi, pad, stage)

@@ -103,13 +103,8 @@ def test_fused_step_with_clipping(n_d, pingpong):
         sc = job.scalars()
         # both sums within the sequential fp64 sum's error bound of each other
         assert sc.sqnorm == pytest.approx(job.ost.scalars.sqnorm, rel=2 * psi * 2.0 ** -53)
-        o_coef = np.float32(job.ost.scalars.clip_coef)
-        assert o_coef < 1.0   # the clip is active in this workload
-        assert abs(int(np.float32(sc.clip_coef).view(np.int32)) - int(o_coef.view(np.int32))) <= 1
-        if np.float32(sc.clip_coef) == o_coef:
-            job.assert_bit_exact()
-        else:
-            job.assert_within_tolerance()
+        assert np.float32(job.ost.scalars.clip_coef) < 1.0   # the clip is active in this workload
+        job.settle()
 
 
 # -------------------------------------------------------------- loss scaling
@@ -149,7 +144,7 @@ def test_fp16_overflow_with_clipping():
         job.gpu_step()
         skipped = job.oracle_step()
         assert bool(job.scalars().overflow) == skipped == (step == 2)
-        job.assert_within_tolerance()
+        job.settle(skipped=skipped)
 
 
 # -------------------------------------------------------------- the parts
@@ -260,6 +255,36 @@ def test_quant_gather_bit_exact(n_d, psi, pad, block):
     assert np.array_equal(codes.cpu().numpy()[:psi], oc[:psi])
     assert np.array_equal(u32(scales.cpu().numpy()), u32(osc))
     assert np.array_equal(u16(gathered), og)
+
+
+@pytest.mark.parametrize("block", [2048, 256])
+def test_quant_gather_non_finite_weights(block):
+    # blocks holding a NaN weight (skipped by the absmax; its code is -127)
+    # or an infinite one (scale inf: finite weights code 0, the infinite one
+    # -127): codes and scales bit for bit; dequantized values bit for bit
+    # where the oracle's are numbers, NaN where they are NaN (a NaN's payload
+    # is not part of the result)
+    n_d, psi = 2, 4 * 2048 + 100
+    plan = z.Plan(psi, n_d, stage=2, shard_pad=8)
+    S = plan.shard
+    x = torch.zeros(plan.padded, dtype=torch.bfloat16)
+    synth.gaussian_(x[:psi], 0.02, 53, psi)
+    for j, val in ((5, float("nan")), (block + 7, float("inf")), (block + 9, float("nan")), (S + 3, float("-inf")),
+                   (S + 2 * block + 1, float("nan"))):
+        x[j] = val
+    xd = x.cuda()
+    nbs = -(-S // block)
+    codes = torch.full((plan.padded,), 99, dtype=torch.int8, device="cuda")
+    scales = torch.full((n_d * nbs,), -1.0, device="cuda")
+    gathered = torch.zeros(psi, dtype=torch.bfloat16, device="cuda")
+    z.zero_quant_gather(plan.handle, xd, block, codes, scales, gathered)
+    oc, osc, og = oracle.quant_gather(u16(x), n_d, psi, S, block)
+    assert np.array_equal(codes.cpu().numpy()[:psi], oc[:psi])
+    assert np.array_equal(u32(scales.cpu().numpy()), u32(osc))
+    got = u16(gathered)
+    o_nan = np.isnan(oracle.bf16_to_f32(og))
+    assert o_nan.any() and np.array_equal(np.isnan(oracle.bf16_to_f32(got)), o_nan)
+    assert np.array_equal(got[~o_nan], og[~o_nan])
 
 
 @pytest.mark.parametrize("n_d,psi,pad", [(2, 1 << 20, 8), (4, 1_000_003, 8), (16, 300_001, 8), (3, 50_001, 1)])
@@ -377,13 +402,7 @@ def test_largest_shard_pad(n_d, psi):
         job.new_grads(step)
         job.gpu_step()
         job.oracle_step()
-        sc = job.scalars()
-        o = np.float32(job.ost.scalars.clip_coef)
-        assert abs(int(np.float32(sc.clip_coef).view(np.int32)) - int(o.view(np.int32))) <= 1
-        if np.float32(sc.clip_coef) == o:
-            job.assert_bit_exact()
-        else:
-            job.assert_within_tolerance()
+        job.settle()
 
 
 def _with_subnormals(g, rng, frac=0.05):

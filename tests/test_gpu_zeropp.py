@@ -36,15 +36,13 @@ def test_two_exchange_step(n_d, psi, pad, clip):
         z.zero_step_fused_qgz_qgather(job.plan.handle, hp, code_rows, scales, 2048, b.master, b.m, b.v, b.master,
                                       b.m, b.v, g_codes, g_scales, gathered, b.scalars, b.ws)
         oc, osc = oracle.quantize_ranks(job.rows, psi, S, 2048)
+        job.snapshot()
         oracle.zero_step_qgz(oc, osc, 2048, oracle_hp(hp), job.ost, pad, 3, psi, lp_shards=job.o_lp_shards)
         sc = job.scalars()
         assert sc.t == step and sc.status == 0
-        o = np.float32(job.ost.scalars.clip_coef)
-        assert abs(int(np.float32(sc.clip_coef).view(np.int32)) - int(o.view(np.int32))) <= 1
-        if clip and np.float32(sc.clip_coef) != o:
-            job.assert_within_tolerance(lp=False)
-            continue
-        job.assert_bit_exact(lp=False)
+        # the state bit for bit (with the GPU's clip coefficient when it is one
+        # ulp off the oracle's), then the int8 gather of those 16-bit weights
+        job.settle(ghat=lambda: oracle.reduce_scatter_q(oc, osc, psi, S, 2048, float(n_d)), lp=False)
         qc, qs, qg = oracle.quant_gather(job.o_lp_shards, n_d, psi, S, 2048)
         assert np.array_equal(g_codes.cpu().numpy()[:psi], qc[:psi])
         assert np.array_equal(u32(g_scales.cpu().numpy()), u32(qs))
