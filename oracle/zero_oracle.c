@@ -577,6 +577,11 @@ void zo_quantize_block(long long n, const uint16_t* x_bf16, int8_t* codes, float
         float q = 0.0f;
         if (s != 0.0f) {
             q = rintf(zo_bf16_to_f32(x_bf16[i]) / s);   /* default rounding mode: ties to even */
+            /* clamp(q) = min(max(q, -127), 127) with IEEE 754 maxNum / minNum,
+             * which return the other operand when one is NaN: a NaN quotient
+             * (a NaN weight, or an infinite one over an infinite scale) has
+             * code -127 */
+            if (q != q) q = -127.0f;
             if (q > 127.0f) q = 127.0f;
             if (q < -127.0f) q = -127.0f;
         }

@@ -214,6 +214,25 @@ def test_quantizer_ties_to_even():
     assert list(codes) == [127, 2, 4, -2, 0, 2]
 
 
+def test_quantizer_non_finite_weights():
+    # clamp(q) = min(max(q, -127), 127) with IEEE maxNum / minNum, which return
+    # the other operand when one is NaN: a NaN quotient has code -127.  The
+    # absmax skips a NaN (max |x| over the numbers), so a NaN weight in a
+    # finite block gets -127 and dequantizes to -127 s; an infinite weight
+    # makes s infinite, so the finite weights' quotients are 0 and the
+    # infinite one's is inf / inf = NaN
+    s_want = np.float32(np.float32(2.0) / np.float32(127.0))
+    codes, s, deq = oracle.quantize_block(_bf16([1.0, np.nan, -2.0, 0.0]))
+    assert s == s_want
+    assert list(codes) == [64, -127, -127, 0]     # 1 / (2/127) = 63.5 -> 64 (ties to even)
+    assert np.array_equal(deq, _bf16(np.array([64, -127, -127, 0], np.float32) * s_want))
+    codes, s, deq = oracle.quantize_block(_bf16([1.0, np.inf, -3.0, np.nan]))
+    assert s == np.inf
+    assert list(codes) == [0, -127, 0, -127]
+    d = oracle.bf16_to_f32(deq)
+    assert np.isnan(d[0]) and d[1] == -np.inf and np.isnan(d[2]) and d[3] == -np.inf   # 0 * inf, -127 * inf
+
+
 @pytest.mark.parametrize("n_d,psi,pad,block", [(2, 5000, 8, 2048), (4, 1003, 1, 256),
                                                (3, 7000, 64, 2048), (8, 100, 8, 32)])
 def test_quant_gather_blocks_follow_shards(n_d, psi, pad, block):
