@@ -406,26 +406,31 @@ ZERO_API zero_status zero_debug_wait_timeout(zero_dev_scalars* scalars_dev, long
                                              void* stream);
 
 /* ------------------------------------------------- allocation-free step --- */
-/* The pages have no counterpart to this entry point; it serves callers that
- * cannot allocate device memory for a workspace: code running where
- * cudaMalloc is not allowed (for example while a stream is being captured
- * into a CUDA graph without a memory pool), programs whose device memory is
- * owned by another allocator that hands out no extra buffers, and
- * latency-bound services that forbid allocation once they are running.
+/* The pages have no counterpart to this entry point.  It serves callers
+ * that cannot allocate device memory for a workspace:
+ *   - plug-ins and callbacks running inside a host framework that owns all
+ *     device memory and hands them no extra buffers;
+ *   - long-running services that forbid allocation once started, because a
+ *     cudaMalloc may synchronise the device and its latency is unbounded;
+ *   - programs whose memory budget is committed up front to a fixed pool,
+ *     where a later allocation would fail.
  *
  * It is zero_step_fused with the caller's workspace replaced by one scratch
  * array that lives in the library (a file-scope __device__ array of
  * ZERO_NOALLOC_SCRATCH_BYTES = 32 KB of partial sums + 4 MB for the reduced
  * gradient; every GPU that loads the library holds it until the process
- * exits).  The call allocates nothing and calls no cudaMalloc/cudaFree.
+ * exits).  The call allocates nothing: no cudaMalloc, no cudaFree, no
+ * allocating library routine.  The caller still passes every input and
+ * output buffer.
  *   - Limit: requests whose zero_workspace_bytes(plan, hp) exceeds the
  *     scratch -- clipping with n_d > 4 and n_d*S > 2^20 parameters -- are
  *     rejected with ZERO_ERR_BOUNDS before anything is launched.  Without
  *     clipping, or with n_d <= 4, any size is accepted.
  *   - Set-up: the first call on a device (with that device current) looks up
- *     the scratch's device address once; make that first call before any
- *     stream capture.
- *   - Every call shares the one scratch array and it keeps the last call's
+ *     the scratch's device address, and so does the first call after a
+ *     device reset (a new context may place the array elsewhere); make that
+ *     first call before any stream capture.
+ *   - Every call shares the one scratch array, which keeps the last call's
  *     contents; each call writes every scratch entry it reads, so nothing has
  *     to be cleared.  Calls that overlap on the GPU (other streams, other
  *     threads, other plans) race on the scratch: order them on one stream.

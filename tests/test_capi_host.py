@@ -254,3 +254,12 @@ def test_overlapping_state_arrays_are_refused(z):
     assert step(S1, S2, S3, T1, T2, S1 + 2048) == 1            # an output overlaps another input
     assert step(S1, S1 + 2048, S3, S1, S1 + 2048, S3) == 1     # in place, but m overlaps master
     assert _raw(z, "zero_adam_shard_step", h, hpp, A, S1, S1 + 16, S3, None, A, None) == 1   # m overlaps master
+
+
+def test_noalloc_scratch_size_matches_the_header(z):
+    # the binding's constant is the header's ZERO_NOALLOC_SCRATCH_BYTES
+    with open(os.path.join(ROOT, "include", "zero.h")) as f:
+        m = re.search(r"#define ZERO_NOALLOC_SCRATCH_BYTES \((\d+)u \+ (\d+)u \* \(1u << (\d+)\)\)", f.read())
+    assert m is not None
+    a, b, c = (int(x) for x in m.groups())
+    assert z.NOALLOC_SCRATCH_BYTES == a + b * (1 << c)

@@ -15,7 +15,7 @@ Importing this package fails if libzero.so has not been built.
 import ctypes
 
 from . import _capi
-from ._capi import (ZERO_BF16, ZERO_FP16, ZERO_DEV_TIMEOUT, ZeroDevScalars, ZeroError, ZeroHparams, hparams,
+from ._capi import (NOALLOC_SCRATCH_BYTES, ZERO_BF16, ZERO_FP16, ZERO_DEV_TIMEOUT, ZeroDevScalars, ZeroError, ZeroHparams, hparams,
                     zero_abi_version, zero_adam_shard_step, zero_all_gather, zero_debug_wait_timeout,
                     zero_dev_scalars_size, zero_grad_sqnorm, zero_launch_count, zero_plan_comm_volume, zero_plan_create,
                     zero_plan_create_ex, zero_plan_destroy, zero_plan_memory, zero_plan_query, zero_quant_gather,
@@ -25,7 +25,7 @@ from ._capi import (ZERO_BF16, ZERO_FP16, ZERO_DEV_TIMEOUT, ZeroDevScalars, Zero
                     zero_step_fused_accum, zero_debug_stream_timeout, zero_step_fused_qgz_qgather, rank_ptrs)
 
 __all__ = ["Plan", "StepBuffers", "read_scalars", "row_len", "hparams", "rank_ptrs", "ZeroError", "ZeroHparams",
-           "ZERO_BF16", "ZERO_FP16", "ZERO_DEV_TIMEOUT"] + [n for n in dir(_capi) if n.startswith("zero_")]
+           "ZERO_BF16", "ZERO_FP16", "ZERO_DEV_TIMEOUT", "NOALLOC_SCRATCH_BYTES"] + [n for n in dir(_capi) if n.startswith("zero_")]
 
 
 class Plan:

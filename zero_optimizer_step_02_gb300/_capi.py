@@ -17,6 +17,7 @@ ZERO_BF16 = 0
 ZERO_FP16 = 1
 ZERO_MAX_RANKS = 256
 ZERO_DEV_TIMEOUT = 1
+NOALLOC_SCRATCH_BYTES = 32768 + 4 * (1 << 20)   # ZERO_NOALLOC_SCRATCH_BYTES
 
 STATUS = {0: "ZERO_OK", 1: "ZERO_ERR_INVALID_ARG", 2: "ZERO_ERR_MISALIGNED", 3: "ZERO_ERR_UNSUPPORTED",
           4: "ZERO_ERR_CUDA", 5: "ZERO_ERR_TIMEOUT", 6: "ZERO_ERR_BOUNDS"}
@@ -304,8 +305,13 @@ def zero_debug_stream_timeout(kernel, scratch, scalars, timeout_ns, stream=None)
 
 def zero_step_fused_noalloc(plan, hp, rank_grads, master_in, m_in, v_in, master_out, m_out, v_out, lp_out,
                             scalars, stream=None):
-    """zero_step_fused without a workspace argument: for callers that cannot
-    allocate device memory (see include/zero.h for the limit and set-up)."""
+    """zero_step_fused without a workspace argument, for callers that cannot
+    allocate device memory: the library's own scratch array of
+    NOALLOC_SCRATCH_BYTES serves as the workspace.  Its limit (clipping with
+    n_d > 4 needs n_d*S <= 2^20), its set-up (the first call on a device, and
+    after a device reset, looks up the array's address: make it before any
+    stream capture) and its sharing rule (overlapping calls race on the one
+    array) are stated in include/zero.h."""
     _check(_lib.zero_step_fused_noalloc(plan, ctypes.byref(hp), _ptr_array(rank_grads), _addr(master_in),
                                         _addr(m_in), _addr(v_in), _addr(master_out), _addr(m_out), _addr(v_out),
                                         _addr(lp_out), _addr(scalars), _stream(stream)),

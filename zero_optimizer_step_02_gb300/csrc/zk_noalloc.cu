@@ -2,7 +2,10 @@
 // cannot allocate a workspace.  The workspace becomes one scratch array that
 // lives in this library (file scope, __device__), so the call allocates
 // nothing.  Contract and limits: include/zero.h.
+#include <cuda.h>
 #include <cuda_runtime.h>
+
+#include <mutex>
 
 #include "zero.h"
 
@@ -16,25 +19,78 @@ constexpr size_t kScratchBytes = ZERO_NOALLOC_SCRATCH_BYTES;
 // looked up below.
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
+// The scratch's device address belongs to the context the library's module
+// was loaded into: a device reset (cudaDeviceReset, or the primary context
+// destroyed and made again) loads the module anew and may move it.  So the
+// address is kept per device together with the id of the context it was
+// looked up in (context ids are never reused within a process), and looked
+// up again when the current context is another one.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+struct DriverFns {
+    CtxGetCurrentFn get_current = nullptr;
+    CtxGetIdFn get_id = nullptr;
+};
+
+const DriverFns& driver_fns()
+{
+    static DriverFns fns;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fns.get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fns.get_id = reinterpret_cast<CtxGetIdFn>(f);
+    });
+    return fns;
+}
+
+// id of the calling thread's current context; 0 when there is none (or the
+// driver cannot say)
+unsigned long long current_context_id()
+{
+    const DriverFns& d = driver_fns();
+    if (d.get_current == nullptr || d.get_id == nullptr) return 0;
+    CUcontext ctx = nullptr;
+    if (d.get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+    unsigned long long id = 0;
+    if (d.get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
 constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices];
-int g_scratch_ready[kMaxDevices];
+struct ScratchEntry {
+    unsigned long long ctx_id;  // context the address was looked up in (0: none yet)
+    void* addr;
+};
+ScratchEntry g_entry[kMaxDevices];
+std::mutex g_entry_mutex;
 
 // Device address of g_scratch on the current device, looked up once per
-// device (the first call on a device does it with that device current).
+// device and context (with that device current).
 zero_status scratch_address(void** out)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return ZERO_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return ZERO_ERR_BOUNDS;
-    if (!__atomic_load_n(&g_scratch_ready[dev], __ATOMIC_ACQUIRE)) {
+    const unsigned long long ctx = current_context_id();
+    std::lock_guard<std::mutex> lock(g_entry_mutex);
+    ScratchEntry& e = g_entry[dev];
+    if (e.addr == nullptr || ctx == 0 || ctx != e.ctx_id) {
         void* p = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
-        if (e != cudaSuccess || p == nullptr) return ZERO_ERR_CUDA;
-        g_scratch_addr[dev] = p;
-        __atomic_store_n(&g_scratch_ready[dev], 1, __ATOMIC_RELEASE);
+        const cudaError_t err = cudaGetSymbolAddress(&p, g_scratch);
+        if (err != cudaSuccess || p == nullptr) return ZERO_ERR_CUDA;
+        e.addr = p;
+        // the lookup makes the device's primary context current if it was not
+        e.ctx_id = ctx != 0 ? ctx : current_context_id();
     }
-    *out = g_scratch_addr[dev];
+    *out = e.addr;
     return ZERO_OK;
 }
 
