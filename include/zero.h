@@ -53,6 +53,7 @@ extern "C" {
 #define ZERO_MAX_RANKS 256      /* largest n_d */
 #define ZERO_MAX_SHARD_PAD 4096 /* largest shard_pad */
 #define ZERO_MAX_MICRO_BATCHES 65536 /* largest gradient-accumulation count */
+#define ZERO_MAX_LAYERS 65536   /* largest layer count of zero_step_layers */
 
 typedef enum {
     ZERO_OK = 0,
@@ -382,6 +383,59 @@ ZERO_API zero_status zero_step_fused_qgz_qgather(const zero_plan* plan, const ze
                                                  float* v_out, signed char* codes_out, float* scales_out,
                                                  void* gathered_bf16, zero_dev_scalars* scalars_dev, void* ws,
                                                  void* stream);
+
+/* ------------------------------------------------------- ZeRO-3 layer loop --- */
+/* One ZeRO-3 step over a stack of layers (itwiki "ZeRO-DP의 세 단계" and
+ * "왜 통신량이 늘지 않는가": with stage 3 each layer's parameters are
+ * all-gathered before they are used, in the forward and again in the
+ * backward pass, and each layer's gradients are reduce-scattered to their
+ * owners; itwiki "DeepSpeed에서 쓰기": overlap_comm and the stage-3 prefetch
+ * overlap the next layer's gather with the current layer's work).
+ *
+ * Per layer l = 0 .. n_layers-1, in order:
+ *   gather(l): zero_all_gather of layer l's 16-bit shards into
+ *              gathered[l % n_gathered], `gathers` times (1: once per step;
+ *              2: forward and backward, the pages' 3-Psi volume);
+ *   step(l):   zero_step_fused of layer l, in place (stage 3: the updated
+ *              16-bit shards overwrite shards_lp).
+ * gather(l) reads the shards as the previous step left them; step(l) comes
+ * after gather(l).  With gather_stream a stream other than `stream` (and
+ * n_gathered >= 2), every gather runs on gather_stream, ordered by events:
+ * gather(l+1) is issued before step(l) so the two overlap, gather(l) waits
+ * for step(l - n_gathered) (the last user of its buffer), step(l) waits for
+ * gather(l), and `stream` waits for gather_stream at the end; the call's work
+ * is complete when `stream` is.  gather_stream NULL (or n_gathered 1): all
+ * on `stream`, gather(l+1) after step(l).  The results do not depend on the
+ * schedule.
+ *
+ * Every layer's Adam takes the same step t (scalars_dev is one block for the
+ * stack, committed once per call).  Each layer has its own stage-3 plan;
+ * all plans share n_d and the dtypes.  gathered: host array of n_gathered
+ * device pointers (1 <= n_gathered <= n_layers), buffer k holding at least
+ * Psi_l 16-bit values for every layer l with l % n_gathered == k.  Per layer:
+ * rank_grads as in zero_step_fused; master, m, v of n_d*S_l floats, updated
+ * in place; shards_lp n_d*S_l 16-bit (plan parameter dtype), 16-byte
+ * aligned.  No clipping or loss scaling across layers (ZERO_ERR_UNSUPPORTED:
+ * the global norm and the overflow check would span every layer).  Events
+ * are created and released inside the call; no device memory is allocated.  */
+typedef struct {
+    const zero_plan* plan;         /* this layer's partition, stage 3             */
+    const void* const* rank_grads; /* host array of n_d device pointers           */
+    float* master;                 /* n_d*S fp32, in place                        */
+    float* m;
+    float* v;
+    void* shards_lp;               /* n_d*S 16-bit parameter shards, flat         */
+    void* grads_ready;             /* cudaEvent_t or NULL: step(l) waits for it
+                                      (the copy or backward pass that wrote the
+                                      layer's rank gradients)                     */
+    void* stepped;                 /* cudaEvent_t or NULL: recorded on `stream`
+                                      after step(l) (its gradient buffers may be
+                                      refilled, its shards read, from then on)    */
+} zero_layer;
+
+ZERO_API zero_status zero_step_layers(const zero_hparams* hp, int n_layers, const zero_layer* layers, int gathers,
+                                      int n_gathered, void* const* gathered, zero_dev_scalars* scalars_dev,
+                                      void* stream, void* gather_stream);
 
 /* ----------------------------------------------------------- diagnostics --- */
 /* Launch one kernel that waits on a barrier nothing completes, with a wait

@@ -263,3 +263,44 @@ def test_noalloc_scratch_size_matches_the_header(z):
     assert m is not None
     a, b, c = (int(x) for x in m.groups())
     assert z.NOALLOC_SCRATCH_BYTES == a + b * (1 << c)
+
+
+def test_layer_loop_argument_checks(z):
+    A, B = 0x10000, 0x20000
+    S1, S2, S3, LP = 0x100000, 0x200000, 0x300000, 0x400000
+    hp = z.hparams(lr=1e-3)
+    p3 = z.Plan(1000, 2, stage=3)
+    p3b = z.Plan(2000, 2, stage=3)
+    p2 = z.Plan(1000, 2, stage=2)
+    p4 = z.Plan(1000, 4, stage=3)
+    ranks = (ctypes.c_void_p * 2)(A, B)
+    ranks4 = (ctypes.c_void_p * 4)(A, B, A, B)
+    gathered = (ctypes.c_void_p * 2)(A, B)
+
+    def stack(*plans):
+        arr = (z.ZeroLayer * len(plans))()
+        for i, p in enumerate(plans):
+            r = ranks4 if p is p4 else ranks
+            arr[i] = z.ZeroLayer(p.handle, ctypes.cast(r, ctypes.c_void_p), S1, S2, S3, LP, None, None)
+        return arr
+
+    def call(h, layers, gathers=1, n_gathered=2, g=gathered, sc=A):
+        return _raw(z, "zero_step_layers", ctypes.byref(h), len(layers), layers, gathers, n_gathered, g, sc, None,
+                    None)
+
+    # no clipping or loss scaling across layers
+    assert call(z.hparams(max_norm=1.0), stack(p3, p3b)) == 3
+    assert call(z.hparams(loss_scaling=True), stack(p3, p3b)) == 3
+    # only stage-3 plans, all with the same n_d
+    assert call(hp, stack(p3, p2)) == 1
+    assert call(hp, stack(p3, p4)) == 1
+    # gathers 1 or 2; 1 <= n_gathered <= n_layers; aligned buffers and scalars
+    assert call(hp, stack(p3, p3b), gathers=3) == 1
+    assert call(hp, stack(p3, p3b), n_gathered=0) == 1
+    assert call(hp, stack(p3, p3b), n_gathered=3) == 1
+    assert call(hp, stack(p3, p3b), g=(ctypes.c_void_p * 2)(A, B + 8)) == 2
+    assert call(hp, stack(p3, p3b), sc=A + 16) == 2
+    # a misaligned shard buffer
+    bad = stack(p3, p3b)
+    bad[1].shards_lp = LP + 2
+    assert call(hp, bad) == 2

@@ -171,51 +171,3 @@ def test_newer_kernels_write_only_their_buffers(n_d, psi, pad, clip):
     for name, (whole, _) in bufs.items():
         assert _intact(whole), "a kernel wrote outside the %s buffer" % name
     assert z.read_scalars(sc).status == 0
-
-
-def test_zero3_loop_with_gathers_on_a_second_stream():
-    # the overlapped ZeRO-3 schedule: layer l+1's gather runs on a second
-    # stream while layer l's step runs; a gather waits for the step that last
-    # wrote its shards, a step for its layer's gather
-    n_d = 8
-    sizes = [70_001, 4096 * 16 + 3, 123_457]
-    hp = z.hparams(lr=1e-3)
-    jobs = [Job(psi, n_d, stage=3, pad=8, hp=hp, seed=200 + i) for i, psi in enumerate(sizes)]
-    comp = torch.cuda.current_stream()
-    gs = torch.cuda.Stream()
-    gathered = [torch.zeros(j.psi, dtype=torch.bfloat16, device="cuda") for j in jobs]
-    stepped = [None] * len(jobs)
-    for step in range(1, 4):
-        for job in jobs:
-            job.new_grads(step)
-        want = []
-        for job in jobs:
-            S = job.plan.shard
-            want.append(oracle.all_gather_u16([job.o_lp_shards[r * S:(r + 1) * S] for r in range(n_d)], job.psi, S))
-        ev_gathered = [torch.cuda.Event() for _ in jobs]
-
-        def gather(l):
-            job = jobs[l]
-            S = job.plan.shard
-            if stepped[l] is not None:
-                gs.wait_event(stepped[l])
-            z.zero_all_gather(job.plan.handle, [job.buf.lp[r * S:(r + 1) * S] for r in range(n_d)], gathered[l],
-                              job.buf.scalars, gs)
-            ev_gathered[l].record(gs)
-
-        gs.wait_stream(comp)
-        gather(0)
-        for l, job in enumerate(jobs):
-            if l + 1 < len(jobs):
-                gather(l + 1)
-            comp.wait_event(ev_gathered[l])
-            job.gpu_step()
-            ev = torch.cuda.Event()
-            ev.record(comp)
-            stepped[l] = ev
-        comp.wait_stream(gs)
-        torch.cuda.synchronize()
-        for l, job in enumerate(jobs):
-            assert np.array_equal(u16(gathered[l]), want[l])
-            job.oracle_step()
-            job.assert_bit_exact()

@@ -56,6 +56,15 @@ _lib = ctypes.CDLL(LIB_PATH)
 _vp, _ll, _i32, _f32, _f64, _sz = (ctypes.c_void_p, ctypes.c_longlong, ctypes.c_int, ctypes.c_float,
                                    ctypes.c_double, ctypes.c_size_t)
 _hp = ctypes.POINTER(ZeroHparams)
+
+
+class ZeroLayer(ctypes.Structure):
+    """zero_layer of zero.h: one layer of the ZeRO-3 layer loop."""
+    _fields_ = [("plan", ctypes.c_void_p), ("rank_grads", ctypes.c_void_p), ("master", ctypes.c_void_p),
+                ("m", ctypes.c_void_p), ("v", ctypes.c_void_p), ("shards_lp", ctypes.c_void_p),
+                ("grads_ready", ctypes.c_void_p), ("stepped", ctypes.c_void_p)]
+
+
 _SIGS = {
     "zero_status_str": (ctypes.c_char_p, [_i32]),
     "zero_abi_version": (_i32, []),
@@ -88,6 +97,7 @@ _SIGS = {
     "zero_step_fused_qgz": (_i32, [_vp, _hp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "zero_step_fused_qgz_qgather": (_i32, [_vp, _hp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                            _vp, _vp, _vp]),
+    "zero_step_layers": (_i32, [_hp, _i32, ctypes.POINTER(ZeroLayer), _i32, _i32, _vp, _vp, _vp, _vp]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -316,6 +326,48 @@ def zero_step_fused_noalloc(plan, hp, rank_grads, master_in, m_in, v_in, master_
                                         _addr(m_in), _addr(v_in), _addr(master_out), _addr(m_out), _addr(v_out),
                                         _addr(lp_out), _addr(scalars), _stream(stream)),
            "zero_step_fused_noalloc")
+
+
+def _event(ev):
+    """cudaEvent_t of a torch.cuda.Event (recorded once if torch has not
+    created it yet), an int handle, or None."""
+    if ev is None or isinstance(ev, int):
+        return ev
+    if not ev.cuda_event:
+        ev.record()
+    return ev.cuda_event
+
+
+class LayerStack:
+    """The zero_layer array of a stack of layers, built once (the pointers it
+    holds stay valid while the caller keeps the tensors alive and in place).
+    layers: sequence of (plan_handle, rank_grads, master, m, v, shards_lp
+    [, grads_ready, stepped]), rank_grads a list of per-rank tensors or a
+    rank_ptrs array, the two events torch.cuda.Event objects or None."""
+
+    def __init__(self, layers):
+        self._ranks = [_ptr_array(l[1]) for l in layers]
+        self.array = (ZeroLayer * len(layers))()
+        for i, l in enumerate(layers):
+            plan, _, master, m, v, shards = l[:6]
+            ready, stepped = (tuple(l[6:8]) + (None, None))[:2]
+            self.array[i] = ZeroLayer(plan, ctypes.cast(self._ranks[i], ctypes.c_void_p), _addr(master), _addr(m),
+                                      _addr(v), _addr(shards), _event(ready), _event(stepped))
+
+    def __len__(self):
+        return len(self.array)
+
+
+def zero_step_layers(hp, layers, gathers, gathered, scalars, stream=None, gather_stream=None):
+    """One ZeRO-3 step over a stack of layers: layer l's gather(s) into
+    gathered[l % len(gathered)], then its fused step; with gather_stream the
+    gathers run there, the next layer's overlapping this layer's step.
+    layers: a LayerStack (or the sequence it is built from)."""
+    stack = layers if isinstance(layers, LayerStack) else LayerStack(layers)
+    gptr = _ptr_array(gathered)
+    gs = None if gather_stream is None else _stream(gather_stream)
+    _check(_lib.zero_step_layers(ctypes.byref(hp), len(stack), stack.array, gathers, len(gptr), gptr,
+                                 _addr(scalars), _stream(stream), gs), "zero_step_layers")
 
 
 def zero_launch_count():

@@ -862,6 +862,116 @@ ZERO_API zero_status zero_debug_stream_timeout(int kernel, void* scratch, zero_d
     return from_cuda(zk::launch_stream(zk::OP_REDUCE, ZERO_BF16, ZERO_BF16, a, as_stream(stream)));
 }
 
+namespace {
+
+// Events of one zero_step_layers call (created per call, released at its end:
+// an event destroyed while work it waits on is pending is released when that
+// work completes).
+struct EventSet {
+    cudaEvent_t* ev = nullptr;
+    int n = 0;
+    explicit EventSet(int count)
+    {
+        ev = new (std::nothrow) cudaEvent_t[count];
+        if (ev == nullptr) return;
+        for (; n < count; ++n)
+            if (cudaEventCreateWithFlags(&ev[n], cudaEventDisableTiming) != cudaSuccess) break;
+    }
+    bool ok(int count) const { return ev != nullptr && n == count; }
+    ~EventSet()
+    {
+        for (int i = 0; i < n; ++i) cudaEventDestroy(ev[i]);
+        delete[] ev;
+    }
+    EventSet(const EventSet&) = delete;
+    EventSet& operator=(const EventSet&) = delete;
+};
+
+}  // namespace
+
+ZERO_API zero_status zero_step_layers(const zero_hparams* hp, int n_layers, const zero_layer* layers, int gathers,
+                                      int n_gathered, void* const* gathered, zero_dev_scalars* sc, void* stream,
+                                      void* gather_stream)
+{
+    ZK_CALL_RANGE();
+    zero_status s;
+    if ((s = check_hparams(hp)) != ZERO_OK) return s;
+    if (hp->max_norm > 0.0f || hp->loss_scaling) return ZERO_ERR_UNSUPPORTED;
+    if (layers == nullptr || n_layers < 1 || n_layers > ZERO_MAX_LAYERS) return ZERO_ERR_INVALID_ARG;
+    if (gathers < 1 || gathers > 2) return ZERO_ERR_INVALID_ARG;
+    if (gathered == nullptr || n_gathered < 1 || n_gathered > n_layers) return ZERO_ERR_INVALID_ARG;
+    for (int k = 0; k < n_gathered; ++k)
+        if ((s = check_dev(gathered[k])) != ZERO_OK) return s;
+    if ((s = check_dev(sc, 256)) != ZERO_OK) return s;
+    const zero_plan* p0 = layers[0].plan;
+    for (int l = 0; l < n_layers; ++l) {
+        const zero_layer& L = layers[l];
+        const zero_plan* p = L.plan;
+        if (p == nullptr || p->stage != 3) return ZERO_ERR_INVALID_ARG;
+        if (p->n_d != p0->n_d || p->grad_dtype != p0->grad_dtype || p->param_dtype != p0->param_dtype)
+            return ZERO_ERR_INVALID_ARG;
+        if ((s = check_ranks(p, L.rank_grads)) != ZERO_OK) return s;
+        if ((s = check_state(p, L.master, L.m, L.v, L.master, L.m, L.v)) != ZERO_OK) return s;
+        if ((s = check_dev(L.shards_lp)) != ZERO_OK) return s;
+    }
+    const cudaStream_t st = as_stream(stream);
+    // a second stream needs a second gathered buffer: with one, every gather
+    // waits for the step before it, which leaves nothing to overlap
+    const cudaStream_t gs = gather_stream != nullptr && n_gathered >= 2 ? as_stream(gather_stream) : st;
+    const bool two = gs != st;
+    // events: [0] the call's start on `stream`, [1 + l] layer l gathered,
+    // [1 + n + l] layer l stepped, [1 + 2n] the gather stream's end
+    const int n_ev = two ? 2 * n_layers + 2 : 0;
+    EventSet ev(n_ev);
+    if (two && !ev.ok(n_ev)) return ZERO_ERR_CUDA;
+    const int n_d = p0->n_d;
+    const void* shard_ptr[ZERO_MAX_RANKS];
+
+    // gather(l): layer l's 16-bit shards into gathered[l % n_gathered], once
+    // or twice (forward and backward); it waits for the step that last used
+    // that buffer (layer l - n_gathered) -- its own shards were last written
+    // before this call, which the gather stream waits for at the start
+    auto gather = [&](int l) -> zero_status {
+        const zero_layer& L = layers[l];
+        const zero_plan* p = L.plan;
+        if (two && l >= n_gathered) ZK_TRY(cudaStreamWaitEvent(gs, ev.ev[1 + n_layers + l - n_gathered], 0));
+        const size_t eb = 2;   // 16-bit parameters
+        for (int r = 0; r < n_d; ++r)
+            shard_ptr[r] = static_cast<const unsigned char*>(L.shards_lp) + eb * static_cast<size_t>(r) * p->shard;
+        for (int g = 0; g < gathers; ++g)
+            ZK_TRY(zk::launch_all_gather(shard_ptr, n_d, p->shard, p->psi, gathered[l % n_gathered], sc, gs));
+        if (two) ZK_TRY(cudaEventRecord(ev.ev[1 + l], gs));
+        return ZERO_OK;
+    };
+
+    if (two) {
+        ZK_TRY(cudaEventRecord(ev.ev[0], st));
+        ZK_TRY(cudaStreamWaitEvent(gs, ev.ev[0], 0));
+    }
+    if ((s = gather(0)) != ZERO_OK) return s;
+    for (int l = 0; l < n_layers; ++l) {
+        // the next layer's gather is issued before this layer's step, so that
+        // with two streams it runs while the step does
+        if (two && l + 1 < n_layers && (s = gather(l + 1)) != ZERO_OK) return s;
+        if (two) ZK_TRY(cudaStreamWaitEvent(st, ev.ev[1 + l], 0));
+        const zero_layer& L = layers[l];
+        if (L.grads_ready != nullptr) ZK_TRY(cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(L.grads_ready), 0));
+        // no scalar commit per layer: every layer's Adam takes this step's t
+        if ((s = run_fused(L.plan, hp, L.rank_grads, L.master, L.m, L.v, L.master, L.m, L.v, L.shards_lp, 0, sc,
+                           st)) != ZERO_OK)
+            return s;
+        if (two) ZK_TRY(cudaEventRecord(ev.ev[1 + n_layers + l], st));
+        if (L.stepped != nullptr) ZK_TRY(cudaEventRecord(static_cast<cudaEvent_t>(L.stepped), st));
+        if (!two && l + 1 < n_layers && (s = gather(l + 1)) != ZERO_OK) return s;
+    }
+    if (two) {
+        ZK_TRY(cudaEventRecord(ev.ev[1 + 2 * n_layers], gs));
+        ZK_TRY(cudaStreamWaitEvent(st, ev.ev[1 + 2 * n_layers], 0));
+    }
+    // the step scalars advance once for the whole stack
+    return from_cuda(zk::launch_epilogue(*hp, sc, st));
+}
+
 ZERO_API unsigned long long zero_launch_count(void) { return zk::launch_count(); }
 
 }  // extern "C"
