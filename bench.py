@@ -2,22 +2,28 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
                     [--config 1..5] [--nd N] [--qgather] [--qgz] [--accum K]
-                    [--offload] [--overlap] [--gathers 1|2] [--row-pad N]
+                    [--offload] [--serial] [--gathers 1|2] [--row-pad N]
+                    [--param-dtype bf16|fp16] [--stage 1|2]
                     [--psi N] [--no-cpu-baseline] [--no-e2e]
 
 A step is one pass of the whole hot path (reduce-scatter of the simulated
 ranks' gradients, global checks, Adam on every shard, 16-bit cast and gather)
 over one batch of synthetic gradients already resident in HBM.  The default
-workload is the GPT-2-small one: Psi = 124,439,808 flat parameters, N_d = 8
-simulated ranks, bf16 gradients ~N(0, 1e-2) with a 1% x100 tail, AdamW
-(lr 3e-4, betas 0.9/0.95, wd 0.1), global-norm clipping at 1.0.
+workload is the largest that fits one GPU: the ZeRO-3 layer-wise step over 8
+Llama-3-8B-shaped decoder layers (Psi_l = 218,112,000 each), N_d = 16
+simulated ranks, bf16 gradients ~N(0, 1e-3), Adam lr 1e-3; per layer the
+all-gather of its bf16 shards, then the reduce-scatter of its ranks'
+gradients, Adam and the bf16 shards, through one call of the layer loop
+(the next layer's gather on a second stream).  --config 2 is the GPT-2-small
+clipped ZeRO-2 step, --config 3 the GPT-2 1.5B fp16 loss-scaled step,
+--config 5 the N_d sweep at Psi = 2^28, --config 1 the small parity case.
 
 One JSON line is printed (rank 0).  value = parameters updated per second over
 the whole job; roofline = the dominant kernel's algorithmic bytes per launch
 over its CUDA-event duration, against the measured HBM copy bandwidth;
 cpu_baseline = the CPU oracle timed on a bounded sample on this host;
 e2e = the same metric with the gradients copied from pinned host memory and
-the gathered parameters copied back inside the timed region.
+the updated 16-bit parameters copied back inside the timed region.
 
 --gpus N under torchrun runs N independent replicas (one per GPU): the
 ranks of the method are buffers inside one GPU, so nothing is exchanged
@@ -43,10 +49,18 @@ L2_BYTES = 129 * 1024 * 1024
 
 
 # ----------------------------------------------------------------- workloads
-def workload(cfg, nd=None, qgather=False, psi=None, qgz=False, gathers=1, offload=False, accum=1, overlap=False):
+def workload(cfg, nd=None, qgather=False, psi=None, qgz=False, gathers=1, offload=False, accum=1, serial=False,
+             param_dtype=None, stage=None):
     """Sizes, hyper-parameters and the algorithmic bytes of one step.  psi
     overrides the parameter count (a smaller case of the same workload, for
-    profiling)."""
+    profiling).  serial: the ZeRO-3 layer loop with every gather on the step's
+    stream (default: the gathers on a second stream, the next layer's
+    overlapping this layer's step).  param_dtype ("bf16"/"fp16"): the 16-bit
+    parameter dtype (default bf16; the fp16-gradient workload pairs fp16
+    parameters with fp16 gradients when asked).  stage: 1 or 2 for the ZeRO-1/2
+    workloads (the same math; the label and the plan's stage)."""
+    args = dict(cfg=cfg, nd=nd, qgather=qgather, psi=psi, qgz=qgz, gathers=gathers, offload=offload, accum=accum,
+                serial=serial, param_dtype=param_dtype, stage=stage)
     if cfg == 1:
         w = dict(name="zero2_psi1000003_nd4_adam", psi=1_000_003, n_d=4, stage=2, pad=8, gdt="bf16",
                  sigma=1e-3, tail=False, lr=1e-3, b2=0.999, wd=0.0, clip=0.0, ls=False, layers=1)
@@ -84,12 +98,26 @@ def workload(cfg, nd=None, qgather=False, psi=None, qgz=False, gathers=1, offloa
         # optimizer state in page-locked host memory, read and written over the CPU-GPU link
         w["offload"] = True
         w["name"] += "_offload"
-    if overlap:
-        if w["stage"] != 3:
-            raise SystemExit("--overlap applies to the ZeRO-3 layer loop (config 4)")
+    if w["stage"] == 3:
         # the next layer's gather on a second stream while this layer's step runs
-        w["overlap"] = True
-        w["name"] += "_overlap"
+        # (the layer loop's overlap), unless asked to keep one stream
+        w["overlap"] = not serial
+        if serial:
+            w["name"] += "_serial"
+    elif serial:
+        raise SystemExit("--serial applies to the ZeRO-3 layer loop (config 4)")
+    w["pdt"] = "bf16"
+    if param_dtype:
+        if w.get("qgather") and param_dtype != "bf16":
+            raise SystemExit("the int8 gather takes bf16 parameters")
+        w["pdt"] = param_dtype
+        w["name"] += "_params_" + param_dtype
+    if stage:
+        if w["stage"] == 3 or stage not in (1, 2):
+            raise SystemExit("--stage 1|2 applies to the ZeRO-1/2 workloads (configs 1, 2, 3, 5)")
+        if stage != w["stage"]:
+            w["stage"] = stage
+            w["name"] = ("zero%d" % stage) + w["name"][5:]
     if accum > 1:
         if w["stage"] == 3 or w.get("qgz") or w.get("qgather") or offload or w["ls"]:
             raise SystemExit("--accum applies to the plain and clipped ZeRO-2 workloads (configs 1, 2, 5)")
@@ -131,7 +159,32 @@ def workload(cfg, nd=None, qgather=False, psi=None, qgz=False, gathers=1, offloa
     else:
         w["bytes_per_param"] = 2 * n_d + 26
     w["psi_total"] = w["psi"] * w["layers"]
+    w["args"] = args
     return w
+
+
+def workload_from_args(args):
+    w = workload(args.config, args.nd, args.qgather, args.psi, args.qgz, args.gathers, args.offload, args.accum,
+                 args.serial, args.param_dtype, args.stage)
+    if args.row_pad:
+        w["row_pad"] = args.row_pad
+        w["name"] += "_rowpad%d" % args.row_pad
+    return w
+
+
+def config_of(w, world):
+    """The JSON line's config: the workload by name and size (both arms print
+    the same)."""
+    small = w["psi_total"] * w["bytes_per_param"] < 4 * L2_BYTES
+    c = {"workload": w["name"], "psi": w["psi"], "layers": w["layers"], "n_d": w["n_d"], "stage": w["stage"],
+         "grad_dtype": w["gdt"], "param_dtype": w["pdt"], "clip": w["clip"], "loss_scaling": w["ls"],
+         "bytes_per_param": w["bytes_per_param"], "micro_batches": w.get("accum", 1),
+         "rank_row_pad": w.get("row_pad", 0), "parallelism": "replicas x%d" % world,
+         "l2": "flushed between steps" if small else "inputs larger than L2"}
+    if w["stage"] == 3:
+        c["gathers_per_layer"] = w.get("gathers", 1)
+        c["gather_stream"] = "second stream, overlapping the steps" if w.get("overlap") else "the step's stream"
+    return c
 
 
 # ------------------------------------------------------------------- clocks
@@ -252,9 +305,12 @@ class Job:
         from zero_optimizer_step_02_gb300 import synth
         self.z, self.torch, self.w = z, torch, w
         gdt = z.ZERO_FP16 if w["gdt"] == "fp16" else z.ZERO_BF16
+        pdt = z.ZERO_FP16 if w["pdt"] == "fp16" else z.ZERO_BF16
         self.hp = z.hparams(lr=w["lr"], beta1=0.9, beta2=w["b2"], eps=1e-8, weight_decay=w["wd"],
                             max_norm=w["clip"], loss_scaling=w["ls"])
-        self.plan = z.Plan(w["psi"], w["n_d"], stage=w["stage"], grad_dtype=gdt, shard_pad=w["pad"])
+        self.plan = z.Plan(w["psi"], w["n_d"], stage=w["stage"], grad_dtype=gdt, shard_pad=w["pad"],
+                           param_dtype=pdt)
+        lp_dt = torch.float16 if pdt == z.ZERO_FP16 else torch.bfloat16
         tdt = torch.float16 if gdt == z.ZERO_FP16 else torch.bfloat16
         row = z.row_len(w["psi"], w.get("row_pad", 0))
         scale = 1024.0 if w["ls"] else 1.0
@@ -282,14 +338,14 @@ class Job:
             self.m2 = [torch.zeros(n, device=device) for _ in range(L)]
             self.v2 = [torch.zeros(n, device=device) for _ in range(L)]
         lp_n = n if w["stage"] == 3 else w["psi"]
-        self.lp = [torch.zeros(lp_n, dtype=torch.bfloat16, device=device) for _ in range(L)]
+        self.lp = [torch.zeros(lp_n, dtype=lp_dt, device=device) for _ in range(L)]
         if w["stage"] == 3:
-            self.gathered = torch.zeros(w["psi"], dtype=torch.bfloat16, device=device)
-        if w.get("overlap"):
-            self.gathered2 = torch.zeros(w["psi"], dtype=torch.bfloat16, device=device)
-            self.gather_stream = torch.cuda.Stream(device=device)
-            self.ev_gathered = [torch.cuda.Event() for _ in range(w["layers"])]
-            self.ev_stepped = [None] * w["layers"]
+            # the ZeRO-3 layer loop: two gathered buffers used in turn (layer l
+            # into buffer l % 2), the gathers on a second stream unless serial
+            self.gathered = [torch.zeros(w["psi"], dtype=lp_dt, device=device) for _ in range(2)]
+            self.gather_stream = torch.cuda.Stream(device=device) if w.get("overlap") else None
+            self.stack = z.LayerStack([(self.plan.handle, self.ranks(l), self.master[l], self.m[l], self.v[l],
+                                        self.lp[l]) for l in range(L)])
         if w.get("qgather"):
             nbs = -(-self.plan.shard // 2048)
             self.gq_codes = torch.zeros(n, dtype=torch.int8, device=device)
@@ -324,13 +380,6 @@ class Job:
             self._rank_ptrs = [self.z.rank_ptrs([g[r] for r in range(n_d)]) for g in self.grads]
         return self._rank_ptrs[l % len(self.grads)]
 
-    def shard_ptrs(self, l):
-        """Layer l's 16-bit shards (ZeRO-3) as a pointer array, built once."""
-        if not hasattr(self, "_shard_ptrs"):
-            S, n_d = self.plan.shard, self.w["n_d"]
-            self._shard_ptrs = [self.z.rank_ptrs([x[r * S:(r + 1) * S] for r in range(n_d)]) for x in self.lp]
-        return self._shard_ptrs[l]
-
     def code_ptrs(self, k):
         if not hasattr(self, "_code_ptrs"):
             n_d = self.w["n_d"]
@@ -344,16 +393,15 @@ class Job:
         if w.get("accum"):
             self.step_accum()
             return
-        if w.get("overlap"):
-            self.step_zero3_overlap()
+        if w["stage"] == 3:
+            # one call for the stack: per layer its gather(s), then its fused
+            # step (reduce-scatter of its ranks' gradients, Adam, 16-bit shards)
+            z.zero_step_layers(self.hp, self.stack, w.get("gathers", 1), self.gathered, self.scalars,
+                               gather_stream=self.gather_stream)
+            self.k += 1
             return
         for l in range(w["layers"]):
-            gsel = l if w["layers"] > 1 else self.k
-            if w["stage"] == 3:
-                # per-layer gather of the bf16 shards before use (itwiki: ZeRO-3
-                # gathers each layer for the forward pass and again for the backward)
-                for _ in range(w.get("gathers", 1)):
-                    z.zero_all_gather(h, self.shard_ptrs(l), self.gathered, self.scalars)
+            gsel = self.k
             if w.get("qgz") and w.get("qgather"):
                 k = gsel % len(self.grads)
                 z.zero_step_fused_qgz_qgather(h, self.hp, self.code_ptrs(k), self.qscales[k], 2048, self.master[l],
@@ -378,38 +426,6 @@ class Job:
                 step = z.zero_step_fused_offload if self.offload else z.zero_step_fused
                 step(h, self.hp, self.ranks(gsel), self.master[l], self.m[l], self.v[l], self.master[l], self.m[l],
                      self.v[l], self.lp[l], self.scalars, self.ws)
-        self.k += 1
-
-    def step_zero3_overlap(self):
-        """The ZeRO-3 layer loop with layer l+1's gather(s) issued on a second
-        stream while layer l's reduce-scatter + Adam runs.  A gather waits for
-        the step that last wrote its layer's shards; a step waits for its
-        layer's gather (which reads the shards the step overwrites)."""
-        torch, z, w = self.torch, self.z, self.w
-        h = self.plan.handle
-        comp = torch.cuda.current_stream()
-        gs = self.gather_stream
-        bufs = (self.gathered, self.gathered2)
-
-        def gather(l):
-            if self.ev_stepped[l] is not None:
-                gs.wait_event(self.ev_stepped[l])
-            for _ in range(w.get("gathers", 1)):
-                z.zero_all_gather(h, self.shard_ptrs(l), bufs[l % 2], self.scalars, gs)
-            self.ev_gathered[l].record(gs)
-
-        gs.wait_stream(comp)
-        gather(0)
-        for l in range(w["layers"]):
-            if l + 1 < w["layers"]:
-                gather(l + 1)
-            comp.wait_event(self.ev_gathered[l])
-            z.zero_step_fused(h, self.hp, self.ranks(l), self.master[l], self.m[l], self.v[l], self.master[l],
-                              self.m[l], self.v[l], self.lp[l], self.scalars, self.ws)
-            ev = torch.cuda.Event()
-            ev.record(comp)
-            self.ev_stepped[l] = ev
-        comp.wait_stream(gs)
         self.k += 1
 
     def step_accum(self, sets=None):
@@ -456,11 +472,7 @@ def l2_flush(torch, device, buf=[]):
 def gpu_arm(args, rank, world, device):
     import torch
     import zero_optimizer_step_02_gb300 as z
-    w = workload(args.config, args.nd, args.qgather, args.psi, args.qgz, args.gathers, args.offload, args.accum,
-                 args.overlap)
-    if args.row_pad:
-        w["row_pad"] = args.row_pad
-        w["name"] += "_rowpad%d" % args.row_pad
+    w = workload_from_args(args)
     torch.cuda.set_device(device)
     job = Job(w, device)
     torch.cuda.synchronize()
@@ -627,12 +639,7 @@ def gpu_arm(args, rank, world, device):
     out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic", "impl": "gb300",
-           "config": {"workload": w["name"], "psi": w["psi"], "layers": w["layers"], "n_d": w["n_d"],
-                      "stage": w["stage"], "grad_dtype": w["gdt"], "clip": w["clip"], "loss_scaling": w["ls"],
-                      "bytes_per_param": w["bytes_per_param"], "micro_batches": w.get("accum", 1),
-                      "rank_row_pad": w.get("row_pad", 0),
-                      "parallelism": "replicas x%d" % world,
-                      "l2": "flushed between steps" if small else "inputs larger than L2"},
+           "config": config_of(w, world),
            "step_gbs": round(step_gbs, 1), "step_frac_of_peak": round(step_gbs / peak, 4),
            "step_frac_of_nominal": round(step_gbs / NOMINAL_HBM_GBS, 4),
            "roofline": roofline, "gpu_launches": int(launches), "e2e": e2e, "clocks": clk}
@@ -693,7 +700,9 @@ def e2e_measure(job, w, args, device, world):
     copy, every launch and the device-to-host read of each step's parameters
     lie inside the timed region."""
     import torch
-    if w["layers"] > 1 or w["psi"] * w["n_d"] * 2 > 8e9 or len(job.grads) < 2:
+    if w["layers"] > 1:
+        return e2e_layers(job, w, args, world)
+    if len(job.grads) < 2:
         return None
     z = job.z
     h = job.plan.handle
@@ -709,7 +718,7 @@ def e2e_measure(job, w, args, device, world):
         ht = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
         ht.copy_(t)
         host_in.append(ht)
-    host_out = torch.empty(job.lp[0].numel(), dtype=torch.bfloat16, pin_memory=True)
+    host_out = torch.empty(job.lp[0].numel(), dtype=job.lp[0].dtype, pin_memory=True)
     steps = max(1, min(args.steps, 10))
     k = w.get("accum", 1)
     n_sets = steps * k                       # gradient sets crossing the link
@@ -760,6 +769,64 @@ def e2e_measure(job, w, args, device, world):
             "inputs": "int8 codes + fp32 block scales of every rank" if qgz else "16-bit gradients of every rank"}
 
 
+def e2e_layers(job, w, args, world):
+    """The ZeRO-3 layer loop end to end: every step, every layer's rank
+    gradients are copied from pinned host memory (a copy stream, layer after
+    layer) and every layer's updated 16-bit shards copied back (a third
+    stream).  One call of the layer loop per step; layer l's step waits for
+    its gradients (grads_ready), and the next step's copy into layer l's
+    buffers waits for layer l's step and the read-back of its shards
+    (stepped), so copies, gathers and steps overlap across layers.  The
+    host holds two of the layers' gradient sets (layer l copies from set
+    l mod 2): the bytes crossing the link each step are every layer's."""
+    import torch
+    z = job.z
+    L = w["layers"]
+    steps = max(1, min(args.steps, 5))
+    host_in = []
+    for i in range(min(2, L)):
+        ht = torch.empty(job.grads[i].shape, dtype=job.grads[i].dtype, pin_memory=True)
+        ht.copy_(job.grads[i])
+        host_in.append(ht)
+    host_out = [torch.empty(job.lp[l].numel(), dtype=job.lp[l].dtype, pin_memory=True) for l in range(L)]
+    comp = torch.cuda.current_stream()
+    copy_s, out_s = torch.cuda.Stream(), torch.cuda.Stream()
+    ready = [torch.cuda.Event() for _ in range(L)]
+    stepped = [torch.cuda.Event() for _ in range(L)]
+    read_back = [torch.cuda.Event() for _ in range(L)]
+    stack = z.LayerStack([(job.plan.handle, job.ranks(l), job.master[l], job.m[l], job.v[l], job.lp[l], ready[l],
+                           stepped[l]) for l in range(L)])
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(comp)
+    copy_s.wait_event(a)
+    for step in range(steps):
+        for l in range(L):
+            if step > 0:
+                copy_s.wait_event(read_back[l])     # layer l's previous step and read-back are done
+            with torch.cuda.stream(copy_s):
+                job.grads[l].copy_(host_in[l % len(host_in)], non_blocking=True)
+            ready[l].record(copy_s)
+        z.zero_step_layers(job.hp, stack, w.get("gathers", 1), job.gathered, job.scalars,
+                           gather_stream=job.gather_stream)
+        for l in range(L):
+            out_s.wait_event(stepped[l])
+            with torch.cuda.stream(out_s):
+                host_out[l].copy_(job.lp[l], non_blocking=True)
+            read_back[l].record(out_s)
+    comp.wait_stream(copy_s)
+    comp.wait_stream(out_s)
+    b.record(comp)
+    torch.cuda.synchronize()
+    ms = dist_max(a.elapsed_time(b), world)
+    return {"value": world * w["psi_total"] * steps / (ms / 1e3), "unit": UNIT,
+            "h2d_bytes_per_step": sum(g.numel() * g.element_size() for g in job.grads[:L]),
+            "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in host_out), "steps": steps,
+            "overlap": "per-layer copies on two copy streams, ordered by the layer loop's events",
+            "inputs": "16-bit gradients of every rank of every layer (host holds two layers' sets, layer l "
+                      "copies set l mod 2)"}
+
+
 # ------------------------------------------------------------- CPU oracle arm
 def oracle_sample(w, budget_s, max_steps=None):
     """Time the CPU oracle (as it stands, one thread) on a bounded sample of the
@@ -771,6 +838,7 @@ def oracle_sample(w, budget_s, max_steps=None):
     psi = min(w["psi"], 4_000_000 * 8 // max(8, n_d * w.get("accum", 1)))
     rng = np.random.default_rng(1)
     dt = oracle.FP16 if w["gdt"] == "fp16" else oracle.BF16
+    pdt = oracle.FP16 if w["pdt"] == "fp16" else oracle.BF16
     scale = 1024.0 if w["ls"] else 1.0
     rows = [oracle.f32_to_lp((rng.standard_normal(psi) * w["sigma"] * scale).astype(np.float32), dt)
             for _ in range(n_d)]
@@ -801,8 +869,13 @@ def oracle_sample(w, budget_s, max_steps=None):
             # the step with its 16-bit output sharded, then the block-int8 gather of the shards
             oracle.zero_step(rows, dt, hp, st, w["pad"], 3, lp_shards=lp, gathered=gath)
             oracle.quant_gather(lp, n_d, psi, S, 2048)
+        elif w["stage"] == 3:
+            # the ZeRO-3 layer step: the all-gather(s) of the 16-bit shards, then the step
+            for _ in range(w.get("gathers", 1)):
+                oracle.all_gather_u16([lp[r * S:(r + 1) * S] for r in range(n_d)], psi, S)
+            oracle.zero_step(rows, dt, hp, st, w["pad"], 3, param_dtype=pdt, lp_shards=lp)
         else:
-            oracle.zero_step(rows, dt, hp, st, w["pad"], min(w["stage"], 3), lp_shards=lp, gathered=gath)
+            oracle.zero_step(rows, dt, hp, st, w["pad"], w["stage"], param_dtype=pdt, lp_shards=lp, gathered=gath)
         steps += 1
         el = time.perf_counter() - t0
         if el >= budget_s or (max_steps and steps >= max_steps):
@@ -811,8 +884,7 @@ def oracle_sample(w, budget_s, max_steps=None):
 
 
 def reference_arm(args, rank, world):
-    w = workload(args.config, args.nd, args.qgather, args.psi, args.qgz, args.gathers, args.offload, args.accum,
-                 args.overlap)
+    w = workload_from_args(args)
     if rank != 0:
         return None
     for _ in range(args.warmup):
@@ -824,7 +896,7 @@ def reference_arm(args, rank, world):
     return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * el / steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "impl": "reference", "config": {"workload": w["name"], "psi": w["psi"], "n_d": n_d},
+            "impl": "reference", "config": config_of(w, world),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
@@ -857,14 +929,16 @@ def dist_max(x, world):
     return float(t.item())
 
 
-def main():
+def build_parser():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200,
                     help="timed steps (the default makes the timed region long enough for several clock samples)")
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--config", type=int, default=4,
+                    help="workload: 1 small ZeRO-2, 2 GPT-2-small clipped, 3 GPT-2 1.5B fp16, "
+                         "4 ZeRO-3 8 Llama-3-8B layers (default: the largest), 5 the N_d sweep at 2^28")
     ap.add_argument("--nd", type=int, default=None)
     ap.add_argument("--qgather", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -875,11 +949,19 @@ def main():
     ap.add_argument("--gathers", type=int, default=1, choices=[1, 2], help="ZeRO-3 gathers per layer and step")
     ap.add_argument("--offload", action="store_true", help="optimizer state in page-locked host memory")
     ap.add_argument("--accum", type=int, default=1, help="micro-batches per optimizer step (gradient accumulation)")
-    ap.add_argument("--overlap", action="store_true",
-                    help="ZeRO-3: next layer's gather on a second stream during this layer's step")
+    ap.add_argument("--serial", action="store_true",
+                    help="ZeRO-3: every gather on the step's stream (default: a second stream, overlapping)")
+    ap.add_argument("--param-dtype", choices=["bf16", "fp16"], default=None,
+                    help="16-bit parameter dtype (default bf16)")
+    ap.add_argument("--stage", type=int, choices=[1, 2], default=None,
+                    help="ZeRO stage of the ZeRO-1/2 workloads (same math, label and plan stage)")
     ap.add_argument("--row-pad", type=int, default=0,
                     help="extra elements between rank rows (breaks power-of-two rank strides)")
-    args = ap.parse_args()
+    return ap
+
+
+def main():
+    args = build_parser().parse_args()
     if args.warmup < 3:
         args.warmup = 3
     rank, world, local = dist_setup()
@@ -893,8 +975,7 @@ def main():
     out = gpu_arm(args, rank, world, device)
     if rank == 0:
         if not args.no_cpu_baseline and world == 1:
-            w = workload(args.config, args.nd, args.qgather, args.psi, args.qgz, args.gathers, args.offload, args.accum,
-                 args.overlap)
+            w = workload_from_args(args)
             psi, n_d, steps, el = oracle_sample(w, args.cpu_budget)
             out["cpu_baseline"] = {"value": psi * steps / el, "unit": UNIT, "cores": 1, "kind": "oracle",
                                    "sample": "%d of %d params, n_d=%d, %d steps in %.1f s, single-threaded C "

@@ -88,4 +88,36 @@ def test_variants_that_do_not_apply_are_refused():
     with pytest.raises(SystemExit):
         bench.workload(4, accum=2)
     with pytest.raises(SystemExit):
-        bench.workload(2, overlap=True)
+        bench.workload(2, serial=True)
+    with pytest.raises(SystemExit):
+        bench.workload(4, stage=2)
+    with pytest.raises(SystemExit):
+        bench.workload(5, qgather=True, param_dtype="fp16")
+
+
+def test_default_workload_is_the_largest_single_gpu_one():
+    # the ZeRO-3 layer loop over 8 Llama-3-8B-shaped layers, gathers on a second stream
+    args = bench.build_parser().parse_args([])
+    w = bench.workload_from_args(args)
+    assert w["name"] == "zero3_llama3_8b_8layers_psil218112000_nd16" and w["overlap"]
+    assert w["psi_total"] == 8 * 218_112_000 == 1_744_896_000
+    assert w["psi_total"] * w["bytes_per_param"] == pytest.approx(108.18e9, rel=1e-3)
+    # the largest workload by bytes per step
+    for cfg in (1, 2, 3, 5):
+        o = bench.workload(cfg)
+        assert o["psi_total"] * o["bytes_per_param"] < w["psi_total"] * w["bytes_per_param"]
+
+
+def test_both_arms_print_the_same_config():
+    for argv in ([], ["--config", "3", "--param-dtype", "fp16", "--stage", "1"], ["--config", "2"]):
+        w = bench.workload_from_args(bench.build_parser().parse_args(argv))
+        assert bench.config_of(w, 1) == bench.config_of(bench.workload_from_args(
+            bench.build_parser().parse_args(argv + ["--impl", "reference"])), 1)
+
+
+def test_fp16_parameter_and_stage_labels():
+    w = bench.workload(3, param_dtype="fp16", stage=1)
+    assert w["name"] == "zero1_gpt2xl_psi1500000000_nd8_fp16_lossscale_params_fp16"
+    assert w["stage"] == 1 and w["pdt"] == "fp16" and w["bytes_per_param"] == 2 * 8 + 26
+    assert bench.config_of(w, 1)["param_dtype"] == "fp16"
+    assert bench.workload(3)["pdt"] == "bf16"

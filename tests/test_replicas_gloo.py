@@ -23,9 +23,8 @@ def _worker(rank, world, port, q):
     bench.dist_barrier(w)
     mx = bench.dist_max(10.0 * (rank + 1), w)
 
-    class A:  # arguments of the reference arm
-        config, nd, qgather, steps, warmup, psi, qgz, gathers, offload, accum, row_pad, overlap = 1, None, False, 1, 0, None, False, 1, False, 1, 0, False
-    ref = bench.reference_arm(A, r, w)
+    args = bench.build_parser().parse_args(["--config", "1", "--steps", "1", "--warmup", "0"])
+    ref = bench.reference_arm(args, r, w)
     q.put((rank, mx, ref is None))
     import torch.distributed as dist
     dist.destroy_process_group()
