@@ -37,8 +37,8 @@ def _sample(psi, seed):
 
 
 class FullJob:
-    def __init__(self, psi, n_d, stage, gdt, hp, seed, pingpong=False, loss_scale=1.0):
-        self.plan = z.Plan(psi, n_d, stage=stage, grad_dtype=gdt, shard_pad=8)
+    def __init__(self, psi, n_d, stage, gdt, hp, seed, pingpong=False, loss_scale=1.0, param_dtype=None):
+        self.plan = z.Plan(psi, n_d, stage=stage, grad_dtype=gdt, shard_pad=8, param_dtype=param_dtype)
         self.hp, self.psi, self.n_d, self.seed = hp, psi, n_d, seed
         self.gdt = gdt
         self.buf = z.StepBuffers(self.plan, hp, device="cuda", pingpong=pingpong)
@@ -135,6 +135,29 @@ def test_gpt2_xl_fp16_loss_scale_full_size():
     sc = job.buf.scalars_host()
     assert sc.overflow == 1 and sc.t == 1 and sc.loss_scale == 512.0 and sc.good_steps == 0
     job.check(idx, want)   # the state (now in the other buffer set) is unchanged
+
+
+@pytest.mark.parametrize("stage", [1, 2])
+def test_gpt2_xl_fp16_parameters_full_size(stage):
+    # the pages pair fp16 parameters with fp16 gradients (DP-notes, "Memory
+    # Consumption Analysis"): the same workload with fp16 16-bit parameters,
+    # as ZeRO-1 and ZeRO-2 (the same math), in place (a check pass, then the
+    # guarded update), two steps on sampled elements
+    psi, n_d = 1_500_000_000, 8
+    if _free_gb() < 70:
+        pytest.skip("needs ~64 GB of free device memory")
+    hp = z.hparams(lr=1e-4, loss_scaling=True)
+    job = FullJob(psi, n_d, stage, z.ZERO_FP16, hp, seed=313 + stage, loss_scale=1024.0, param_dtype=z.ZERO_FP16)
+    assert job.buf.lp.dtype == torch.float16
+    idx = _sample(psi, 5)
+    for step in (1, 2):
+        job.fill_grads(step, 1e-4, scale=1024.0)
+        rows, st = job.take(idx)
+        job.buf.step(hp)
+        sc = job.buf.scalars_host()
+        assert sc.overflow == 0 and sc.t == step and sc.status == 0
+        want = job.oracle_sampled(rows, st, float(n_d) * 1024.0)
+        job.check(idx, want, lp_dtype=oracle.FP16)
 
 
 def test_llama_layer_zero3_full_size():

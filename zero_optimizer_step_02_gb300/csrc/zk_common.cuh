@@ -289,7 +289,7 @@ __device__ __forceinline__ bool is_finite_f32(float x)
 struct StepConsts {
     float b1, b2, omb1, omb2, step, eps, decay, coef;   // step, eps: bias-corrected (see set_adam)
     float divisor, inv_divisor;
-    int wd, clip, div_pow2, skip;
+    int wd, clip, div_pow2;
 };
 
 // The divisor of the mean: n_d times the loss scale (when loss scaling).
@@ -334,11 +334,15 @@ __device__ __forceinline__ float mean_of(const StepConsts& c, float sum)
 }
 
 // The mean of four sums: the divisor's form is tested once for the four.
+// With a power-of-two divisor the mean is an exact multiplication, done on
+// register pairs (the products feed only multiplications and stores, so
+// nothing can be contracted into them).
 __device__ __forceinline__ void mean_of4(const StepConsts& c, const float (&sum)[4], float (&g)[4])
 {
     if (c.div_pow2) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) g[e] = __fmul_rn(sum[e], c.inv_divisor);
+        const f32x2 inv = pack2(c.inv_divisor, c.inv_divisor);
+        unpack2(mul2(pack2(sum[0], sum[1]), inv), g[0], g[1]);
+        unpack2(mul2(pack2(sum[2], sum[3]), inv), g[2], g[3]);
     } else {
 #pragma unroll
         for (int e = 0; e < 4; ++e) g[e] = __fdiv_rn(sum[e], c.divisor);
@@ -376,14 +380,20 @@ __device__ __forceinline__ void adam_elem(const StepConsts& c, float g, float& p
 // Squared-norm accumulation with an error-free product and a compensated sum
 // in fp32 (the per-thread partial is then carried in fp64): the result agrees
 // with an fp64 sum of the exact squares to ~1e-14 relative, so the clipping
-// coefficient comes out the same as a sequential fp64 sum's.
+// coefficient comes out the same as a sequential fp64 sum's.  Every term and
+// the running sum are non-negative, so ordering the pair by max / min makes
+// Dekker's Fast2Sum (s = a + b, e = b - (s - a), exact for a >= b >= 0) do
+// what Knuth's TwoSum does, with one floating-point operation fewer and the
+// ordering on the integer-side pipe.  Adding g = 0 changes nothing (hi stays,
+// e = 0), so padding past a tile's valid length needs no test.
 __device__ __forceinline__ void sq_accumulate(float g, float& hi, float& lo)
 {
     const float p = __fmul_rn(g, g);
     const float pe = __fmaf_rn(g, g, -p);
-    const float s = __fadd_rn(hi, p);
-    const float bp = __fsub_rn(s, hi);
-    const float e = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(p, bp));
+    const float a = fmaxf(hi, p);
+    const float b = fminf(hi, p);
+    const float s = __fadd_rn(a, b);
+    const float e = __fsub_rn(b, __fsub_rn(s, a));
     hi = s;
     lo = __fadd_rn(lo, __fadd_rn(e, pe));
 }

@@ -31,12 +31,43 @@ struct Shared {
     uint64_t empty[kMaxStages];
     int issued_parity[kMaxStages];
     int abort;
-    int pad0;
+    int skip;   // a guarded pass whose step is flagged: the CTA writes nothing
     StepConsts c;
     alignas(16) float red_f[2][kChunksPerThread][kConsumerWarps];
     double red_d[kConsumerWarps + 1];
 };
 static_assert(sizeof(Shared) <= kStageOffset, "shared header too large");
+
+// The step constants of a launch, computed by warp 0 of a CTA into sh->c.
+// F_FINALIZE: the whole warp sums the reduce pass's per-CTA partials in the
+// order k_finalize uses, so every CTA gets the same bits, and CTA 0 records
+// the norm and the coefficient in the step scalars.
+__device__ __forceinline__ void step_constants(const StreamArgs& a, Shared* sh, int lane)
+{
+    double sq = 0.0;
+    if (a.flags & F_FINALIZE) {
+        for (int i = lane; i < a.fin_n; i += 32) sq = __dadd_rn(sq, a.fin_partials[i]);
+        sq = warp_sum_f64(sq);
+    }
+    if (lane != 0) return;
+    StepConsts c = {};
+    zero_dev_scalars* sc = a.sc;
+    set_divisor(c, (a.n_ranks > 0 ? a.n_ranks : 1) * (a.micro > 0 ? a.micro : 1),
+                (a.flags & F_LSCALE) ? sc->loss_scale : 1.0f);
+    if (sc != nullptr) set_adam(c, a.hp, sc->beta1_pow, sc->beta2_pow);   // null: plain sums only
+    c.clip = (a.flags & F_CLIP) != 0;
+    if (a.flags & F_FINALIZE) {
+        const float coef = clip_coefficient(a.hp.max_norm, sq);
+        c.coef = c.clip ? coef : 1.0f;
+        if (blockIdx.x == 0) {
+            sc->sqnorm = sq;
+            sc->clip_coef = coef;
+        }
+    } else {
+        c.coef = c.clip ? sc->clip_coef : 1.0f;
+    }
+    sh->c = c;
+}
 
 // rank-group shapes of a launch (the FULL parameter of k_stream); kFullHalf:
 // the int8-rank reduce pass only, one group holding exactly half the slots
@@ -97,12 +128,59 @@ __device__ __forceinline__ float rank_scale(const StreamArgs& a, int r, long lon
                  r);
 }
 
-// rank-ordered add of one rank's dequantized codes: acc += fl(code * scale)
+// Which elements of a tile a consumer thread takes: chunk ch of thread tid
+// covers the tile's elements [4q, 4q + 4), q = chunk_of(ch, tid).  By default
+// the chunks form rows (row ch = all consumers, one 2048-element block per
+// row).  With the fused int8 gather (kHalves) each half of the consumers
+// takes one 2048-element block (warps 0-7 the first, 8-15 the second), so the
+// block's absmax is a barrier of 8 warps instead of 16.
+template <bool kHalves>
+__device__ __forceinline__ int chunk_of(int ch, int tid)
+{
+    if constexpr (kHalves) {
+        constexpr int kHalf = kConsumers / 2;
+        return (tid / kHalf) * (kQuantBlock / kChunk) + ch * kHalf + (tid % kHalf);
+    } else {
+        return ch * kConsumers + tid;
+    }
+}
+
+// the 2048-element block (0 or 1) of the tile that chunk ch of thread tid lies in
+template <bool kHalves>
+__device__ __forceinline__ int block_of(int ch, int tid)
+{
+    return kHalves ? tid / (kConsumers / 2) : ch;
+}
+
+// rank-ordered add of one rank's dequantized codes: acc += fl(code * scale).
+// kDecode 0: scalar; 1: the codes decoded (an exact subtraction) and scaled
+// on register pairs, then added one by one; 2: all three on register pairs.
+// Each is the same rounding sequence, one IEEE operation per step (checked
+// bit for bit against the oracle); the pair forms issue fewer instructions.
+template <int kDecode>
 __device__ __forceinline__ void add_codes(float (&acc)[4], uint32_t w, float s)
 {
     const uint32_t wb = w ^ 0x80808080u;
+    if constexpr (kDecode == 0) {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) acc[e] = __fadd_rn(acc[e], __fmul_rn(code_f32(wb, e), s));
+        for (int e = 0; e < 4; ++e) acc[e] = __fadd_rn(acc[e], __fmul_rn(code_f32(wb, e), s));
+    } else {
+        const f32x2 bias = pack2(8388736.0f, 8388736.0f), sc = pack2(s, s);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const f32x2 x = pack2(__uint_as_float(__byte_perm(wb, 0x4B000000u, 0x7540u + 2 * h)),
+                                  __uint_as_float(__byte_perm(wb, 0x4B000000u, 0x7541u + 2 * h)));
+            const f32x2 prod = mul2(sub2(x, bias), sc);
+            if constexpr (kDecode == 1) {
+                float p0, p1;
+                unpack2(prod, p0, p1);
+                acc[2 * h] = __fadd_rn(acc[2 * h], p0);
+                acc[2 * h + 1] = __fadd_rn(acc[2 * h + 1], p1);
+            } else {
+                unpack2(add2(pack2(acc[2 * h], acc[2 * h + 1]), prod), acc[2 * h], acc[2 * h + 1]);
+            }
+        }
+    }
 }
 
 template <int GT>
@@ -133,46 +211,33 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
     const int warp = tid >> 5;
     const int lane = tid & 31;
     constexpr bool quant = OP == OP_QFUSED;
+    // the int8 gather over int8 rank streams takes one quantization block per
+    // half of the consumers (an 8-warp absmax barrier): 7% faster at N_d = 8
+    // than one block per chunk row; with 16-bit rank streams the chunk rows
+    // (a 16-warp barrier) measured 1-8% faster, and stay
+    constexpr bool kHalves = quant && GT == kGradQ8;
+    // int8 rank streams: the codes decoded and scaled on register pairs (the
+    // reduce pass 4%, the int8-gather step 11% faster at N_d = 8), except in
+    // the fused step with a partly filled rank group, which measured 2% faster
+    // with the scalar form
+    constexpr int kDecode = (OP == OP_FUSED && FULL == kPartial) ? 0 : 1;
 
-    if (warp == 0) {
-        // F_FINALIZE: the whole warp sums the reduce pass's per-CTA partials in
-        // the order k_finalize uses, so every CTA gets the same bits
-        double sq = 0.0;
-        if (a.flags & F_FINALIZE) {
-            for (int i = lane; i < a.fin_n; i += 32) sq = __dadd_rn(sq, a.fin_partials[i]);
-            sq = warp_sum_f64(sq);
+    // The ring's barriers first, so that the producer can start copying while
+    // the consumers read the step scalars (their latency then overlaps the
+    // first copies).  Only a guarded pass reads its flag before producing.
+    if (tid == 0) {
+        for (int s = 0; s < a.stages; ++s) {
+            mbar_init(&sh->full[s], 1);
+            mbar_init(&sh->empty[s], kConsumerWarps);
+            sh->issued_parity[s] = -1;
         }
-        if (lane == 0) {
-            for (int s = 0; s < a.stages; ++s) {
-                mbar_init(&sh->full[s], 1);
-                mbar_init(&sh->empty[s], kConsumerWarps);
-                sh->issued_parity[s] = -1;
-            }
-            sh->abort = 0;
-            StepConsts c = {};
-            zero_dev_scalars* sc = a.sc;
-            c.skip = (a.flags & F_GUARD) ? (sc->nonfinite != 0) : 0;
-            set_divisor(c, (a.n_ranks > 0 ? a.n_ranks : 1) * (a.micro > 0 ? a.micro : 1),
-                        (a.flags & F_LSCALE) ? sc->loss_scale : 1.0f);
-            if (sc != nullptr) set_adam(c, a.hp, sc->beta1_pow, sc->beta2_pow);   // null: plain sums only
-            c.clip = (a.flags & F_CLIP) != 0;
-            if (a.flags & F_FINALIZE) {
-                const float coef = clip_coefficient(a.hp.max_norm, sq);
-                c.coef = c.clip ? coef : 1.0f;
-                if (blockIdx.x == 0) {
-                    sc->sqnorm = sq;
-                    sc->clip_coef = coef;
-                }
-            } else {
-                c.coef = c.clip ? sc->clip_coef : 1.0f;
-            }
-            sh->c = c;
-            fence_barrier_init();
-        }
+        sh->abort = 0;
+        sh->skip = (a.flags & F_GUARD) ? (a.sc->nonfinite != 0) : 0;
+        fence_barrier_init();
     }
     __syncthreads();
     // a flagged loss-scaling step writes nothing (uniform over the CTA)
-    const bool skip = sh->c.skip != 0;
+    const bool skip = sh->skip != 0;
 
     const int n_groups = a.n_ranks > 0 ? (a.n_ranks + kG - 1) / kG : 1;
     const int rank_slots = a.n_ranks < kG ? a.n_ranks : kG;
@@ -186,7 +251,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
     float sq_hi = 0.0f, sq_lo = 0.0f;
 
     if (skip) {
-        // nothing to do; fall through to the end (the epilogue still runs)
+        // nothing to do but record the norm (CTA 0); fall through to the end
+        // (the epilogue still runs)
+        if (warp == 0 && blockIdx.x == 0 && (a.flags & F_FINALIZE)) step_constants(a, sh, lane);
     } else if (warp == kConsumerWarps) {
         // ------------------------------------------------------- producer
         if (lane == 0 && !(a.flags & F_DEBUG_STARVE)) {
@@ -245,6 +312,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
         uint32_t ph = 0;
         bool alive = true;
         int qiter = 0;  // quantizer barriers passed: picks the reduction buffer
+        // the step constants: warp 0 computes them while the producer issues
+        // the first copies; then the consumers (only) wait for them
+        if (warp == 0) step_constants(a, sh, lane);
+        named_bar_sync(3, kConsumers);
         // constants in registers: a reference into shared memory would be
         // re-read for every element (the stores in the loop may alias it)
         const StepConsts c = sh->c;
@@ -285,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
                 if (a.n_side_tma < a.n_side && alive) {
 #pragma unroll
                     for (int ch = 0; ch < kChunksPerThread; ++ch) {
-                        const long long jc = j0 + (ch * kConsumers + tid) * 4;
+                        const long long jc = j0 + chunk_of<kHalves>(ch, tid) * 4;
 #pragma unroll
                         for (int k = 0; k < kMaxSide; ++k) {
                             if (k >= a.n_side_tma && k < a.n_side) {
@@ -317,21 +388,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
                             const float* ssc = reinterpret_cast<const float*>(st + scale_off);
 #pragma unroll
                             for (int ch = 0; ch < kChunksPerThread; ++ch) {
-                                const int q = ch * kConsumers + tid;
+                                const int q = chunk_of<kHalves>(ch, tid);
+                                const int qb = block_of<kHalves>(ch, tid);   // the chunk's block: its scales
                                 if constexpr (FULL == kFullMulti) {
                                     const uint32_t* cw = reinterpret_cast<const uint32_t*>(st) + q;
 #pragma unroll
-                                    for (int k = 0; k < kG; ++k) add_codes(acc[ch], cw[k * (kTile / 4)], ssc[ch * kG + k]);
+                                    for (int k = 0; k < kG; ++k) add_codes<kDecode>(acc[ch], cw[k * (kTile / 4)], ssc[qb * kG + k]);
                                 } else if constexpr (FULL == kFullOne || FULL == kFullHalf) {
                                     // four ranks' scales per 16-byte shared load
                                     const uint32_t* cw = reinterpret_cast<const uint32_t*>(st) + q;
-                                    const float4* s4 = reinterpret_cast<const float4*>(ssc + ch * kG);
+                                    const float4* s4 = reinterpret_cast<const float4*>(ssc + qb * kG);
                                     auto four = [&](int k4) {
                                         const float4 sc4 = s4[k4];
-                                        add_codes(acc[ch], cw[(4 * k4 + 0) * (kTile / 4)], sc4.x);
-                                        add_codes(acc[ch], cw[(4 * k4 + 1) * (kTile / 4)], sc4.y);
-                                        add_codes(acc[ch], cw[(4 * k4 + 2) * (kTile / 4)], sc4.z);
-                                        add_codes(acc[ch], cw[(4 * k4 + 3) * (kTile / 4)], sc4.w);
+                                        add_codes<kDecode>(acc[ch], cw[(4 * k4 + 0) * (kTile / 4)], sc4.x);
+                                        add_codes<kDecode>(acc[ch], cw[(4 * k4 + 1) * (kTile / 4)], sc4.y);
+                                        add_codes<kDecode>(acc[ch], cw[(4 * k4 + 2) * (kTile / 4)], sc4.z);
+                                        add_codes<kDecode>(acc[ch], cw[(4 * k4 + 3) * (kTile / 4)], sc4.w);
                                     };
                                     if constexpr (FULL == kFullOne) {
 #pragma unroll 2
@@ -344,14 +416,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
 #pragma unroll 4
                                     for (int k = 0; k < nr; ++k) {
                                         const uint32_t w = reinterpret_cast<const uint32_t*>(st + k * kTile)[q];
-                                        add_codes(acc[ch], w, ssc[ch * kG + k]);
+                                        add_codes<kDecode>(acc[ch], w, ssc[qb * kG + k]);
                                     }
                                 }
                             }
                         } else {
 #pragma unroll
                             for (int ch = 0; ch < kChunksPerThread; ++ch) {
-                                const int q = ch * kConsumers + tid;  // chunk index within the tile
+                                const int q = chunk_of<kHalves>(ch, tid);  // chunk index within the tile
                                 const uint2* rw = reinterpret_cast<const uint2*>(st) + q;
                                 if constexpr (FULL != kPartial && OP == OP_QFUSED) {
                                     // the int8-gather step measured fastest in this form
@@ -374,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
                         if (g == n_groups - 1) {
 #pragma unroll
                             for (int ch = 0; ch < kChunksPerThread; ++ch) {
-                                const int q = ch * kConsumers + tid;
+                                const int q = chunk_of<kHalves>(ch, tid);
 #pragma unroll
                                 for (int k = 0; k < kMaxSide; ++k) {
                                     if (k < a.n_side_tma) {
@@ -400,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
                 // plain-load path: per element, bounds-checked against len
 #pragma unroll
                 for (int ch = 0; ch < kChunksPerThread; ++ch) {
-                    const int q = ch * kConsumers + tid;
+                    const int q = chunk_of<kHalves>(ch, tid);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int idx = q * 4 + e;
@@ -409,7 +481,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
                             for (int r = 0; r < a.n_ranks; ++r) {
                                 if constexpr (GT == kGradQ8) {
                                     const float code = static_cast<float>(static_cast<const signed char*>(a.rank[r])[j]);
-                                    acc[ch][e] = __fadd_rn(acc[ch][e], __fmul_rn(code, rank_scale(a, r, cur.seg, cur.t, ch)));
+                                    acc[ch][e] = __fadd_rn(acc[ch][e], __fmul_rn(code, rank_scale(a, r, cur.seg, cur.t,
+                                                                                                  block_of<kHalves>(ch, tid))));
                                 } else {
                                     acc[ch][e] = Lp<GT>::add(acc[ch][e], static_cast<const uint16_t*>(a.rank[r])[j]);
                                 }
@@ -426,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
             float xq[kChunksPerThread][4];  // 16-bit results kept for the quantizer
 #pragma unroll
             for (int ch = 0; ch < kChunksPerThread; ++ch) {
-                const int q = ch * kConsumers + tid;
+                const int q = chunk_of<kHalves>(ch, tid);
                 const long long jc = j0 + q * 4;
                 int cnt = len - q * 4;
                 cnt = cnt < 0 ? 0 : (cnt > 4 ? 4 : cnt);
@@ -446,15 +519,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
                     } else {
                         mean_of4(c, sum, gv);
                     }
+                    // elements past the tile's valid length are +0 here (nothing was
+                    // added to them): finite, and their squares add nothing
                     if (detect) {
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
-                            if (e < cnt && !is_finite_f32(gv[e])) nonfinite = true;
+                            if (!is_finite_f32(gv[e])) nonfinite = true;
                     }
                     if (want_sq) {
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            if (e < cnt) sq_accumulate(gv[e], sq_hi, sq_lo);
+                        for (int e = 0; e < 4; ++e) sq_accumulate(gv[e], sq_hi, sq_lo);
                     }
                     if (alive && a.out_f32[0] != nullptr) {
                         if (fast) {
@@ -551,60 +625,121 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
             }
 
             if constexpr (quant) {
-                // one quantization block per chunk row (all consumers x 4 elements):
-                // amax per row over the consumers, then codes + dequantized bf16
-                float amax[kChunksPerThread];
+                if constexpr (kHalves) {
+                    // one quantization block per half of the consumers: the thread's
+                    // chunks lie in block qb = tid / 256; absmax over the block's 8
+                    // warps, then codes + dequantized bf16
+                    constexpr int kHalf = kConsumers / 2;
+                    const int qb = tid / kHalf;
+                    float amax = 0.0f;
 #pragma unroll
-                for (int ch = 0; ch < kChunksPerThread; ++ch) {
-                    amax[ch] = 0.0f;
+                    for (int ch = 0; ch < kChunksPerThread; ++ch)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        if ((ch * kConsumers + tid) * 4 + e < len) amax[ch] = fmaxf(amax[ch], fabsf(xq[ch][e]));
-                    amax[ch] = warp_max_f32(amax[ch]);
-                }
-                // two buffers used alternately: between two uses of one buffer every
-                // consumer has passed the barrier of the other, so reads are done
-                const int par = qiter & 1;
-                ++qiter;
-                if (lane == 0) {
-#pragma unroll
-                    for (int ch = 0; ch < kChunksPerThread; ++ch) sh->red_f[par][ch][warp] = amax[ch];
-                }
-                named_bar_sync(1, kConsumers);
-#pragma unroll
-                for (int ch = 0; ch < kChunksPerThread; ++ch) {
+                        for (int e = 0; e < 4; ++e)
+                            if (chunk_of<true>(ch, tid) * 4 + e < len) amax = fmaxf(amax, fabsf(xq[ch][e]));
+                    amax = warp_max_f32(amax);
+                    // two buffers used alternately: between two uses of one buffer every
+                    // warp of the half has passed the barrier of the other, so reads are done
+                    const int par = qiter & 1;
+                    ++qiter;
+                    if (lane == 0) sh->red_f[par][0][warp] = amax;
+                    named_bar_sync(1 + qb, kHalf);
                     float m = 0.0f;
-                    const float4* rv = reinterpret_cast<const float4*>(sh->red_f[par][ch]);
+                    {
+                        const float4* rv = reinterpret_cast<const float4*>(sh->red_f[par][0] + qb * (kConsumerWarps / 2));
 #pragma unroll
-                    for (int w = 0; w < kConsumerWarps / 4; ++w) {
-                        const float4 f = rv[w];
-                        m = fmaxf(m, fmaxf(fmaxf(f.x, f.y), fmaxf(f.z, f.w)));
+                        for (int w = 0; w < kConsumerWarps / 8; ++w) {
+                            const float4 f = rv[w];
+                            m = fmaxf(m, fmaxf(fmaxf(f.x, f.y), fmaxf(f.z, f.w)));
+                        }
                     }
                     const float scale = __fdiv_rn(m, 127.0f);
-                    const long long blk = cur.t * kChunksPerThread + ch;   // block index within the shard
-                    if (tid == 0 && alive && blk < a.q_blocks_per_shard)
-                        a.q_scales[cur.seg * a.q_blocks_per_shard + blk] = (len > ch * kQuantBlock) ? scale : 0.0f;
+                    const long long blk = cur.t * kChunksPerThread + qb;   // block index within the shard
+                    if (tid % kHalf == 0 && alive && blk < a.q_blocks_per_shard)
+                        a.q_scales[cur.seg * a.q_blocks_per_shard + blk] = (len > qb * kQuantBlock) ? scale : 0.0f;
                     const float inv_scale = quant_reciprocal(scale);
-                    const int q = ch * kConsumers + tid;
-                    const long long jc = j0 + q * 4;
-                    int cnt = len - q * 4;
-                    cnt = cnt < 0 ? 0 : (cnt > 4 ? 4 : cnt);
-                    float cf[4];
-                    const uint32_t cw = quant_code4(xq[ch], scale, inv_scale, cf);
-                    const uint32_t d01 = Lp<ZERO_BF16>::narrow2(__fmul_rn(cf[0], scale), __fmul_rn(cf[1], scale));
-                    const uint32_t d23 = Lp<ZERO_BF16>::narrow2(__fmul_rn(cf[2], scale), __fmul_rn(cf[3], scale));
-                    const uint16_t dq[4] = {static_cast<uint16_t>(d01), static_cast<uint16_t>(d01 >> 16),
-                                            static_cast<uint16_t>(d23), static_cast<uint16_t>(d23 >> 16)};
-                    if (!alive) continue;
-                    if (fast) {
-                        *reinterpret_cast<uint32_t*>(a.q_codes + jc) = cw;
-                        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.q_gathered) + jc) = make_uint2(d01, d23);
-                    } else {
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            if (e < cnt) {
-                                a.q_codes[jc + e] = static_cast<signed char>(static_cast<uint8_t>(cw >> (8 * e)));
-                                static_cast<uint16_t*>(a.q_gathered)[jc + e] = dq[e];
+                    for (int ch = 0; ch < kChunksPerThread; ++ch) {
+                        const int q = chunk_of<true>(ch, tid);
+                        const long long jc = j0 + q * 4;
+                        int cnt = len - q * 4;
+                        cnt = cnt < 0 ? 0 : (cnt > 4 ? 4 : cnt);
+                        float cf[4];
+                        const uint32_t cw = quant_code4(xq[ch], scale, inv_scale, cf);
+                        const uint32_t d01 = Lp<ZERO_BF16>::narrow2(__fmul_rn(cf[0], scale), __fmul_rn(cf[1], scale));
+                        const uint32_t d23 = Lp<ZERO_BF16>::narrow2(__fmul_rn(cf[2], scale), __fmul_rn(cf[3], scale));
+                        const uint16_t dq[4] = {static_cast<uint16_t>(d01), static_cast<uint16_t>(d01 >> 16),
+                                                static_cast<uint16_t>(d23), static_cast<uint16_t>(d23 >> 16)};
+                        if (!alive) continue;
+                        if (fast) {
+                            *reinterpret_cast<uint32_t*>(a.q_codes + jc) = cw;
+                            *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.q_gathered) + jc) = make_uint2(d01, d23);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                if (e < cnt) {
+                                    a.q_codes[jc + e] = static_cast<signed char>(static_cast<uint8_t>(cw >> (8 * e)));
+                                    static_cast<uint16_t*>(a.q_gathered)[jc + e] = dq[e];
+                                }
+                            }
+                        }
+                    }
+                } else {
+                    // one quantization block per chunk row (all consumers x 4 elements):
+                    // amax per row over the consumers, then codes + dequantized bf16
+                    float amax[kChunksPerThread];
+#pragma unroll
+                    for (int ch = 0; ch < kChunksPerThread; ++ch) {
+                        amax[ch] = 0.0f;
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if ((ch * kConsumers + tid) * 4 + e < len) amax[ch] = fmaxf(amax[ch], fabsf(xq[ch][e]));
+                        amax[ch] = warp_max_f32(amax[ch]);
+                    }
+                    // two buffers used alternately: between two uses of one buffer every
+                    // consumer has passed the barrier of the other, so reads are done
+                    const int par = qiter & 1;
+                    ++qiter;
+                    if (lane == 0) {
+#pragma unroll
+                        for (int ch = 0; ch < kChunksPerThread; ++ch) sh->red_f[par][ch][warp] = amax[ch];
+                    }
+                    named_bar_sync(1, kConsumers);
+#pragma unroll
+                    for (int ch = 0; ch < kChunksPerThread; ++ch) {
+                        float m = 0.0f;
+                        const float4* rv = reinterpret_cast<const float4*>(sh->red_f[par][ch]);
+#pragma unroll
+                        for (int w = 0; w < kConsumerWarps / 4; ++w) {
+                            const float4 f = rv[w];
+                            m = fmaxf(m, fmaxf(fmaxf(f.x, f.y), fmaxf(f.z, f.w)));
+                        }
+                        const float scale = __fdiv_rn(m, 127.0f);
+                        const long long blk = cur.t * kChunksPerThread + ch;   // block index within the shard
+                        if (tid == 0 && alive && blk < a.q_blocks_per_shard)
+                            a.q_scales[cur.seg * a.q_blocks_per_shard + blk] = (len > ch * kQuantBlock) ? scale : 0.0f;
+                        const float inv_scale = quant_reciprocal(scale);
+                        const int q = ch * kConsumers + tid;
+                        const long long jc = j0 + q * 4;
+                        int cnt = len - q * 4;
+                        cnt = cnt < 0 ? 0 : (cnt > 4 ? 4 : cnt);
+                        float cf[4];
+                        const uint32_t cw = quant_code4(xq[ch], scale, inv_scale, cf);
+                        const uint32_t d01 = Lp<ZERO_BF16>::narrow2(__fmul_rn(cf[0], scale), __fmul_rn(cf[1], scale));
+                        const uint32_t d23 = Lp<ZERO_BF16>::narrow2(__fmul_rn(cf[2], scale), __fmul_rn(cf[3], scale));
+                        const uint16_t dq[4] = {static_cast<uint16_t>(d01), static_cast<uint16_t>(d01 >> 16),
+                                                static_cast<uint16_t>(d23), static_cast<uint16_t>(d23 >> 16)};
+                        if (!alive) continue;
+                        if (fast) {
+                            *reinterpret_cast<uint32_t*>(a.q_codes + jc) = cw;
+                            *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.q_gathered) + jc) = make_uint2(d01, d23);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                if (e < cnt) {
+                                    a.q_codes[jc + e] = static_cast<signed char>(static_cast<uint8_t>(cw >> (8 * e)));
+                                    static_cast<uint16_t*>(a.q_gathered)[jc + e] = dq[e];
+                                }
                             }
                         }
                     }
