@@ -389,15 +389,17 @@ ZERO_API zero_status zero_step_fused_qgz_qgather(const zero_plan* plan, const ze
  * "왜 통신량이 늘지 않는가": with stage 3 each layer's parameters are
  * all-gathered before they are used, in the forward and again in the
  * backward pass, and each layer's gradients are reduce-scattered to their
- * owners; itwiki "DeepSpeed에서 쓰기": overlap_comm and the stage-3 prefetch
- * overlap the next layer's gather with the current layer's work).
+ * owners; itwiki "DeepSpeed에서 쓰기": its example configuration is stage 3
+ * with gradient_clipping 1.0, gradient_accumulation_steps, overlap_comm and
+ * the stage-3 prefetch, which overlaps the next layer's gather with the
+ * current layer's work).
  *
  * Per layer l = 0 .. n_layers-1, in order:
  *   gather(l): zero_all_gather of layer l's 16-bit shards into
  *              gathered[l % n_gathered], `gathers` times (1: once per step;
  *              2: forward and backward, the pages' 3-Psi volume);
- *   step(l):   zero_step_fused of layer l, in place (stage 3: the updated
- *              16-bit shards overwrite shards_lp).
+ *   step(l):   zero_step_fused_accum of layer l in place (stage 3: the
+ *              updated 16-bit shards overwrite shards_lp).
  * gather(l) reads the shards as the previous step left them; step(l) comes
  * after gather(l).  With gather_stream a stream other than `stream` (and
  * n_gathered >= 2), every gather runs on gather_stream, ordered by events:
@@ -408,34 +410,59 @@ ZERO_API zero_status zero_step_fused_qgz_qgather(const zero_plan* plan, const ze
  * on `stream`, gather(l+1) after step(l).  The results do not depend on the
  * schedule.
  *
- * Every layer's Adam takes the same step t (scalars_dev is one block for the
- * stack, committed once per call).  Each layer has its own stage-3 plan;
- * all plans share n_d and the dtypes.  gathered: host array of n_gathered
- * device pointers (1 <= n_gathered <= n_layers), buffer k holding at least
- * Psi_l 16-bit values for every layer l with l % n_gathered == k.  Per layer:
- * rank_grads as in zero_step_fused; master, m, v of n_d*S_l floats, updated
- * in place; shards_lp n_d*S_l 16-bit (plan parameter dtype), 16-byte
- * aligned.  No clipping or loss scaling across layers (ZERO_ERR_UNSUPPORTED:
- * the global norm and the overflow check would span every layer).  Events
- * are created and released inside the call; no device memory is allocated.  */
+ * The stack is one model: its step scalars (one block) are committed once
+ * per call, so every layer's Adam takes the same t, and the global checks
+ * span every layer.  With clipping the norm is that of the whole stack's
+ * averaged gradient, the same coefficient for every layer; with loss scaling
+ * a non-finite value in any layer skips the step for all of them (and the
+ * scale halves).  Then a reduce pass over every layer comes first (norm
+ * partials, the non-finite flag, and with clipping and n_d > 4 the fp32
+ * reduced gradient, which the update pass reads instead of the ranks), the
+ * norm is finished once, and the updates follow.  ws: with clipping or loss
+ * scaling, zero_layers_workspace_bytes(hp, n_layers, layers) bytes, 256-byte
+ * aligned (NULL allowed without either).
+ *
+ * micro_batches = k (gradient accumulation, as zero_step_fused_accum): each
+ * layer's rank_grads are its k-th micro-batch's gradients, acc the sum
+ * zero_accumulate_grads left for micro-batches 1..k-1 (NULL exactly when
+ * k == 1); the mean divides by n_d * k.
+ *
+ * Each layer has its own stage-3 plan; all plans share n_d and the dtypes.
+ * gathered: host array of n_gathered device pointers (1 <= n_gathered <=
+ * n_layers), buffer k holding at least Psi_l 16-bit values for every layer l
+ * with l % n_gathered == k.  Per layer: rank_grads as in zero_step_fused;
+ * master, m, v of n_d*S_l floats, updated in place; shards_lp n_d*S_l 16-bit
+ * (plan parameter dtype), 16-byte aligned.  A layer with state_on_host
+ * keeps master/m/v in page-locked host memory mapped at the same address
+ * (else ZERO_ERR_INVALID_ARG).  Events are created and released inside the
+ * call; no device memory is allocated.                                     */
 typedef struct {
     const zero_plan* plan;         /* this layer's partition, stage 3             */
     const void* const* rank_grads; /* host array of n_d device pointers           */
+    const float* acc;              /* accumulated earlier micro-batches, or NULL  */
     float* master;                 /* n_d*S fp32, in place                        */
     float* m;
     float* v;
     void* shards_lp;               /* n_d*S 16-bit parameter shards, flat         */
-    void* grads_ready;             /* cudaEvent_t or NULL: step(l) waits for it
-                                      (the copy or backward pass that wrote the
-                                      layer's rank gradients)                     */
+    void* grads_ready;             /* cudaEvent_t or NULL: the layer's first read
+                                      of its gradients waits for it (the copy or
+                                      backward pass that wrote them)              */
     void* stepped;                 /* cudaEvent_t or NULL: recorded on `stream`
                                       after step(l) (its gradient buffers may be
                                       refilled, its shards read, from then on)    */
+    int state_on_host;             /* 1: master, m, v are page-locked host memory
+                                      read and written over the CPU-GPU link, as
+                                      in zero_step_fused_offload (itwiki DeepSpeed
+                                      example: offload_optimizer to the CPU)     */
 } zero_layer;
 
-ZERO_API zero_status zero_step_layers(const zero_hparams* hp, int n_layers, const zero_layer* layers, int gathers,
-                                      int n_gathered, void* const* gathered, zero_dev_scalars* scalars_dev,
-                                      void* stream, void* gather_stream);
+/* Workspace bytes zero_step_layers needs with these hyper-parameters and
+ * layers (the same on every device); 0 for invalid arguments.               */
+ZERO_API size_t zero_layers_workspace_bytes(const zero_hparams* hp, int n_layers, const zero_layer* layers);
+
+ZERO_API zero_status zero_step_layers(const zero_hparams* hp, int n_layers, const zero_layer* layers,
+                                      int micro_batches, int gathers, int n_gathered, void* const* gathered,
+                                      zero_dev_scalars* scalars_dev, void* ws, void* stream, void* gather_stream);
 
 /* ----------------------------------------------------------- diagnostics --- */
 /* Launch one kernel that waits on a barrier nothing completes, with a wait

@@ -267,7 +267,7 @@ def test_noalloc_scratch_size_matches_the_header(z):
 
 def test_layer_loop_argument_checks(z):
     A, B = 0x10000, 0x20000
-    S1, S2, S3, LP = 0x100000, 0x200000, 0x300000, 0x400000
+    S1, S2, S3, LP, ACC = 0x100000, 0x200000, 0x300000, 0x400000, 0x500000
     hp = z.hparams(lr=1e-3)
     p3 = z.Plan(1000, 2, stage=3)
     p3b = z.Plan(2000, 2, stage=3)
@@ -277,20 +277,22 @@ def test_layer_loop_argument_checks(z):
     ranks4 = (ctypes.c_void_p * 4)(A, B, A, B)
     gathered = (ctypes.c_void_p * 2)(A, B)
 
-    def stack(*plans):
+    def stack(*plans, acc=None):
         arr = (z.ZeroLayer * len(plans))()
         for i, p in enumerate(plans):
             r = ranks4 if p is p4 else ranks
-            arr[i] = z.ZeroLayer(p.handle, ctypes.cast(r, ctypes.c_void_p), S1, S2, S3, LP, None, None)
+            arr[i] = z.ZeroLayer(p.handle, ctypes.cast(r, ctypes.c_void_p), acc, S1, S2, S3, LP, None, None, 0)
         return arr
 
-    def call(h, layers, gathers=1, n_gathered=2, g=gathered, sc=A):
-        return _raw(z, "zero_step_layers", ctypes.byref(h), len(layers), layers, gathers, n_gathered, g, sc, None,
-                    None)
+    def call(h, layers, gathers=1, n_gathered=2, g=gathered, sc=A, ws=None, k=1):
+        return _raw(z, "zero_step_layers", ctypes.byref(h), len(layers), layers, k, gathers, n_gathered, g, sc, ws,
+                    None, None)
 
-    # no clipping or loss scaling across layers
-    assert call(z.hparams(max_norm=1.0), stack(p3, p3b)) == 3
-    assert call(z.hparams(loss_scaling=True), stack(p3, p3b)) == 3
+    # clipping or loss scaling need the workspace (256-byte aligned)
+    clip, ls = z.hparams(max_norm=1.0), z.hparams(loss_scaling=True)
+    assert call(clip, stack(p3, p3b)) == 1
+    assert call(ls, stack(p3, p3b)) == 1
+    assert call(clip, stack(p3, p3b), ws=A + 16) == 2
     # only stage-3 plans, all with the same n_d
     assert call(hp, stack(p3, p2)) == 1
     assert call(hp, stack(p3, p4)) == 1
@@ -304,3 +306,30 @@ def test_layer_loop_argument_checks(z):
     bad = stack(p3, p3b)
     bad[1].shards_lp = LP + 2
     assert call(hp, bad) == 2
+    # accumulation: acc given exactly when micro_batches > 1, 16-byte aligned
+    assert call(hp, stack(p3, p3b), k=2) == 1
+    assert call(hp, stack(p3, p3b, acc=ACC), k=1) == 1
+    assert call(hp, stack(p3, p3b, acc=ACC + 4), k=2) == 2
+    assert call(hp, stack(p3, p3b), k=0) == 1
+    # state in host memory must be page-locked host memory (these addresses are not)
+    host = stack(p3, p3b)
+    host[0].state_on_host = 1
+    assert call(hp, host) == 1
+    host[0].state_on_host = 2
+    assert call(hp, host) == 1
+
+
+def test_layer_loop_workspace_size(z):
+    # per layer room for its reduce pass's partial sums; with clipping and
+    # n_d > 4 each layer's fp32 reduced gradient too (256-byte aligned)
+    p8a, p8b = z.Plan(10_000, 8, stage=3), z.Plan(3_001, 8, stage=3)
+    p2 = z.Plan(10_000, 2, stage=3)
+    layers8 = [(p8a.handle, [0x10000] * 8, 0x100000, 0x200000, 0x300000, 0x400000),
+               (p8b.handle, [0x10000] * 8, 0x100000, 0x200000, 0x300000, 0x400000)]
+    part = 2 * 32768
+    assert z.zero_layers_workspace_bytes(z.hparams(), layers8) == part
+    assert z.zero_layers_workspace_bytes(z.hparams(loss_scaling=True), layers8) == part
+    want = part + sum((4 * p.padded + 255) // 256 * 256 for p in (p8a, p8b))
+    assert z.zero_layers_workspace_bytes(z.hparams(max_norm=1.0), layers8) == want
+    layers2 = [(p2.handle, [0x10000] * 2, 0x100000, 0x200000, 0x300000, 0x400000)]
+    assert z.zero_layers_workspace_bytes(z.hparams(max_norm=1.0), layers2) == 32768

@@ -14,7 +14,7 @@ import torch
 
 import oracle
 import zero_optimizer_step_02_gb300 as z
-from gpu_helpers import Job, u16
+from gpu_helpers import ORACLE_DT, Job, _note_clipped_step, accum_ghat, coef_ulps, oracle_hp, step_with_coef, u16
 
 pytestmark = pytest.mark.gpu
 
@@ -129,3 +129,164 @@ def test_layer_loop_waits_for_each_layers_gradients():
             job.oracle_step()
             job.assert_bit_exact()
             assert np.array_equal(u16(snaps[l]), job.o_lp_shards)
+
+
+# ----------------------------------------------- global checks across layers
+def _global_step(jobs, hp, ghats, b1p, b2p, gpu_coef=None):
+    """The oracle's view of one step of a stack that is one model: the clip
+    norm over every layer's averaged gradient, in layer order (the oracle's
+    sequential fp64 sum over the concatenation), one coefficient for all
+    layers, each layer's Adam from its state before the step.  gpu_coef: the
+    GPU's coefficient when it is one fp32 ulp from the oracle's (the norm is
+    summed in another order), which the re-run then uses.  Returns the
+    oracle's coefficient and squared norm; updates each job's oracle state
+    and 16-bit shards."""
+    ohp = oracle_hp(hp)
+    coef, sq = np.float32(1.0), 0.0
+    if hp.max_norm > 0:
+        sq = oracle.sqnorm(np.concatenate([g[:j.psi] for g, j in zip(ghats, jobs)]))
+        c, applied = oracle.clip_coef(hp.max_norm, sq)
+        coef = np.float32(c) if applied else np.float32(1.0)
+    use = coef if gpu_coef is None else np.float32(gpu_coef)
+    for g, job in zip(ghats, jobs):
+        st, lp = step_with_coef(job.ost, g, use, ohp, b1p, b2p, job.psi, ORACLE_DT[job.pdt])
+        job.ost.master, job.ost.m, job.ost.v = st.master, st.m, st.v
+        job.o_lp_shards[:job.psi] = lp
+    return coef, sq
+
+
+@pytest.mark.parametrize("n_d,second_stream,k", [(8, True, 1), (4, False, 1), (8, True, 2), (3, True, 3)])
+def test_layer_loop_clips_by_the_norm_of_the_whole_stack(n_d, second_stream, k):
+    # n_d = 8: the reduced gradients go through the workspace; n_d <= 4: the
+    # update re-reads the ranks; k > 1: accumulated micro-batches
+    hp = z.hparams(lr=3e-4, beta2=0.95, weight_decay=0.1, max_norm=1.0)
+    sizes = (70_001, 4096 * 10 + 5, 30_000)
+    jobs = [Job(psi, n_d, stage=3, pad=8, hp=hp, seed=500 + i) for i, psi in enumerate(sizes)]
+    scalars = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    z.zero_scalars_init(scalars)
+    layers = [(j.plan.handle, j.buf.rank_ptrs(), j.buf.master, j.buf.m, j.buf.v, j.buf.lp) for j in jobs]
+    gathered = [torch.zeros(max(sizes), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    gs = torch.cuda.Stream() if second_stream else None
+    b1p = b2p = 1.0
+    taken = 0
+    for step in range(1, 4):
+        accs, ghats = [], []
+        for job in jobs:
+            acc = None
+            for mu in range(1, k):
+                job.new_grads(100 * step + mu, sigma=1e-2, heavy_tail=True)
+                job.buf.accumulate(first=mu == 1)
+                acc = oracle.accumulate_grads(job.rows, oracle.BF16, acc)
+            job.new_grads(100 * step + k, sigma=1e-2, heavy_tail=True)
+            accs.append(acc)
+            job.snapshot()
+            ghats.append(accum_ghat(job, acc, k))
+        stack = z.LayerStack([l + (None, None, j.buf.acc if k > 1 else None) for l, j in zip(layers, jobs)])
+        ws = torch.zeros(max(z.zero_layers_workspace_bytes(hp, stack), 256), dtype=torch.uint8, device="cuda")
+        z.zero_step_layers(hp, stack, 1, gathered, scalars, ws=ws, micro_batches=k, gather_stream=gs)
+        torch.cuda.synchronize()
+        sc = z.read_scalars(scalars)
+        assert sc.t == step and sc.status == 0
+        b1p *= float(np.float32(hp.beta1))
+        b2p *= float(np.float32(hp.beta2))
+        coef, sq = _global_step(jobs, hp, ghats, b1p, b2p)
+        assert coef < 1.0                                      # the clip is active
+        psi_total = sum(sizes)
+        assert sc.sqnorm == pytest.approx(sq, rel=2 * psi_total * 2.0 ** -53)
+        d = coef_ulps(sc.clip_coef, coef)
+        assert d <= 1
+        _note_clipped_step(d == 1)
+        if d == 1:
+            taken += 1
+            for job in jobs:
+                job.ost = job.pre.copy()
+            _global_step(jobs, hp, ghats, b1p, b2p, gpu_coef=sc.clip_coef)
+        for job in jobs:
+            job.assert_bit_exact()
+
+
+@pytest.mark.parametrize("clip", [0.0, 1e-3])
+def test_layer_loop_overflow_in_one_layer_skips_every_layer(clip):
+    # fp16 gradients with a loss scale; at step 2 one layer holds +inf: no
+    # layer changes, t stays, the scale halves
+    n_d = 4
+    hp = z.hparams(lr=1e-4, loss_scaling=True, max_norm=clip)
+    sizes = (50_003, 20_000)
+    jobs = [Job(psi, n_d, stage=3, pad=8, gdt=z.ZERO_FP16, hp=hp, seed=600 + i, loss_scale=1024.0)
+            for i, psi in enumerate(sizes)]
+    scalars = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    z.zero_scalars_init(scalars, 1024.0)
+    stack = z.LayerStack([(j.plan.handle, j.buf.rank_ptrs(), j.buf.master, j.buf.m, j.buf.v, j.buf.lp) for j in jobs])
+    ws = torch.zeros(max(z.zero_layers_workspace_bytes(hp, stack), 256), dtype=torch.uint8, device="cuda")
+    gathered = [torch.zeros(max(sizes), dtype=torch.float16, device="cuda") for _ in range(2)]
+    b1p = b2p = 1.0
+    scale = 1024.0
+    for step in range(1, 4):
+        ghats = []
+        for i, job in enumerate(jobs):
+            inf_at = (1, 777) if (step == 2 and i == 1) else None
+            job.new_grads(step, sigma=1e-4, scale=scale, inf_at=inf_at)
+            ghats.append(oracle.reduce_scatter(job.rows, oracle.FP16, n_d * scale, job.plan.shard))
+        before = [job.gpu_state() for job in jobs]
+        z.zero_step_layers(hp, stack, 1, gathered, scalars, ws=ws, gather_stream=torch.cuda.Stream())
+        torch.cuda.synchronize()
+        sc = z.read_scalars(scalars)
+        skipped = not all(np.all(np.isfinite(g[:j.psi])) for g, j in zip(ghats, jobs))
+        assert skipped == (step == 2) and bool(sc.overflow) == skipped
+        if skipped:
+            scale /= 2
+            for job, b in zip(jobs, before):
+                for x, y in zip(b, job.gpu_state()):
+                    assert np.array_equal(x, y)
+        else:
+            b1p *= float(np.float32(hp.beta1))
+            b2p *= float(np.float32(hp.beta2))
+            pre = [job.ost.copy() for job in jobs]
+            coef, _ = _global_step(jobs, hp, ghats, b1p, b2p)
+            if clip > 0:
+                d = coef_ulps(sc.clip_coef, coef)
+                assert coef < 1.0 and d <= 1
+                _note_clipped_step(d == 1)
+                if d == 1:
+                    for job, p in zip(jobs, pre):
+                        job.ost = p
+                    _global_step(jobs, hp, ghats, b1p, b2p, gpu_coef=sc.clip_coef)
+            for job in jobs:
+                job.assert_bit_exact()
+        assert sc.loss_scale == scale and sc.t == (step if step < 2 else step - 1)
+
+
+@pytest.mark.parametrize("n_d,clip", [(8, 1.0), (4, 1.0), (8, 0.0)])
+def test_layer_loop_with_state_in_host_memory(n_d, clip):
+    # the itwiki DeepSpeed example offloads the optimizer state to the CPU:
+    # layer 1 keeps master/m/v in page-locked host memory; the stack must give
+    # the bits of the same stack with every state in HBM
+    hp = z.hparams(lr=3e-4, beta2=0.95, weight_decay=0.1, max_norm=clip)
+    sizes = (60_001, 4096 * 6 + 3)
+    dev = [Job(psi, n_d, stage=3, pad=8, hp=hp, seed=700 + i) for i, psi in enumerate(sizes)]
+    off = [Job(psi, n_d, stage=3, pad=8, hp=hp, seed=700 + i) for i, psi in enumerate(sizes)]
+    hm, hmm, hv = (t.cpu().pin_memory() for t in (off[1].buf.master, off[1].buf.m, off[1].buf.v))
+    gathered = [torch.zeros(max(sizes), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    sa, sb = (torch.zeros(256, dtype=torch.uint8, device="cuda") for _ in range(2))
+    z.zero_scalars_init(sa)
+    z.zero_scalars_init(sb)
+    a = z.LayerStack([(j.plan.handle, j.buf.rank_ptrs(), j.buf.master, j.buf.m, j.buf.v, j.buf.lp) for j in dev])
+    b = z.LayerStack([(off[0].plan.handle, off[0].buf.rank_ptrs(), off[0].buf.master, off[0].buf.m, off[0].buf.v,
+                       off[0].buf.lp),
+                      (off[1].plan.handle, off[1].buf.rank_ptrs(), hm, hmm, hv, off[1].buf.lp, None, None, None, True)])
+    wa = torch.zeros(max(z.zero_layers_workspace_bytes(hp, a), 256), dtype=torch.uint8, device="cuda")
+    wb = torch.zeros(max(z.zero_layers_workspace_bytes(hp, b), 256), dtype=torch.uint8, device="cuda")
+    for step in (1, 2, 3):
+        for x, y in zip(dev, off):
+            x.new_grads(step, sigma=1e-2, heavy_tail=True)
+            y.new_grads(step, sigma=1e-2, heavy_tail=True)
+        z.zero_step_layers(hp, a, 1, gathered, sa, ws=wa, gather_stream=torch.cuda.Stream())
+        z.zero_step_layers(hp, b, 1, gathered, sb, ws=wb, gather_stream=torch.cuda.Stream())
+        torch.cuda.synchronize()
+        for x, y, host in ((dev[0], off[0], None), (dev[1], off[1], (hm, hmm, hv))):
+            ys = host if host else (y.buf.master, y.buf.m, y.buf.v)
+            for t, u in zip((x.buf.master, x.buf.m, x.buf.v), ys):
+                assert torch.equal(t.cpu().view(torch.int32), u.cpu().view(torch.int32))
+            assert torch.equal(x.buf.lp.view(torch.int16), y.buf.lp.view(torch.int16))
+        ra, rb = z.read_scalars(sa), z.read_scalars(sb)
+        assert ra.t == rb.t == step and ra.sqnorm == rb.sqnorm and ra.status == rb.status == 0

@@ -23,7 +23,7 @@ from ._capi import (NOALLOC_SCRATCH_BYTES, ZERO_BF16, ZERO_FP16, ZERO_DEV_TIMEOU
                     zero_step_fused_noalloc, zero_step_fused_qgather, zero_workspace_bytes,
                     zero_quantize_grads, zero_step_fused_qgz, zero_step_fused_offload, zero_accumulate_grads,
                     zero_step_fused_accum, zero_debug_stream_timeout, zero_step_fused_qgz_qgather, rank_ptrs,
-                    zero_step_layers, LayerStack, ZeroLayer)
+                    zero_step_layers, zero_layers_workspace_bytes, LayerStack, ZeroLayer)
 
 __all__ = ["Plan", "StepBuffers", "read_scalars", "row_len", "hparams", "rank_ptrs", "ZeroError", "ZeroHparams",
            "LayerStack", "ZeroLayer",

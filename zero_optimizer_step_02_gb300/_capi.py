@@ -60,9 +60,10 @@ _hp = ctypes.POINTER(ZeroHparams)
 
 class ZeroLayer(ctypes.Structure):
     """zero_layer of zero.h: one layer of the ZeRO-3 layer loop."""
-    _fields_ = [("plan", ctypes.c_void_p), ("rank_grads", ctypes.c_void_p), ("master", ctypes.c_void_p),
-                ("m", ctypes.c_void_p), ("v", ctypes.c_void_p), ("shards_lp", ctypes.c_void_p),
-                ("grads_ready", ctypes.c_void_p), ("stepped", ctypes.c_void_p)]
+    _fields_ = [("plan", ctypes.c_void_p), ("rank_grads", ctypes.c_void_p), ("acc", ctypes.c_void_p),
+                ("master", ctypes.c_void_p), ("m", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("shards_lp", ctypes.c_void_p), ("grads_ready", ctypes.c_void_p), ("stepped", ctypes.c_void_p),
+                ("state_on_host", ctypes.c_int)]
 
 
 _SIGS = {
@@ -97,7 +98,8 @@ _SIGS = {
     "zero_step_fused_qgz": (_i32, [_vp, _hp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "zero_step_fused_qgz_qgather": (_i32, [_vp, _hp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                            _vp, _vp, _vp]),
-    "zero_step_layers": (_i32, [_hp, _i32, ctypes.POINTER(ZeroLayer), _i32, _i32, _vp, _vp, _vp, _vp]),
+    "zero_step_layers": (_i32, [_hp, _i32, ctypes.POINTER(ZeroLayer), _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),
+    "zero_layers_workspace_bytes": (_sz, [_hp, _i32, ctypes.POINTER(ZeroLayer)]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -342,32 +344,46 @@ class LayerStack:
     """The zero_layer array of a stack of layers, built once (the pointers it
     holds stay valid while the caller keeps the tensors alive and in place).
     layers: sequence of (plan_handle, rank_grads, master, m, v, shards_lp
-    [, grads_ready, stepped]), rank_grads a list of per-rank tensors or a
-    rank_ptrs array, the two events torch.cuda.Event objects or None."""
+    [, grads_ready, stepped[, acc[, state_on_host]]]), rank_grads a list of
+    per-rank tensors or a rank_ptrs array, the two events torch.cuda.Event
+    objects or None, acc the layer's accumulated earlier micro-batches or
+    None, state_on_host True when master/m/v are page-locked host tensors."""
 
     def __init__(self, layers):
         self._ranks = [_ptr_array(l[1]) for l in layers]
         self.array = (ZeroLayer * len(layers))()
         for i, l in enumerate(layers):
             plan, _, master, m, v, shards = l[:6]
-            ready, stepped = (tuple(l[6:8]) + (None, None))[:2]
-            self.array[i] = ZeroLayer(plan, ctypes.cast(self._ranks[i], ctypes.c_void_p), _addr(master), _addr(m),
-                                      _addr(v), _addr(shards), _event(ready), _event(stepped))
+            ready, stepped, acc, host = (tuple(l[6:10]) + (None, None, None, False))[:4]
+            self.array[i] = ZeroLayer(plan, ctypes.cast(self._ranks[i], ctypes.c_void_p), _addr(acc), _addr(master),
+                                      _addr(m), _addr(v), _addr(shards), _event(ready), _event(stepped), int(bool(host)))
 
     def __len__(self):
         return len(self.array)
 
 
-def zero_step_layers(hp, layers, gathers, gathered, scalars, stream=None, gather_stream=None):
+def _stack(layers):
+    return layers if isinstance(layers, LayerStack) else LayerStack(layers)
+
+
+def zero_layers_workspace_bytes(hp, layers):
+    stack = _stack(layers)
+    return _lib.zero_layers_workspace_bytes(ctypes.byref(hp), len(stack), stack.array)
+
+
+def zero_step_layers(hp, layers, gathers, gathered, scalars, ws=None, micro_batches=1, stream=None,
+                     gather_stream=None):
     """One ZeRO-3 step over a stack of layers: layer l's gather(s) into
     gathered[l % len(gathered)], then its fused step; with gather_stream the
-    gathers run there, the next layer's overlapping this layer's step.
-    layers: a LayerStack (or the sequence it is built from)."""
-    stack = layers if isinstance(layers, LayerStack) else LayerStack(layers)
+    gathers run there, the next layer's overlapping this layer's step.  With
+    clipping or loss scaling the global checks span every layer (ws: see
+    zero_layers_workspace_bytes).  layers: a LayerStack (or the sequence it
+    is built from)."""
+    stack = _stack(layers)
     gptr = _ptr_array(gathered)
     gs = None if gather_stream is None else _stream(gather_stream)
-    _check(_lib.zero_step_layers(ctypes.byref(hp), len(stack), stack.array, gathers, len(gptr), gptr,
-                                 _addr(scalars), _stream(stream), gs), "zero_step_layers")
+    _check(_lib.zero_step_layers(ctypes.byref(hp), len(stack), stack.array, micro_batches, gathers, len(gptr), gptr,
+                                 _addr(scalars), _addr(ws), _stream(stream), gs), "zero_step_layers")
 
 
 def zero_launch_count():

@@ -289,6 +289,19 @@ zero_status run_fused_q8(const zero_plan* p, const zero_hparams* hp, const signe
 }
 
 // two arrays of n bytes share a byte
+// page-locked host memory the device reaches at the same address (state kept
+// in host memory); anything else is refused before a launch
+bool host_mapped(const void* q)
+{
+    if (q == nullptr) return false;
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, q) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return at.type == cudaMemoryTypeHost && at.devicePointer == q;
+}
+
 bool overlaps(const void* a, const void* b, uintptr_t n)
 {
     const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
@@ -592,18 +605,9 @@ ZERO_API zero_status zero_step_fused_offload(const zero_plan* p, const zero_hpar
                                              void* stream)
 {
     ZK_CALL_RANGE();
-    // every state pointer must be page-locked host memory the device reaches
-    // at the same address; anything else is refused before a launch
     const void* ptrs[] = {mi, m_in, vi, mo, m_out, vo};
-    for (const void* q : ptrs) {
-        if (q == nullptr) return ZERO_ERR_INVALID_ARG;
-        cudaPointerAttributes at;
-        if (cudaPointerGetAttributes(&at, q) != cudaSuccess) {
-            cudaGetLastError();
-            return ZERO_ERR_INVALID_ARG;
-        }
-        if (at.type != cudaMemoryTypeHost || at.devicePointer != q) return ZERO_ERR_INVALID_ARG;
-    }
+    for (const void* q : ptrs)
+        if (!host_mapped(q)) return ZERO_ERR_INVALID_ARG;
     return fused_step(p, hp, ranks, mi, m_in, vi, mo, m_out, vo, lp, sc, ws, stream, true);
 }
 
@@ -887,22 +891,45 @@ struct EventSet {
     EventSet& operator=(const EventSet&) = delete;
 };
 
+// Workspace of the layer loop: per layer room for the partial sums of its
+// reduce pass (written one after another, then finished once), then, when the
+// reduced gradient goes through HBM (clipping with n_d > 4), each layer's fp32
+// reduced gradient at 256-byte aligned offsets.
+size_t layers_ws_bytes(const zero_hparams* hp, int n_layers, const zero_layer* layers)
+{
+    if (hp == nullptr || layers == nullptr || n_layers < 1) return 0;
+    size_t bytes = kPartialBytes * static_cast<size_t>(n_layers);
+    if (hp->max_norm > 0.0f && layers[0].plan != nullptr && clip_materialises(layers[0].plan))
+        for (int l = 0; l < n_layers; ++l)
+            if (layers[l].plan != nullptr)
+                bytes += (sizeof(float) * static_cast<size_t>(layers[l].plan->padded) + 255) / 256 * 256;
+    return bytes;
+}
+
 }  // namespace
 
-ZERO_API zero_status zero_step_layers(const zero_hparams* hp, int n_layers, const zero_layer* layers, int gathers,
-                                      int n_gathered, void* const* gathered, zero_dev_scalars* sc, void* stream,
-                                      void* gather_stream)
+ZERO_API size_t zero_layers_workspace_bytes(const zero_hparams* hp, int n_layers, const zero_layer* layers)
+{
+    return layers_ws_bytes(hp, n_layers, layers);
+}
+
+ZERO_API zero_status zero_step_layers(const zero_hparams* hp, int n_layers, const zero_layer* layers,
+                                      int micro_batches, int gathers, int n_gathered, void* const* gathered,
+                                      zero_dev_scalars* sc, void* ws, void* stream, void* gather_stream)
 {
     ZK_CALL_RANGE();
     zero_status s;
     if ((s = check_hparams(hp)) != ZERO_OK) return s;
-    if (hp->max_norm > 0.0f || hp->loss_scaling) return ZERO_ERR_UNSUPPORTED;
     if (layers == nullptr || n_layers < 1 || n_layers > ZERO_MAX_LAYERS) return ZERO_ERR_INVALID_ARG;
+    if (micro_batches < 1 || micro_batches > ZERO_MAX_MICRO_BATCHES) return ZERO_ERR_INVALID_ARG;
     if (gathers < 1 || gathers > 2) return ZERO_ERR_INVALID_ARG;
     if (gathered == nullptr || n_gathered < 1 || n_gathered > n_layers) return ZERO_ERR_INVALID_ARG;
     for (int k = 0; k < n_gathered; ++k)
         if ((s = check_dev(gathered[k])) != ZERO_OK) return s;
     if ((s = check_dev(sc, 256)) != ZERO_OK) return s;
+    const bool clip = hp->max_norm > 0.0f;
+    const bool ls = hp->loss_scaling != 0;
+    if ((clip || ls) && (s = check_dev(ws, 256)) != ZERO_OK) return s;
     const zero_plan* p0 = layers[0].plan;
     for (int l = 0; l < n_layers; ++l) {
         const zero_layer& L = layers[l];
@@ -913,6 +940,11 @@ ZERO_API zero_status zero_step_layers(const zero_hparams* hp, int n_layers, cons
         if ((s = check_ranks(p, L.rank_grads)) != ZERO_OK) return s;
         if ((s = check_state(p, L.master, L.m, L.v, L.master, L.m, L.v)) != ZERO_OK) return s;
         if ((s = check_dev(L.shards_lp)) != ZERO_OK) return s;
+        if ((L.acc == nullptr) != (micro_batches == 1)) return ZERO_ERR_INVALID_ARG;
+        if (L.acc != nullptr && !aligned(L.acc, 16)) return ZERO_ERR_MISALIGNED;
+        if (L.state_on_host != 0 && L.state_on_host != 1) return ZERO_ERR_INVALID_ARG;
+        if (L.state_on_host && !(host_mapped(L.master) && host_mapped(L.m) && host_mapped(L.v)))
+            return ZERO_ERR_INVALID_ARG;
     }
     const cudaStream_t st = as_stream(stream);
     // a second stream needs a second gathered buffer: with one, every gather
@@ -926,6 +958,36 @@ ZERO_API zero_status zero_step_layers(const zero_hparams* hp, int n_layers, cons
     if (two && !ev.ok(n_ev)) return ZERO_ERR_CUDA;
     const int n_d = p0->n_d;
     const void* shard_ptr[ZERO_MAX_RANKS];
+    const bool materialise = clip && clip_materialises(p0);
+    auto acc_of = [&](const zero_layer& L) { return Accum{L.acc, micro_batches}; };
+    // the workspace: partial sums of every layer's reduce pass, one after
+    // another, then the layers' reduced gradients
+    double* partials = partials_of(ws);
+    auto ghat_at = [&](int l) -> float* {
+        size_t off = kPartialBytes * static_cast<size_t>(n_layers);
+        for (int m = 0; m < l; ++m)
+            off += (sizeof(float) * static_cast<size_t>(layers[m].plan->padded) + 255) / 256 * 256;
+        return reinterpret_cast<float*>(static_cast<char*>(ws) + off);
+    };
+
+    // The global checks span every layer: with clipping or loss scaling a
+    // reduce pass over each layer first (norm partials, the non-finite flag;
+    // the reduced gradient too when it goes through HBM), the norm finished
+    // once, then the updates, each applying the one coefficient (and all
+    // skipped together when a value was not finite).
+    if (clip || ls) {
+        int n_part = 0;
+        for (int l = 0; l < n_layers; ++l) {
+            const zero_layer& L = layers[l];
+            if (L.grads_ready != nullptr) ZK_TRY(cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(L.grads_ready), 0));
+            int grid = 0;
+            if ((s = run_reduce(L.plan, hp, L.rank_grads, materialise ? ghat_at(l) : nullptr, clip,
+                                partials + n_part, sc, st, &grid, acc_of(L))) != ZERO_OK)
+                return s;
+            if (clip) n_part += grid;
+        }
+        if (clip) ZK_TRY(zk::launch_finalize_sqnorm(partials, n_part, *hp, sc, st));
+    }
 
     // gather(l): layer l's 16-bit shards into gathered[l % n_gathered], once
     // or twice (forward and backward); it waits for the step that last used
@@ -949,17 +1011,24 @@ ZERO_API zero_status zero_step_layers(const zero_hparams* hp, int n_layers, cons
         ZK_TRY(cudaStreamWaitEvent(gs, ev.ev[0], 0));
     }
     if ((s = gather(0)) != ZERO_OK) return s;
+    const int flags = (clip ? zk::F_CLIP : 0) | (ls ? (zk::F_GUARD | zk::F_LSCALE) : 0);
     for (int l = 0; l < n_layers; ++l) {
         // the next layer's gather is issued before this layer's step, so that
         // with two streams it runs while the step does
         if (two && l + 1 < n_layers && (s = gather(l + 1)) != ZERO_OK) return s;
         if (two) ZK_TRY(cudaStreamWaitEvent(st, ev.ev[1 + l], 0));
         const zero_layer& L = layers[l];
-        if (L.grads_ready != nullptr) ZK_TRY(cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(L.grads_ready), 0));
+        if (!(clip || ls) && L.grads_ready != nullptr)
+            ZK_TRY(cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(L.grads_ready), 0));
         // no scalar commit per layer: every layer's Adam takes this step's t
-        if ((s = run_fused(L.plan, hp, L.rank_grads, L.master, L.m, L.v, L.master, L.m, L.v, L.shards_lp, 0, sc,
-                           st)) != ZERO_OK)
-            return s;
+        const bool host = L.state_on_host != 0;
+        if (materialise)
+            s = run_adam(L.plan, hp, ghat_at(l), L.master, L.m, L.v, L.master, L.m, L.v, L.shards_lp,
+                         flags & ~zk::F_LSCALE, sc, st, nullptr, 0, host);
+        else
+            s = run_fused(L.plan, hp, L.rank_grads, L.master, L.m, L.v, L.master, L.m, L.v, L.shards_lp, flags, sc,
+                          st, nullptr, 0, host, acc_of(L));
+        if (s != ZERO_OK) return s;
         if (two) ZK_TRY(cudaEventRecord(ev.ev[1 + n_layers + l], st));
         if (L.stepped != nullptr) ZK_TRY(cudaEventRecord(static_cast<cudaEvent_t>(L.stepped), st));
         if (!two && l + 1 < n_layers && (s = gather(l + 1)) != ZERO_OK) return s;
@@ -968,7 +1037,8 @@ ZERO_API zero_status zero_step_layers(const zero_hparams* hp, int n_layers, cons
         ZK_TRY(cudaEventRecord(ev.ev[1 + 2 * n_layers], gs));
         ZK_TRY(cudaStreamWaitEvent(st, ev.ev[1 + 2 * n_layers], 0));
     }
-    // the step scalars advance once for the whole stack
+    // the step scalars advance once for the whole stack (or, after a
+    // non-finite value, the step is skipped and the scale halves)
     return from_cuda(zk::launch_epilogue(*hp, sc, st));
 }
 
