@@ -136,10 +136,14 @@ def workload(cfg, nd=None, qgather=False, psi=None, qgz=False, gathers=1, offloa
             final = 2 * n_d + 30
         w["bytes_per_param"] = micro + final
     elif w.get("qgz") and w.get("qgather"):
-        # int8 codes in, int8 gather out; clipped, a read-only reduce pass
-        # over the codes first
+        # int8 codes in, int8 gather out; clipped, a reduce pass over the codes
+        # first: for n_d > 4 it writes the fp32 reduced gradient, which the
+        # Adam pass with the int8 gather reads, else the update re-reads the codes
         q = n_d * (1 + 4.0 / 2048)
-        w["bytes_per_param"] = q + 27 + 4.0 / 2048 + (q if w["clip"] > 0 else 0)
+        if w["clip"] > 0 and n_d > 4:
+            w["bytes_per_param"] = (q + 4) + (4 + 27 + 4.0 / 2048)
+        else:
+            w["bytes_per_param"] = q + 27 + 4.0 / 2048 + (q if w["clip"] > 0 else 0)
     elif w.get("qgz"):
         # the receiver reads int8 codes + one fp32 scale per 2048 per rank;
         # clipped, the reduce pass over them comes first, writing the fp32
@@ -150,8 +154,13 @@ def workload(cfg, nd=None, qgather=False, psi=None, qgz=False, gathers=1, offloa
         else:
             w["bytes_per_param"] = q + 26
     elif w.get("qgather"):
-        # clipped: a read-only reduce pass, then the fused step re-reads the ranks
-        w["bytes_per_param"] = 2 * n_d + 27 + 4.0 / 2048 + (2 * n_d if w["clip"] > 0 else 0)
+        # clipped: for n_d > 4 the reduce pass writes the fp32 reduced gradient
+        # and the Adam pass with the int8 gather reads it; else a read-only
+        # reduce pass, then the fused step re-reads the ranks
+        if w["clip"] > 0 and n_d > 4:
+            w["bytes_per_param"] = (2 * n_d + 4) + (4 + 27 + 4.0 / 2048)
+        else:
+            w["bytes_per_param"] = 2 * n_d + 27 + 4.0 / 2048 + (2 * n_d if w["clip"] > 0 else 0)
     elif w["clip"] > 0:
         w["bytes_per_param"] = 2 * n_d + 34 if n_d > 4 else 4 * n_d + 26
     elif w["stage"] == 3:

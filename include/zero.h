@@ -306,12 +306,14 @@ ZERO_API zero_status zero_quant_gather(const zero_plan* plan, const void* shards
 /* The fused step of zero_step_fused whose epilogue is the quantized gather
  * above instead of the plain 16-bit write: codes, scales and dequantized bf16
  * gathered values come from the updated master of each block (block must be
- * 2048; parameter dtype bf16).  With clipping or loss scaling a read-only
- * reduce pass comes first (squared-norm partials and the non-finite flag, in
- * ws: zero_workspace_bytes(plan, hp) bytes, 256-byte aligned); the update
- * pass then re-reads the rank gradients, finishes the norm in its prologue,
- * and with the flag set writes nothing (state, codes, scales and gathered
- * values keep the last step's) while the scalar epilogue halves the scale.
+ * 2048; parameter dtype bf16).  With clipping or loss scaling a reduce pass
+ * comes first (squared-norm partials and the non-finite flag, in ws:
+ * zero_workspace_bytes(plan, hp) bytes, 256-byte aligned; with clipping and
+ * n_d > 4 also the fp32 reduced gradient); the update pass then reads that
+ * reduced gradient (or, without it, re-reads the rank gradients), finishes
+ * the norm in its prologue, and with the flag set writes nothing (state,
+ * codes, scales and gathered values keep the last step's) while the scalar
+ * epilogue halves the scale.
  * Loss scaling needs the state in place (master_out == master_in, likewise
  * m, v), else ZERO_ERR_UNSUPPORTED.  ws may be NULL with neither.           */
 ZERO_API zero_status zero_step_fused_qgather(const zero_plan* plan, const zero_hparams* hp,
@@ -372,9 +374,10 @@ ZERO_API zero_status zero_step_fused_qgz(const zero_plan* plan, const zero_hpara
  * zero_step_fused_qgather (codes_out, scales_out and the dequantized bf16
  * gathered values from the updated master, blocks of 2048 from each shard's
  * first element).  Layouts as in those two entry points.  With clipping a
- * read-only reduce pass over the codes comes first (norm partials in ws:
+ * reduce pass over the codes comes first (norm partials in ws:
  * zero_workspace_bytes(plan, hp) bytes, 256-byte aligned; ws may be NULL
- * without clipping) and the update pass re-reads them.  block must be 2048,
+ * without clipping); for n_d > 4 it also writes the fp32 reduced gradient,
+ * which the update pass reads, else the update pass re-reads the codes.  block must be 2048,
  * the parameter dtype bf16; no loss scaling (ZERO_ERR_UNSUPPORTED).         */
 ZERO_API zero_status zero_step_fused_qgz_qgather(const zero_plan* plan, const zero_hparams* hp,
                                                  const signed char* const* rank_codes, const float* rank_scales,

@@ -59,9 +59,13 @@ def test_quantized_variants_of_the_other_zero2_workloads(cfg, n_d, clip):
     # clipped qgZ with n_d > 4: reduce pass over codes + scales writing the fp32
     # reduced gradient (4), then the Adam pass (30)
     assert bench.workload(cfg, qgz=True)["bytes_per_param"] == (q + 34 if clip else q + 26)
-    # clipped int8 gather: a read-only reduce pass (2 n_d) before the fused step
-    want = 2 * n_d + 27 + 4.0 / 2048 + (2 * n_d if clip else 0)
+    # clipped int8 gather with n_d > 4: the reduce pass writes the fp32
+    # reduced gradient (2 n_d + 4), the Adam pass with the int8 gather reads it
+    # with the state and writes state, codes and dequantized bf16 (4 + 24 + 3)
+    want = (2 * n_d + 4) + (4 + 27 + 4.0 / 2048) if clip else 2 * n_d + 27 + 4.0 / 2048
     assert bench.workload(cfg, qgather=True)["bytes_per_param"] == want
+    # n_d <= 4: a read-only reduce pass (2 n_d) before the fused step
+    assert bench.workload(5, nd=4, qgather=True)["bytes_per_param"] == 2 * 4 + 27 + 4.0 / 2048
 
 
 def test_quantized_variant_names():
@@ -73,11 +77,12 @@ def test_quantized_variant_names():
 
 @pytest.mark.parametrize("cfg,n_d,clip", [(5, 8, False), (2, 8, True)])
 def test_both_quantized_exchanges(cfg, n_d, clip):
-    # int8 codes + scales in, int8 codes + scale + dequantized bf16 out; clipped,
-    # a read-only reduce pass over the codes first
+    # int8 codes + scales in, int8 codes + scale + dequantized bf16 out; clipped
+    # (n_d > 4), a reduce pass over the codes writing the fp32 reduced gradient
+    # first, which the Adam pass with the int8 gather reads
     q = n_d * (1 + 4.0 / 2048)
     w = bench.workload(cfg, qgz=True, qgather=True)
-    assert w["bytes_per_param"] == q + 27 + 4.0 / 2048 + (q if clip else 0)
+    assert w["bytes_per_param"] == ((q + 4) + (4 + 27 + 4.0 / 2048) if clip else q + 27 + 4.0 / 2048)
     assert w["name"].endswith("_qgz_qgather") and w["pad"] == 16
 
 

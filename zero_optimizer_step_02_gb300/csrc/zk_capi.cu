@@ -289,6 +289,42 @@ zero_status run_fused_q8(const zero_plan* p, const zero_hparams* hp, const signe
 }
 
 // two arrays of n bytes share a byte
+// Adam from the fp32 reduced gradient g with the int8 gather as its epilogue
+// (tiles inside shards: each 2048-element block starts in its shard); flags
+// hold F_QUANT | F_EPILOGUE and F_CLIP | F_FINALIZE (the partials in ws) and
+// F_GUARD as the schedule needs
+zero_status run_qadam(const zero_plan* p, const zero_hparams* hp, const float* g, const float* mi,
+                      const float* m_in, const float* vi, float* mo, float* m_out, float* vo, signed char* codes,
+                      float* scales, void* gathered, int flags, zero_dev_scalars* sc, cudaStream_t st, void* fin_ws,
+                      int fin_n)
+{
+    StreamArgs a = base_args(hp, sc);
+    if (flags & zk::F_FINALIZE) set_finalize(a, fin_ws, fin_n);
+    a.n_ranks = 0;
+    a.base = 0;
+    a.seg_stride = p->shard;
+    a.seg_len = p->shard;
+    a.limit = p->psi;
+    a.n_seg = p->n_d;
+    a.tiles_per_seg = tiles_of(p->shard);
+    a.q_blocks_per_shard = (p->shard + zk::kQuantBlock - 1) / zk::kQuantBlock;
+    a.tma_ok = (p->shard % 4) == 0 ? 1 : 0;   // every fp32 stream of a tile starts 16-byte aligned
+    a.n_side = 4;
+    a.n_side_tma = 4;
+    a.side[0] = g;
+    a.side[1] = mi;
+    a.side[2] = m_in;
+    a.side[3] = vi;
+    a.out_f32[0] = mo;
+    a.out_f32[1] = m_out;
+    a.out_f32[2] = vo;
+    a.q_codes = codes;
+    a.q_scales = scales;
+    a.q_gathered = gathered;
+    a.flags = flags;
+    return from_cuda(zk::launch_stream(zk::OP_QADAM, ZERO_BF16, p->param_dtype, a, st));
+}
+
 // page-locked host memory the device reaches at the same address (state kept
 // in host memory); anything else is refused before a launch
 bool host_mapped(const void* q)
@@ -690,6 +726,15 @@ ZERO_API zero_status zero_step_fused_qgather(const zero_plan* p, const zero_hpar
     const cudaStream_t st = as_stream(stream);
     int flags = zk::F_QUANT | zk::F_EPILOGUE;
     int n = 0;
+    if (clip && clip_materialises(p)) {
+        // the reduce pass writes the fp32 reduced gradient (and the norm
+        // partials, and under loss scaling the non-finite flag); the Adam pass
+        // with the int8 gather reads it instead of the ranks
+        float* g = ghat_of(ws);
+        if ((s = run_reduce(p, hp, ranks, g, true, ws, sc, st, &n)) != ZERO_OK) return s;
+        return run_qadam(p, hp, g, mi, m_in, vi, mo, m_out, vo, codes, scales, gathered,
+                         flags | zk::F_CLIP | zk::F_FINALIZE | (ls ? zk::F_GUARD : 0), sc, st, ws, n);
+    }
     if (clip || ls) {
         // a read-only reduce pass first: the squared-norm partials (clipping)
         // and the non-finite flag (loss scaling); the update pass re-reads the
@@ -800,6 +845,14 @@ ZERO_API zero_status zero_step_fused_qgz_qgather(const zero_plan* p, const zero_
     const cudaStream_t st = as_stream(stream);
     int flags = zk::F_QUANT | zk::F_EPILOGUE;
     int n = 0;
+    if (clip && clip_materialises(p)) {
+        // the reduce pass over the codes writes the fp32 reduced gradient; the
+        // Adam pass with the int8 gather reads it instead of decoding again
+        float* g = ghat_of(ws);
+        if ((s = run_reduce_q8(p, hp, codes, scales, g, ws, sc, st, &n)) != ZERO_OK) return s;
+        return run_qadam(p, hp, g, mi, m_in, vi, mo, m_out, vo, codes_out, scales_out, gathered,
+                         flags | zk::F_CLIP | zk::F_FINALIZE, sc, st, ws, n);
+    }
     if (clip) {
         // a read-only reduce pass over the codes; the update pass re-reads them
         if ((s = run_reduce_q8(p, hp, codes, scales, nullptr, ws, sc, st, &n)) != ZERO_OK) return s;

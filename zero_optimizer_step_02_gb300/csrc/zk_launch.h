@@ -7,7 +7,13 @@
 
 namespace zk {
 
-enum { OP_FUSED = 0, OP_REDUCE = 1, OP_ADAM = 2, OP_QFUSED = 3 /* fused step + int8 gather epilogue */ };
+enum {
+    OP_FUSED = 0,
+    OP_REDUCE = 1,
+    OP_ADAM = 2,
+    OP_QFUSED = 3,  // fused step + int8 gather epilogue
+    OP_QADAM = 4    // Adam from an fp32 reduced gradient + int8 gather epilogue
+};
 
 // rank streams that carry int8 codes with per-rank fp32 block scales (the
 // quantized gradient exchange) instead of bf16 / fp16 values
@@ -21,9 +27,10 @@ constexpr int kGradQ8 = 2;
 // at limit (= Psi), so that no tile crosses a shard boundary.
 struct StreamArgs {
     const void* rank[ZERO_MAX_RANKS];  // 16-bit gradient buffers, rank order
-    const float* side[4];              // fp32 inputs: OP_FUSED {master, m, v, carry}; OP_ADAM {g, master, m, v};
-                                       // OP_REDUCE {carry}  (carry: F_CARRY only)
-    float* out_f32[3];                 // OP_FUSED/OP_ADAM {master, m, v}; OP_REDUCE {g or null}
+    const float* side[4];              // fp32 inputs: OP_FUSED/OP_QFUSED {master, m, v, carry};
+                                       // OP_ADAM/OP_QADAM {g, master, m, v}; OP_REDUCE {carry}
+                                       // (carry: F_CARRY only)
+    float* out_f32[3];                 // OP_FUSED/OP_ADAM/OP_QFUSED/OP_QADAM {master, m, v}; OP_REDUCE {g or null}
     void* out_lp;                      // 16-bit parameters out (null: none)
     const float* q_rank_scales;        // kGradQ8 ranks: scales, block-major, rank-minor:
     long long q_rank_scale_stride;     //   [(shard * blocks_per_shard + block) * stride + rank], stride % 4 == 0
@@ -36,7 +43,7 @@ struct StreamArgs {
     int fin_n;                         // ... and how many
     long long base, seg_stride, seg_len, limit, tiles_per_seg, q_blocks_per_shard;
     int n_seg;
-    int n_ranks;                       // rank streams (0 for OP_ADAM)
+    int n_ranks;                       // rank streams (0 for OP_ADAM and OP_QADAM)
     int micro;                         // micro-batches in the mean (divisor n_ranks * micro); 0 reads as 1
     int n_side;                        // fp32 side streams
     int n_side_tma;                    // the first n_side_tma of them are staged by bulk copies; the

@@ -17,6 +17,8 @@
 //               partials, non-finite detection), or one micro-batch's
 //               undivided rank sum added to an fp32 accumulator
 //   OP_ADAM   : Adam from an fp32 reduced gradient + 16-bit cast
+//   OP_QFUSED / OP_QADAM : OP_FUSED / OP_ADAM with the fused int8 gather as
+//               the epilogue (tiles inside shards, one block per 2048)
 //
 // Sources: DP-notes "ZeRO-2: Gradient Partitioning" (reduce-scatter, then
 // each rank updates its own partition), itwiki "FSDP와의 관계" (fp32
@@ -210,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    constexpr bool quant = OP == OP_QFUSED;
+    constexpr bool quant = OP == OP_QFUSED || OP == OP_QADAM;
     // the int8 gather over int8 rank streams takes one quantization block per
     // half of the consumers (an 8-warp absmax barrier): 7% faster at N_d = 8
     // than one block per chunk row; with 16-bit rank streams the chunk rows
@@ -540,18 +542,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
                         }
                     }
                 } else {
-                    // OP_FUSED: side = {master, m, v[, carry]}; OP_ADAM: side = {g, master, m, v}
-                    constexpr int P = (OP == OP_ADAM) ? 1 : 0;
+                    // OP_FUSED / OP_QFUSED: side = {master, m, v[, carry]};
+                    // OP_ADAM / OP_QADAM: side = {g, master, m, v}
+                    constexpr int P = (OP == OP_ADAM || OP == OP_QADAM) ? 1 : 0;
                     // uniform tests (divisor form, carry, detection, clip, decay)
                     // made once per chunk, not once per element -- except in the
                     // int8-gather step and with int8 ranks, whose register budget
                     // measured faster with the per-element form
                     float pv[4], mv[4], vv[4], gv[4];
                     uint16_t lp[4];
-                    if constexpr (OP == OP_QFUSED || GT == kGradQ8) {
+                    if constexpr (quant || GT == kGradQ8) {
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            float g = mean_of(c, carry ? __fadd_rn(sv[ch][kCarry][e], acc[ch][e]) : acc[ch][e]);
+                            float g;
+                            if constexpr (OP == OP_QADAM)
+                                g = sv[ch][0][e];
+                            else
+                                g = mean_of(c, carry ? __fadd_rn(sv[ch][kCarry][e], acc[ch][e]) : acc[ch][e]);
                             if (detect && e < cnt && !is_finite_f32(g)) nonfinite = true;
                             if (c.clip) g = __fmul_rn(g, c.coef);
                             pv[e] = sv[ch][P + 0][e];
@@ -862,7 +869,7 @@ template <int GT, int PT, int OP>
 cudaError_t launch_one(StreamArgs& a, cudaStream_t st)
 {
     constexpr int kG = group_ranks<GT>();
-    if constexpr (OP == OP_ADAM) {
+    if constexpr (OP == OP_ADAM || OP == OP_QADAM) {
         return launch_one_k<GT, PT, OP, kPartial>(a, st);
     } else {
         // eight int8 ranks: the reduce pass measured 3% faster with the loop of
@@ -897,6 +904,8 @@ cudaError_t launch_stream(int op, int grad_dtype, int param_dtype, StreamArgs& a
         return gb ? launch_one<ZERO_BF16, ZERO_BF16, OP_REDUCE>(a, st) : launch_one<ZERO_FP16, ZERO_BF16, OP_REDUCE>(a, st);
     case OP_ADAM:
         return pb ? launch_one<ZERO_BF16, ZERO_BF16, OP_ADAM>(a, st) : launch_one<ZERO_BF16, ZERO_FP16, OP_ADAM>(a, st);
+    case OP_QADAM:    // the int8 gather reads bf16 parameters only
+        return pb ? launch_one<ZERO_BF16, ZERO_BF16, OP_QADAM>(a, st) : cudaErrorInvalidValue;
     case OP_QFUSED:   // the int8 gather reads bf16 parameters only
         if (!pb) return cudaErrorInvalidValue;
         return gb ? launch_one<ZERO_BF16, ZERO_BF16, OP_QFUSED>(a, st) : launch_one<ZERO_FP16, ZERO_BF16, OP_QFUSED>(a, st);
