@@ -400,7 +400,13 @@ ZERO_API zero_status zero_step_fused_qgz_qgather(const zero_plan* plan, const ze
  * Per layer l = 0 .. n_layers-1, in order:
  *   gather(l): zero_all_gather of layer l's 16-bit shards into
  *              gathered[l % n_gathered], `gathers` times (1: once per step;
- *              2: forward and backward, the pages' 3-Psi volume);
+ *              2: forward and backward, the pages' 3-Psi volume); with
+ *              gathered_codes and gathered_scales (itwiki "후속 기법",
+ *              ZeRO++ row: qwZ block-quantizes the weight all-gather) it is
+ *              zero_quant_gather with block 2048 instead: codes into
+ *              gathered_codes[k] (n_d*S_l int8), scales into
+ *              gathered_scales[k] (n_d*ceil(S_l/2048) floats), dequantized
+ *              bf16 into gathered[k], k = l % n_gathered (bf16 parameters);
  *   step(l):   zero_step_fused_accum of layer l in place (stage 3: the
  *              updated 16-bit shards overwrite shards_lp).
  * gather(l) reads the shards as the previous step left them; step(l) comes
@@ -465,6 +471,7 @@ ZERO_API size_t zero_layers_workspace_bytes(const zero_hparams* hp, int n_layers
 
 ZERO_API zero_status zero_step_layers(const zero_hparams* hp, int n_layers, const zero_layer* layers,
                                       int micro_batches, int gathers, int n_gathered, void* const* gathered,
+                                      signed char* const* gathered_codes, float* const* gathered_scales,
                                       zero_dev_scalars* scalars_dev, void* ws, void* stream, void* gather_stream);
 
 /* ----------------------------------------------------------- diagnostics --- */

@@ -284,9 +284,9 @@ def test_layer_loop_argument_checks(z):
             arr[i] = z.ZeroLayer(p.handle, ctypes.cast(r, ctypes.c_void_p), acc, S1, S2, S3, LP, None, None, 0)
         return arr
 
-    def call(h, layers, gathers=1, n_gathered=2, g=gathered, sc=A, ws=None, k=1):
-        return _raw(z, "zero_step_layers", ctypes.byref(h), len(layers), layers, k, gathers, n_gathered, g, sc, ws,
-                    None, None)
+    def call(h, layers, gathers=1, n_gathered=2, g=gathered, sc=A, ws=None, k=1, codes=None, scales=None):
+        return _raw(z, "zero_step_layers", ctypes.byref(h), len(layers), layers, k, gathers, n_gathered, g, codes,
+                    scales, sc, ws, None, None)
 
     # clipping or loss scaling need the workspace (256-byte aligned)
     clip, ls = z.hparams(max_norm=1.0), z.hparams(loss_scaling=True)
@@ -311,6 +311,13 @@ def test_layer_loop_argument_checks(z):
     assert call(hp, stack(p3, p3b, acc=ACC), k=1) == 1
     assert call(hp, stack(p3, p3b, acc=ACC + 4), k=2) == 2
     assert call(hp, stack(p3, p3b), k=0) == 1
+    # quantized gathers: codes and scales for every buffer, or none; bf16 parameters only
+    arr2 = (ctypes.c_void_p * 2)(A, B)
+    assert call(hp, stack(p3, p3b), codes=arr2) == 1
+    assert call(hp, stack(p3, p3b), scales=arr2) == 1
+    assert call(hp, stack(p3, p3b), codes=arr2, scales=(ctypes.c_void_p * 2)(A, B + 4)) == 2
+    p16a, p16b = z.Plan(1000, 2, stage=3, param_dtype=z.ZERO_FP16), z.Plan(2000, 2, stage=3, param_dtype=z.ZERO_FP16)
+    assert call(hp, stack(p16a, p16b), codes=arr2, scales=arr2) == 3
     # state in host memory must be page-locked host memory (these addresses are not)
     host = stack(p3, p3b)
     host[0].state_on_host = 1

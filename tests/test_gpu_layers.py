@@ -290,3 +290,40 @@ def test_layer_loop_with_state_in_host_memory(n_d, clip):
             assert torch.equal(x.buf.lp.view(torch.int16), y.buf.lp.view(torch.int16))
         ra, rb = z.read_scalars(sa), z.read_scalars(sb)
         assert ra.t == rb.t == step and ra.sqnorm == rb.sqnorm and ra.status == rb.status == 0
+
+
+@pytest.mark.parametrize("second_stream,gathers", [(True, 1), (False, 2)])
+def test_layer_loop_with_quantized_gathers(second_stream, gathers):
+    # ZeRO++ qwZ on the ZeRO-3 weight gathers (itwiki "후속 기법", ZeRO++ row):
+    # each layer's gather block-quantizes its bf16 shards; codes, scales and
+    # dequantized values bit for bit against the oracle's quantizer over the
+    # shards the step started from; the steps themselves are unchanged
+    n_d = 8
+    hp = z.hparams(lr=1e-3, weight_decay=0.01)
+    sizes = (70_001, 4096 * 9 + 7, 5)
+    jobs = [Job(psi, n_d, stage=3, pad=8, hp=hp, seed=800 + i) for i, psi in enumerate(sizes)]
+    scalars = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    z.zero_scalars_init(scalars)
+    stack = z.LayerStack([(j.plan.handle, j.buf.rank_ptrs(), j.buf.master, j.buf.m, j.buf.v, j.buf.lp) for j in jobs])
+    n_g = len(jobs)
+    gathered = [torch.zeros(j.psi, dtype=torch.bfloat16, device="cuda") for j in jobs]
+    codes = [torch.full((j.plan.padded,), 99, dtype=torch.int8, device="cuda") for j in jobs]
+    scales = [torch.full((n_d * -(-j.plan.shard // 2048),), -1.0, device="cuda") for j in jobs]
+    gs = torch.cuda.Stream() if second_stream else None
+    for step in (1, 2, 3):
+        want = []
+        for job in jobs:
+            job.new_grads(step, sigma=1e-2)
+            want.append(oracle.quant_gather(job.o_lp_shards.copy(), n_d, job.psi, job.plan.shard, 2048))
+        z.zero_step_layers(hp, stack, gathers, gathered, scalars, gather_stream=gs, gathered_codes=codes,
+                           gathered_scales=scales)
+        torch.cuda.synchronize()
+        assert z.read_scalars(scalars).t == step
+        for l, job in enumerate(jobs):
+            oc, osc, og = want[l]
+            assert np.array_equal(codes[l].cpu().numpy()[:job.psi], oc[:job.psi]), (step, l)
+            assert np.array_equal(scales[l].cpu().numpy().view(np.uint32), osc.view(np.uint32)), (step, l)
+            assert np.array_equal(u16(gathered[l]), og), (step, l)
+            job.oracle_step()
+            job.assert_bit_exact()
+    assert n_g == len(gathered)

@@ -98,7 +98,8 @@ _SIGS = {
     "zero_step_fused_qgz": (_i32, [_vp, _hp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "zero_step_fused_qgz_qgather": (_i32, [_vp, _hp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                            _vp, _vp, _vp]),
-    "zero_step_layers": (_i32, [_hp, _i32, ctypes.POINTER(ZeroLayer), _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),
+    "zero_step_layers": (_i32, [_hp, _i32, ctypes.POINTER(ZeroLayer), _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp,
+                                _vp]),
     "zero_layers_workspace_bytes": (_sz, [_hp, _i32, ctypes.POINTER(ZeroLayer)]),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -372,18 +373,21 @@ def zero_layers_workspace_bytes(hp, layers):
 
 
 def zero_step_layers(hp, layers, gathers, gathered, scalars, ws=None, micro_batches=1, stream=None,
-                     gather_stream=None):
+                     gather_stream=None, gathered_codes=None, gathered_scales=None):
     """One ZeRO-3 step over a stack of layers: layer l's gather(s) into
     gathered[l % len(gathered)], then its fused step; with gather_stream the
     gathers run there, the next layer's overlapping this layer's step.  With
     clipping or loss scaling the global checks span every layer (ws: see
-    zero_layers_workspace_bytes).  layers: a LayerStack (or the sequence it
-    is built from)."""
+    zero_layers_workspace_bytes).  With gathered_codes / gathered_scales (one
+    per gathered buffer) the gathers are block-int8 quantized (qwZ).
+    layers: a LayerStack (or the sequence it is built from)."""
     stack = _stack(layers)
     gptr = _ptr_array(gathered)
+    cptr = None if gathered_codes is None else _ptr_array(gathered_codes)
+    sptr = None if gathered_scales is None else _ptr_array(gathered_scales)
     gs = None if gather_stream is None else _stream(gather_stream)
     _check(_lib.zero_step_layers(ctypes.byref(hp), len(stack), stack.array, micro_batches, gathers, len(gptr), gptr,
-                                 _addr(scalars), _addr(ws), _stream(stream), gs), "zero_step_layers")
+                                 cptr, sptr, _addr(scalars), _addr(ws), _stream(stream), gs), "zero_step_layers")
 
 
 def zero_launch_count():

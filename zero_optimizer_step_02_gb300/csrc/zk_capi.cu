@@ -968,6 +968,7 @@ ZERO_API size_t zero_layers_workspace_bytes(const zero_hparams* hp, int n_layers
 
 ZERO_API zero_status zero_step_layers(const zero_hparams* hp, int n_layers, const zero_layer* layers,
                                       int micro_batches, int gathers, int n_gathered, void* const* gathered,
+                                      signed char* const* gathered_codes, float* const* gathered_scales,
                                       zero_dev_scalars* sc, void* ws, void* stream, void* gather_stream)
 {
     ZK_CALL_RANGE();
@@ -979,6 +980,15 @@ ZERO_API zero_status zero_step_layers(const zero_hparams* hp, int n_layers, cons
     if (gathered == nullptr || n_gathered < 1 || n_gathered > n_layers) return ZERO_ERR_INVALID_ARG;
     for (int k = 0; k < n_gathered; ++k)
         if ((s = check_dev(gathered[k])) != ZERO_OK) return s;
+    // quantized gathers (ZeRO++ qwZ): codes and scales for every gathered buffer, or none
+    const bool qwz = gathered_codes != nullptr;
+    if (qwz != (gathered_scales != nullptr)) return ZERO_ERR_INVALID_ARG;
+    if (qwz) {
+        for (int k = 0; k < n_gathered; ++k) {
+            if ((s = check_dev(gathered_codes[k])) != ZERO_OK) return s;
+            if ((s = check_dev(gathered_scales[k])) != ZERO_OK) return s;
+        }
+    }
     if ((s = check_dev(sc, 256)) != ZERO_OK) return s;
     const bool clip = hp->max_norm > 0.0f;
     const bool ls = hp->loss_scaling != 0;
@@ -990,6 +1000,7 @@ ZERO_API zero_status zero_step_layers(const zero_hparams* hp, int n_layers, cons
         if (p == nullptr || p->stage != 3) return ZERO_ERR_INVALID_ARG;
         if (p->n_d != p0->n_d || p->grad_dtype != p0->grad_dtype || p->param_dtype != p0->param_dtype)
             return ZERO_ERR_INVALID_ARG;
+        if (qwz && p->param_dtype != ZERO_BF16) return ZERO_ERR_UNSUPPORTED;
         if ((s = check_ranks(p, L.rank_grads)) != ZERO_OK) return s;
         if ((s = check_state(p, L.master, L.m, L.v, L.master, L.m, L.v)) != ZERO_OK) return s;
         if ((s = check_dev(L.shards_lp)) != ZERO_OK) return s;
@@ -1053,8 +1064,14 @@ ZERO_API zero_status zero_step_layers(const zero_hparams* hp, int n_layers, cons
         const size_t eb = 2;   // 16-bit parameters
         for (int r = 0; r < n_d; ++r)
             shard_ptr[r] = static_cast<const unsigned char*>(L.shards_lp) + eb * static_cast<size_t>(r) * p->shard;
-        for (int g = 0; g < gathers; ++g)
-            ZK_TRY(zk::launch_all_gather(shard_ptr, n_d, p->shard, p->psi, gathered[l % n_gathered], sc, gs));
+        const int k = l % n_gathered;
+        for (int g = 0; g < gathers; ++g) {
+            if (qwz)
+                ZK_TRY(zk::launch_quant_gather(L.shards_lp, n_d, p->shard, p->psi, zk::kQuantBlock,
+                                               gathered_codes[k], gathered_scales[k], gathered[k], gs));
+            else
+                ZK_TRY(zk::launch_all_gather(shard_ptr, n_d, p->shard, p->psi, gathered[k], sc, gs));
+        }
         if (two) ZK_TRY(cudaEventRecord(ev.ev[1 + l], gs));
         return ZERO_OK;
     };
