@@ -181,7 +181,43 @@ def test_llama_layer_zero3_full_size():
     assert job.buf.scalars_host().status == 0
 
 
-@pytest.mark.parametrize("n_d", [2, 64])
+def test_llama_8_layers_zero3_layer_loop_full_size():
+    # the default bench workload in its launch configuration: 8 Llama-3-8B-
+    # shaped layers (Psi_l = 218,112,000), N_d = 16, one zero_step_layers call
+    # per step with the gathers on a second stream and two gathered buffers;
+    # every layer's sampled elements against the oracle, the gathered values
+    # of the last two layers against the shards the step started from
+    psi, n_d, L = 218_112_000, 16, 8
+    if _free_gb() < 100:
+        pytest.skip("needs ~90 GB of free device memory")
+    hp = z.hparams(lr=1e-3)
+    jobs = [FullJob(psi, n_d, 3, z.ZERO_BF16, hp, seed=440 + l) for l in range(L)]
+    scalars = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    z.zero_scalars_init(scalars)
+    stack = z.LayerStack([(j.plan.handle, j.buf.rank_ptrs(), j.buf.master, j.buf.m, j.buf.v, j.buf.lp) for j in jobs])
+    gathered = [torch.zeros(psi, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    idx = _sample(psi, 9)
+    ii = torch.from_numpy(idx).cuda()
+    for step in (1, 2):
+        taken, before = [], []
+        for j in jobs:
+            j.fill_grads(step, 1e-3)
+            taken.append(j.take(idx))
+            before.append(j.buf.lp[ii].clone())
+        z.zero_step_layers(hp, stack, 1, gathered, scalars, gather_stream=torch.cuda.Stream())
+        torch.cuda.synchronize()
+        assert z.read_scalars(scalars).t == step
+        for l, j in enumerate(jobs):
+            rows, st = taken[l]
+            j.check(idx, j.oracle_sampled(rows, st, float(n_d)))
+        # layers 6 and 7 were the last gathered into buffers 0 and 1: the
+        # shards as the step found them
+        for l in (L - 2, L - 1):
+            assert torch.equal(gathered[l % 2][ii].view(torch.int16), before[l].view(torch.int16))
+    assert z.read_scalars(scalars).status == 0
+
+
+@pytest.mark.parametrize("n_d", [2, 4, 8, 16, 64])
 def test_psi_2_28_full_size(n_d):
     psi = 1 << 28
     if _free_gb() < 2 * n_d * psi / 1e9 + 20:

@@ -1027,12 +1027,13 @@ ZERO_API zero_status zero_step_layers(const zero_hparams* hp, int n_layers, cons
     // the workspace: partial sums of every layer's reduce pass, one after
     // another, then the layers' reduced gradients
     double* partials = partials_of(ws);
-    auto ghat_at = [&](int l) -> float* {
-        size_t off = kPartialBytes * static_cast<size_t>(n_layers);
-        for (int m = 0; m < l; ++m)
-            off += (sizeof(float) * static_cast<size_t>(layers[m].plan->padded) + 255) / 256 * 256;
-        return reinterpret_cast<float*>(static_cast<char*>(ws) + off);
+    // layer l's reduced gradient: walked layer by layer in both loops below
+    // (each region 256-byte aligned), so no layer is looked up by a search
+    const size_t ghat_base = kPartialBytes * static_cast<size_t>(n_layers);
+    auto ghat_size = [&](int l) {
+        return (sizeof(float) * static_cast<size_t>(layers[l].plan->padded) + 255) / 256 * 256;
     };
+    auto ghat_ptr = [&](size_t off) { return reinterpret_cast<float*>(static_cast<char*>(ws) + ghat_base + off); };
 
     // The global checks span every layer: with clipping or loss scaling a
     // reduce pass over each layer first (norm partials, the non-finite flag;
@@ -1041,14 +1042,16 @@ ZERO_API zero_status zero_step_layers(const zero_hparams* hp, int n_layers, cons
     // skipped together when a value was not finite).
     if (clip || ls) {
         int n_part = 0;
+        size_t g_off = 0;
         for (int l = 0; l < n_layers; ++l) {
             const zero_layer& L = layers[l];
             if (L.grads_ready != nullptr) ZK_TRY(cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(L.grads_ready), 0));
             int grid = 0;
-            if ((s = run_reduce(L.plan, hp, L.rank_grads, materialise ? ghat_at(l) : nullptr, clip,
+            if ((s = run_reduce(L.plan, hp, L.rank_grads, materialise ? ghat_ptr(g_off) : nullptr, clip,
                                 partials + n_part, sc, st, &grid, acc_of(L))) != ZERO_OK)
                 return s;
             if (clip) n_part += grid;
+            g_off += ghat_size(l);
         }
         if (clip) ZK_TRY(zk::launch_finalize_sqnorm(partials, n_part, *hp, sc, st));
     }
@@ -1082,6 +1085,7 @@ ZERO_API zero_status zero_step_layers(const zero_hparams* hp, int n_layers, cons
     }
     if ((s = gather(0)) != ZERO_OK) return s;
     const int flags = (clip ? zk::F_CLIP : 0) | (ls ? (zk::F_GUARD | zk::F_LSCALE) : 0);
+    size_t g_off = 0;
     for (int l = 0; l < n_layers; ++l) {
         // the next layer's gather is issued before this layer's step, so that
         // with two streams it runs while the step does
@@ -1092,8 +1096,10 @@ ZERO_API zero_status zero_step_layers(const zero_hparams* hp, int n_layers, cons
             ZK_TRY(cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(L.grads_ready), 0));
         // no scalar commit per layer: every layer's Adam takes this step's t
         const bool host = L.state_on_host != 0;
+        float* ghat = ghat_ptr(g_off);
+        g_off += ghat_size(l);
         if (materialise)
-            s = run_adam(L.plan, hp, ghat_at(l), L.master, L.m, L.v, L.master, L.m, L.v, L.shards_lp,
+            s = run_adam(L.plan, hp, ghat, L.master, L.m, L.v, L.master, L.m, L.v, L.shards_lp,
                          flags & ~zk::F_LSCALE, sc, st, nullptr, 0, host);
         else
             s = run_fused(L.plan, hp, L.rank_grads, L.master, L.m, L.v, L.master, L.m, L.v, L.shards_lp, flags, sc,
