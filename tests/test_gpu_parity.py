@@ -40,6 +40,28 @@ def test_fused_step_bit_exact(n_d, psi, pad, stage):
     assert job.scalars().t == 3
 
 
+def _small_limit():
+    # a plain step below two 4096-element tiles per SM takes the small-problem
+    # kernel (one thread per 4 elements, no staging); at and above, the engine
+    return 2 * torch.cuda.get_device_properties(0).multi_processor_count * 4096
+
+
+@pytest.mark.parametrize("offset", [-3, -1, 0, 1])
+@pytest.mark.parametrize("gdt,pdt,stage", [(z.ZERO_BF16, z.ZERO_BF16, 2), (z.ZERO_FP16, z.ZERO_FP16, 3),
+                                           (z.ZERO_FP16, z.ZERO_BF16, 1)])
+def test_fused_step_either_side_of_the_small_problem_limit(offset, gdt, pdt, stage):
+    # the small-problem kernel and the engine give the oracle's bits alike,
+    # with a ragged tail on either side of the limit
+    psi = _small_limit() + offset
+    job = Job(psi, 3, stage=stage, pad=1, gdt=gdt, pdt=pdt, hp=z.hparams(lr=1e-3, weight_decay=0.1), seed=7)
+    for step in range(1, 3):
+        job.new_grads(step, sigma=1e-2)
+        job.gpu_step()
+        job.oracle_step()
+        job.assert_bit_exact()
+    assert job.scalars().t == 2
+
+
 @pytest.mark.parametrize("gdt,pdt", [(z.ZERO_FP16, z.ZERO_BF16), (z.ZERO_FP16, z.ZERO_FP16),
                                      (z.ZERO_BF16, z.ZERO_FP16)])
 def test_fused_step_dtypes(gdt, pdt):

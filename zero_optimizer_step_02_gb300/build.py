@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libzero.so")
 BUILD = os.path.join(PKG, "_build")
 
-SOURCES = ["zk_stream.cu", "zk_aux.cu", "zk_capi.cu", "zk_noalloc.cu"]
+SOURCES = ["zk_stream.cu", "zk_aux.cu", "zk_capi.cu", "zk_noalloc.cu", "zk_small.cu"]
 HEADERS = ["zk_common.cuh", "zk_launch.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -187,6 +187,28 @@ zero_status run_fused(const zero_plan* p, const zero_hparams* hp, const void* co
         (flags & (zk::F_CLIP | zk::F_GUARD | zk::F_DETECT | zk::F_FINALIZE)) ? p->psi : p->bucket;
     for (long long lo = 0; lo < p->psi; lo += step) {
         const long long hi = lo + step < p->psi ? lo + step : p->psi;
+        // a plain step too small to fill the engine's pipeline: the small-problem kernel
+        if ((flags & ~zk::F_EPILOGUE) == 0 && !host_state && acc.carry == nullptr && zk::small_step_fits(hi - lo)) {
+            zk::SmallArgs b;
+            std::memset(&b, 0, sizeof(b));
+            for (int r = 0; r < p->n_d; ++r) b.rank[r] = ranks[r];
+            b.master_in = mi;
+            b.m_in = m_in;
+            b.v_in = vi;
+            b.master_out = mo;
+            b.m_out = m_out;
+            b.v_out = vo;
+            b.lp_out = lp;
+            b.sc = sc;
+            b.lo = lo;
+            b.hi = hi;
+            b.n_ranks = p->n_d;
+            b.epilogue = (hi == p->psi && (flags & zk::F_EPILOGUE)) ? 1 : 0;
+            b.hp = *hp;
+            const zero_status s = from_cuda(zk::launch_small_step(p->grad_dtype, p->param_dtype, b, st));
+            if (s != ZERO_OK) return s;
+            continue;
+        }
         StreamArgs a = base_args(hp, sc);
         if (flags & zk::F_FINALIZE) set_finalize(a, fin_ws, fin_n);
         set_ranks(a, p, ranks);

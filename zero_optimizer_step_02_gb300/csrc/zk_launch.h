@@ -59,6 +59,28 @@ struct StreamArgs {
 
 cudaError_t launch_stream(int op, int grad_dtype, int param_dtype, StreamArgs& a, cudaStream_t st);
 
+// Arguments of the small-problem fused step (zk_small.cu): the plain fused
+// step over [lo, hi) (lo a multiple of 4), state in device memory.
+struct SmallArgs {
+    const void* rank[ZERO_MAX_RANKS];  // 16-bit gradient buffers, rank order
+    const float* master_in;
+    const float* m_in;
+    const float* v_in;
+    float* master_out;
+    float* m_out;
+    float* v_out;
+    void* lp_out;                      // 16-bit parameters out (null: none)
+    zero_dev_scalars* sc;
+    long long lo, hi;
+    int n_ranks;
+    int epilogue;                      // the last CTA commits the step scalars
+    zero_hparams hp;
+};
+
+// true when n elements would give the streaming engine under two tiles per SM
+bool small_step_fits(long long n);
+cudaError_t launch_small_step(int grad_dtype, int param_dtype, const SmallArgs& a, cudaStream_t st);
+
 // every kernel launch of the library adds one (zero_launch_count)
 void count_launch();
 unsigned long long launch_count();
