@@ -279,16 +279,11 @@ NOMINAL_HBM_GBS = 8000.0
 # kernel and workload, with a hash of the kernel sources they were taken on;
 # reported as null once the sources change.
 TRAFFIC = {
-    # Psi_l = 2^24 case of the same workload, 738.30 MB read + 201.61 MB written
-    # per launch; reads scaled by 218,112,000 / 2^24, writes the algorithmic
-    # 14 B/param less the 33 MB still in L2 at the kernel's end
-    ("fused_step", "zero3_llama3_8b_8layers_psil218112000_nd16"): {"bytes": 12.619e9, "src": "3f15f35e2a21"},
-    ("adam_shard", "zero2_gpt2small_psi124439808_nd8_adamw_clip1"): {"bytes": 3.623e9, "src": "e92f70f96686"},
-    ("fused_step", "zero2_psi2p28_nd8"): {"bytes": 11.106e9, "src": "e92f70f96686"},
-    ("fused_step_qgather", "zero2_psi2p28_nd2_qgather"): {"bytes": 8.081e9, "src": "e92f70f96686"},
-    ("fused_step_qgz", "zero2_psi2p28_nd8_qgz"): {"bytes": 8.917e9, "src": "e92f70f96686"},
-    ("accumulate_grads", "zero2_gpt2small_psi124439808_nd8_adamw_clip1_accum4"): {"bytes": 2.952e9,
-                                                                                   "src": "e92f70f96686"},
+    # one-pass full-size captures (dram__bytes_read.sum + dram__bytes_write.sum):
+    # the per-layer fused step of the 8-layer workload, 9.597 GB read + 3.019 GB
+    # written; the GPT-2-small clipped step's Adam pass, 1.991 + 1.680 GB
+    ("fused_step", "zero3_llama3_8b_8layers_psil218112000_nd16"): {"bytes": 12.616e9, "src": "bdf7aeb6ad4d"},
+    ("adam_shard", "zero2_gpt2small_psi124439808_nd8_adamw_clip1"): {"bytes": 3.671e9, "src": "bdf7aeb6ad4d"},
 }
 
 
