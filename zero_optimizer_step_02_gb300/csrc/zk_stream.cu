@@ -321,10 +321,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
         // constants in registers: a reference into shared memory would be
         // re-read for every element (the stores in the loop may alias it)
         const StepConsts c = sh->c;
-        const bool detect = (a.flags & F_DETECT) != 0;   // recorded only under loss scaling
-        const bool want_sq = (a.flags & F_SQNORM) != 0;
-        const bool carry = (a.flags & F_CARRY) != 0;
-        const bool raw = (a.flags & F_RAW) != 0;
+        // the reduce pass over int8 codes (the clipped quantized exchange) has
+        // no side stream, carry or raw sum, no non-finite test, and always sums
+        // squares: its flags are constants, and the tests of the other
+        // passes' flags drop out of its loop
+        constexpr bool kCodesReduce = OP == OP_REDUCE && GT == kGradQ8;
+        constexpr int kSides = kCodesReduce ? 0 : kMaxSide;   // side streams this pass can have
+        const bool detect = !kCodesReduce && (a.flags & F_DETECT) != 0;   // recorded only under loss scaling
+        const bool want_sq = kCodesReduce || (a.flags & F_SQNORM) != 0;
+        const bool carry = !kCodesReduce && (a.flags & F_CARRY) != 0;
+        const bool raw = !kCodesReduce && (a.flags & F_RAW) != 0;
         constexpr int kCarry = (OP == OP_REDUCE) ? 0 : 3;   // side slot of the carry stream
         TileCursor cur;
         for (cur.start(a); cur.valid(a); cur.next(a)) {
@@ -349,13 +355,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
                 for (int e = 0; e < 4; ++e) {
                     acc[ch][e] = 0.0f;
 #pragma unroll
-                    for (int k = 0; k < kMaxSide; ++k) sv[ch][k][e] = 0.0f;
+                    for (int k = 0; k < kSides; ++k) sv[ch][k][e] = 0.0f;
                 }
 
             if (fast) {
                 // side streams not staged (state in host memory): 16-byte loads issued
                 // now, before the wait for the gradient stage, so their latency overlaps it
-                if (a.n_side_tma < a.n_side && alive) {
+                if (kSides > 0 && a.n_side_tma < a.n_side && alive) {
 #pragma unroll
                     for (int ch = 0; ch < kChunksPerThread; ++ch) {
                         const long long jc = j0 + chunk_of<kHalves>(ch, tid) * 4;
@@ -450,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
                             for (int ch = 0; ch < kChunksPerThread; ++ch) {
                                 const int q = chunk_of<kHalves>(ch, tid);
 #pragma unroll
-                                for (int k = 0; k < kMaxSide; ++k) {
+                                for (int k = 0; k < kSides; ++k) {
                                     if (k < a.n_side_tma) {
                                         const float4 f = reinterpret_cast<const float4*>(
                                             st + side_off + k * kTile * 4)[q];
@@ -490,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ 
                                 }
                             }
 #pragma unroll
-                            for (int k = 0; k < kMaxSide; ++k)
+                            for (int k = 0; k < kSides; ++k)
                                 if (k < a.n_side) sv[ch][k][e] = a.side[k][j];
                         }
                     }
