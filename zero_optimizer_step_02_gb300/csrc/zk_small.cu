@@ -24,6 +24,9 @@ namespace zk {
 namespace {
 
 constexpr int kSmallThreads = 256;
+// gradient words of this many ranks are loaded before the first is added, so
+// their DRAM latencies overlap instead of following one another
+constexpr int kRankGroup = 4;
 
 // the four 16-bit values of an 8-byte word added to acc, one rounding each
 template <int GT>
@@ -36,26 +39,36 @@ __device__ __forceinline__ void add4(float (&acc)[4], uint2 w)
     for (int e = 0; e < 4; ++e) acc[e] = Lp<GT>::add(acc[e], h[e]);
 }
 
+// one rank's 16-bit gradients of elements [j, j + cnt) as an 8-byte word
+// (zeros past cnt; those lanes are never stored)
+__device__ __forceinline__ uint2 load_grads(const void* rank, long long j, int cnt)
+{
+    const uint16_t* g = static_cast<const uint16_t*>(rank) + j;
+    if (cnt == 4) return *reinterpret_cast<const uint2*>(g);
+    uint32_t h[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+        if (e < cnt) h[e] = g[e];
+    return make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+}
+
+// at most 48 registers with one chunk (5 CTAs per SM), 64 with two (4 CTAs:
+// the largest problem given to this kernel, 2 x 152 x 4096 elements, then
+// fits on the GPU at once)
 template <int GT, int PT, int kChunks>
-__global__ void __launch_bounds__(kSmallThreads) k_small_step(const __grid_constant__ SmallArgs a)
+__global__ void __launch_bounds__(kSmallThreads, kChunks == 1 ? 5 : 4) k_small_step(const __grid_constant__ SmallArgs a)
 {
     __shared__ StepConsts shc;
     zero_dev_scalars* sc = a.sc;
-    if (threadIdx.x == 0) {
-        StepConsts c = {};
-        set_divisor(c, a.n_ranks, 1.0f);
-        set_adam(c, a.hp, sc->beta1_pow, sc->beta2_pow);
-        c.clip = 0;
-        c.coef = 1.0f;
-        shc = c;
-    }
-    __syncthreads();
-    const StepConsts c = shc;
-    // chunk k of this thread: elements [4 (t0 + k * nth), + 4); every chunk's
-    // loads are issued before any chunk is computed
+    // chunk k of this thread: elements [4 (t0 + k * nth), + 4).  Every chunk's
+    // master/m/v and its first kRankGroup ranks' gradients are loaded first;
+    // thread 0 reads the step scalars and forms the constants while they are
+    // in flight
     const long long nth = static_cast<long long>(gridDim.x) * kSmallThreads;
     const long long t0 = static_cast<long long>(blockIdx.x) * kSmallThreads + threadIdx.x;
+    const int g0 = a.n_ranks < kRankGroup ? a.n_ranks : kRankGroup;
     float acc[kChunks][4], p[kChunks][4], m[kChunks][4], v[kChunks][4];
+    uint2 w[kChunks][kRankGroup];
     int cnt[kChunks];
     long long jj[kChunks];
 #pragma unroll
@@ -65,9 +78,12 @@ __global__ void __launch_bounds__(kSmallThreads) k_small_step(const __grid_const
         cnt[k] = j >= a.hi ? 0 : (a.hi - j >= 4 ? 4 : static_cast<int>(a.hi - j));
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[k][e] = p[k][e] = m[k][e] = v[k][e] = 0.0f;
+#pragma unroll
+        for (int r = 0; r < kRankGroup; ++r) {
+            w[k][r] = make_uint2(0u, 0u);
+            if (r < g0 && cnt[k] > 0) w[k][r] = load_grads(a.rank[r], j, cnt[k]);
+        }
         if (cnt[k] == 4) {
-            for (int r = 0; r < a.n_ranks; ++r)
-                add4<GT>(acc[k], *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(a.rank[r]) + j));
             const float4 fp = *reinterpret_cast<const float4*>(a.master_in + j);
             const float4 fm = *reinterpret_cast<const float4*>(a.m_in + j);
             const float4 fv = *reinterpret_cast<const float4*>(a.v_in + j);
@@ -78,14 +94,42 @@ __global__ void __launch_bounds__(kSmallThreads) k_small_step(const __grid_const
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 if (e < cnt[k]) {
-                    for (int r = 0; r < a.n_ranks; ++r)
-                        acc[k][e] = Lp<GT>::add(acc[k][e], static_cast<const uint16_t*>(a.rank[r])[j + e]);
                     p[k][e] = a.master_in[j + e];
                     m[k][e] = a.m_in[j + e];
                     v[k][e] = a.v_in[j + e];
                 }
             }
         }
+    }
+    if (threadIdx.x == 0) {
+        StepConsts c = {};
+        set_divisor(c, a.n_ranks, 1.0f);
+        set_adam(c, a.hp, sc->beta1_pow, sc->beta2_pow);
+        c.clip = 0;
+        c.coef = 1.0f;
+        shc = c;
+    }
+    __syncthreads();
+    const StepConsts c = shc;
+    // the rank-ordered sums from +0: the loaded group, then any further
+    // groups, each loaded whole before it is added
+#pragma unroll
+    for (int k = 0; k < kChunks; ++k)
+#pragma unroll
+        for (int r = 0; r < kRankGroup; ++r)
+            if (r < g0) add4<GT>(acc[k], w[k][r]);
+    for (int r0 = kRankGroup; r0 < a.n_ranks; r0 += kRankGroup) {
+        const int gn = a.n_ranks - r0 < kRankGroup ? a.n_ranks - r0 : kRankGroup;
+#pragma unroll
+        for (int k = 0; k < kChunks; ++k)
+#pragma unroll
+            for (int r = 0; r < kRankGroup; ++r)
+                if (r < gn && cnt[k] > 0) w[k][r] = load_grads(a.rank[r0 + r], jj[k], cnt[k]);
+#pragma unroll
+        for (int k = 0; k < kChunks; ++k)
+#pragma unroll
+            for (int r = 0; r < kRankGroup; ++r)
+                if (r < gn) add4<GT>(acc[k], w[k][r]);
     }
 #pragma unroll
     for (int k = 0; k < kChunks; ++k) {
@@ -102,10 +146,10 @@ __global__ void __launch_bounds__(kSmallThreads) k_small_step(const __grid_const
             *reinterpret_cast<float4*>(a.m_out + j) = make_float4(m[k][0], m[k][1], m[k][2], m[k][3]);
             *reinterpret_cast<float4*>(a.v_out + j) = make_float4(v[k][0], v[k][1], v[k][2], v[k][3]);
             if (a.lp_out != nullptr) {
-                uint2 w;
-                w.x = static_cast<uint32_t>(lp[0]) | (static_cast<uint32_t>(lp[1]) << 16);
-                w.y = static_cast<uint32_t>(lp[2]) | (static_cast<uint32_t>(lp[3]) << 16);
-                *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.lp_out) + j) = w;
+                uint2 o;
+                o.x = static_cast<uint32_t>(lp[0]) | (static_cast<uint32_t>(lp[1]) << 16);
+                o.y = static_cast<uint32_t>(lp[2]) | (static_cast<uint32_t>(lp[3]) << 16);
+                *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.lp_out) + j) = o;
             }
         } else {
 #pragma unroll
@@ -144,8 +188,8 @@ bool small_step_fits(long long n)
 
 // One 4-element chunk per thread when the step's threads fit on the GPU at
 // once; else two per thread, so that they do again (the 1M-parameter step:
-// 14.5 instead of 15.3 us with L2 flushed; 600k parameters keep one chunk,
-// 11.3 against 13.1 us with two).
+// 13.6 instead of 15.3 us with L2 flushed; 600k parameters keep one chunk,
+// 11.4 against 13.1 us with two).
 template <int GT, int PT>
 cudaError_t launch_small_typed(const SmallArgs& a, long long chunks, cudaStream_t st)
 {
