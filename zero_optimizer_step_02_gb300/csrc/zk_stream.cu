@@ -200,10 +200,19 @@ __device__ __forceinline__ void add_slice(float (&acc)[4], uint2 w)
 template <int GT>
 __host__ __device__ constexpr int group_ranks() { return GT == kGradQ8 ? 2 * kGroupRanks : kGroupRanks; }
 
+// CTAs of one launch resident per SM.  The reduce pass over int8 codes is
+// bound by instruction issue, not by DRAM: two CTAs per SM (56 registers a
+// thread, which it needs no more than) give each scheduler twice the warps
+// to pick from, and took the clipped GPT-2-small qgZ step from 0.838 to
+// 0.806 ms.  Every other pass needs its 96 registers (at 56 they spill).
+template <int GT, int OP>
+__host__ __device__ constexpr int ctas_per_sm() { return (OP == OP_REDUCE && GT == kGradQ8) ? 2 : 1; }
+
 // 17 warps spread over an SM's 4 sub-partitions put 5 on one of them, whose
-// 16K registers then allow 96 per thread: the bound ptxas works to here.
+// 16K registers then allow 96 per thread: the bound ptxas works to here (with
+// one CTA per SM).
 template <int GT, int PT, int OP, int FULL>
-__global__ void __launch_bounds__(kThreads, 1) k_stream(const __grid_constant__ StreamArgs a)
+__global__ void __launch_bounds__(kThreads, ctas_per_sm<GT, OP>()) k_stream(const __grid_constant__ StreamArgs a)
 {
     constexpr int kG = group_ranks<GT>();
     extern __shared__ __align__(1024) unsigned char smem[];
@@ -804,6 +813,8 @@ namespace {
 struct DevInfo {
     int sms = 0;
     int smem_optin = 0;
+    int smem_per_sm = 0;
+    int smem_reserved = 0;   // per CTA, by the runtime
 };
 
 DevInfo device_info(int dev)
@@ -815,6 +826,8 @@ DevInfo device_info(int dev)
         DevInfo d;
         cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
         cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+        cudaDeviceGetAttribute(&d.smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
         cache[dev] = d;
         __atomic_store_n(&ready[dev], 1, __ATOMIC_RELEASE);
     }
@@ -849,7 +862,12 @@ cudaError_t launch_one_k(StreamArgs& a, cudaStream_t st)
         __atomic_store_n(&attr_done[dev], 1, __ATOMIC_RELEASE);
     }
     const long long ntiles = a.tiles_per_seg * a.n_seg;
-    long long grid = ntiles < di.sms ? ntiles : di.sms;
+    // two CTAs per SM where the kernel is built for it and both rings fit in
+    // the SM's shared memory (int8 codes up to 12 ranks); else one
+    long long per_sm = ctas_per_sm<GT, OP>();
+    if (per_sm > 1 && per_sm * (static_cast<long long>(smem) + di.smem_reserved) > di.smem_per_sm) per_sm = 1;
+    const long long resident = per_sm * di.sms;
+    long long grid = ntiles < resident ? ntiles : resident;
     // The Adam pass and the 16-bit fused step with one rank group and its state
     // staged ran 3-8% faster on 27/32 of the SMs (128 of 152) than on all of
     // them (measured from 100 to 152 CTAs: a step between 140 and 132); fewer
