@@ -282,9 +282,9 @@ TRAFFIC = {
     # one-pass full-size captures (dram__bytes_read.sum + dram__bytes_write.sum):
     # the per-layer fused step of the 8-layer workload, 9.597 GB read + 3.020 GB
     # written (two launches' mean); the GPT-2-small clipped step's Adam pass,
-    # 1.991 + 1.679 GB
-    ("fused_step", "zero3_llama3_8b_8layers_psil218112000_nd16"): {"bytes": 12.617e9, "src": "f148dacfd885"},
-    ("adam_shard", "zero2_gpt2small_psi124439808_nd8_adamw_clip1"): {"bytes": 3.671e9, "src": "f148dacfd885"},
+    # 1.991 + 1.680 GB
+    ("fused_step", "zero3_llama3_8b_8layers_psil218112000_nd16"): {"bytes": 12.617e9, "src": "ec5007d3abf1"},
+    ("adam_shard", "zero2_gpt2small_psi124439808_nd8_adamw_clip1"): {"bytes": 3.672e9, "src": "ec5007d3abf1"},
 }
 
 
