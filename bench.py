@@ -32,6 +32,7 @@ ranks is taken.  --impl reference times the CPU oracle instead.
 """
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -283,25 +284,33 @@ TRAFFIC = {
     # the per-layer fused step of the 8-layer workload, 9.597 GB read + 3.020 GB
     # written (two launches' mean); the GPT-2-small clipped step's Adam pass,
     # 1.991 + 1.680 GB
-    ("fused_step", "zero3_llama3_8b_8layers_psil218112000_nd16"): {"bytes": 12.617e9, "src": "ec5007d3abf1"},
-    ("adam_shard", "zero2_gpt2small_psi124439808_nd8_adamw_clip1"): {"bytes": 3.672e9, "src": "ec5007d3abf1"},
+    ("fused_step", "zero3_llama3_8b_8layers_psil218112000_nd16"): {"bytes": 12.617e9, "src": "77430f78e679"},
+    ("adam_shard", "zero2_gpt2small_psi124439808_nd8_adamw_clip1"): {"bytes": 3.672e9, "src": "77430f78e679"},
 }
+
+
+def _code_only(text):
+    """C++ source without its comments and with its whitespace collapsed (the
+    engine's sources hold no string literal containing a comment marker)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
 
 
 def kernel_source_hash():
     """Hash of the streaming engine's device code and of its argument block
-    (the StreamArgs definition): the kernels whose traffic TRAFFIC records.
-    Host-only changes elsewhere leave those kernels, and their traffic, as
-    they were."""
+    (the StreamArgs definition), comments and layout left out: the kernels
+    whose traffic TRAFFIC records.  Host-only changes elsewhere, and edits
+    of comments, leave those kernels, and their traffic, as they were."""
     h = hashlib.sha1()
     csrc = os.path.join(ROOT, "zero_optimizer_step_02_gb300", "csrc")
     for f in ("zk_stream.cu", "zk_common.cuh"):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(csrc, f)) as fh:
+            h.update(_code_only(fh.read()).encode())
     with open(os.path.join(csrc, "zk_launch.h")) as fh:
         text = fh.read()
     a = text.index("struct StreamArgs {")
-    h.update(text[a:text.index("};", a)].encode())
+    h.update(_code_only(text[a:text.index("};", a)]).encode())
     return h.hexdigest()[:12]
 
 

@@ -126,3 +126,13 @@ def test_fp16_parameter_and_stage_labels():
     assert w["stage"] == 1 and w["pdt"] == "fp16" and w["bytes_per_param"] == 2 * 8 + 26
     assert bench.config_of(w, 1)["param_dtype"] == "fp16"
     assert bench.workload(3)["pdt"] == "bf16"
+
+
+def test_kernel_source_hash_ignores_comments_and_layout():
+    # the traffic table is keyed on the engine's code: a comment or a
+    # re-indented line leaves the key as it was, a changed token does not
+    code = "int a = 1; // one\n/* two\n three */  float b  =\n 2.0f;"
+    assert bench._code_only(code) == "int a = 1; float b = 2.0f;"
+    assert bench._code_only(code.replace("// one", "// uno")) == bench._code_only(code)
+    assert bench._code_only(code.replace("2.0f", "3.0f")) != bench._code_only(code)
+    assert len(bench.kernel_source_hash()) == 12

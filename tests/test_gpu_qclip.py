@@ -82,8 +82,11 @@ def test_quantized_gather_overflow_skip(max_norm):
         q.assert_outputs()
 
 
+# 13 and 14 ranks: either side of the largest rank count whose reduce pass
+# over the codes runs two CTAs per SM (both rings in 228 KB of shared
+# memory), with more tiles than two CTAs on every SM take at once
 @pytest.mark.parametrize("n_d,psi,pad", [(2, 300_001, 16), (8, 400_003, 16), (17, 70_001, 1), (4, 5_000, 16),
-                                         (8, 7, 16), (3, 1, 1)])
+                                         (8, 7, 16), (3, 1, 1), (13, 2_500_001, 16), (14, 2_500_001, 16)])
 @pytest.mark.parametrize("stage", [2, 3])
 def test_quantized_exchange_with_clipping(n_d, psi, pad, stage):
     # n_d <= 4: reduce pass over the codes, then the fused step re-reads them;

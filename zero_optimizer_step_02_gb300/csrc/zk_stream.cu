@@ -863,7 +863,8 @@ cudaError_t launch_one_k(StreamArgs& a, cudaStream_t st)
     }
     const long long ntiles = a.tiles_per_seg * a.n_seg;
     // two CTAs per SM where the kernel is built for it and both rings fit in
-    // the SM's shared memory (int8 codes up to 12 ranks); else one
+    // the SM's shared memory (int8 codes of up to 13 ranks with 228 KB per
+    // SM); else one
     long long per_sm = ctas_per_sm<GT, OP>();
     if (per_sm > 1 && per_sm * (static_cast<long long>(smem) + di.smem_reserved) > di.smem_per_sm) per_sm = 1;
     const long long resident = per_sm * di.sms;
