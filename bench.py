@@ -83,11 +83,18 @@ def workload(cfg, nd=None, qgather=False, psi=None, qgz=False, gathers=1, offloa
                  tail=False, lr=1e-3, b2=0.999, wd=0.0, clip=0.0, ls=False, layers=1)
     else:
         raise SystemExit("unknown config %r" % cfg)
-    if qgather or qgz:
+    if qgather and not qgz and w["stage"] == 3:
+        # the ZeRO-3 layer loop with block-int8 quantized gathers (qwZ): each
+        # layer's gather writes int8 codes, block scales and the dequantized
+        # bf16 values instead of the bf16 shards
+        w["qgather"] = True
+        w["name"] += "_qgather"
+    elif qgather or qgz:
         # the ZeRO++ variants of the bf16 ZeRO-2 workloads: the int8 gather
         # epilogue, int8 codes + block scales as the ranks' gradients, or both
         if w["stage"] == 3 or w["gdt"] != "bf16":
-            raise SystemExit("--qgather and --qgz apply to the bf16 ZeRO-2 workloads (configs 1, 2, 5)")
+            raise SystemExit("--qgather applies to the bf16 workloads (configs 1, 2, 4, 5), --qgz to the bf16 "
+                             "ZeRO-2 ones (configs 1, 2, 5)")
         w["qgather"], w["qgz"] = qgather, qgz
         w["name"] += ("_qgz" if qgz else "") + ("_qgather" if qgather else "")
         if qgz:
@@ -154,6 +161,11 @@ def workload(cfg, nd=None, qgather=False, psi=None, qgz=False, gathers=1, offloa
             w["bytes_per_param"] = q + 34 if n_d > 4 else 2 * q + 26
         else:
             w["bytes_per_param"] = q + 26
+    elif w["stage"] == 3:
+        # per gather: the 16-bit shards read and the gathered values written,
+        # or with qwZ the shards read, codes + block scales + dequantized bf16 written
+        per_gather = (5 + 4.0 / 2048) if w.get("qgather") else 4
+        w["bytes_per_param"] = 2 * n_d + 26 + per_gather * w.get("gathers", 1)
     elif w.get("qgather"):
         # clipped: for n_d > 4 the reduce pass writes the fp32 reduced gradient
         # and the Adam pass with the int8 gather reads it; else a read-only
@@ -164,8 +176,6 @@ def workload(cfg, nd=None, qgather=False, psi=None, qgz=False, gathers=1, offloa
             w["bytes_per_param"] = 2 * n_d + 27 + 4.0 / 2048 + (2 * n_d if w["clip"] > 0 else 0)
     elif w["clip"] > 0:
         w["bytes_per_param"] = 2 * n_d + 34 if n_d > 4 else 4 * n_d + 26
-    elif w["stage"] == 3:
-        w["bytes_per_param"] = 2 * n_d + 26 + 4 * w.get("gathers", 1)
     else:
         w["bytes_per_param"] = 2 * n_d + 26
     w["psi_total"] = w["psi"] * w["layers"]
@@ -364,10 +374,15 @@ class Job:
             self.gather_stream = torch.cuda.Stream(device=device) if w.get("overlap") else None
             self.stack = z.LayerStack([(self.plan.handle, self.ranks(l), self.master[l], self.m[l], self.v[l],
                                         self.lp[l]) for l in range(L)])
+        self.gq_codes_l = self.gq_scales_l = None
         if w.get("qgather"):
             nbs = -(-self.plan.shard // 2048)
             self.gq_codes = torch.zeros(n, dtype=torch.int8, device=device)
             self.gq_scales = torch.zeros(w["n_d"] * nbs, device=device)
+            if w["stage"] == 3:
+                # codes and scales beside each of the two gathered buffers
+                self.gq_codes_l = [self.gq_codes, torch.zeros(n, dtype=torch.int8, device=device)]
+                self.gq_scales_l = [self.gq_scales, torch.zeros(w["n_d"] * nbs, device=device)]
         if w.get("qgz"):
             # the int8 wire format of every gradient set (sender pass, untimed here)
             nbs = -(-self.plan.shard // 2048)
@@ -415,7 +430,8 @@ class Job:
             # one call for the stack: per layer its gather(s), then its fused
             # step (reduce-scatter of its ranks' gradients, Adam, 16-bit shards)
             z.zero_step_layers(self.hp, self.stack, w.get("gathers", 1), self.gathered, self.scalars,
-                               gather_stream=self.gather_stream)
+                               gather_stream=self.gather_stream, gathered_codes=self.gq_codes_l,
+                               gathered_scales=self.gq_scales_l)
             self.k += 1
             return
         for l in range(w["layers"]):
@@ -826,7 +842,8 @@ def e2e_layers(job, w, args, world):
                 job.grads[l].copy_(host_in[l % len(host_in)], non_blocking=True)
             ready[l].record(copy_s)
         z.zero_step_layers(job.hp, stack, w.get("gathers", 1), job.gathered, job.scalars,
-                           gather_stream=job.gather_stream)
+                           gather_stream=job.gather_stream, gathered_codes=job.gq_codes_l,
+                           gathered_scales=job.gq_scales_l)
         for l in range(L):
             out_s.wait_event(stepped[l])
             with torch.cuda.stream(out_s):
@@ -883,15 +900,19 @@ def oracle_sample(w, budget_s, max_steps=None):
             else:
                 oracle.zero_step_qgz(codes, scales, 2048, hp, st, w["pad"], min(w["stage"], 3), psi, lp_shards=lp,
                                      gathered=gath)
+        elif w["stage"] == 3:
+            # the ZeRO-3 layer step: the gather(s) of the 16-bit shards (block
+            # int8 with qwZ), then the step
+            for _ in range(w.get("gathers", 1)):
+                if w.get("qgather"):
+                    oracle.quant_gather(lp, n_d, psi, S, 2048)
+                else:
+                    oracle.all_gather_u16([lp[r * S:(r + 1) * S] for r in range(n_d)], psi, S)
+            oracle.zero_step(rows, dt, hp, st, w["pad"], 3, param_dtype=pdt, lp_shards=lp)
         elif w.get("qgather"):
             # the step with its 16-bit output sharded, then the block-int8 gather of the shards
             oracle.zero_step(rows, dt, hp, st, w["pad"], 3, lp_shards=lp, gathered=gath)
             oracle.quant_gather(lp, n_d, psi, S, 2048)
-        elif w["stage"] == 3:
-            # the ZeRO-3 layer step: the all-gather(s) of the 16-bit shards, then the step
-            for _ in range(w.get("gathers", 1)):
-                oracle.all_gather_u16([lp[r * S:(r + 1) * S] for r in range(n_d)], psi, S)
-            oracle.zero_step(rows, dt, hp, st, w["pad"], 3, param_dtype=pdt, lp_shards=lp)
         else:
             oracle.zero_step(rows, dt, hp, st, w["pad"], w["stage"], param_dtype=pdt, lp_shards=lp, gathered=gath)
         steps += 1

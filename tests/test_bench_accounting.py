@@ -39,6 +39,10 @@ def test_zero3_layer(gathers):
     # each gather reads a 16-bit shard and writes the gathered layer
     assert w["bytes_per_param"] == 2 * 16 + 26 + 4 * gathers
     assert w["psi_total"] == 8 * 218_112_000
+    # with block-int8 gathers (qwZ): the shard read, codes + scales + dequantized bf16 written
+    q = bench.workload(4, gathers=gathers, qgather=True)
+    assert q["bytes_per_param"] == 2 * 16 + 26 + (5 + 4.0 / 2048) * gathers
+    assert q["name"].endswith("_qgather") and q["stage"] == 3
 
 
 @pytest.mark.parametrize("k", [2, 4, 8])
@@ -87,7 +91,8 @@ def test_both_quantized_exchanges(cfg, n_d, clip):
 
 
 def test_variants_that_do_not_apply_are_refused():
-    for cfg, kw in ((3, dict(qgz=True)), (4, dict(qgather=True)), (4, dict(qgz=True, qgather=True))):
+    for cfg, kw in ((3, dict(qgz=True)), (4, dict(qgz=True)), (4, dict(qgz=True, qgather=True)),
+                    (4, dict(qgather=True, param_dtype="fp16"))):
         with pytest.raises(SystemExit):
             bench.workload(cfg, **kw)
     with pytest.raises(SystemExit):

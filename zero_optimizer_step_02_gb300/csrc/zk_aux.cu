@@ -4,8 +4,8 @@
 //                    ring of shared-memory stages filled and drained by 1-D
 //                    bulk copies (DP-notes "ZeRO-1": gather the updated
 //                    partitions; itwiki: ZeRO-3 gathers each layer before use)
-//   k_quant_gather   block-int8 quantize + dequantize (itwiki "후속 기법",
-//                    ZeRO++ qwZ), one warp per block
+//   k_quant_gather   block-int8 quantize + dequantize of the bf16 shards
+//                    (itwiki "후속 기법", ZeRO++ qwZ), per-warp bulk-copy slots
 //   k_quantize_ranks every rank's gradient through the block quantizer in one
 //                    launch (ZeRO++ qgZ sender), per-warp bulk-copy slots
 //   k_sqnorm_f32     per-CTA partial sums of g^2 of an fp32 array
@@ -329,100 +329,222 @@ cudaError_t launch_all_gather(const void* const* shards, int n_d, long long shar
     return cudaGetLastError();
 }
 
-// ---------------------------------------------------------- quantized gather
-// One warp per block of `block` elements of a shard.  Pass 1: amax (16-byte
-// loads when aligned).  Pass 2: re-read (the block is hot in L1/L2), quantize,
-// write codes and dequantized bf16.
-__global__ void __launch_bounds__(256) k_quant_gather(const uint16_t* __restrict__ x, int n_d, long long shard,
-                                                      long long psi, int block, long long nbs,
-                                                      signed char* __restrict__ codes, float* __restrict__ scales,
-                                                      uint16_t* __restrict__ gathered)
+// ------------------------------------------------------- quantized gather
+// The qwZ weight gather: the flat bf16 shards through the block quantizer,
+// codes and dequantized bf16 at the global index, scales at [r * nbs + b].
+// The same pipeline as the gradient sender below: one warp per 2048-element
+// block at a time, kQgSlots shared-memory slots per warp that its lane 0
+// fills with 1-D bulk copies kQgSlots blocks ahead, no block-wide barrier.
+// 20 warps (96 registers: the dequantized output needs more than 24 warps
+// leave).  Blocks that are not full, 16-byte aligned 2048-element blocks
+// (ragged shard ends, other block sizes) are read from global memory twice
+// (amax, then codes).  A wait that runs out is reported when a scalars block
+// is given, and the warp then reads that block and every later one from
+// global memory, so the results stay complete either way.
+constexpr int kQgWarps = 20;
+constexpr int kQgSlots = 2;
+constexpr int kQgSlotBytes = kQuantBlock * 2;
+
+struct QgArgs {
+    const uint16_t* shards;
+    signed char* codes;
+    uint16_t* gathered;
+    float* scales;
+    zero_dev_scalars* sc;                 // may be null
+    long long shard, psi, nbs, total;     // total = n_d * nbs blocks
+    int block, ring_ok;                   // ring_ok: block == 2048, shard % 8 == 0, 16-byte aligned buffers
+    unsigned long long timeout_ns;
+};
+
+struct QgBlock {
+    long long bi;    // block index r * nbs + b (its scale's index)
+    long long j0;    // first element (global index)
+    int n;           // valid elements (0: past psi)
+};
+
+__device__ __forceinline__ QgBlock qg_block(const QgArgs& a, long long bi)
 {
+    QgBlock k;
+    k.bi = bi;
+    const long long r = bi / a.nbs;
+    const long long lo = (bi - r * a.nbs) * a.block;
+    long long valid = a.psi - r * a.shard;
+    valid = valid < 0 ? 0 : (valid > a.shard ? a.shard : valid);
+    const long long hi = lo + a.block < valid ? lo + a.block : valid;
+    k.j0 = r * a.shard + lo;
+    k.n = hi > lo ? static_cast<int>(hi - lo) : 0;
+    return k;
+}
+
+// |x| maxima of a slot's 2048 bf16 values on bf16 pairs (a max picks one of
+// its inputs, so it is exact in bf16; a NaN input is passed over as fmaxf
+// does), over the warp: the block's scale amax / 127
+__device__ __forceinline__ float slot_scale(const uint4* src, int lane)
+{
+    __nv_bfloat162 am[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) am[e] = __float2bfloat162_rn(0.0f);
+#pragma unroll
+    for (int v = 0; v < 8; ++v) {
+        const uint4 wv = src[v * 32 + lane];
+        const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) am[e] = __hmax2(am[e], __habs2(*reinterpret_cast<const __nv_bfloat162*>(&ws[e])));
+    }
+    const __nv_bfloat162 m2 = __hmax2(__hmax2(am[0], am[1]), __hmax2(am[2], am[3]));
+    const float amax = warp_max_f32(fmaxf(__low2float(m2), __high2float(m2)));
+    return __fdiv_rn(amax, 127.0f);
+}
+
+__global__ void __launch_bounds__(kQgWarps * 32, 1) k_quant_gather(const __grid_constant__ QgArgs a)
+{
+    extern __shared__ __align__(1024) unsigned char smem[];
+    const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
-    const long long nblocks = nbs * n_d;
-    const bool vec = (shard % 8) == 0;
-    for (long long bi = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); bi < nblocks;
-         bi += warps) {
-        const int r = static_cast<int>(bi / nbs);
-        const long long b = bi - static_cast<long long>(r) * nbs;
-        long long valid = psi - static_cast<long long>(r) * shard;
-        valid = valid < 0 ? 0 : (valid > shard ? shard : valid);
-        const long long lo = b * block;
-        const long long hi = lo + block < valid ? lo + block : valid;
-        if (hi <= lo) {
-            if (lane == 0) scales[bi] = 0.0f;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem) + warp * kQgSlots;
+    unsigned char* slot0 = smem + 1024 + static_cast<size_t>(warp) * kQgSlots * kQgSlotBytes;
+    const long long step = static_cast<long long>(gridDim.x) * kQgWarps;
+    const long long first = static_cast<long long>(blockIdx.x) * kQgWarps + warp;
+
+    if (lane == 0) {
+        for (int s = 0; s < kQgSlots; ++s) mbar_init(&bar[s], 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+
+    bool ring = true;       // warp-uniform: cleared when a wait runs out
+    uint32_t pending = 0;   // lane 0: slots with a copy in flight
+    long long ib = first;   // issue cursor, kQgSlots blocks ahead of the work cursor
+    auto issue = [&](int s) {
+        if (ib < a.total) {
+            const QgBlock k = qg_block(a, ib);
+            if (ring && a.ring_ok && k.n == kQuantBlock && lane == 0) {
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(&bar[s], kQgSlotBytes);
+                bulk_load(slot0 + s * kQgSlotBytes, a.shards + k.j0, kQgSlotBytes, &bar[s]);
+                pending |= 1u << s;
+            }
+        }
+        ib += step;
+    };
+    // a block read from global memory twice (amax, then codes)
+    auto from_global = [&](const QgBlock& k) {
+        const uint16_t* x = a.shards + k.j0;
+        float amax = 0.0f;
+        for (int i = lane; i < k.n; i += 32) amax = fmaxf(amax, fabsf(Lp<ZERO_BF16>::widen(x[i])));
+        amax = warp_max_f32(amax);
+        const float sc = __fdiv_rn(amax, 127.0f);
+        if (lane == 0) a.scales[k.bi] = sc;
+        const float inv = quant_reciprocal(sc);
+        for (int i = lane; i < k.n; i += 32) {
+            const float cf = quant_code_f(Lp<ZERO_BF16>::widen(x[i]), sc, inv);
+            a.codes[k.j0 + i] = static_cast<signed char>(static_cast<uint8_t>(code_bits(cf)));
+            a.gathered[k.j0 + i] = Lp<ZERO_BF16>::narrow(__fmul_rn(cf, sc));
+        }
+    };
+    for (int s = 0; s < kQgSlots; ++s) issue(s);
+
+    uint32_t phase = 0;     // per slot: parity of its next completion
+    bool timed_out = false;
+    int s = 0;
+    for (long long bi = first; bi < a.total; bi += step, s = (s + 1 == kQgSlots) ? 0 : s + 1) {
+        const QgBlock k = qg_block(a, bi);
+        if (k.n <= 0) {
+            if (lane == 0) a.scales[k.bi] = 0.0f;
+            issue(s);
             continue;
         }
-        const long long j0 = static_cast<long long>(r) * shard + lo;
-        const int n = static_cast<int>(hi - lo);
-        const int nv = vec ? n / 8 : 0;  // 16-byte vectors
-        float amax = 0.0f;
-        for (int v = lane; v < nv; v += 32) {
-            const uint4 w = reinterpret_cast<const uint4*>(x + j0)[v];
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                amax = fmaxf(amax, fmaxf(fabsf(Lp<ZERO_BF16>::lo(ws[k])), fabsf(Lp<ZERO_BF16>::hi(ws[k]))));
-        }
-        for (int i = nv * 8 + lane; i < n; i += 32) amax = fmaxf(amax, fabsf(Lp<ZERO_BF16>::widen(x[j0 + i])));
-        amax = warp_max_f32(amax);
-        const float s = __fdiv_rn(amax, 127.0f);
-        if (lane == 0) scales[bi] = s;
-        const float inv = quant_reciprocal(s);
-        auto quant = [&](float xv, signed char& q, uint16_t& d) {
-            const float cf = quant_code_f(xv, s, inv);
-            q = static_cast<signed char>(static_cast<uint8_t>(code_bits(cf)));
-            d = Lp<ZERO_BF16>::narrow(__fmul_rn(cf, s));
-        };
-        for (int v = lane; v < nv; v += 32) {
-            const uint4 w = reinterpret_cast<const uint4*>(x + j0)[v];
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-            uint16_t d[8];
-            uint2 cq;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const float xs[4] = {Lp<ZERO_BF16>::lo(ws[2 * h]), Lp<ZERO_BF16>::hi(ws[2 * h]),
-                                     Lp<ZERO_BF16>::lo(ws[2 * h + 1]), Lp<ZERO_BF16>::hi(ws[2 * h + 1])};
-                float cf[4];
-                const uint32_t c4 = quant_code4(xs, s, inv, cf);
-                if (h == 0) cq.x = c4; else cq.y = c4;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) d[4 * h + e] = Lp<ZERO_BF16>::narrow(__fmul_rn(cf[e], s));
+        if (ring && a.ring_ok && k.n == kQuantBlock) {
+            const bool got = mbar_wait_bounded(&bar[s], (phase >> s) & 1u, nullptr, a.timeout_ns);
+            if (!__all_sync(0xffffffffu, got)) {
+                // the copy did not land in time: this block and the rest from global memory
+                timed_out = true;
+                ring = false;
+                issue(s);
+                from_global(k);
+                continue;
             }
-            reinterpret_cast<uint2*>(codes + j0)[v] = cq;
-            if (gathered == nullptr) continue;   // codes and scales only (gradient sender)
-            uint4 dv;
-            dv.x = d[0] | ((uint32_t)d[1] << 16);
-            dv.y = d[2] | ((uint32_t)d[3] << 16);
-            dv.z = d[4] | ((uint32_t)d[5] << 16);
-            dv.w = d[6] | ((uint32_t)d[7] << 16);
-            reinterpret_cast<uint4*>(gathered + j0)[v] = dv;
+            phase ^= 1u << s;
+            if (lane == 0) pending &= ~(1u << s);
+            // the block is read from its slot twice (amax, then codes) so that a
+            // lane holds 16 bytes of it at a time
+            const uint4* src = reinterpret_cast<const uint4*>(slot0 + s * kQgSlotBytes);
+            const float sc = slot_scale(src, lane);
+            if (lane == 0) a.scales[k.bi] = sc;
+            const float inv = quant_reciprocal(sc);
+            uint2* dst = reinterpret_cast<uint2*>(a.codes + k.j0);
+            uint4* gdst = reinterpret_cast<uint4*>(a.gathered + k.j0);
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+                const uint4 wv = src[v * 32 + lane];
+                const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
+                uint32_t packed[2], dq[4];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float xs[4] = {Lp<ZERO_BF16>::lo(ws[2 * h]), Lp<ZERO_BF16>::hi(ws[2 * h]),
+                                         Lp<ZERO_BF16>::lo(ws[2 * h + 1]), Lp<ZERO_BF16>::hi(ws[2 * h + 1])};
+                    float cf[4];
+                    packed[h] = quant_code4(xs, sc, inv, cf);
+                    dq[2 * h] = Lp<ZERO_BF16>::narrow2(__fmul_rn(cf[0], sc), __fmul_rn(cf[1], sc));
+                    dq[2 * h + 1] = Lp<ZERO_BF16>::narrow2(__fmul_rn(cf[2], sc), __fmul_rn(cf[3], sc));
+                }
+                dst[v * 32 + lane] = make_uint2(packed[0], packed[1]);
+                gdst[v * 32 + lane] = make_uint4(dq[0], dq[1], dq[2], dq[3]);
+            }
+            // every lane's reads of the slot are complete (their values were used): refill it
+            __syncwarp();
+            issue(s);
+        } else {
+            issue(s);
+            from_global(k);
         }
-        for (int i = nv * 8 + lane; i < n; i += 32) {
-            signed char q;
-            uint16_t d;
-            quant(Lp<ZERO_BF16>::widen(x[j0 + i]), q, d);
-            codes[j0 + i] = q;
-            if (gathered != nullptr) gathered[j0 + i] = d;
-        }
+    }
+    if (timed_out && lane == 0) {
+        // let the copies in flight land before the CTA's shared memory is released
+        for (int t = 0; t < kQgSlots; ++t)
+            if (pending & (1u << t)) mbar_wait_bounded(&bar[t], (phase >> t) & 1u, nullptr, a.timeout_ns);
+        if (a.sc != nullptr) atomicOr(&a.sc->status, ZERO_DEV_TIMEOUT);
     }
 }
 
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
 cudaError_t launch_quant_gather(const void* shards, int n_d, long long shard, long long psi, int block,
-                                signed char* codes, float* scales, void* gathered, cudaStream_t st)
+                                signed char* codes, float* scales, void* gathered, zero_dev_scalars* sc,
+                                cudaStream_t st)
 {
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
-    const long long nbs = (shard + block - 1) / block;
-    const long long nblocks = nbs * n_d;
-    if (nblocks <= 0) return cudaSuccess;
-    long long grid = (nblocks + 7) / 8;
-    if (grid > 16LL * sms) grid = 16LL * sms;
+    QgArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.shards = static_cast<const uint16_t*>(shards);
+    a.codes = codes;
+    a.gathered = static_cast<uint16_t*>(gathered);
+    a.scales = scales;
+    a.sc = sc;
+    a.shard = shard;
+    a.psi = psi;
+    a.block = block;
+    a.nbs = (shard + block - 1) / block;
+    a.total = static_cast<long long>(n_d) * a.nbs;
+    a.ring_ok = (block == kQuantBlock && shard % 8 == 0 && aligned16(shards) && aligned16(codes) &&
+                 aligned16(gathered)) ? 1 : 0;
+    a.timeout_ns = kDefaultTimeoutNs;
+    if (a.total <= 0) return cudaSuccess;
+    const size_t smem = 1024 + static_cast<size_t>(kQgWarps) * kQgSlots * kQgSlotBytes;
+    static int attr_done[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    if (dev < 64 && !__atomic_load_n(&attr_done[dev], __ATOMIC_ACQUIRE)) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(k_quant_gather, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        __atomic_store_n(&attr_done[dev], 1, __ATOMIC_RELEASE);
+    }
+    long long grid = (a.total + kQgWarps - 1) / kQgWarps;
+    if (grid > sms) grid = sms;
     count_launch();
-    k_quant_gather<<<static_cast<unsigned>(grid), 256, 0, st>>>(static_cast<const uint16_t*>(shards), n_d, shard,
-                                                                psi, block, nbs, codes, scales,
-                                                                static_cast<uint16_t*>(gathered));
+    k_quant_gather<<<static_cast<unsigned>(grid), kQgWarps * 32, smem, st>>>(a);
     return cudaGetLastError();
 }
 

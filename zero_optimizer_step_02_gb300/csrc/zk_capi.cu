@@ -719,7 +719,7 @@ ZERO_API zero_status zero_quant_gather(const zero_plan* p, const void* shards, i
     if ((s = check_dev(scales)) != ZERO_OK) return s;
     if ((s = check_dev(gathered)) != ZERO_OK) return s;
     return from_cuda(zk::launch_quant_gather(shards, p->n_d, p->shard, p->psi, block, codes, scales, gathered,
-                                             as_stream(stream)));
+                                             nullptr, as_stream(stream)));
 }
 
 ZERO_API zero_status zero_step_fused_qgather(const zero_plan* p, const zero_hparams* hp, const void* const* ranks,
@@ -1093,7 +1093,7 @@ ZERO_API zero_status zero_step_layers(const zero_hparams* hp, int n_layers, cons
         for (int g = 0; g < gathers; ++g) {
             if (qwz)
                 ZK_TRY(zk::launch_quant_gather(L.shards_lp, n_d, p->shard, p->psi, zk::kQuantBlock,
-                                               gathered_codes[k], gathered_scales[k], gathered[k], gs));
+                                               gathered_codes[k], gathered_scales[k], gathered[k], sc, gs));
             else
                 ZK_TRY(zk::launch_all_gather(shard_ptr, n_d, p->shard, p->psi, gathered[k], sc, gs));
         }
