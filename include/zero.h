@@ -483,13 +483,18 @@ ZERO_API zero_status zero_step_layers(const zero_hparams* hp, int n_layers, cons
  *   kernel 0: the streaming engine (reduce op, one 4096-element tile),
  *   kernel 1: the all-gather ring (one 8192-element shard),
  *   kernel 2: the gradient sender (one 2048-element block),
+ *   kernel 3: the quantized weight gather (one 2048-element shard),
  * whose bulk copies are never issued, so every bounded wait runs out (after
- * timeout_ns for kernel 0, at most 10 s; after 2 ms for kernels 1 and 2).
- * The kernel gives up, lets nothing in flight land (nothing was issued), sets
- * ZERO_DEV_TIMEOUT in scalars->status and returns.  scratch: a 16-byte
- * aligned device buffer of at least 32 KB; the gradient or shard region (its
- * first 16 KB) is never read; kernel 2 may write its scale row (16 bytes at
- * offset 8 KB).  Exists so that the timeout handling can be tested.         */
+ * timeout_ns for kernel 0, at most 10 s; after 2 ms for kernels 1 to 3).
+ * Kernels 0 to 2 give up, let nothing in flight land (nothing was issued),
+ * set ZERO_DEV_TIMEOUT in scalars->status and return.  scratch: a 16-byte
+ * aligned device buffer of at least 32 KB; for kernels 0 to 2 the gradient
+ * or shard region (its first 16 KB) is never read; kernel 2 may write its
+ * scale row (16 bytes at offset 8 KB).  Kernel 3 sets ZERO_DEV_TIMEOUT too
+ * but then quantizes its block from global memory instead, as it does on
+ * any run-out wait: the bf16 values at offset 0 (2048 of them), codes at
+ * 4 KB, dequantized bf16 at 8 KB, the scale at 12 KB, as zero_quant_gather
+ * would write them.  Exists so that the timeout handling can be tested.     */
 ZERO_API zero_status zero_debug_stream_timeout(int kernel, void* scratch, zero_dev_scalars* scalars_dev,
                                                long long timeout_ns, void* stream);
 

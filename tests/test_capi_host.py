@@ -150,7 +150,7 @@ def test_calls_check_arguments_before_touching_the_device(z):
     assert _raw(z, "zero_debug_stream_timeout", 0, A + 8, A, 1000, None) == 2
     assert _raw(z, "zero_debug_stream_timeout", 0, A, A + 16, 1000, None) == 2
     assert _raw(z, "zero_debug_stream_timeout", 0, A, A, 0, None) == 1
-    assert _raw(z, "zero_debug_stream_timeout", 3, A, A, 1000, None) == 1
+    assert _raw(z, "zero_debug_stream_timeout", 4, A, A, 1000, None) == 1
     # fp16 parameters cannot take the bf16 quantizer
     p16 = z.Plan(1000, 2, stage=2, param_dtype=z.ZERO_FP16)
     assert _raw(z, "zero_quant_gather", p16.handle, A, 2048, A, A, A, None) == 3

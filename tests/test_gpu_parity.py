@@ -354,6 +354,26 @@ def test_pipelined_kernel_timeout_path_reports_and_context_survives(kernel):
     job.assert_bit_exact()
 
 
+def test_quant_gather_run_out_wait_reports_and_falls_back_to_global_memory():
+    # the weight gather's copies are never issued: its wait runs out, it
+    # reports, then quantizes the block from global memory (the same codes,
+    # scale and dequantized values as the oracle's)
+    sc = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    scratch = torch.zeros(32768, dtype=torch.uint8, device="cuda")
+    x = torch.zeros(2048, dtype=torch.bfloat16)
+    synth.gaussian_(x, 0.02, 53, 0)
+    x[::97] = 0.0
+    scratch[:4096] = x.view(torch.uint8).cuda()
+    z.zero_scalars_init(sc)
+    z.zero_debug_stream_timeout(3, scratch, sc, 2_000_000)
+    assert z.read_scalars(sc).status & z.ZERO_DEV_TIMEOUT
+    oc, osc, og = oracle.quant_gather(u16(x), 1, 2048, 2048, 2048)
+    got = scratch.cpu()
+    assert np.array_equal(got[4096:6144].view(torch.int8).numpy(), oc)
+    assert np.array_equal(u32(got[12288:12292].view(torch.float32).numpy()), u32(osc))
+    assert np.array_equal(got[8192:12288].view(torch.int16).numpy().view(np.uint16), og)
+
+
 def test_bounded_wait_reports_timeout_and_context_survives():
     sc = torch.zeros(256, dtype=torch.uint8, device="cuda")
     z.zero_scalars_init(sc)

@@ -353,6 +353,7 @@ struct QgArgs {
     zero_dev_scalars* sc;                 // may be null
     long long shard, psi, nbs, total;     // total = n_d * nbs blocks
     int block, ring_ok;                   // ring_ok: block == 2048, shard % 8 == 0, 16-byte aligned buffers
+    int starve;                           // issue no copy: every wait runs out (tests the fallback)
     unsigned long long timeout_ns;
 };
 
@@ -418,7 +419,7 @@ __global__ void __launch_bounds__(kQgWarps * 32, 1) k_quant_gather(const __grid_
     auto issue = [&](int s) {
         if (ib < a.total) {
             const QgBlock k = qg_block(a, ib);
-            if (ring && a.ring_ok && k.n == kQuantBlock && lane == 0) {
+            if (ring && a.ring_ok && k.n == kQuantBlock && lane == 0 && !a.starve) {
                 fence_proxy_async_smem();
                 mbar_arrive_expect_tx(&bar[s], kQgSlotBytes);
                 bulk_load(slot0 + s * kQgSlotBytes, a.shards + k.j0, kQgSlotBytes, &bar[s]);
@@ -511,7 +512,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 
 cudaError_t launch_quant_gather(const void* shards, int n_d, long long shard, long long psi, int block,
                                 signed char* codes, float* scales, void* gathered, zero_dev_scalars* sc,
-                                cudaStream_t st)
+                                cudaStream_t st, bool starve)
 {
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
@@ -529,7 +530,8 @@ cudaError_t launch_quant_gather(const void* shards, int n_d, long long shard, lo
     a.total = static_cast<long long>(n_d) * a.nbs;
     a.ring_ok = (block == kQuantBlock && shard % 8 == 0 && aligned16(shards) && aligned16(codes) &&
                  aligned16(gathered)) ? 1 : 0;
-    a.timeout_ns = kDefaultTimeoutNs;
+    a.timeout_ns = starve ? 2000000ull : kDefaultTimeoutNs;
+    a.starve = starve ? 1 : 0;
     if (a.total <= 0) return cudaSuccess;
     const size_t smem = 1024 + static_cast<size_t>(kQgWarps) * kQgSlots * kQgSlotBytes;
     static int attr_done[64];

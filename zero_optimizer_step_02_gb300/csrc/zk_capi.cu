@@ -929,6 +929,14 @@ ZERO_API zero_status zero_debug_stream_timeout(int kernel, void* scratch, zero_d
         return from_cuda(zk::launch_quantize_grads(ranks, 1, 2048, 2048, zk::kQuantBlock, codes,
                                                    reinterpret_cast<float*>(buf + 8192), sc, as_stream(stream), true));
     }
+    if (kernel == 3) {
+        // one 2048-element shard: bf16 values in the first 4 KB, codes in the
+        // next 2 KB, dequantized values at 8 KB, the scale at 12 KB
+        return from_cuda(zk::launch_quant_gather(buf, 1, 2048, 2048, zk::kQuantBlock,
+                                                 reinterpret_cast<signed char*>(buf + 4096),
+                                                 reinterpret_cast<float*>(buf + 12288), buf + 8192, sc,
+                                                 as_stream(stream), true));
+    }
     if (kernel != 0) return ZERO_ERR_INVALID_ARG;
     // one full tile of one bf16 rank: the consumers wait for a stage the
     // producer never fills

@@ -99,10 +99,11 @@ cudaError_t launch_repair(const float* master_in, const float* m_in, const float
 cudaError_t launch_all_gather(const void* const* shards, int n_d, long long shard, long long psi,
                               void* gathered, zero_dev_scalars* sc, cudaStream_t st, bool starve = false);
 // sc may be null (a wait that runs out is then not reported; the results are
-// complete either way)
+// complete either way); starve: issue no copy, so every wait runs out and the
+// blocks are read from global memory (tests that path)
 cudaError_t launch_quant_gather(const void* shards, int n_d, long long shard, long long psi,
                                 int block, signed char* codes, float* scales, void* gathered,
-                                zero_dev_scalars* sc, cudaStream_t st);
+                                zero_dev_scalars* sc, cudaStream_t st, bool starve = false);
 cudaError_t launch_quantize_grads(const void* const* ranks, int n_d, long long shard, long long psi, int block,
                                   signed char* const* codes, float* scales, zero_dev_scalars* sc, cudaStream_t st,
                                   bool starve = false);
