@@ -713,9 +713,14 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<GT, OP>()) k_stream(cons
 #pragma unroll
                     for (int ch = 0; ch < kChunksPerThread; ++ch) {
                         amax[ch] = 0.0f;
+                        if (fast) {   // every element valid: no per-element bound test
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            if ((ch * kConsumers + tid) * 4 + e < len) amax[ch] = fmaxf(amax[ch], fabsf(xq[ch][e]));
+                            for (int e = 0; e < 4; ++e) amax[ch] = fmaxf(amax[ch], fabsf(xq[ch][e]));
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                if ((ch * kConsumers + tid) * 4 + e < len) amax[ch] = fmaxf(amax[ch], fabsf(xq[ch][e]));
+                        }
                         amax[ch] = warp_max_f32(amax[ch]);
                     }
                     // two buffers used alternately: between two uses of one buffer every
@@ -747,8 +752,13 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<GT, OP>()) k_stream(cons
                         cnt = cnt < 0 ? 0 : (cnt > 4 ? 4 : cnt);
                         float cf[4];
                         const uint32_t cw = quant_code4(xq[ch], scale, inv_scale, cf);
-                        const uint32_t d01 = Lp<ZERO_BF16>::narrow2(__fmul_rn(cf[0], scale), __fmul_rn(cf[1], scale));
-                        const uint32_t d23 = Lp<ZERO_BF16>::narrow2(__fmul_rn(cf[2], scale), __fmul_rn(cf[3], scale));
+                        // the dequantized products on register pairs (they feed the
+                        // bf16 conversion, nothing to contract with)
+                        float q0, q1, q2, q3;
+                        unpack2(mul2(pack2(cf[0], cf[1]), pack2(scale, scale)), q0, q1);
+                        unpack2(mul2(pack2(cf[2], cf[3]), pack2(scale, scale)), q2, q3);
+                        const uint32_t d01 = Lp<ZERO_BF16>::narrow2(q0, q1);
+                        const uint32_t d23 = Lp<ZERO_BF16>::narrow2(q2, q3);
                         const uint16_t dq[4] = {static_cast<uint16_t>(d01), static_cast<uint16_t>(d01 >> 16),
                                                 static_cast<uint16_t>(d23), static_cast<uint16_t>(d23 >> 16)};
                         if (!alive) continue;
