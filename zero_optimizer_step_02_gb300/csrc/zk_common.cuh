@@ -33,7 +33,9 @@ constexpr int kMaxStages = 8;
 // 0.940 ms); 152 SMs x 2 stages of up to 112 KB already keep ~20-34 MB in
 // flight, and more only adds L2 and DRAM contention.  With the state in host
 // memory the ring stages only the small reduced-gradient tiles and keeps the
-// deeper ring (up to kMaxStages), which that path measured faster with.
+// deeper ring (up to kMaxStages), which that path measured faster with; so
+// does the fused step over several groups of int8 ranks, whose state is read
+// directly (the stages then hold codes only: three of 64 KB fit).
 constexpr int kRingStages = 2;
 constexpr int kStageOffset = 1024;          // dynamic smem bytes before the stage ring
 constexpr int kMaxPartials = 4096;          // per-CTA partial sums kept in the workspace
