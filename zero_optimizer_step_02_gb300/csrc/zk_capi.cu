@@ -298,13 +298,15 @@ zero_status run_fused_q8(const zero_plan* p, const zero_hparams* hp, const signe
     if (flags & zk::F_FINALIZE) set_finalize(a, fin_ws, fin_n);
     set_q8_ranks(a, p, codes, scales);
     a.n_side = 3;
-    // more int8 ranks than one stage holds (several rank groups per tile): the
-    // state is read with direct 16-byte loads instead of being staged, so the
-    // stages hold codes only and the ring gets three of them (N_d = 64: 3.93
-    // -> 3.55 ms, 92% -> 102% of the copy rate; N_d = 32: 2.26 -> 2.18 ms).
-    // The 16-bit fused step measured slower that way (N_d = 16: 2.16 -> 2.22
-    // ms) and keeps its state staged.
-    a.n_side_tma = p->n_d > 2 * zk::kGroupRanks ? 0 : 3;
+    // a full stage of int8 ranks or more (N_d >= 16, one or several rank groups
+    // per tile): the state is read with direct 16-byte loads instead of being
+    // staged, so the stages hold codes only and the ring gets three of them
+    // (N_d = 64: 3.93 -> 3.55 ms, 92% -> 102% of the copy rate; N_d = 32: 2.26
+    // -> 2.18 ms; N_d = 16: 1.69 -> 1.67 ms).  With fewer ranks the loads' latency
+    // is not hidden (N_d = 8: 1.37 -> 1.69 ms), and the 16-bit fused step
+    // measured slower that way at any N_d (16: 2.16 -> 2.22 ms): both keep the
+    // state staged.
+    a.n_side_tma = p->n_d >= 2 * zk::kGroupRanks ? 0 : 3;
     a.side[0] = mi;
     a.side[1] = m_in;
     a.side[2] = vi;
@@ -890,9 +892,10 @@ ZERO_API zero_status zero_step_fused_qgz_qgather(const zero_plan* p, const zero_
     if (clip) set_finalize(a, ws, n);
     set_q8_ranks(a, p, codes, scales);
     a.n_side = 3;
-    // several groups of int8 ranks: the state read directly, as in run_fused_q8
-    // (both ZeRO++ exchanges at N_d = 64: 4.18 -> 3.69 ms, 87% -> 99%)
-    a.n_side_tma = p->n_d > 2 * zk::kGroupRanks ? 0 : 3;
+    // N_d >= 16 int8 ranks: the state read directly, as in run_fused_q8 (both
+    // ZeRO++ exchanges at N_d = 64: 4.18 -> 3.69 ms, 87% -> 99%; at N_d = 2
+    // direct loads measured 22% slower)
+    a.n_side_tma = p->n_d >= 2 * zk::kGroupRanks ? 0 : 3;
     a.side[0] = mi;
     a.side[1] = m_in;
     a.side[2] = vi;
