@@ -60,10 +60,16 @@ __global__ void __launch_bounds__(kSmallThreads, kChunks == 1 ? 5 : 4) k_small_s
 {
     __shared__ StepConsts shc;
     zero_dev_scalars* sc = a.sc;
-    // chunk k of this thread: elements [4 (t0 + k * nth), + 4).  Every chunk's
-    // master/m/v and its first kRankGroup ranks' gradients are loaded first;
-    // thread 0 reads the step scalars and forms the constants while they are
-    // in flight
+    // Thread 0's read of the step scalars goes out first, ahead of the data
+    // (behind 20 MB of requests it would come back last); then chunk k of
+    // this thread, elements [4 (t0 + k * nth), + 4): every chunk's master/m/v
+    // and its first kRankGroup ranks' gradients are loaded before anything
+    // waits on them, and thread 0 forms the constants while they are in flight
+    double b1pow = 0.0, b2pow = 0.0;
+    if (threadIdx.x == 0) {
+        b1pow = sc->beta1_pow;
+        b2pow = sc->beta2_pow;
+    }
     const long long nth = static_cast<long long>(gridDim.x) * kSmallThreads;
     const long long t0 = static_cast<long long>(blockIdx.x) * kSmallThreads + threadIdx.x;
     const int g0 = a.n_ranks < kRankGroup ? a.n_ranks : kRankGroup;
@@ -104,7 +110,7 @@ __global__ void __launch_bounds__(kSmallThreads, kChunks == 1 ? 5 : 4) k_small_s
     if (threadIdx.x == 0) {
         StepConsts c = {};
         set_divisor(c, a.n_ranks, 1.0f);
-        set_adam(c, a.hp, sc->beta1_pow, sc->beta2_pow);
+        set_adam(c, a.hp, b1pow, b2pow);
         c.clip = 0;
         c.coef = 1.0f;
         shc = c;
