@@ -259,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<GT, OP>()) k_stream(cons
     const uint32_t side_off = scale_off + kScaleBytes;
 
     bool nonfinite = false;
-    float sq_hi = 0.0f, sq_lo = 0.0f;
+    f32x2 sq_hi = pack2(0.0f, 0.0f), sq_lo = pack2(0.0f, 0.0f);
 
     if (skip) {
         // nothing to do but record the norm (CTA 0); fall through to the end
@@ -545,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<GT, OP>()) k_stream(cons
                     }
                     if (want_sq) {
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) sq_accumulate(gv[e], sq_hi, sq_lo);
+                        for (int e = 0; e < 4; e += 2) sq_accumulate2(gv[e], gv[e + 1], sq_hi, sq_lo);
                     }
                     if (alive && a.out_f32[0] != nullptr) {
                         if (fast) {
@@ -784,7 +784,11 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<GT, OP>()) k_stream(cons
     const int any_nonfinite = __syncthreads_or(nonfinite ? 1 : 0);
     if (tid == 0 && any_nonfinite && (a.flags & F_DETECT)) atomicOr(&a.sc->nonfinite, 1);
     if (OP == OP_REDUCE && (a.flags & F_SQNORM)) {
-        double part = warp < kConsumerWarps ? __dadd_rn(static_cast<double>(sq_hi), static_cast<double>(sq_lo)) : 0.0;
+        float h0, h1, l0, l1;
+        unpack2(sq_hi, h0, h1);
+        unpack2(sq_lo, l0, l1);
+        double part = warp < kConsumerWarps ? __dadd_rn(__dadd_rn(static_cast<double>(h0), static_cast<double>(l0)),
+                                                        __dadd_rn(static_cast<double>(h1), static_cast<double>(l1))) : 0.0;
         part = warp_sum_f64(part);
         if (lane == 0 && warp < kConsumerWarps) sh->red_d[warp] = part;
         __syncthreads();
