@@ -294,8 +294,8 @@ TRAFFIC = {
     # the per-layer fused step of the 8-layer workload, 9.597 GB read + 3.020 GB
     # written (two launches' mean); the GPT-2-small clipped step's Adam pass,
     # 1.991 + 1.680 GB
-    ("fused_step", "zero3_llama3_8b_8layers_psil218112000_nd16"): {"bytes": 12.617e9, "src": "3b081f06db42"},
-    ("adam_shard", "zero2_gpt2small_psi124439808_nd8_adamw_clip1"): {"bytes": 3.671e9, "src": "3b081f06db42"},
+    ("fused_step", "zero3_llama3_8b_8layers_psil218112000_nd16"): {"bytes": 12.617e9, "src": "89dae4f5ae82"},
+    ("adam_shard", "zero2_gpt2small_psi124439808_nd8_adamw_clip1"): {"bytes": 3.671e9, "src": "89dae4f5ae82"},
 }
 
 
