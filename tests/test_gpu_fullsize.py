@@ -7,7 +7,8 @@ the whole input (the clipping norm) or from properties fixed by the inputs
 Workloads (seeded synthetic inputs; see the design notes for the recipe):
   GPT-2-small ZeRO-2, Psi = 124,439,808, N_d = 8, AdamW, clip 1.0, heavy tail
   GPT-2-1.5B ZeRO-2, Psi = 1.5e9, N_d = 8, fp16 grads, loss scale 1024, skip
-  Llama-3-8B-shaped ZeRO-3 layer, Psi_l = 218,112,000, N_d = 16
+  Llama-3-8B-shaped ZeRO-3 layer, Psi_l = 218,112,000, N_d = 16 (also the
+  8-layer loop, and the layer's quantized weight gather)
   Psi = 2^28 sweep ends, N_d = 2 (with the fused int8 gather) and N_d = 64
 """
 import numpy as np
@@ -309,3 +310,42 @@ def test_psi_2_28_quantized_gradient_exchange_full_size(n_d):
     p, m, v = (a.copy() for a in st)
     oracle.adam_update(hpo, c, g, p, m, v)
     job.check(idx, (p, m, v))
+
+
+def test_llama_layer_quantized_weight_gather_full_size():
+    # the layer loop's qwZ gather at its full size (Psi_l = 218,112,000, N_d =
+    # 16 shards of 13,632,000): the bulk-copy pipeline on every full aligned
+    # block, the plain loads on each shard's last (partial) block; sampled
+    # whole blocks against the oracle's block quantizer, every scale checked
+    psi, n_d = 218_112_000, 16
+    plan = z.Plan(psi, n_d, stage=3, shard_pad=8)
+    S = plan.shard
+    nbs = -(-S // 2048)
+    shards = torch.zeros(plan.padded, dtype=torch.bfloat16, device="cuda")
+    synth.gaussian_(shards[:psi], 0.02, 707, 0)
+    shards[5 * S + 4096:5 * S + 6144] = 0.0          # an all-zero block: scale 0, codes 0
+    codes = torch.full((plan.padded,), 77, dtype=torch.int8, device="cuda")
+    scales = torch.full((n_d * nbs,), -1.0, device="cuda")
+    gathered = torch.zeros(psi, dtype=torch.bfloat16, device="cuda")
+    z.zero_quant_gather(plan.handle, shards, 2048, codes, scales, gathered)
+    torch.cuda.synchronize()
+    # every full block's scale: its absmax / 127 (one fp32 division), from the
+    # bf16 values on the host
+    full = (S // 2048) * 2048
+    x = u16(shards).reshape(n_d, S)[:, :full].astype(np.uint32) << 16
+    amax = np.abs(x.view(np.float32)).reshape(n_d, S // 2048, 2048).max(axis=2)
+    want_s = (amax / np.float32(127.0)).astype(np.float32)
+    got_s = scales.view(n_d, nbs)[:, :S // 2048].cpu().numpy()
+    assert np.array_equal(u32(got_s), u32(want_s))
+    # sampled whole blocks (full ones, each shard's last, the zero one) bit for bit
+    rng = np.random.default_rng(17)
+    picks = [(r, int(b)) for r in range(n_d) for b in rng.choice(S // 2048, 3, replace=False)]
+    picks += [(r, nbs - 1) for r in range(n_d)] + [(5, 2)]
+    for r, b in picks:
+        lo = r * S + b * 2048
+        hi = min(lo + 2048, r * S + S, psi)
+        x = u16(shards[lo:hi])
+        c, s, d = oracle.quantize_block(x)
+        assert u32(np.float32(scales[r * nbs + b].item())) == u32(np.float32(s))
+        assert np.array_equal(codes[lo:hi].cpu().numpy(), c)
+        assert np.array_equal(u16(gathered[lo:hi]), d)
