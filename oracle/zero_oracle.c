@@ -17,7 +17,7 @@
  *   [MP-notes]  "Model parallelism (tensor, pipeline) -- Hinglish notes" (6.1.7)
  * Where the pages are silent (the Adam equations, the clipping rule, loss
  * scaling, the quantizer's rounding) the reading used is stated at the
- * function and listed with the other readings in the design notes.
+ * function that follows it.
  */
 #include "zero_oracle.h"
 

@@ -75,7 +75,8 @@ void zo_all_gather_u16(int n_d, long long psi, long long shard, const uint16_t* 
 void zo_all_gather_f32(int n_d, long long psi, long long shard, const float* const* shards,
                        float* gathered);
 
-/* ---- Adam (the reading stated in the design notes) ---- */
+/* ---- Adam: textbook Adam (Kingma & Ba) in the efficient order of their
+ * Section 2, decoupled weight decay as in AdamW (the pages give no equations) */
 typedef struct {
     float step_size; /* lr * sqrt(1 - beta2^t) / (1 - beta1^t) */
     float eps_hat;   /* eps * sqrt(1 - beta2^t)                */

@@ -4,7 +4,7 @@ computes element by element.  Global quantities come from the oracle over
 the whole input (the clipping norm) or from properties fixed by the inputs
 (exactly one injected non-finite value).
 
-Workloads (seeded synthetic inputs; see the design notes for the recipe):
+Workloads (seeded synthetic inputs from zero_optimizer_step_02_gb300.synth):
   GPT-2-small ZeRO-2, Psi = 124,439,808, N_d = 8, AdamW, clip 1.0, heavy tail
   GPT-2-1.5B ZeRO-2, Psi = 1.5e9, N_d = 8, fp16 grads, loss scale 1024, skip
   Llama-3-8B-shaped ZeRO-3 layer, Psi_l = 218,112,000, N_d = 16 (also the
