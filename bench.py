@@ -654,6 +654,14 @@ def gpu_arm(args, rank, world, device):
                 "kernel_ms": round(kms, 4), "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)"}
 
     e2e = None if args.no_e2e else e2e_measure(job, w, args, device, world)
+    if e2e is not None:
+        # the link the end-to-end number is bound by, measured on this machine in
+        # this run: the step's host-to-device rate against a plain 1 GiB copy's
+        ms_e2e = w["psi_total"] * world / e2e["value"] * 1e3
+        e2e["h2d_gbs"] = round(e2e["h2d_bytes_per_step"] / (ms_e2e / 1e3) / 1e9, 1)
+        link = host_link_gbs(torch, device)
+        e2e["host_link_gbs"] = link
+        e2e["h2d_frac_of_link"] = round(e2e["h2d_gbs"] / link["h2d"], 4)
     sender = None
     if w.get("qgz"):
         # the sender pass (every rank quantizes its bf16 gradient): 2 + 1 + 4/2048 bytes per param per rank
